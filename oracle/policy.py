@@ -1,0 +1,93 @@
+"""Sampling policy: logits -> the distribution that enters the acceptance rule.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  float64 throughout.
+
+Pages followed
+  whoami-wesleyyou.top "Speculative Decoding" notes, § 从 LM head 到 sampling
+  distribution: the LM head gives logits z; temperature, softmax and top-k
+  turn them into the sampling distribution; greedy decoding puts all mass on
+  the argmax token; p and q may use different policies, but q must be the
+  distribution the draft was actually drawn from.
+  wineandchord.com "推测解码：接受规则、状态与收益边界", § 与 Logit Processor
+  的组合: the acceptance ratio uses the processed p_i and q_i (temperature,
+  top-k among the listed processors).
+  tannlonggtaoo.github.io "Speculative Decoding", § Greedy Sampling:
+  temperature 0 reduces verification to comparing against the argmax.
+
+Readings where the pages are silent (listed in the design doc):
+  * greedy / argmax tie-break: the lowest index among the maxima;
+  * top-k selects on the raw logits (before temperature); the threshold is the
+    k-th largest raw value and every entry >= threshold is kept, so ties at the
+    threshold are all kept; k <= 0 or k >= V means no filtering;
+  * a row is "non-finite" when the temperature is NaN, negative or infinite,
+    or the logits hold a NaN or +inf, or no finite logit at all; such a row is
+    flagged and replaced by the one-hot distribution at the finite argmax
+    (index 0 when nothing is finite).  The pages only say such inputs are
+    errors (verify_candidate raises ValueError on non-finite probabilities).
+"""
+
+import numpy as np
+
+FLAG_NONFINITE = 4
+
+
+class Dist:
+    """A policy result: either one-hot at ``index`` or a probability vector."""
+
+    __slots__ = ("onehot", "index", "probs", "flags")
+
+    def __init__(self, onehot, index=None, probs=None, flags=0):
+        self.onehot = onehot
+        self.index = index
+        self.probs = probs
+        self.flags = flags
+
+    def dense(self, V, dtype=np.float64):
+        """The distribution as a length-V vector."""
+        if self.onehot:
+            out = np.zeros(V, dtype=dtype)
+            out[self.index] = 1
+            return out
+        return self.probs
+
+
+def finite_argmax(z):
+    """Lowest index of the largest finite logit; 0 when no logit is finite."""
+    z = np.asarray(z, dtype=np.float64)
+    finite = np.isfinite(z)
+    if not finite.any():
+        return 0
+    best = z[finite].max()
+    return int(np.flatnonzero(finite & (z == best))[0])
+
+
+def topk_threshold(z, k):
+    """k-th largest raw logit value (k counted from 1), or None for no filter."""
+    V = z.shape[0]
+    if k <= 0 or k >= V:
+        return None
+    ordered = np.sort(z)[::-1]
+    return ordered[k - 1]
+
+
+def policy_distribution(z, temperature, top_k=0):
+    """Apply one row's policy (temperature T, top-k) to logits z.
+
+    T == 0      -> greedy: one-hot at the argmax (lowest index on ties).
+    T > 0       -> softmax(z / T) over the entries kept by top-k.
+    bad input   -> one-hot at the finite argmax, flagged FLAG_NONFINITE.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    T = float(temperature)
+    bad = (not np.isfinite(T)) or T < 0.0
+    bad = bad or bool(np.isnan(z).any()) or bool(np.isposinf(z).any())
+    bad = bad or not bool(np.isfinite(z).any())
+    if bad:
+        return Dist(True, index=finite_argmax(z), flags=FLAG_NONFINITE)
+    if T == 0.0:
+        return Dist(True, index=finite_argmax(z))
+    thr = topk_threshold(z, int(top_k))
+    kept = z if thr is None else np.where(z >= thr, z, -np.inf)
+    m = kept.max()
+    weights = np.exp((kept - m) / T)
+    return Dist(False, probs=weights / weights.sum())
