@@ -1,0 +1,319 @@
+"""Throughput of speculative-sampling verification on GB300.
+
+One step = one chain verification of a batch of B = 256 sequences with
+gamma = 7 drafts over a V = 128256 bf16 vocabulary (2048 target rows + 1792
+draft rows, 985,006,080 bytes of logits): every stage of the path (policy and
+softmax statistics, acceptance, residual and bonus draws) runs inside the
+timed call.  Inputs are resident in HBM and larger than L2, so every step
+streams them from DRAM.  Metric: verified vocabulary rows per second,
+B * (gamma + 1) per step.
+
+Arms:
+  default           the CUDA library through its Python binding
+  --impl reference  the CPU oracle (the plain float64 restatement of the
+                    method) on this host's cores, on a bounded sample
+
+Under torchrun each rank verifies its own batch on its own GPU (weak
+scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = 2
+METRIC = "verified vocab rows/s (B*(gamma+1))"
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_temp_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "unit_kernel_traffic.json")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_rate(w, n_seqs):
+    """The CPU oracle on the first n_seqs sequences: verified rows per second."""
+    from oracle import verify as ov
+    gamma = w["gamma"]
+    t0 = time.perf_counter()
+    ov.verify_chain(w["target"], w["draft"], w["tokens"], w["target_temperature"],
+                    w["draft_temperature"], w["target_top_k"], w["draft_top_k"], seed=w["seed"],
+                    seqs=range(n_seqs))
+    dt = time.perf_counter() - t0
+    return n_seqs * (gamma + 1) / dt, dt
+
+
+def config_entry(w):
+    return {"workload": f"chain verify B={w['B']} gamma={w['gamma']} V={w['V']} {w['dtype']} "
+                        "(temperature 1, Zipf logits, draft sigma 0.4)",
+            "B": w["B"], "gamma": w["gamma"], "V": w["V"],
+            "logit_bytes_per_step": logit_bytes(w),
+            "l2": "inputs larger than L2 (985 MB of logits per step)"}
+
+
+def logit_bytes(w):
+    esize = 2 if w["dtype"] == "bf16" else 4
+    return (w["B"] * (w["gamma"] + 1) + w["B"] * w["gamma"]) * w["V"] * esize
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_temp_gb300 import workloads
+    w = workloads.config(WORKLOAD)
+    n_seqs = args.reference_seqs
+    rows_per_step = n_seqs * (w["gamma"] + 1)
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, min(n_seqs, 4))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_rate(w, n_seqs)
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_entry(w),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {n_seqs} of {w['B']} sequences per step"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verification_temp_gb300 as sv
+    from speculative_decoding_verification_temp_gb300 import workloads
+
+    w = workloads.config(WORKLOAD)
+    B, gamma, V = w["B"], w["gamma"], w["V"]
+    seed = w["seed"] + rank  # each rank verifies its own batch
+    rows = B * (gamma + 1)
+    nbytes = logit_bytes(w)
+
+    target_h = torch.from_numpy(w["target"]).to(torch.bfloat16).pin_memory()
+    draft_h = torch.from_numpy(w["draft"]).to(torch.bfloat16).pin_memory()
+    tokens_h = torch.from_numpy(w["tokens"]).pin_memory()
+    target = target_h.to(dev)
+    draft = draft_h.to(dev)
+    tokens = tokens_h.to(dev)
+    tp = torch.from_numpy(w["target_temperature"]).to(dev)
+    tq = torch.from_numpy(w["draft_temperature"]).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return sv.verify_chain(target, draft, tokens, tp, tq, seed=seed)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    # device-timed region: per-launch events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * rows * args.steps / (elapsed_ms / 1e3)
+
+    # end to end through the binding: pinned host inputs in, results back out
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        t_d = target_h.to(dev, non_blocking=True)
+        d_d = draft_h.to(dev, non_blocking=True)
+        k_d = tokens_h.to(dev, non_blocking=True)
+        r = sv.verify_chain(t_d, d_d, k_d, tp, tq, seed=seed)
+        n_out = r.num_accepted.to("cpu")
+        t_out = r.tokens.to("cpu")
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = target_h.numel() * 2 + draft_h.numel() * 2 + tokens_h.numel() * 4
+    d2h = n_out.numel() * 4 + t_out.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    avg_launch_ms = statistics.mean(launch_ms)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_entry(w),
+        "clocks": clk.summary(),
+        "e2e": {"value": world * rows / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(),
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "unit_kernel", "launch_ms_avg": avg_launch_ms,
+                     "launch_ms_median": statistics.median(launch_ms)},
+        "hbm_gbs_vs_8tbs_nominal": achieved / 8000.0,
+    }
+    if not args.no_cpu_baseline:
+        rate, dt = oracle_sample_rate(w, args.cpu_seqs)
+        line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {args.cpu_seqs} of {B} sequences, one pass, "
+                                          f"{dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seqs", type=int, default=256)
+    ap.add_argument("--reference-seqs", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * specverify.h - C ABI of the GB300 speculative-sampling verification library
+ * (libspecverify.so, CUDA for sm_103a).
+ *
+ * What is computed (citations name the page and its section):
+ *   - Acceptance: draft token x is accepted iff u < min(1, p(x)/q(x)) with u an
+ *     independent uniform in [0,1).  whoami-wesleyyou.top "Speculative
+ *     Decoding" notes, section "Acceptance 与 correction"; wineandchord.com
+ *     "推测解码：接受规则、状态与收益边界", section "单位置接受 reference".
+ *   - Correction: at the first rejection the replacement token is drawn from
+ *     norm([p - q]+); if all drafts are accepted a bonus token is drawn from
+ *     the next target row.  Same notes, section "从单个 token 接到一段 draft";
+ *     tannlonggtaoo.github.io "Speculative Decoding", section "算法".
+ *   - Policy: p and q come from logits through each side's temperature,
+ *     top-k and softmax; temperature 0 is greedy (accept iff the draft equals
+ *     the argmax, correction = argmax).  Notes section "从 LM head 到 sampling
+ *     distribution"; "Speculative Decoding" (tannlonggtaoo), section "Greedy
+ *     Sampling".
+ *   - Tree: recursive rejection over siblings (after a rejection p becomes
+ *     norm([p - q]+) and the next sibling is tested).  Notes section "Token
+ *     Tree Verifier"; zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE",
+ *     section 6.2.
+ *   - Tree mask: each node sees itself and its ancestors; position = depth.
+ *     Notes section "Token Tree Verifier: topology-aware causal mask";
+ *     jennyma11.github.io "11.3 Self-Draft", section 11.3.4 Tree Attention.
+ *
+ * Readings where the pages are silent (fixed here, identical in the tests):
+ *   greedy/argmax ties -> lowest index; top-k keeps every logit >= the k-th
+ *   largest raw logit (k <= 0 or k >= V: no filter); draws use the inverse CDF
+ *   in index order (smallest v whose running sum exceeds u * total; if
+ *   rounding leaves none, the largest v with positive weight); uniforms are
+ *   Philox4x32-10 with key (seed lo, seed hi), counter (seq, pos, draw, 0),
+ *   u = (word0 >> 8) * 2^-24; draw 0 = acceptance uniform, draw 1 = draw
+ *   uniform.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing.  Work is enqueued on `stream` and the call returns
+ *     without synchronising.
+ *   - Host-checkable problems (a NULL required pointer, a negative size, a
+ *     stride shorter than the row, a size above the limits below, a workspace
+ *     that is too small) return SPEC_ERR_INVALID_ARG before anything is
+ *     launched.  SPEC_ERR_UNSUPPORTED means the shape cannot be run by this
+ *     build (vocabulary too large for one thread-block cluster).
+ *     SPEC_ERR_CUDA reports a failed launch (cudaGetLastError).
+ *   - Data-dependent problems never trap the GPU: they set per-sequence flag
+ *     bits (SPEC_FLAG_*) and the sequence takes the defined fallback.
+ *   - Logit rows must start on 16-byte boundaries for the vectorised path;
+ *     other strides are accepted and take a scalar-load path.
+ *   - The workspace must be zero-filled once before its first use (for
+ *     example with cudaMemsetAsync); every completed call leaves it zeroed
+ *     again.  Calls that share one workspace must not overlap on the GPU.
+ *
+ * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; V >= 1 and small enough that a
+ * target+draft row pair fits in 16 thread blocks' shared memory (about
+ * 800k bf16 or 400k fp32 entries).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *spec_stream_t;
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,
+  SPEC_ERR_CUDA = 2,
+  SPEC_ERR_UNSUPPORTED = 3
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Per-sequence (or per-tree) policy arrays, device memory.
+ *   temperature [B]: 0 -> greedy; > 0 -> softmax(z / T); NaN, < 0 or inf ->
+ *                    the row is flagged SPEC_FLAG_NONFINITE.  Required.
+ *   top_k [B]:       k-th largest raw logit filter; <= 0 or >= V: off.
+ *                    May be NULL (no filtering). */
+typedef struct {
+  const float *temperature;
+  const int32_t *top_k;
+} spec_policy;
+
+/* Per-sequence flag bits (uint32). */
+#define SPEC_FLAG_BAD_TOKEN 1u           /* draft token outside [0, V): rejected there */
+#define SPEC_FLAG_ZERO_Q 2u              /* q(x) == 0 for a draft token: rejected there */
+#define SPEC_FLAG_NONFINITE 4u           /* NaN/+inf logit, no finite logit, or bad T:
+                                            the row becomes one-hot at its finite argmax
+                                            (index 0 if none) */
+#define SPEC_FLAG_DEGENERATE_RESIDUAL 8u /* sum [p - q]+ <= 0 at a rejection: the chain
+                                            draws from p; the tree keeps its current p */
+#define SPEC_FLAG_DEPTH 16u              /* a tree node deeper than max_depth */
+#define SPEC_FLAG_TIMEOUT 32u            /* a bounded on-device wait gave up */
+#define SPEC_FLAG_BAD_TREE 64u           /* parent[0] != -1 or parent[n] not in [0, n) */
+
+/* Bytes of workspace spec_verify_chain needs for B sequences of gamma drafts. */
+size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtype);
+
+/* Chain verification of B sequences with gamma drafts each.
+ *
+ * target_logits [B, gamma+1, V]: row (b, i) at target_logits + (b*(gamma+1)+i)*ld_target
+ *                                elements; rows i < gamma score draft i, row gamma is
+ *                                the bonus position.
+ * draft_logits  [B, gamma, V]:   row (b, i) at draft_logits + (b*gamma+i)*ld_draft; the
+ *                                distribution draft token i was drawn from.  Never read
+ *                                for sequences whose target temperature is 0.
+ * draft_tokens  [B, gamma] int32.
+ * uniform_override: NULL -> Philox keyed (seed, b, i, draw); else float [B, gamma+1, 2]
+ *                   in [0,1): [b,i,0] acceptance uniform of draft i, [b,i,1] draw
+ *                   uniform when position i samples (correction or bonus).
+ * Outputs (device):
+ *   out_num_accepted [B]: number of accepted drafts j (0..gamma).
+ *   out_tokens [B, gamma+1]: the j accepted drafts, then the correction (j < gamma)
+ *                            or bonus (j == gamma) token, then -1.
+ *   out_flags [B] (nullable): OR of the SPEC_FLAG_* raised on positions 0..j.
+ *   out_residual [B, V] float (nullable): the distribution the correction token was
+ *                            drawn from (norm([p_j - q_j]+), p_j on a degenerate
+ *                            residual, one-hot for greedy rows); zeros when all
+ *                            drafts were accepted.
+ */
+spec_status spec_verify_chain(
+    const void *target_logits, int64_t ld_target,
+    const void *draft_logits, int64_t ld_draft,
+    spec_dtype dtype, int B, int gamma, int V,
+    const int32_t *draft_tokens,
+    spec_policy target_policy, spec_policy draft_policy,
+    uint64_t seed, const float *uniform_override,
+    int32_t *out_num_accepted, int32_t *out_tokens,
+    uint32_t *out_flags, float *out_residual,
+    void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Bytes of workspace spec_verify_tree needs for T trees of N nodes. */
+size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype);
+
+/* Tree verification of T candidate trees of N nodes each (recursive rejection).
+ *
+ * target_logits [T, N, V]: row (t, n) = target next-token logits after the path
+ *                          root..n, at target_logits + (t*N+n)*ld_target.
+ * draft_logits  [T, N, V]: row (t, n) = the draft logits the children of n were
+ *                          drawn from (rows of leaves are never read).
+ * node_tokens [T, N], parent [T, N] int32: node 0 is the root (token ignored,
+ *                          parent -1); parent[n] < n.  Children of a node are
+ *                          tested in ascending node id.
+ * max_depth >= 0: the deepest allowed node; outputs hold max_depth+1 entries.
+ * uniform_override: NULL or float [T, N, 2]: [t,c,0] acceptance uniform of child
+ *                   c, [t,n,1] draw uniform at node n.  Philox keys: (seed, t, c, 0)
+ *                   and (seed, t, n, 1).
+ * Outputs:
+ *   out_num_accepted [T]: accepted draft nodes on the path; -1 when the tree is
+ *                          invalid (SPEC_FLAG_BAD_TREE) or too deep (SPEC_FLAG_DEPTH).
+ *   out_path [T, max_depth+1]: accepted node ids, root first, then -1.
+ *   out_tokens [T, max_depth+1]: accepted node tokens, then the final (correction
+ *                          or bonus) token, then -1.
+ *   out_flags [T] (nullable), out_residual [T, V] (nullable): the distribution the
+ *                          final token was drawn from when every child of the last
+ *                          node was rejected; zeros for a bonus draw at a leaf.
+ */
+spec_status spec_verify_tree(
+    const void *target_logits, int64_t ld_target,
+    const void *draft_logits, int64_t ld_draft,
+    spec_dtype dtype, int T, int N, int V, int max_depth,
+    const int32_t *node_tokens, const int32_t *parent,
+    spec_policy target_policy, spec_policy draft_policy,
+    uint64_t seed, const float *uniform_override,
+    int32_t *out_num_accepted, int32_t *out_path, int32_t *out_tokens,
+    uint32_t *out_flags, float *out_residual,
+    void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Ancestor-or-self masks and depth position ids for T trees of N nodes.
+ *
+ * out_mask [T, N, (N+63)/64] uint64: bit m of word m/64 of node n is set iff m == n
+ *          or m is an ancestor of n.
+ * out_position [T, N] int32: depth of n (root 0); -1 when n's parent chain hits an
+ *          invalid link before the root (the mask then holds the part reached).
+ * out_flags [T] (nullable): SPEC_FLAG_BAD_TREE, SPEC_FLAG_DEPTH (depth > max_depth).
+ */
+spec_status spec_tree_mask(const int32_t *parent, int T, int N, int max_depth,
+                           uint64_t *out_mask, int32_t *out_position,
+                           uint32_t *out_flags, spec_stream_t stream);
+
+/* Static description of a status code. */
+const char *spec_status_string(spec_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

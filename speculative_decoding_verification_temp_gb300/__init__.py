@@ -1,1 +1,24 @@
-"""GB300-native speculative-sampling verification (placeholder, binding follows)."""
+"""GB300-native speculative-sampling verification.
+
+The computation lives in libspecverify.so (CUDA for sm_103a, C ABI declared
+in include/specverify.h); ``api`` is a thin torch binding over it.
+
+  verify_chain   accept drafts with probability min(1, p/q), stop at the first
+                 rejection, draw the correction from norm([p - q]+) or a bonus
+                 token from p
+  verify_tree    recursive rejection over sibling candidates of token trees
+  tree_mask      ancestor-or-self attention masks and depth position ids
+"""
+
+from ._abi import (FLAG_BAD_TOKEN, FLAG_BAD_TREE, FLAG_DEGENERATE_RESIDUAL, FLAG_DEPTH,  # noqa: F401
+                   FLAG_NONFINITE, FLAG_TIMEOUT, FLAG_ZERO_Q)
+
+
+def __getattr__(name):
+    # the torch binding is imported on first use, so the workload generator
+    # and the build step do not need torch
+    if name in ("verify_chain", "verify_tree", "tree_mask", "SpecVerifyError", "workspace",
+                "ChainResult", "TreeResult", "MaskResult", "api"):
+        from . import api
+        return api if name == "api" else getattr(api, name)
+    raise AttributeError(name)

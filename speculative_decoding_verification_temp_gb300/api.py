@@ -1,0 +1,210 @@
+"""Thin torch binding over the C ABI: argument marshalling only.
+
+Every step of the verification runs inside libspecverify.so on the GPU; this
+module checks tensor placement and layout, allocates the outputs, and passes
+raw device pointers and torch's current CUDA stream to the C functions.
+"""
+
+import ctypes
+from collections import namedtuple
+
+import torch
+
+from . import _abi
+
+ChainResult = namedtuple("ChainResult", "num_accepted tokens flags residual")
+TreeResult = namedtuple("TreeResult", "num_accepted path tokens flags residual")
+MaskResult = namedtuple("MaskResult", "mask position flags")
+
+_DTYPES = {torch.float32: _abi.SPEC_F32, torch.bfloat16: _abi.SPEC_BF16}
+
+
+class SpecVerifyError(RuntimeError):
+    """A non-OK status returned by the C ABI."""
+
+
+def _check(code):
+    if code != _abi.SPEC_OK:
+        raise SpecVerifyError(_abi.status_string(code))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+_WORKSPACES = {}
+
+
+def workspace(device, nbytes):
+    """A zero-filled device workspace of at least nbytes, cached per device.
+
+    The library leaves a workspace zeroed after every completed call, so the
+    cached buffer can be reused by successive calls on one stream.  Calls that
+    run concurrently on different streams need workspaces of their own.
+    """
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+        _WORKSPACES[key] = ws
+    return ws
+
+
+def _rows(x, name):
+    """x viewed as rows with one uniform row stride over all leading dims."""
+    if x.dim() < 2:
+        raise ValueError(f"{name} must have a vocabulary dimension")
+    if x.stride(-1) != 1:
+        x = x.contiguous()
+    ld = x.stride(-2)
+    if ld < x.shape[-1]:
+        x = x.contiguous()
+        ld = x.shape[-1]
+    expect = ld
+    for d in range(x.dim() - 2, 0, -1):
+        expect *= x.shape[d]
+        if x.shape[d - 1] > 1 and x.stride(d - 1) != expect:
+            x = x.contiguous()
+            ld = x.shape[-1]
+            break
+    return x, ld
+
+
+def _vec(x, n, dtype, name, device):
+    t = torch.as_tensor(x, device=device)
+    if t.dim() == 0:
+        t = t.expand(n)
+    t = t.to(dtype).contiguous()
+    if t.numel() != n:
+        raise ValueError(f"{name} must hold {n} values")
+    return t
+
+
+def _cuda_tensor(x, name):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return x
+
+
+def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
+                 draft_temperature, target_top_k=None, draft_top_k=None, seed=0,
+                 uniform_override=None, return_residual=False, workspace_tensor=None):
+    """Chain speculative-sampling verification on the GPU (see spec_verify_chain).
+
+    target_logits [B, gamma+1, V] and draft_logits [B, gamma, V] (float32 or
+    bfloat16, CUDA), draft_tokens [B, gamma] integer; temperatures and top-k
+    per sequence (scalars broadcast).  Returns ChainResult with
+    num_accepted [B] int32, tokens [B, gamma+1] int32, flags [B] int32 (bit
+    pattern of the SPEC_FLAG_* values) and residual [B, V] float32 or None.
+    """
+    _cuda_tensor(target_logits, "target_logits")
+    dev = target_logits.device
+    if target_logits.dtype not in _DTYPES:
+        raise ValueError("logits must be float32 or bfloat16")
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    tl, ld_t = _rows(target_logits, "target_logits")
+    if gamma > 0:
+        _cuda_tensor(draft_logits, "draft_logits")
+        if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, gamma, V):
+            raise ValueError("draft_logits must be [B, gamma, V] with the target's dtype")
+        dl, ld_d = _rows(draft_logits, "draft_logits")
+        toks = _vec(draft_tokens, B * gamma, torch.int32, "draft_tokens", dev).view(B, gamma)
+    else:
+        dl, ld_d, toks = None, 0, None
+    tp = _vec(target_temperature, B, torch.float32, "target_temperature", dev)
+    tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
+    kp = None if target_top_k is None else _vec(target_top_k, B, torch.int32, "target_top_k", dev)
+    kq = None if draft_top_k is None else _vec(draft_top_k, B, torch.int32, "draft_top_k", dev)
+    uov = None
+    if uniform_override is not None:
+        uov = _vec(uniform_override, B * G1 * 2, torch.float32, "uniform_override", dev)
+    num = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    flags = torch.empty(B, dtype=torch.int32, device=dev)
+    resid = torch.empty((B, V), dtype=torch.float32, device=dev) if return_residual else None
+    lib = _abi.load()
+    dt = _DTYPES[target_logits.dtype]
+    nbytes = lib.spec_verify_chain_workspace_size(B, gamma, V, dt)
+    ws = workspace(dev, nbytes) if workspace_tensor is None else workspace_tensor
+    code = lib.spec_verify_chain(
+        _ptr(tl), ld_t, _ptr(dl), ld_d, dt, B, gamma, V, _ptr(toks),
+        _abi.spec_policy(tp.data_ptr(), None if kp is None else kp.data_ptr()),
+        _abi.spec_policy(tq.data_ptr(), None if kq is None else kq.data_ptr()),
+        int(seed) & ((1 << 64) - 1), _ptr(uov), _ptr(num), _ptr(out), _ptr(flags), _ptr(resid),
+        _ptr(ws), ws.numel(), _stream(dev))
+    _check(code)
+    return ChainResult(num, out, flags, resid)
+
+
+def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
+                target_temperature, draft_temperature, target_top_k=None, draft_top_k=None,
+                seed=0, uniform_override=None, return_residual=False, workspace_tensor=None):
+    """Tree verification by recursive rejection on the GPU (see spec_verify_tree).
+
+    target_logits, draft_logits [T, N, V]; node_tokens, parent [T, N].
+    Returns TreeResult with num_accepted [T], path and tokens [T, max_depth+1],
+    flags [T] and residual [T, V] or None.
+    """
+    _cuda_tensor(target_logits, "target_logits")
+    _cuda_tensor(draft_logits, "draft_logits")
+    dev = target_logits.device
+    if target_logits.dtype not in _DTYPES or draft_logits.dtype != target_logits.dtype:
+        raise ValueError("logits must both be float32 or both bfloat16")
+    T, N, V = target_logits.shape
+    if tuple(draft_logits.shape) != (T, N, V):
+        raise ValueError("draft_logits must be [T, N, V]")
+    tl, ld_t = _rows(target_logits, "target_logits")
+    dl, ld_d = _rows(draft_logits, "draft_logits")
+    toks = _vec(node_tokens, T * N, torch.int32, "node_tokens", dev)
+    par = _vec(parent, T * N, torch.int32, "parent", dev)
+    tp = _vec(target_temperature, T, torch.float32, "target_temperature", dev)
+    tq = _vec(draft_temperature, T, torch.float32, "draft_temperature", dev)
+    kp = None if target_top_k is None else _vec(target_top_k, T, torch.int32, "target_top_k", dev)
+    kq = None if draft_top_k is None else _vec(draft_top_k, T, torch.int32, "draft_top_k", dev)
+    uov = None
+    if uniform_override is not None:
+        uov = _vec(uniform_override, T * N * 2, torch.float32, "uniform_override", dev)
+    W = int(max_depth) + 1
+    num = torch.empty(T, dtype=torch.int32, device=dev)
+    path = torch.empty((T, W), dtype=torch.int32, device=dev)
+    out = torch.empty((T, W), dtype=torch.int32, device=dev)
+    flags = torch.empty(T, dtype=torch.int32, device=dev)
+    resid = torch.empty((T, V), dtype=torch.float32, device=dev) if return_residual else None
+    lib = _abi.load()
+    dt = _DTYPES[target_logits.dtype]
+    nbytes = lib.spec_verify_tree_workspace_size(T, N, V, dt)
+    ws = workspace(dev, nbytes) if workspace_tensor is None else workspace_tensor
+    code = lib.spec_verify_tree(
+        _ptr(tl), ld_t, _ptr(dl), ld_d, dt, T, N, V, int(max_depth), _ptr(toks), _ptr(par),
+        _abi.spec_policy(tp.data_ptr(), None if kp is None else kp.data_ptr()),
+        _abi.spec_policy(tq.data_ptr(), None if kq is None else kq.data_ptr()),
+        int(seed) & ((1 << 64) - 1), _ptr(uov), _ptr(num), _ptr(path), _ptr(out), _ptr(flags),
+        _ptr(resid), _ptr(ws), ws.numel(), _stream(dev))
+    _check(code)
+    return TreeResult(num, path, out, flags, resid)
+
+
+def tree_mask(parent, max_depth):
+    """Ancestor-or-self masks and depth positions (see spec_tree_mask).
+
+    parent [T, N] (CUDA).  Returns MaskResult with mask [T, N, ceil(N/64)]
+    int64 (the uint64 bit words), position [T, N] int32, flags [T] int32.
+    """
+    _cuda_tensor(parent, "parent")
+    dev = parent.device
+    T, N = parent.shape
+    par = parent.to(torch.int32).contiguous()
+    words = (N + 63) // 64
+    mask = torch.empty((T, N, words), dtype=torch.int64, device=dev)
+    pos = torch.empty((T, N), dtype=torch.int32, device=dev)
+    flags = torch.empty(T, dtype=torch.int32, device=dev)
+    code = _abi.load().spec_tree_mask(_ptr(par), T, N, int(max_depth), _ptr(mask), _ptr(pos),
+                                      _ptr(flags), _stream(dev))
+    _check(code)
+    return MaskResult(mask, pos, flags)

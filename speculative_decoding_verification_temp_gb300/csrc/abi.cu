@@ -1,0 +1,226 @@
+// C ABI of libspecverify: argument checks, workspace layout, launch planning.
+// The operations themselves are documented in include/specverify.h.
+#include <cstddef>
+#include <cstdint>
+
+#include "specverify.h"
+#include "verify_units.cuh"
+
+namespace sv {
+cudaError_t launch_units(const Params &P, int esize, bool vec, int n_units, size_t smem,
+                         cudaStream_t stream);
+cudaError_t launch_residual(const Params &P, int esize, float *out, cudaStream_t stream);
+cudaError_t launch_tree_mask(const int32_t *parent, int T, int N, int max_depth, uint64_t *mask,
+                             int32_t *position, uint32_t *flags, cudaStream_t stream);
+}  // namespace sv
+
+namespace {
+
+constexpr int kMaxGamma = 4095;
+constexpr int kMaxNodes = 4096;
+constexpr size_t kSmemTarget = 72 * 1024;  // three clusters' CTAs per SM
+constexpr size_t kSmemHard = 227 * 1024;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+  int cluster;
+  int slice;
+  size_t ctl_bytes;
+  size_t smem;
+};
+
+// Smallest cluster whose CTAs hold their slice of a target+draft row pair in
+// shared memory within the occupancy target; the largest cluster otherwise.
+bool make_plan(long long V, int esize, size_t extra, Plan &pl) {
+  pl.ctl_bytes = align_up(sizeof(sv::Ctl), 128);
+  for (int C = 1; C <= sv::kMaxCluster; C *= 2) {
+    const long long slice = static_cast<long long>(align_up(static_cast<size_t>((V + C - 1) / C), 8));
+    const size_t data = 2 * static_cast<size_t>(slice) * esize;
+    const size_t smem = pl.ctl_bytes + (data > extra ? data : extra);
+    if (smem <= kSmemTarget || (C == sv::kMaxCluster && smem <= kSmemHard)) {
+      pl.cluster = C;
+      pl.slice = static_cast<int>(slice);
+      pl.smem = smem;
+      return true;
+    }
+  }
+  return false;
+}
+
+struct Layout {
+  size_t counters, outs, stats, final_unit, total;
+};
+
+Layout layout(long long nseq, long long units) {
+  Layout L;
+  size_t off = 0;
+  L.counters = off;
+  off = align_up(off + static_cast<size_t>(nseq) * sizeof(uint32_t), 256);
+  L.outs = off;
+  off = align_up(off + static_cast<size_t>(units) * sizeof(sv::UnitOut), 256);
+  L.stats = off;
+  off = align_up(off + static_cast<size_t>(units) * sizeof(sv::UnitStats), 256);
+  L.final_unit = off;
+  off = align_up(off + static_cast<size_t>(nseq) * sizeof(int32_t), 256);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+spec_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
+
+int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0); }
+
+// Shared launch path of the chain and tree verifiers.
+spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
+                      float *out_residual, void *workspace, size_t workspace_bytes,
+                      cudaStream_t stream, bool need_draft_rows) {
+  Plan pl;
+  if (!make_plan(P.V, esize, extra, pl)) return SPEC_ERR_UNSUPPORTED;
+  const Layout L = layout(P.nseq, n_units);
+  if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
+  if (n_units * pl.cluster > 0x7FFFFFFFll) return SPEC_ERR_INVALID_ARG;
+  char *ws = static_cast<char *>(workspace);
+  P.counters = reinterpret_cast<uint32_t *>(ws + L.counters);
+  P.outs = reinterpret_cast<sv::UnitOut *>(ws + L.outs);
+  P.stats = reinterpret_cast<sv::UnitStats *>(ws + L.stats);
+  P.final_unit = reinterpret_cast<int32_t *>(ws + L.final_unit);
+  P.slice = pl.slice;
+  P.cluster = pl.cluster;
+  P.ctl_bytes = static_cast<int>(pl.ctl_bytes);
+  const bool vec = aligned16(P.target) && (P.ld_t * esize) % 16 == 0 &&
+                   (!need_draft_rows || (aligned16(P.draft) && (P.ld_d * esize) % 16 == 0));
+  cudaError_t e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
+  if (e != cudaSuccess) return map_cuda(e);
+  if (out_residual) {
+    e = sv::launch_residual(P, esize, out_residual, stream);
+    if (e != cudaSuccess) return map_cuda(e);
+  }
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *spec_status_string(spec_status status) {
+  switch (status) {
+    case SPEC_OK: return "SPEC_OK";
+    case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG: an argument failed a host-side check";
+    case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA: a CUDA launch failed";
+    case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED: shape not supported by this build";
+  }
+  return "unknown spec_status";
+}
+
+size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
+  (void)V;
+  (void)dtype;
+  if (B < 0 || gamma < 0) return 0;
+  return layout(B, static_cast<long long>(B) * (gamma + 1)).total;
+}
+
+size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
+  (void)V;
+  (void)dtype;
+  if (T < 0 || N < 0) return 0;
+  return layout(T, static_cast<long long>(T) * N).total;
+}
+
+spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,
+                              const void *draft_logits, int64_t ld_draft, spec_dtype dtype, int B,
+                              int gamma, int V, const int32_t *draft_tokens,
+                              spec_policy target_policy, spec_policy draft_policy, uint64_t seed,
+                              const float *uniform_override, int32_t *out_num_accepted,
+                              int32_t *out_tokens, uint32_t *out_flags, float *out_residual,
+                              void *workspace, size_t workspace_bytes, spec_stream_t stream) {
+  const int esize = esize_of(dtype);
+  if (esize == 0 || B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || ld_target < V || !target_policy.temperature ||
+      !draft_policy.temperature || !out_num_accepted || !out_tokens || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  if (gamma > 0 && (!draft_logits || ld_draft < V || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
+  sv::Params P = {};
+  P.target = target_logits;
+  P.ld_t = ld_target;
+  P.draft = gamma > 0 ? draft_logits : target_logits;
+  P.ld_d = gamma > 0 ? ld_draft : ld_target;
+  P.V = V;
+  P.mode = sv::kModeChain;
+  P.nseq = B;
+  P.ups = gamma + 1;
+  P.gamma = gamma;
+  P.max_depth = gamma;
+  P.tokens = draft_tokens;
+  P.parent = nullptr;
+  P.Tp = target_policy.temperature;
+  P.Tq = draft_policy.temperature;
+  P.kp = target_policy.top_k;
+  P.kq = draft_policy.top_k;
+  P.seed = seed;
+  P.uov = uniform_override;
+  P.out_num = out_num_accepted;
+  P.out_path = nullptr;
+  P.out_tokens = out_tokens;
+  P.out_flags = out_flags;
+  return run_units(P, esize, static_cast<long long>(B) * (gamma + 1), 0, out_residual, workspace,
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), gamma > 0);
+}
+
+spec_status spec_verify_tree(const void *target_logits, int64_t ld_target,
+                             const void *draft_logits, int64_t ld_draft, spec_dtype dtype, int T,
+                             int N, int V, int max_depth, const int32_t *node_tokens,
+                             const int32_t *parent, spec_policy target_policy,
+                             spec_policy draft_policy, uint64_t seed,
+                             const float *uniform_override, int32_t *out_num_accepted,
+                             int32_t *out_path, int32_t *out_tokens, uint32_t *out_flags,
+                             float *out_residual, void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream) {
+  const int esize = esize_of(dtype);
+  if (esize == 0 || T < 0 || N < 1 || N > kMaxNodes || V < 1 || max_depth < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (T == 0) return SPEC_OK;
+  if (!target_logits || ld_target < V || !draft_logits || ld_draft < V || !node_tokens ||
+      !parent || !target_policy.temperature || !draft_policy.temperature || !out_num_accepted ||
+      !out_path || !out_tokens || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  sv::Params P = {};
+  P.target = target_logits;
+  P.ld_t = ld_target;
+  P.draft = draft_logits;
+  P.ld_d = ld_draft;
+  P.V = V;
+  P.mode = sv::kModeTree;
+  P.nseq = T;
+  P.ups = N;
+  P.gamma = 0;
+  P.max_depth = max_depth;
+  P.tokens = node_tokens;
+  P.parent = parent;
+  P.Tp = target_policy.temperature;
+  P.Tq = draft_policy.temperature;
+  P.kp = target_policy.top_k;
+  P.kq = draft_policy.top_k;
+  P.seed = seed;
+  P.uov = uniform_override;
+  P.out_num = out_num_accepted;
+  P.out_path = out_path;
+  P.out_tokens = out_tokens;
+  P.out_flags = out_flags;
+  return run_units(P, esize, static_cast<long long>(T) * N, 2 * sizeof(int) * N, out_residual,
+                   workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+spec_status spec_tree_mask(const int32_t *parent, int T, int N, int max_depth, uint64_t *out_mask,
+                           int32_t *out_position, uint32_t *out_flags, spec_stream_t stream) {
+  if (T < 0 || N < 1 || N > kMaxNodes || max_depth < 0) return SPEC_ERR_INVALID_ARG;
+  if (T == 0) return SPEC_OK;
+  if (!parent || !out_mask || !out_position) return SPEC_ERR_INVALID_ARG;
+  return map_cuda(sv::launch_tree_mask(parent, T, N, max_depth, out_mask, out_position, out_flags,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

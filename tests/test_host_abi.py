@@ -1,0 +1,145 @@
+"""C-ABI library: it builds, loads, exports what include/specverify.h declares,
+and rejects bad host-side arguments before launching anything.  No GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from speculative_decoding_verification_temp_gb300 import _abi
+from speculative_decoding_verification_temp_gb300 import build as build_mod
+
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return _abi.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_abi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, 1, 2, 3):
+        assert _abi.status_string(code).startswith("SPEC_")
+    assert "unknown" in _abi.status_string(42)
+
+
+def test_workspace_sizes(lib):
+    a = lib.spec_verify_chain_workspace_size(4, 4, 32000, 0)
+    b = lib.spec_verify_chain_workspace_size(256, 7, 128256, 1)
+    assert 0 < a < b
+    assert lib.spec_verify_chain_workspace_size(-1, 4, 10, 0) == 0
+    assert lib.spec_verify_tree_workspace_size(32, 60, 128256, 1) > 0
+    assert lib.spec_verify_tree_workspace_size(1, -1, 10, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails its host checks
+
+
+def policy():
+    return _abi.spec_policy(FAKE.value, None)
+
+
+def chain(lib, B=2, gamma=3, V=100, dtype=0, target=FAKE, ld_t=None, draft=FAKE, ld_d=None,
+          tokens=FAKE, out=FAKE, ws=FAKE, ws_bytes=0, pol=None):
+    pol = pol or policy()
+    return lib.spec_verify_chain(target, ld_t if ld_t is not None else V, draft,
+                                 ld_d if ld_d is not None else V, dtype, B, gamma, V, tokens,
+                                 pol, pol, 1234, None, out, out, None, None, ws, ws_bytes, None)
+
+
+def test_chain_rejects_bad_arguments(lib):
+    INV = _abi.SPEC_ERR_INVALID_ARG
+    assert chain(lib, B=-1) == INV
+    assert chain(lib, gamma=-1) == INV
+    assert chain(lib, gamma=4096) == INV
+    assert chain(lib, V=0) == INV
+    assert chain(lib, dtype=7) == INV
+    assert chain(lib, target=None) == INV
+    assert chain(lib, draft=None) == INV
+    assert chain(lib, tokens=None) == INV
+    assert chain(lib, out=None) == INV
+    assert chain(lib, ws=None) == INV
+    assert chain(lib, ld_t=99) == INV
+    assert chain(lib, ld_d=50) == INV
+    assert chain(lib, pol=_abi.spec_policy(None, None)) == INV
+    # a workspace smaller than the query is rejected before any launch
+    need = lib.spec_verify_chain_workspace_size(2, 3, 100, 0)
+    assert chain(lib, ws_bytes=need - 1) == INV
+
+
+def test_chain_empty_batch_is_a_no_op(lib):
+    assert chain(lib, B=0, target=None, draft=None, tokens=None, out=None, ws=None) == _abi.SPEC_OK
+
+
+def test_chain_unsupported_vocabulary(lib):
+    # a float32 row pair of 10^8 entries cannot fit one cluster's shared memory
+    assert chain(lib, V=100_000_000) == _abi.SPEC_ERR_UNSUPPORTED
+
+
+def tree(lib, T=2, N=5, V=100, max_depth=3, parent=FAKE, tokens=FAKE, out=FAKE, ws_bytes=0):
+    pol = policy()
+    return lib.spec_verify_tree(FAKE, V, FAKE, V, 1, T, N, V, max_depth, tokens, parent, pol, pol,
+                                1, None, out, out, out, None, None, FAKE, ws_bytes, None)
+
+
+def test_tree_rejects_bad_arguments(lib):
+    INV = _abi.SPEC_ERR_INVALID_ARG
+    assert tree(lib, N=0) == INV
+    assert tree(lib, N=4097) == INV
+    assert tree(lib, max_depth=-1) == INV
+    assert tree(lib, T=-1) == INV
+    assert tree(lib, parent=None) == INV
+    assert tree(lib, tokens=None) == INV
+    assert tree(lib, out=None) == INV
+    assert tree(lib) == INV  # workspace too small
+    assert tree(lib, T=0, parent=None, tokens=None, out=None) == _abi.SPEC_OK
+
+
+def test_mask_rejects_bad_arguments(lib):
+    INV = _abi.SPEC_ERR_INVALID_ARG
+    m = lib.spec_tree_mask
+    assert m(FAKE, -1, 4, 2, FAKE, FAKE, None, None) == INV
+    assert m(FAKE, 1, 0, 2, FAKE, FAKE, None, None) == INV
+    assert m(FAKE, 1, 4097, 2, FAKE, FAKE, None, None) == INV
+    assert m(FAKE, 1, 4, -1, FAKE, FAKE, None, None) == INV
+    assert m(None, 1, 4, 2, FAKE, FAKE, None, None) == INV
+    assert m(FAKE, 1, 4, 2, None, FAKE, None, None) == INV
+    assert m(None, 0, 4, 2, None, None, None, None) == _abi.SPEC_OK
+
+
+def test_flag_values_match_header():
+    src = open(HEADER).read()
+    for name in ("BAD_TOKEN", "ZERO_Q", "NONFINITE", "DEGENERATE_RESIDUAL", "DEPTH", "TIMEOUT",
+                 "BAD_TREE"):
+        m = re.search(rf"#define SPEC_FLAG_{name} (\d+)u", src)
+        assert int(m.group(1)) == getattr(_abi, f"FLAG_{name}")
+
+
+def test_library_links_no_torch(lib):
+    """The library's dynamic dependencies (ELF NEEDED entries) name no torch library."""
+    import shutil
+    import subprocess
+    if shutil.which("readelf") is None:
+        pytest.skip("readelf not available")
+    out = subprocess.run(["readelf", "-d", _abi.library_path()], capture_output=True,
+                         text=True).stdout
+    needed = re.findall(r"\(NEEDED\).*\[(.*)\]", out)
+    assert needed and not any("torch" in n or "c10" in n for n in needed)
