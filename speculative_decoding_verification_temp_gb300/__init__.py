@@ -19,6 +19,7 @@ def __getattr__(name):
     # and the build step do not need torch
     if name in ("verify_chain", "verify_tree", "tree_mask", "SpecVerifyError", "workspace",
                 "ChainResult", "TreeResult", "MaskResult", "api"):
-        from . import api
+        import importlib
+        api = importlib.import_module(__name__ + ".api")
         return api if name == "api" else getattr(api, name)
     raise AttributeError(name)
