@@ -12,6 +12,9 @@ cudaError_t launch_units(const Params &P, int esize, bool vec, int n_units, size
 cudaError_t launch_residual(const Params &P, int esize, float *out, cudaStream_t stream);
 cudaError_t launch_tree_mask(const int32_t *parent, int T, int N, int max_depth, uint64_t *mask,
                              int32_t *position, uint32_t *flags, cudaStream_t stream);
+cudaError_t launch_stream(const Params &P, int esize, size_t smem, cudaStream_t stream);
+cudaError_t launch_first_child(const int32_t *parent, int T, int N, int32_t *first_child,
+                               cudaStream_t stream);
 }  // namespace sv
 
 namespace {
@@ -26,21 +29,24 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Plan {
   int cluster;
   int slice;
-  size_t ctl_bytes;
+  size_t data_off;
+  size_t hist_off;
   size_t smem;
 };
 
 // Smallest cluster whose CTAs hold their slice of a target+draft row pair in
 // shared memory within the occupancy target; the largest cluster otherwise.
-bool make_plan(long long V, int esize, size_t extra, Plan &pl) {
-  pl.ctl_bytes = align_up(sizeof(sv::Ctl), 128);
+bool make_plan(long long V, int esize, size_t extra, bool topk, Plan &pl) {
+  pl.data_off = align_up(sizeof(sv::Ctl), 128);
   for (int C = 1; C <= sv::kMaxCluster; C *= 2) {
     const long long slice = static_cast<long long>(align_up(static_cast<size_t>((V + C - 1) / C), 8));
     const size_t data = 2 * static_cast<size_t>(slice) * esize;
-    const size_t smem = pl.ctl_bytes + (data > extra ? data : extra);
+    const size_t region = align_up(data > extra ? data : extra, 128);
+    const size_t smem = pl.data_off + region + (topk ? sizeof(sv::TopkScratch) : 0);
     if (smem <= kSmemTarget || (C == sv::kMaxCluster && smem <= kSmemHard)) {
       pl.cluster = C;
       pl.slice = static_cast<int>(slice);
+      pl.hist_off = topk ? pl.data_off + region : 0;
       pl.smem = smem;
       return true;
     }
@@ -48,21 +54,72 @@ bool make_plan(long long V, int esize, size_t extra, Plan &pl) {
   return false;
 }
 
-struct Layout {
-  size_t counters, outs, stats, final_unit, total;
+// Streaming kernel: a unit's rows are cut into slices of at most 32 KB (the
+// tasks), streamed through a ring of four slots of at most 16 KB per CTA.
+struct StreamPlan {
+  int slices;
+  int slice;
+  int slot_bytes;
+  int chunks;
+  int ring;
+  size_t data_off;
+  size_t smem;
 };
+
+bool make_stream_plan(long long V, int esize, StreamPlan &sp) {
+  constexpr size_t kSlot = 16 * 1024;
+  for (int C = 1; C <= 64; C *= 2) {
+    const size_t slice = align_up(static_cast<size_t>((V + C - 1) / C), 8);
+    const size_t sb = slice * esize;
+    if (sb > 2 * kSlot) continue;
+    const size_t chunks = (sb + kSlot - 1) / kSlot;
+    const size_t slot = ((sb / 16 + chunks - 1) / chunks) * 16;
+    sp.slices = C;
+    sp.slice = static_cast<int>(slice);
+    sp.slot_bytes = static_cast<int>(slot > 16 ? slot : 16);
+    sp.chunks = static_cast<int>(chunks);
+    sp.ring = 4;  // a weight task holds both rows' chunks at once: ring >= 2 * chunks
+    if (sp.ring < 2 * sp.chunks) return false;
+    sp.data_off = align_up(sizeof(sv::Ctl3), 128);
+    sp.smem = sp.data_off + static_cast<size_t>(sp.ring) * sp.slot_bytes;
+    return true;
+  }
+  return false;
+}
+
+struct Layout {
+  size_t counters, outs, stats, final_unit, first_child, unit_done, w_done, partials, dstate,
+      wpart, wblk, wq, wq_ctr, total;
+  long long wq_cap;
+};
+
+// Slices per unit of the streaming kernel (an upper bound for the workspace).
+constexpr long long kMaxSlices = 64;
+constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
 Layout layout(long long nseq, long long units) {
   Layout L;
   size_t off = 0;
-  L.counters = off;
-  off = align_up(off + static_cast<size_t>(nseq) * sizeof(uint32_t), 256);
-  L.outs = off;
-  off = align_up(off + static_cast<size_t>(units) * sizeof(sv::UnitOut), 256);
-  L.stats = off;
-  off = align_up(off + static_cast<size_t>(units) * sizeof(sv::UnitStats), 256);
-  L.final_unit = off;
-  off = align_up(off + static_cast<size_t>(nseq) * sizeof(int32_t), 256);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.counters = take(static_cast<size_t>(nseq) * sizeof(uint32_t));
+  L.outs = take(static_cast<size_t>(units) * sizeof(sv::UnitOut));
+  L.stats = take(static_cast<size_t>(units) * sizeof(sv::UnitStats));
+  L.final_unit = take(static_cast<size_t>(nseq) * sizeof(int32_t));
+  L.first_child = take(static_cast<size_t>(units) * sizeof(int32_t));
+  L.unit_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
+  L.w_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
+  L.partials = take(static_cast<size_t>(units * kMaxSlices * 2) * sizeof(sv::SlicePartial));
+  L.dstate = take(static_cast<size_t>(units) * sizeof(sv::DrawState));
+  L.wpart = take(static_cast<size_t>(units * kMaxSlices) * sizeof(float));
+  L.wblk = take(static_cast<size_t>(units * kMaxSlices * kMaxSliceBlocks) * sizeof(float));
+  // weight-task queue: at most (children + 2) rounds of every node, one entry per slice
+  L.wq_cap = 3 * units * kMaxSlices;
+  L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
+  L.wq_ctr = take(4 * sizeof(uint32_t));
   L.total = off;
   return L;
 }
@@ -73,26 +130,63 @@ spec_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_E
 
 int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0); }
 
-// Shared launch path of the chain and tree verifiers.
+// Shared launch path of the chain and tree verifiers: the streaming kernel for
+// 16-byte aligned rows without top-k filtering, the resident kernel otherwise.
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                       float *out_residual, void *workspace, size_t workspace_bytes,
                       cudaStream_t stream, bool need_draft_rows) {
+  const bool topk = P.kp != nullptr || P.kq != nullptr;
+  const bool vec = aligned16(P.target) && (P.ld_t * esize) % 16 == 0 &&
+                   (!need_draft_rows || (aligned16(P.draft) && (P.ld_d * esize) % 16 == 0));
+  StreamPlan sp;
   Plan pl;
-  if (!make_plan(P.V, esize, extra, pl)) return SPEC_ERR_UNSUPPORTED;
+  const bool streaming = vec && !topk && make_stream_plan(P.V, esize, sp);
+  if (!streaming && !make_plan(P.V, esize, extra, topk, pl)) return SPEC_ERR_UNSUPPORTED;
   const Layout L = layout(P.nseq, n_units);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
-  if (n_units * pl.cluster > 0x7FFFFFFFll) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
   P.counters = reinterpret_cast<uint32_t *>(ws + L.counters);
   P.outs = reinterpret_cast<sv::UnitOut *>(ws + L.outs);
   P.stats = reinterpret_cast<sv::UnitStats *>(ws + L.stats);
   P.final_unit = reinterpret_cast<int32_t *>(ws + L.final_unit);
-  P.slice = pl.slice;
-  P.cluster = pl.cluster;
-  P.ctl_bytes = static_cast<int>(pl.ctl_bytes);
-  const bool vec = aligned16(P.target) && (P.ld_t * esize) % 16 == 0 &&
-                   (!need_draft_rows || (aligned16(P.draft) && (P.ld_d * esize) % 16 == 0));
-  cudaError_t e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
+  P.n_units = static_cast<int>(n_units);
+  cudaError_t e;
+  if (streaming) {
+    P.slice = sp.slice;
+    P.cluster = sp.slices;
+    P.data_off = static_cast<int>(sp.data_off);
+    P.hist_off = 0;
+    P.ring = sp.ring;
+    P.slot_bytes = sp.slot_bytes;
+    P.chunks = sp.chunks;
+    P.slice_blocks = sp.chunks * sv::kBlocksPerChunk + 1;
+    P.unit_done = reinterpret_cast<uint32_t *>(ws + L.unit_done);
+    P.w_done = reinterpret_cast<uint32_t *>(ws + L.w_done);
+    P.partials = reinterpret_cast<sv::SlicePartial *>(ws + L.partials);
+    P.dstate = reinterpret_cast<sv::DrawState *>(ws + L.dstate);
+    P.wpart = reinterpret_cast<float *>(ws + L.wpart);
+    P.wblk = reinterpret_cast<float *>(ws + L.wblk);
+    P.wq = reinterpret_cast<int4 *>(ws + L.wq);
+    P.wq_ctr = reinterpret_cast<uint32_t *>(ws + L.wq_ctr);
+    P.wq_cap = static_cast<int>(L.wq_cap);
+    static uint32_t epoch = 0;  // tags this call's queue entries (stale ones never match)
+    epoch = epoch + 1 == 0 ? 1 : epoch + 1;
+    P.epoch = epoch;
+    if (P.mode == sv::kModeTree) {
+      int32_t *fc = reinterpret_cast<int32_t *>(ws + L.first_child);
+      e = sv::launch_first_child(P.parent, P.nseq, P.ups, fc, stream);
+      if (e != cudaSuccess) return map_cuda(e);
+      P.first_child = fc;
+    }
+    e = sv::launch_stream(P, esize, sp.smem, stream);
+  } else {
+    if (n_units * pl.cluster > 0x7FFFFFFFll) return SPEC_ERR_INVALID_ARG;
+    P.slice = pl.slice;
+    P.cluster = pl.cluster;
+    P.data_off = static_cast<int>(pl.data_off);
+    P.hist_off = static_cast<int>(pl.hist_off);
+    e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
+  }
   if (e != cudaSuccess) return map_cuda(e);
   if (out_residual) {
     e = sv::launch_residual(P, esize, out_residual, stream);

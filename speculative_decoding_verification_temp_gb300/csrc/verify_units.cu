@@ -1,528 +1,48 @@
-// Fused chain/tree verification kernel and the residual-output kernel.
-// See verify_units.cuh for the design.
-#include <climits>
-
-#include "verify_units.cuh"
+// Resident verification kernel (every CTA keeps its slice of the unit's row
+// pair in shared memory for the whole unit) and the residual-output kernel.
+// Used for launches with top-k filtering or rows that are not 16-byte aligned;
+// see verify_units.cuh for the design and verify_stream.cu for the streaming
+// kernel that serves the other launches.
+#include "ops.cuh"
 
 namespace sv {
 
+// Cluster sum of the current draw weights; fills ctl.parts (per-CTA totals in
+// rank order) and returns the total.  Cluster-collective.
 template <typename TE>
-struct Elem;
-template <>
-struct Elem<float> {
-  static constexpr int kKeyRounds = 4;
-};
-template <>
-struct Elem<uint16_t> {
-  static constexpr int kKeyRounds = 2;
-};
-
-// ---------------------------------------------------------------------------
-// per-element probability and draw weight
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ float prob(const RowDesc &d, float z, int v) {
-  if (d.onehot) return v == d.a ? 1.f : 0.f;
-  return z >= d.thr ? fast_exp2(fmaf(z, d.k, d.nmk)) * d.invS : 0.f;
-}
-
-// Weight of vocabulary entry v in the distribution the node currently holds:
-// p itself, or the repeated residual [p - c q]_+ (unnormalised).
-__device__ __forceinline__ float weight(const RowDesc &dp, const RowDesc &dq, int residual,
-                                        float c, float zp, float zq, int v) {
-  const float pv = prob(dp, zp, v);
-  if (!residual) return pv;
-  return fmaxf(fmaf(-c, prob(dq, zq, v), pv), 0.f);
-}
-
-// ---------------------------------------------------------------------------
-// loading a vocabulary slice into shared memory
-// ---------------------------------------------------------------------------
-
-template <typename TE, bool kVec>
-__device__ __forceinline__ void load_slice(TE *dst, const TE *src, int len) {
-  if (kVec) {
-    constexpr int kPer = 16 / sizeof(TE);
-    const int nvec = len / kPer;
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-    int i = threadIdx.x;
-    for (; i + 3 * kThreads < nvec; i += 4 * kThreads) {
-      const uint4 a = __ldcs(s4 + i);
-      const uint4 b = __ldcs(s4 + i + kThreads);
-      const uint4 c = __ldcs(s4 + i + 2 * kThreads);
-      const uint4 d = __ldcs(s4 + i + 3 * kThreads);
-      d4[i] = a;
-      d4[i + kThreads] = b;
-      d4[i + 2 * kThreads] = c;
-      d4[i + 3 * kThreads] = d;
-    }
-    for (; i < nvec; i += kThreads) d4[i] = __ldcs(s4 + i);
-    for (int e = nvec * kPer + threadIdx.x; e < len; e += kThreads) dst[e] = src[e];
-  } else {
-    for (int e = threadIdx.x; e < len; e += kThreads) dst[e] = src[e];
-  }
-}
-
-// Eight consecutive shared-memory entries starting at `base` (a multiple of 8);
-// entries at or beyond len read as -inf.
-template <typename TE>
-__device__ __forceinline__ void load8(const TE *s, int base, int len, float z[8]);
-
-template <>
-__device__ __forceinline__ void load8<uint16_t>(const uint16_t *s, int base, int len, float z[8]) {
-  if (base + 8 <= len) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(s + base);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      z[2 * j] = __uint_as_float(ws[j] << 16);
-      z[2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) z[e] = base + e < len ? to_f32(s[base + e]) : -INFINITY;
-  }
-}
-
-template <>
-__device__ __forceinline__ void load8<float>(const float *s, int base, int len, float z[8]) {
-  if (base + 8 <= len) {
-    const float4 a = *reinterpret_cast<const float4 *>(s + base);
-    const float4 b = *reinterpret_cast<const float4 *>(s + base + 4);
-    z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
-    z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) z[e] = base + e < len ? s[base + e] : -INFINITY;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// per-CTA statistics of one slice
-// ---------------------------------------------------------------------------
-
-// Online max / sum of 2^((z - m) k) over the slice, optionally masked below
-// the top-k threshold.  NaN shows up as a NaN sum (or flag bit 0 while the
-// running max is still -inf), +inf as an infinite max.
-template <typename TE>
-__device__ void softmax_slice(const TE *s, int len, float k, float thr, bool masked, float &m,
-                              float &S, int &fl) {
-  m = -INFINITY;
-  S = 0.f;
-  fl = 0;
-  float nmk = 0.f;
-  for (int base = threadIdx.x * 8; base < len; base += kThreads * 8) {
-    float z[8];
-    load8<TE>(s, base, len, z);
-    if (masked) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (z[e] != z[e]) fl |= 1;
-        z[e] = z[e] >= thr ? z[e] : -INFINITY;
-      }
-    }
-    float vm = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
-                     fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
-    if (vm > m) {
-      S *= fast_exp2((m - vm) * k);
-      m = vm;
-      nmk = -m * k;
-    }
-    if (m == -INFINITY) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (z[e] != z[e]) fl |= 1;
-      continue;
-    }
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc += fast_exp2(fmaf(z[e], k, nmk));
-    S += acc;
-  }
-}
-
-// Argmax over the finite entries of the slice (lowest index on ties);
-// flag bit 0: NaN seen, bit 1: +inf seen.
-template <typename TE>
-__device__ void argmax_slice(const TE *s, int len, int v0, float &bv, int &bi, int &fl) {
-  bv = -INFINITY;
-  bi = INT_MAX;
-  fl = 0;
-  for (int base = threadIdx.x * 8; base < len; base += kThreads * 8) {
-    float z[8];
-    load8<TE>(s, base, len, z);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float x = z[e];
-      if (x != x) {
-        fl |= 1;
-      } else if (x == INFINITY) {
-        fl |= 2;
-      } else if (x > bv) {
-        bv = x;
-        bi = v0 + base + e;
-      }
-    }
-  }
-}
-
-// Reduce a per-thread online (m, S, flags) triple over the CTA; the result is
-// valid in every thread.
-__device__ void block_online(float &m, float &S, int &fl, float k, Ctl &ctl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-    const float S2 = __shfl_xor_sync(0xFFFFFFFFu, S, o);
-    online_merge(m, S, m2, S2, k);
-    fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
-  }
-  if (lane == 0) {
-    ctl.red_f[0][warp] = m;
-    ctl.red_f[1][warp] = S;
-    ctl.red_i[0][warp] = fl;
-  }
+__device__ float cluster_total(const RowDesc &dp, const RowDesc &dq, int residual, float c,
+                               const TE *sp, const TE *sq, int v0, int len, Ctl &ctl,
+                               cg::cluster_group &cluster, int C, int &xround) {
+  float acc = slice_total<TE>(dp, dq, residual, c, sp, sq, v0, len);
+  acc = block_sum(acc, ctl.rs);
+  const int buf = xround & 1;
+  ++xround;
+  if (threadIdx.x == 0) ctl.wx[buf][0] = acc;
+  cluster_sync_all();
+  if (threadIdx.x < C) ctl.parts[threadIdx.x] = cluster.map_shared_rank(&ctl.wx[buf][0], threadIdx.x)[0];
   __syncthreads();
-  m = -INFINITY;
-  S = 0.f;
-  fl = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    online_merge(m, S, ctl.red_f[0][w], ctl.red_f[1][w], k);
-    fl |= ctl.red_i[0][w];
-  }
-  __syncthreads();
-}
-
-__device__ void block_argmax(float &bv, int &bi, int &fl, Ctl &ctl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-    argmax_merge(bv, bi, v2, i2);
-    fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, o);
-  }
-  if (lane == 0) {
-    ctl.red_f[0][warp] = bv;
-    ctl.red_i[0][warp] = bi;
-    ctl.red_i[1][warp] = fl;
-  }
-  __syncthreads();
-  bv = -INFINITY;
-  bi = INT_MAX;
-  fl = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    argmax_merge(bv, bi, ctl.red_f[0][w], ctl.red_i[0][w]);
-    fl |= ctl.red_i[1][w];
-  }
-  __syncthreads();
-}
-
-__device__ float block_sum(float v, Ctl &ctl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum(v);
-  if (lane == 0) ctl.red_f[0][warp] = v;
-  __syncthreads();
-  float r = 0.f;
-  for (int w = 0; w < kWarps; ++w) r += ctl.red_f[0][w];
-  __syncthreads();
-  return r;
-}
-
-// ---------------------------------------------------------------------------
-// cluster-wide top-k threshold: radix select on order keys, 8 bits per round
-// ---------------------------------------------------------------------------
-
-template <typename TE>
-__device__ void topk_thresholds(const TE *sp, const TE *sq, int len, bool do_p, bool do_q,
-                                int kp, int kq, Ctl &ctl, cg::cluster_group &cluster, int C,
-                                float &thr_p, float &thr_q) {
-  constexpr int R = Elem<TE>::kKeyRounds;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 2) {
-    ctl.prefix[tid] = 0u;
-    ctl.kk[tid] = tid == 0 ? kp : kq;
-  }
-  for (int round = 0; round < R; ++round) {
-    const int buf = round & 1;
-    const int shift = (R - 1 - round) * 8;
-    for (int i = tid; i < 512; i += kThreads) (&ctl.hist[buf][0][0])[i] = 0;
-    __syncthreads();
-    const uint32_t hmask = static_cast<uint32_t>(~0ull << (shift + 8));
-#pragma unroll
-    for (int row = 0; row < 2; ++row) {
-      if (row == 0 ? !do_p : !do_q) continue;
-      const TE *s = row == 0 ? sp : sq;
-      const uint32_t want =
-          static_cast<uint32_t>(static_cast<unsigned long long>(ctl.prefix[row]) << (shift + 8));
-      for (int v = tid; v < len; v += kThreads) {
-        const uint32_t key = order_key(s[v]);
-        if ((key & hmask) == want) atomicAdd(&ctl.hist[buf][row][(key >> shift) & 255u], 1);
-      }
-    }
-    __syncthreads();
-    cluster.sync();
-    for (int i = tid; i < 512; i += kThreads) {
-      int g = 0;
-      for (int r = 0; r < C; ++r) g += cluster.map_shared_rank(&ctl.hist[buf][0][0], r)[i];
-      (&ctl.ghist[0][0])[i] = g;
-    }
-    __syncthreads();
-    if (warp < 2 && (warp == 0 ? do_p : do_q)) {
-      const int row = warp;
-      int cnt[8];
-      int s = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        cnt[j] = ctl.ghist[row][255 - 8 * lane - j];
-        s += cnt[j];
-      }
-      int incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int kk = ctl.kk[row];
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, incl >= kk);
-      const int first = __ffs(bal) - 1;
-      if (lane == first) {
-        int acc = incl - s;
-        int d = 255 - 8 * lane - 7, knew = kk - acc;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (acc + cnt[j] >= kk) {
-            d = 255 - 8 * lane - j;
-            knew = kk - acc;
-            break;
-          }
-          acc += cnt[j];
-        }
-        ctl.prefix[row] = (ctl.prefix[row] << 8) | static_cast<uint32_t>(d);
-        ctl.kk[row] = knew;
-      }
-    }
-    __syncthreads();
-  }
-  if (sizeof(TE) == 2) {
-    thr_p = key_value_bf16(ctl.prefix[0]);
-    thr_q = key_value_bf16(ctl.prefix[1]);
-  } else {
-    thr_p = key_value_f32(ctl.prefix[0]);
-    thr_q = key_value_f32(ctl.prefix[1]);
-  }
-  __syncthreads();
-}
-
-// ---------------------------------------------------------------------------
-// inverse-CDF search inside the CTA that owns the threshold
-// ---------------------------------------------------------------------------
-
-// Smallest slice entry whose running weight sum exceeds t (relative to the
-// slice start); on a rounding miss, the last entry with positive weight.
-// Returns the vocabulary index, valid in every thread.
-template <typename TE>
-__device__ int cta_search(const RowDesc &dp, const RowDesc &dq, int residual, float c,
-                          const TE *sp, const TE *sq, int v0, int len, float t, Ctl &ctl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int L = ((len + kWarps - 1) / kWarps + 255) / 256 * 256;
-  const int cs = warp * L, ce = min(len, cs + L);
-  float sum = 0.f;
-  int lastpos = -1;
-  for (int base = cs + lane * 8; base < ce; base += 256) {
-    float zp[8], zq[8];
-    load8<TE>(sp, base, len, zp);
-    if (residual) load8<TE>(sq, base, len, zq);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int v = base + e;
-      if (v < ce) {
-        const float w = weight(dp, dq, residual, c, zp[e], residual ? zq[e] : 0.f, v0 + v);
-        sum += w;
-        if (w > 0.f) lastpos = v;
-      }
-    }
-  }
-  sum = warp_sum(sum);
-  lastpos = warp_max_i(lastpos);
-  if (lane == 0) {
-    ctl.red_f[0][warp] = sum;
-    ctl.red_i[0][warp] = lastpos;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float acc = 0.f;
-    int owner = -1;
-    float trel = INFINITY;
-    for (int w = 0; w < kWarps; ++w) {
-      const float tw = ctl.red_f[0][w];
-      if (acc + tw > t) {
-        owner = w;
-        trel = t - acc;
-        break;
-      }
-      acc += tw;
-    }
-    if (owner < 0) {
-      for (int w = kWarps - 1; w >= 0; --w)
-        if (ctl.red_i[0][w] >= 0) {
-          owner = w;
-          break;
-        }
-      trel = INFINITY;
-    }
-    ctl.owner_warp = owner;
-    ctl.owner_t = trel;
-    ctl.token_local = -1;
-  }
-  __syncthreads();
-  if (warp == ctl.owner_warp) {
-    const float trel = ctl.owner_t;
-    const int ocs = warp * L, oce = min(len, ocs + L);
-    float base_sum = 0.f;
-    int result = -1;
-    for (int rb = ocs; rb < oce && result < 0; rb += 256) {
-      const int base = rb + lane * 8;
-      float zp[8], zq[8];
-      load8<TE>(sp, base, len, zp);
-      if (residual) load8<TE>(sq, base, len, zq);
-      float w[8];
-      float s = 0.f;
-      int lp = -1;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int v = base + e;
-        w[e] = v < oce ? weight(dp, dq, residual, c, zp[e], residual ? zq[e] : 0.f, v0 + v) : 0.f;
-        s += w[e];
-        if (w[e] > 0.f) lp = v;
-      }
-      float incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-      if (lane == 0) excl = 0.f;
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, base_sum + incl > trel);
-      if (hit) {
-        const int first = __ffs(hit) - 1;
-        int found = -1;
-        if (lane == first) {
-          float run = base_sum + excl;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            run += w[e];
-            if (found < 0 && w[e] > 0.f && run > trel) found = base + e;
-          }
-          if (found < 0) found = lp;
-        }
-        result = __shfl_sync(0xFFFFFFFFu, found, first);
-      }
-      base_sum += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
-    if (result < 0) result = ctl.red_i[0][warp];
-    if (lane == 0) ctl.token_local = v0 + result;
-  }
-  __syncthreads();
-  const int tok = ctl.token_local;
-  __syncthreads();
-  return tok;
+  float total = 0.f;
+  for (int r = 0; r < C; ++r) total += ctl.parts[r];
+  return total;
 }
 
 // ---------------------------------------------------------------------------
 // the unit kernel
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ const void *row_ptr(const void *base, long long row, long long ld,
-                                               int esize) {
-  return static_cast<const char *>(base) + (row * ld) * esize;
-}
-
-// Next child of `node` with id > after, or -1 (CTA-collective).
-__device__ int next_child(const Params &P, int seq, int node, int after, Ctl &ctl) {
-  if (P.mode == kModeChain) return (node < P.gamma && after < node + 1) ? node + 1 : -1;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int32_t *par = P.parent + static_cast<long long>(seq) * P.ups;
-    int found = -1;
-    for (int base = max(after, node) + 1; base < P.ups && found < 0; base += 32) {
-      const int c = base + lane;
-      const bool hit = c < P.ups && __ldg(par + c) == node;
-      const unsigned b = __ballot_sync(0xFFFFFFFFu, hit);
-      if (b) found = base + __ffs(b) - 1;
-    }
-    if (lane == 0) ctl.child = found;
-  }
-  __syncthreads();
-  const int r = ctl.child;
-  __syncthreads();
-  return r;
-}
-
-__device__ __forceinline__ int child_token(const Params &P, int seq, int node, int child) {
-  if (P.mode == kModeChain) return __ldg(P.tokens + static_cast<long long>(seq) * P.gamma + node);
-  return __ldg(P.tokens + static_cast<long long>(seq) * P.ups + child);
-}
-
-__device__ __forceinline__ float unit_uniform(const Params &P, int seq, int pos, int draw) {
-  if (P.uov) return __ldg(P.uov + (static_cast<long long>(seq) * P.ups + pos) * 2 + draw);
-  return philox_uniform(P.seed, static_cast<uint32_t>(seq), static_cast<uint32_t>(pos),
-                        static_cast<uint32_t>(draw));
-}
-
-template <typename TE>
-__device__ __forceinline__ float gather_z(const TE *row_base, int x, int slice,
-                                          cg::cluster_group &cluster) {
-  const int r = x / slice;
-  const TE *remote = cluster.map_shared_rank(row_base, r);
-  return to_f32(remote[x - r * slice]);
-}
-
-// Sum of the current draw weights over the cluster; fills ctl.parts with the
-// per-CTA totals in rank order.  Cluster-collective.
-template <typename TE>
-__device__ float cluster_total(const RowDesc &dp, const RowDesc &dq, int residual, float c,
-                               const TE *sp, const TE *sq, int v0, int len, Ctl &ctl,
-                               cg::cluster_group &cluster, int C, int &xround) {
-  float acc = 0.f;
-  for (int base = threadIdx.x * 8; base < len; base += kThreads * 8) {
-    float zp[8], zq[8];
-    load8<TE>(sp, base, len, zp);
-    if (residual) load8<TE>(sq, base, len, zq);
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (base + e < len)
-        acc += weight(dp, dq, residual, c, zp[e], residual ? zq[e] : 0.f, v0 + base + e);
-  }
-  acc = block_sum(acc, ctl);
-  const int buf = xround & 1;
-  ++xround;
-  if (threadIdx.x == 0) ctl.wx[buf][0] = acc;
-  cluster.sync();
-  float total = 0.f;
-  for (int r = 0; r < C; ++r) {
-    const float pr = cluster.map_shared_rank(&ctl.wx[buf][0], r)[0];
-    if (threadIdx.x == 0) ctl.parts[r] = pr;
-    total += pr;
-  }
-  __syncthreads();
-  return total;
-}
-
 template <typename TE, bool kVec>
 __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Ctl &ctl = *reinterpret_cast<Ctl *>(smem_raw);
-  TE *sp = reinterpret_cast<TE *>(smem_raw + P.ctl_bytes);
+  TE *sp = reinterpret_cast<TE *>(smem_raw + P.data_off);
   TE *sq = sp + P.slice;
   cg::cluster_group cluster = cg::this_cluster();
+  constexpr int PV = Elem<TE>::kPerVec;
   const int C = P.cluster;
   const int rank = static_cast<int>(cluster.block_rank());
   const int unit = blockIdx.x / C;
   const int seq = unit / P.ups, node = unit % P.ups;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = P.V;
   const int v0 = rank * P.slice;
   const int len = max(0, min(V, v0 + P.slice) - v0);
@@ -535,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
   const bool p_arg = tp_bad || Tp == 0.f;  // p decided by argmax
   const bool q_arg = tq_bad || Tq == 0.f;
 
-  int child = next_child(P, seq, node, -1, ctl);
+  int child = next_child(P, seq, node, -1, ctl.rs);
   const bool has_children = child >= 0;
   const bool load_q = has_children && !p_arg;
 
@@ -547,54 +67,166 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
     prow = static_cast<long long>(seq) * P.ups + node;
     qrow = prow;
   }
-  const TE *gp = static_cast<const TE *>(row_ptr(P.target, prow, P.ld_t, sizeof(TE))) + v0;
-  load_slice<TE, kVec>(sp, gp, len);
-  if (load_q) {
-    const TE *gq = static_cast<const TE *>(row_ptr(P.draft, qrow, P.ld_d, sizeof(TE))) + v0;
-    load_slice<TE, kVec>(sq, gq, len);
+  const TE *gp_row = static_cast<const TE *>(row_ptr(P.target, prow, P.ld_t, sizeof(TE)));
+  const TE *gq_row = static_cast<const TE *>(row_ptr(P.draft, qrow, P.ld_d, sizeof(TE)));
+  const TE *gp = gp_row + v0;
+  const TE *gq = gq_row + v0;
+
+  // ---- 1. issue the slice loads
+  const int nvec = kVec ? (len * static_cast<int>(sizeof(TE))) / 16 : 0;
+  const int nvs = (nvec + kStages - 1) / kStages;
+  if (kVec) {
+    if (tid == 0) {
+      for (int s = 0; s < kStages; ++s) mbar_init(&ctl.bar[s], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      uint64_t policy;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+      for (int s = 0; s < kStages; ++s) {
+        const int vb = min(nvec, s * nvs), ve = min(nvec, (s + 1) * nvs);
+        const uint32_t bytes = static_cast<uint32_t>(ve - vb) * 16u;
+        mbar_arrive_expect_tx(&ctl.bar[s], load_q ? 2u * bytes : bytes);
+        if (bytes) {
+          bulk_g2s(sp + vb * PV, gp + vb * PV, bytes, &ctl.bar[s], policy);
+          if (load_q) bulk_g2s(sq + vb * PV, gq + vb * PV, bytes, &ctl.bar[s], policy);
+        }
+      }
+      for (int e = nvec * PV; e < len; ++e) {
+        sp[e] = gp[e];
+        if (load_q) sq[e] = gq[e];
+      }
+    }
+  } else {
+    for (int e = tid; e < len; e += kThreads) {
+      sp[e] = gp[e];
+      if (load_q) sq[e] = gq[e];
+    }
+  }
+  // gather the first child's logits (thread 0) while the slices stream in
+  float pre_zp = 0.f, pre_zq = 0.f;
+  if (tid == 0 && has_children) {
+    const int x = child_token(P, seq, node, child);
+    if (x >= 0 && x < V) {
+      pre_zp = to_f32(gp_row[x]);
+      if (load_q) pre_zq = to_f32(gq_row[x]);
+    }
   }
   __syncthreads();
 
-  // ---- top-k thresholds
+  // ---- 2. row statistics
   const bool topk_p = !p_arg && kp_raw > 0 && kp_raw < V;
   const bool topk_q = load_q && !q_arg && kq_raw > 0 && kq_raw < V;
   float thr_p = -INFINITY, thr_q = -INFINITY;
-  if (topk_p || topk_q) {
-    float tp, tq;
-    topk_thresholds<TE>(sp, sq, len, topk_p, topk_q, kp_raw, kq_raw, ctl, cluster, C, tp, tq);
-    if (topk_p) thr_p = tp;
-    if (topk_q) thr_q = tq;
-  }
-
-  // ---- row statistics
   const float kpv = p_arg ? 0.f : kLog2e / Tp;
   const float kqv = q_arg ? 0.f : kLog2e / Tq;
+  RowAcc ap, aq;
+  acc_init(ap);
+  acc_init(aq);
+  int tflag = 0;
+  if (!(topk_p || topk_q)) {
+    for (int s = 0; s < kStages; ++s) {
+      const int vb = min(nvec, s * nvs), ve = min(nvec, (s + 1) * nvs);
+      if (kVec && !mbar_wait_bounded(&ctl.bar[s], 0)) tflag = 4;
+      if (!kVec && s > 0) break;
+      const int eb = kVec ? vb * PV : 0, ee = kVec ? ve * PV : len;
+      if (p_arg) stage_argmax<TE>(sp, eb, ee, v0, ap);
+      else if (kVec) stage_softmax(sp, vb, ve, kpv, ap);
+      else stage_softmax_masked<TE>(sp, eb, ee, kpv, -INFINITY, ap);
+      if (load_q) {
+        if (q_arg) stage_argmax<TE>(sq, eb, ee, v0, aq);
+        else if (kVec) stage_softmax(sq, vb, ve, kqv, aq);
+        else stage_softmax_masked<TE>(sq, eb, ee, kqv, -INFINITY, aq);
+      }
+    }
+    if (kVec && tid == 0) {  // the ragged tail that the bulk copies did not cover
+      for (int e = nvec * PV; e < len; ++e) {
+        if (p_arg) acc_scalar_argmax(ap, to_f32(sp[e]), v0 + e);
+        else acc_scalar_softmax(ap, to_f32(sp[e]), kpv);
+        if (load_q) {
+          if (q_arg) acc_scalar_argmax(aq, to_f32(sq[e]), v0 + e);
+          else acc_scalar_softmax(aq, to_f32(sq[e]), kqv);
+        }
+      }
+    }
+  } else {
+    if (kVec)
+      for (int s = 0; s < kStages; ++s)
+        if (!mbar_wait_bounded(&ctl.bar[s], 0)) tflag = 4;
+    __syncthreads();
+    float tp, tq;
+    TopkScratch &tk = *reinterpret_cast<TopkScratch *>(smem_raw + P.hist_off);
+    topk_thresholds<TE>(sp, sq, len, topk_p, topk_q, kp_raw, kq_raw, ctl, tk, cluster, C, tp, tq);
+    if (topk_p) thr_p = tp;
+    if (topk_q) thr_q = tq;
+    if (p_arg) stage_argmax<TE>(sp, 0, len, v0, ap);
+    else stage_softmax_masked<TE>(sp, 0, len, kpv, thr_p, ap);
+    if (load_q) {
+      if (q_arg) stage_argmax<TE>(sq, 0, len, v0, aq);
+      else stage_softmax_masked<TE>(sq, 0, len, kqv, thr_q, aq);
+    }
+  }
+  ap.fl |= tflag;
+  aq.fl |= tflag;
+
+  // CTA partials
 #pragma unroll
   for (int row = 0; row < 2; ++row) {
     if (row == 1 && !load_q) break;
-    const TE *s = row == 0 ? sp : sq;
+    RowAcc &a = row == 0 ? ap : aq;
     const bool arg = row == 0 ? p_arg : q_arg;
     Partial pt;
     if (arg) {
-      argmax_slice<TE>(s, len, v0, pt.av, pt.ai, pt.flags);
-      block_argmax(pt.av, pt.ai, pt.flags, ctl);
+      block_argmax(a.bv, a.bi, a.fl, ctl.rs);
       pt.m = 0.f;
       pt.S = 0.f;
+      pt.av = a.bv;
+      pt.ai = a.bi;
     } else {
-      const float kk = row == 0 ? kpv : kqv;
-      const float thr = row == 0 ? thr_p : thr_q;
-      const bool masked = row == 0 ? topk_p : topk_q;
-      softmax_slice<TE>(s, len, kk, thr, masked, pt.m, pt.S, pt.flags);
-      block_online(pt.m, pt.S, pt.flags, kk, ctl);
+      block_online(a.m, a.S, a.fl, row == 0 ? kpv : kqv, ctl.rs);
+      pt.m = a.m;
+      pt.S = a.S;
       pt.av = 0.f;
       pt.ai = 0;
     }
+    pt.flags = a.fl;
     if (tid == 0) ctl.part[row] = pt;
   }
-  cluster.sync();
+  cluster_sync_all();
+  // merge across the cluster (warp 0, lane r reads rank r)
+  if (warp == 0) {
+#pragma unroll
+    for (int row = 0; row < 2; ++row) {
+      if (row == 1 && !load_q) break;
+      const bool arg = row == 0 ? p_arg : q_arg;
+      const float kk = row == 0 ? kpv : kqv;
+      Partial o;
+      if (lane < C) {
+        o = cluster.map_shared_rank(&ctl.part[row], lane)[0];
+      } else {
+        o.m = -INFINITY;
+        o.S = 0.f;
+        o.av = -INFINITY;
+        o.ai = INT_MAX;
+        o.flags = 0;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, o.m, off);
+        const float S2 = __shfl_xor_sync(0xFFFFFFFFu, o.S, off);
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, o.av, off);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, o.ai, off);
+        o.flags |= __shfl_xor_sync(0xFFFFFFFFu, o.flags, off);
+        if (arg) argmax_merge(o.av, o.ai, v2, i2);
+        else online_merge(o.m, o.S, m2, S2, kk);
+      }
+      if (lane == 0) ctl.merged[row] = o;
+    }
+  }
+  __syncthreads();
 
   RowDesc dp, dq;
   bool need_fallback[2] = {false, false};
+  uint32_t tmo = 0u;
 #pragma unroll
   for (int row = 0; row < 2; ++row) {
     RowDesc d;
@@ -611,28 +243,17 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       dq = d;
       break;
     }
+    const Partial o = ctl.merged[row];
+    if (o.flags & 4) tmo = SPEC_FLAG_TIMEOUT;
     if (arg) {
-      float bv = -INFINITY;
-      int bi = INT_MAX, fl = 0;
-      for (int r = 0; r < C; ++r) {
-        const Partial o = cluster.map_shared_rank(&ctl.part[row], r)[0];
-        argmax_merge(bv, bi, o.av, o.ai);
-        fl |= o.flags;
-      }
       d.onehot = 1;
-      d.a = bi == INT_MAX ? 0 : bi;
+      d.a = o.ai == INT_MAX ? 0 : o.ai;
       d.k = d.nmk = d.invS = 0.f;
-      if (tbad || fl || bi == INT_MAX) d.flags = SPEC_FLAG_NONFINITE;
+      if (tbad || (o.flags & 3) || o.ai == INT_MAX) d.flags = SPEC_FLAG_NONFINITE;
     } else {
-      float M = -INFINITY, S = 0.f;
-      int fl = 0;
-      for (int r = 0; r < C; ++r) {
-        const Partial o = cluster.map_shared_rank(&ctl.part[row], r)[0];
-        online_merge(M, S, o.m, o.S, kk);
-        fl |= o.flags;
-      }
-      const bool bad = fl || !(M > -INFINITY) || M == INFINITY || !(S > 0.f) || S == INFINITY ||
-                       S != S;
+      const float M = o.m, S = o.S;
+      const bool bad = (o.flags & 3) || !(M > -INFINITY) || M == INFINITY || !(S > 0.f) ||
+                       S == INFINITY || S != S;
       d.onehot = 0;
       d.a = 0;
       d.k = kk;
@@ -647,17 +268,23 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
     if (row == 0) dp = d; else dq = d;
   }
 
-  // ---- finite-argmax fallback for non-finite sampling rows (rare)
+  // finite-argmax fallback for non-finite sampling rows (rare)
   if (need_fallback[0] || need_fallback[1]) {
 #pragma unroll
     for (int row = 0; row < 2; ++row) {
       if (!need_fallback[row]) continue;
+      RowAcc a;
+      acc_init(a);
+      stage_argmax<TE>(row == 0 ? sp : sq, 0, len, v0, a);
+      block_argmax(a.bv, a.bi, a.fl, ctl.rs);
       Partial pt;
-      argmax_slice<TE>(row == 0 ? sp : sq, len, v0, pt.av, pt.ai, pt.flags);
-      block_argmax(pt.av, pt.ai, pt.flags, ctl);
+      pt.m = pt.S = 0.f;
+      pt.av = a.bv;
+      pt.ai = a.bi;
+      pt.flags = 0;
       if (tid == 0) ctl.amax[row] = pt;
     }
-    cluster.sync();
+    cluster_sync_all();
 #pragma unroll
     for (int row = 0; row < 2; ++row) {
       if (!need_fallback[row]) continue;
@@ -672,8 +299,8 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
     }
   }
 
-  // ---- local walk over the children
-  uint32_t uflags = dp.flags;
+  // ---- 3. local walk over the children
+  uint32_t uflags = dp.flags | tmo;
   int next = -1, token = -1;
   int residual = 0;
   float c = 0.f, Wcur = 0.f;
@@ -681,8 +308,9 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
   int xround = 0;
   int kind = 0;
   float total = 0.f;
+  bool draw = false;
   if (dp.onehot) {
-    for (; child >= 0; child = next_child(P, seq, node, child, ctl)) {
+    for (; child >= 0; child = next_child(P, seq, node, child, ctl.rs)) {
       const int x = child_token(P, seq, node, child);
       if (x < 0 || x >= V) uflags |= SPEC_FLAG_BAD_TOKEN;
       if (x == dp.a) {
@@ -695,27 +323,43 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       kind = has_children ? 1 : 0;
     }
   } else {
-    if (child >= 0) uflags |= dq.flags;
-    for (; child >= 0; child = next_child(P, seq, node, child, ctl)) {
-      const int x = child_token(P, seq, node, child);
-      const int keypos = P.mode == kModeChain ? node : child;
-      const float u = unit_uniform(P, seq, keypos, 0);
-      bool acc = false;
-      if (x < 0 || x >= V) {
-        uflags |= SPEC_FLAG_BAD_TOKEN;
-      } else {
-        const float zpx = gather_z<TE>(sp, x, P.slice, cluster);
-        const float zqx = dq.onehot ? 0.f : gather_z<TE>(sq, x, P.slice, cluster);
-        const float qx = prob(dq, zqx, x);
-        if (!(qx > 0.f)) {
-          uflags |= SPEC_FLAG_ZERO_Q;
+    if (has_children) uflags |= dq.flags;
+    bool first = true;
+    for (; child >= 0; child = next_child(P, seq, node, child, ctl.rs)) {
+      if (tid == 0) {
+        const int x = child_token(P, seq, node, child);
+        const int keypos = P.mode == kModeChain ? node : child;
+        const float u = unit_uniform(P, seq, keypos, 0);
+        int verdict = 0;  // 0 reject, 1 accept, 2 bad token, 3 zero q
+        if (x < 0 || x >= V) {
+          verdict = 2;
         } else {
-          const float px = residual ? weight(dp, dq, 1, c, zpx, zqx, x) / Wcur : prob(dp, zpx, x);
-          const float alpha = fminf(1.f, px / qx);
-          acc = u < alpha;
+          float zpx, zqx;
+          if (first) {
+            zpx = pre_zp;
+            zqx = pre_zq;
+          } else {
+            zpx = to_f32(gp_row[x]);
+            zqx = dq.onehot ? 0.f : to_f32(gq_row[x]);
+          }
+          const float qx = prob(dq, zqx, x);
+          if (!(qx > 0.f)) {
+            verdict = 3;
+          } else {
+            const float px =
+                residual ? weight(dp, dq, 1, c, zpx, zqx, x) / Wcur : prob(dp, zpx, x);
+            verdict = u < fminf(1.f, px / qx) ? 1 : 0;
+          }
         }
+        ctl.decision = verdict;
       }
-      if (acc) {
+      __syncthreads();
+      const int verdict = ctl.decision;
+      __syncthreads();
+      first = false;
+      if (verdict == 2) uflags |= SPEC_FLAG_BAD_TOKEN;
+      if (verdict == 3) uflags |= SPEC_FLAG_ZERO_Q;
+      if (verdict == 1) {
         next = child;
         break;
       }
@@ -732,7 +376,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       }
     }
     if (next < 0) {
-      // ---- inverse-CDF draw over the cluster
+      // ---- 4. inverse-CDF draw over the cluster: choose the owning CTA
       float Z;
       if (have_parts) {
         Z = Wcur;
@@ -740,41 +384,50 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
         Z = cluster_total<TE>(dp, dq, residual, residual ? c : 0.f, sp, sq, v0, len, ctl,
                               cluster, C, xround);
       }
-      const float u = unit_uniform(P, seq, node, 1);
-      const float t = u * Z;
-      int owner = -1;
-      float acc = 0.f, trel = INFINITY;
-      for (int r = 0; r < C; ++r) {
-        const float pr = ctl.parts[r];
-        if (acc + pr > t) {
-          owner = r;
-          trel = t - acc;
-          break;
-        }
-        acc += pr;
-      }
-      if (owner < 0) {
-        for (int r = C - 1; r >= 0; --r)
-          if (ctl.parts[r] > 0.f) {
+      if (tid == 0) {
+        const float u = unit_uniform(P, seq, node, 1);
+        const float t = u * Z;
+        int owner = -1;
+        float acc = 0.f, trel = INFINITY;
+        for (int r = 0; r < C; ++r) {
+          const float pr = ctl.parts[r];
+          if (acc + pr > t) {
             owner = r;
+            trel = t - acc;
             break;
           }
-        trel = INFINITY;
+          acc += pr;
+        }
+        if (owner < 0) {
+          for (int r = C - 1; r >= 0; --r)
+            if (ctl.parts[r] > 0.f) {
+              owner = r;
+              break;
+            }
+          trel = INFINITY;
+        }
+        ctl.owner = owner;
+        ctl.trel = trel;
       }
-      if (rank == owner) {
-        const int tok = cta_search<TE>(dp, dq, residual, c, sp, sq, v0, len, trel, ctl);
-        if (tid == 0) cluster.map_shared_rank(&ctl.token, 0)[0] = tok;
-      }
+      __syncthreads();
+      draw = true;
       kind = has_children ? 2 : 0;
       total = Z;
     }
   }
-  cluster.sync();
+  // A bounded wait that gave up may leave a copy in flight: wait again (also
+  // bounded) before this CTA can leave.
+  if (kVec && tflag)
+    for (int s = 0; s < kStages; ++s) mbar_wait_bounded(&ctl.bar[s], 0);
+  // Every DSMEM read of this unit is done: release the cluster; the publishing
+  // CTA carries on while the others leave.
+  cluster_arrive();
+  const int owner = draw ? ctl.owner : 0;
+  if (rank == owner) {
+    if (draw) token = cta_search<TE>(dp, dq, residual, c, sp, sq, v0, len, ctl.trel, ctl);
 
-  // ---- publish this unit's outcome; the last unit of the sequence stitches
-  if (rank == 0) {
+    // ---- 5. publish this unit's outcome; the last unit of the sequence stitches
     if (tid == 0) {
-      if (next < 0 && !dp.onehot) token = ctl.token;
       UnitOut o;
       o.next = next;
       o.token = token;
@@ -799,7 +452,6 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       const long long ubase = static_cast<long long>(seq) * P.ups;
       if (P.mode == kModeChain) {
         if (tid < 32) {
-          const int lane = tid;
           int j = -1;
           for (int base = 0; base <= P.gamma && j < 0; base += 32) {
             const int i = base + lane;
@@ -829,7 +481,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
         // validate the tree: links, then depth by pointer jumping
         const int N = P.ups;
         const int32_t *par = P.parent + ubase;
-        int *anc = reinterpret_cast<int *>(smem_raw + P.ctl_bytes);
+        int *anc = reinterpret_cast<int *>(smem_raw + P.data_off);
         int *dep = anc + N;
         uint32_t bad = 0u;
         for (int n = tid; n < N; n += kThreads) {
@@ -839,10 +491,10 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
           dep[n] = n == 0 ? 0 : 1;
         }
         bad = warp_or(bad);
-        if ((tid & 31) == 0) ctl.red_u[tid >> 5] = bad;
+        if (lane == 0) ctl.rs.red_u[warp] = bad;
         __syncthreads();
         bad = 0u;
-        for (int w = 0; w < kWarps; ++w) bad |= ctl.red_u[w];
+        for (int w = 0; w < kWarps; ++w) bad |= ctl.rs.red_u[w];
         __syncthreads();
         uint32_t tflags = bad ? SPEC_FLAG_BAD_TREE : 0u;
         if (!bad) {
@@ -866,10 +518,10 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
           for (int n = tid; n < N; n += kThreads)
             if (dep[n] > P.max_depth) deep = 1u;
           deep = warp_or(deep);
-          if ((tid & 31) == 0) ctl.red_u[tid >> 5] = deep;
+          if (lane == 0) ctl.rs.red_u[warp] = deep;
           __syncthreads();
           deep = 0u;
-          for (int w = 0; w < kWarps; ++w) deep |= ctl.red_u[w];
+          for (int w = 0; w < kWarps; ++w) deep |= ctl.rs.red_u[w];
           __syncthreads();
           if (deep) tflags = SPEC_FLAG_DEPTH;
         }
@@ -911,6 +563,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       }
     }
   }
+  cluster_wait();
 }
 
 // ---------------------------------------------------------------------------

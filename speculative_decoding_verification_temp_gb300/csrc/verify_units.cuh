@@ -15,19 +15,24 @@
 // (top-k selection, residual sums, the inverse-CDF draw).
 //
 // Steps inside a unit (all CTAs of the cluster run the same control flow):
-//   1. load this CTA's vocabulary slice of p_n (and q_n if it has children
-//      and p_n is not one-hot) into shared memory with 128-bit loads;
-//   2. top-k threshold by a cluster-wide radix select over shared memory;
-//   3. one pass of online max / sum of 2^((z - m) log2(e) / T) per row
-//      (argmax for temperature 0), merged across the cluster through DSMEM;
-//   4. the local walk: each child in ascending id gets u < min(1, p(x)/q(x));
-//      on rejection p becomes norm([p - c q]_+) with c_1 = 1,
-//      c_{s+1} = c_s + W_s (the closed form of repeated residuals), whose sum
-//      W is reduced over the cluster;
-//   5. when no child is accepted: inverse-CDF draw over the cluster: per-CTA
+//   1. thread 0 issues bulk asynchronous copies (TMA, cp.async.bulk) of this
+//      CTA's vocabulary slice of p_n (and of q_n when the node has children
+//      and p_n is not one-hot) in four stages, each completing on its own
+//      mbarrier, so the whole slice is in flight at once;
+//   2. as each stage lands, every thread folds its part into a running
+//      max / sum of 2^((z - m) log2(e) / T) (argmax for temperature 0); the
+//      per-CTA partials are merged across the cluster through DSMEM;
+//      (rows with top-k first wait for the whole slice and run a cluster-wide
+//      radix select for the k-th largest logit);
+//   3. the local walk: each child in ascending id is accepted iff
+//      u < min(1, p(x)/q(x)), with z(x) read from global memory; on rejection
+//      p becomes norm([p - c q]_+) with c_1 = 1, c_{s+1} = c_s + W_s (the
+//      closed form of repeated residuals), W reduced over the cluster;
+//   4. when no child is accepted: inverse-CDF draw over the cluster: per-CTA
 //      totals pick the CTA, per-warp totals the warp, a warp scan the lane;
-//   6. the last unit of a sequence stitches the path (warp ballot on the
-//      first rejection for chains, a walk from the root for trees).
+//   5. one CTA publishes the unit's outcome; the last unit of a sequence to
+//      publish stitches the path (warp ballot on the first rejection for
+//      chains, a walk from the root for trees).
 #pragma once
 
 #include "common.cuh"
@@ -35,6 +40,7 @@
 namespace sv {
 
 enum { kModeChain = 0, kModeTree = 1 };
+constexpr int kStages = 4;
 
 // Distribution of one row after its policy.
 struct RowDesc {
@@ -93,34 +99,121 @@ struct Params {
   int32_t *final_unit;
   int slice;      // vocabulary entries per CTA (multiple of 8)
   int cluster;    // CTAs per cluster
-  int ctl_bytes;  // offset of the data slices in dynamic shared memory
+  int data_off;   // byte offset of the data slices in dynamic shared memory
+  int hist_off;   // byte offset of the top-k histograms (0: no top-k in this launch)
+  // streaming (persistent) kernel only
+  const int32_t *first_child;  // [T*N] first child of each tree node, -1 for leaves
+  int n_units;
+  int ring;                       // ring slots per CTA
+  int slot_bytes;                 // bytes per ring slot
+  int chunks;                     // ring chunks per row slice
+  int slice_blocks;               // draw blocks per slice (chunks * 16 + 1)
+  struct SlicePartial *partials;  // [n_units][slices][2]
+  struct DrawState *dstate;       // [n_units]
+  float *wpart;                   // [n_units][slices] slice totals of the round
+  float *wblk;                    // [n_units][slices][slice_blocks] block totals
+  uint32_t *unit_done;            // [n_units] stats slices finished
+  uint32_t *w_done;               // [n_units] weight slices finished in the round
+  int4 *wq;                       // weight-task queue: (unit, slice, round, epoch)
+  uint32_t *wq_ctr;               // [0] head, [1] tail, [2] units completed
+  uint32_t epoch;                 // tags this call's queue entries
+  int wq_cap;
 };
+
+
 
 struct __align__(16) Partial {
   float m, S, av;
   int ai;
-  int flags;  // bit 0: NaN seen, bit 1: +inf seen
+  int flags;  // bit 0: NaN seen, bit 1: +inf seen, bit 2: bounded wait timed out
   int pad[3];
 };
 
-struct __align__(16) Ctl {
-  Partial part[2];
-  Partial amax[2];
-  float wx[2][4];
+// Scratch of the CTA-wide reductions and of the child scan.
+struct RedScratch {
+  float red_f[2][kWarps];
+  int red_i[2][kWarps];
+  uint32_t red_u[kWarps];
+  int child;
+};
+
+struct TopkScratch {
   int hist[2][2][256];
   int ghist[2][256];
+};
+
+struct __align__(16) Ctl {
+  unsigned long long bar[kStages];
+  Partial part[2];
+  Partial amax[2];
+  Partial merged[2];
+  float wx[2][4];
+  float parts[kMaxCluster];
   uint32_t prefix[2];
   int kk[2];
-  int child;
-  int token;      // written by the owner CTA of a draw into rank 0
   int token_local;
   int owner_warp;
   float owner_t;
   int is_last;
-  float parts[kMaxCluster];
-  float red_f[2][kWarps];
-  int red_i[2][kWarps];
-  uint32_t red_u[kWarps];
+  int decision;  // broadcast of thread 0's per-child verdict
+  int owner;
+  float trel;
+  RedScratch rs;
+};
+
+// ---------------------------------------------------------------------------
+// streaming kernel state
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxRing = 8;
+constexpr int kBlocksPerChunk = 16;  // draw-weight blocks per ring chunk (search granularity)
+constexpr int kMaxSliceBlocks = 2 * kBlocksPerChunk + 1;  // two chunks and the ragged tail
+
+enum { kTaskStats = 0, kTaskWeights = 1, kTaskEnd = 2 };
+
+// One CTA's statistics of its slice of one row, published for the unit's
+// deciding CTA.
+struct __align__(16) SlicePartial {
+  float m, S, av;
+  int ai;
+  int flags;  // bit 0: NaN seen, bit 1: +inf seen, bit 2: bounded wait timed out
+  int pad[3];
+};
+
+// A unit's draw state between weight rounds (workspace, one per unit).
+struct __align__(16) DrawState {
+  RowDesc dp, dq;
+  float c;       // multiplier of the round in flight (0: the weights are p itself)
+  float c_cur;   // multiplier of the distribution the node holds (0: p)
+  float W_cur;   // its total (valid when c_cur > 0)
+  int child;     // the last child tested
+  uint32_t flags;
+  int round;
+  int blocks_c_valid;  // 1 when the stored block totals belong to the held distribution
+  int pad;
+};
+
+// What the producer warp tells the compute threads about a task.
+struct __align__(16) TaskInfo {
+  int type, unit, slice, round;
+  int bits;  // stats: 1 p_arg, 2 q_arg, 4 tp_bad, 8 tq_bad, 16 load_q, 32 has_children
+  float kp, kq;
+  float c;   // weights: round multiplier
+  RowDesc dp, dq;
+};
+
+struct __align__(16) Ctl3 {
+  unsigned long long full[kMaxRing];
+  unsigned long long empty[kMaxRing];
+  TaskInfo tinfo[kMaxRing];
+  float btot[kMaxSliceBlocks + 15];
+  Partial merged[2];
+  DrawState ds_share;  // draw state handed from thread 0 to warp 0
+  int decision;
+  int is_last;
+  int token;
+  float trel;
+  RedScratch rs;
 };
 
 }  // namespace sv
