@@ -47,9 +47,10 @@
  *     bits (SPEC_FLAG_*) and the sequence takes the defined fallback.
  *   - Logit rows must start on 16-byte boundaries for the vectorised path;
  *     other strides are accepted and take a scalar-load path.
- *   - The workspace must be zero-filled once before its first use (for
- *     example with cudaMemsetAsync); every completed call leaves it zeroed
- *     again.  Calls that share one workspace must not overlap on the GPU.
+ *   - The workspace needs no initialisation: each call first clears, with
+ *     one cudaMemsetAsync on `stream`, the part of it that must start at zero
+ *     (arrival counters and the weight-task queue).  Calls that share one
+ *     workspace must not overlap on the GPU.
  *
  * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; V >= 1 and small enough that a
  * target+draft row pair fits in 16 thread blocks' shared memory (about
@@ -99,7 +100,8 @@ typedef struct {
 #define SPEC_FLAG_TIMEOUT 32u            /* a bounded on-device wait gave up */
 #define SPEC_FLAG_BAD_TREE 64u           /* parent[0] != -1 or parent[n] not in [0, n) */
 
-/* Bytes of workspace spec_verify_chain needs for B sequences of gamma drafts. */
+/* Bytes of workspace spec_verify_chain needs for B sequences of gamma drafts
+ * (0 for a negative size, V < 1 or an unknown dtype). */
 size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtype);
 
 /* Chain verification of B sequences with gamma drafts each.
@@ -135,7 +137,7 @@ spec_status spec_verify_chain(
     uint32_t *out_flags, float *out_residual,
     void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
-/* Bytes of workspace spec_verify_tree needs for T trees of N nodes. */
+/* Bytes of workspace spec_verify_tree needs for T trees of N nodes (0 as above). */
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype);
 
 /* Tree verification of T candidate trees of N nodes each (recursive rejection).

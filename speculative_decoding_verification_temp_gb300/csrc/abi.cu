@@ -87,17 +87,21 @@ bool make_stream_plan(long long V, int esize, StreamPlan &sp) {
   return false;
 }
 
+// Workspace layout.  The regions that must read zero when the kernels start
+// (arrival counters, the weight-task queue and its counters) come first and
+// are cleared by every call; everything after them is written before it is
+// read within a call.
 struct Layout {
-  size_t counters, outs, stats, final_unit, first_child, unit_done, w_done, partials, dstate,
-      wpart, wblk, wq, wq_ctr, total;
+  size_t wq_ctr, counters, unit_done, w_done, wq, zero_bytes;
+  size_t outs, stats, final_unit, first_child, partials, dstate, wpart, wblk, total;
   long long wq_cap;
 };
 
-// Slices per unit of the streaming kernel (an upper bound for the workspace).
-constexpr long long kMaxSlices = 64;
 constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
-Layout layout(long long nseq, long long units) {
+// slices: slices per unit of the streaming kernel, 0 when only the resident
+// kernel can run the shape.
+Layout layout(long long nseq, long long units, long long slices) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -105,23 +109,32 @@ Layout layout(long long nseq, long long units) {
     off = align_up(off + bytes, 256);
     return at;
   };
+  L.wq_ctr = take(4 * sizeof(uint32_t));
   L.counters = take(static_cast<size_t>(nseq) * sizeof(uint32_t));
+  L.unit_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
+  L.w_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
+  // weight-task queue: a tree of N nodes runs at most (N - 1) + 2N weight
+  // rounds in all (one per rejected child, plus a degenerate fallback and the
+  // final draw at each node), one entry per slice
+  L.wq_cap = 3 * units * slices;
+  L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
+  L.zero_bytes = off;
   L.outs = take(static_cast<size_t>(units) * sizeof(sv::UnitOut));
   L.stats = take(static_cast<size_t>(units) * sizeof(sv::UnitStats));
   L.final_unit = take(static_cast<size_t>(nseq) * sizeof(int32_t));
   L.first_child = take(static_cast<size_t>(units) * sizeof(int32_t));
-  L.unit_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
-  L.w_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
-  L.partials = take(static_cast<size_t>(units * kMaxSlices * 2) * sizeof(sv::SlicePartial));
-  L.dstate = take(static_cast<size_t>(units) * sizeof(sv::DrawState));
-  L.wpart = take(static_cast<size_t>(units * kMaxSlices) * sizeof(float));
-  L.wblk = take(static_cast<size_t>(units * kMaxSlices * kMaxSliceBlocks) * sizeof(float));
-  // weight-task queue: at most (children + 2) rounds of every node, one entry per slice
-  L.wq_cap = 3 * units * kMaxSlices;
-  L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
-  L.wq_ctr = take(4 * sizeof(uint32_t));
+  L.partials = take(static_cast<size_t>(units * slices * 2) * sizeof(sv::SlicePartial));
+  L.dstate = take(static_cast<size_t>(slices ? units : 0) * sizeof(sv::DrawState));
+  L.wpart = take(static_cast<size_t>(units * slices) * sizeof(float));
+  L.wblk = take(static_cast<size_t>(units * slices * kMaxSliceBlocks) * sizeof(float));
   L.total = off;
   return L;
+}
+
+// Slices of the streaming plan for rows of V entries (0: no streaming plan).
+long long stream_slices(long long V, int esize) {
+  StreamPlan sp;
+  return esize > 0 && make_stream_plan(V, esize, sp) ? sp.slices : 0;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -142,15 +155,16 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   Plan pl;
   const bool streaming = vec && !topk && make_stream_plan(P.V, esize, sp);
   if (!streaming && !make_plan(P.V, esize, extra, topk, pl)) return SPEC_ERR_UNSUPPORTED;
-  const Layout L = layout(P.nseq, n_units);
+  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, stream);
+  if (e != cudaSuccess) return map_cuda(e);
   P.counters = reinterpret_cast<uint32_t *>(ws + L.counters);
   P.outs = reinterpret_cast<sv::UnitOut *>(ws + L.outs);
   P.stats = reinterpret_cast<sv::UnitStats *>(ws + L.stats);
   P.final_unit = reinterpret_cast<int32_t *>(ws + L.final_unit);
   P.n_units = static_cast<int>(n_units);
-  cudaError_t e;
   if (streaming) {
     P.slice = sp.slice;
     P.cluster = sp.slices;
@@ -210,17 +224,15 @@ const char *spec_status_string(spec_status status) {
 }
 
 size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
-  (void)V;
-  (void)dtype;
-  if (B < 0 || gamma < 0) return 0;
-  return layout(B, static_cast<long long>(B) * (gamma + 1)).total;
+  const int esize = esize_of(dtype);
+  if (B < 0 || gamma < 0 || V < 1 || esize == 0) return 0;
+  return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize)).total;
 }
 
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
-  (void)V;
-  (void)dtype;
-  if (T < 0 || N < 0) return 0;
-  return layout(T, static_cast<long long>(T) * N).total;
+  const int esize = esize_of(dtype);
+  if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize)).total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

@@ -54,6 +54,8 @@ def pytest_sessionfinish(session, exitstatus):
     if _LOG.rows:
         n = len(_LOG.entries)
         print(f"\n[parity] rows checked {_LOG.rows}, excused disagreements {n}")
+        for where, margin in _LOG.entries:
+            print(f"[parity] excused: {where}: margin {margin:.3e}")
         if n > 1e-5 * _LOG.rows:
             print("[parity] FAIL: excused disagreements exceed 1e-5 of rows")
             session.exitstatus = 1

@@ -18,12 +18,25 @@ MARGIN = 1e-5
 RESID_TOL = {"f32": 1e-5, "bf16": 2e-3}
 
 
+def top_k_arg(k, V, force_resident):
+    """The top-k argument of a call: None when no row filters (every k <= 0 or
+    >= V), which lets the library take its streaming kernel; the array itself
+    when force_resident (any top-k array selects the resident kernel)."""
+    if k is None:
+        return None
+    k = np.asarray(k)
+    if force_resident or np.any((k > 0) & (k < V)):
+        return k
+    return None
+
+
 def to_dev(arr, dtype):
     t = torch.from_numpy(np.ascontiguousarray(arr)).cuda()
     return t.to(torch.bfloat16) if dtype == "bf16" else t
 
 
-def run_chain(w, uniform_override=None, return_residual=False, seed=None, pad_to=None):
+def run_chain(w, uniform_override=None, return_residual=False, seed=None, pad_to=None,
+              workspace_tensor=None, force_resident=False):
     dt = w["dtype"]
     target = w["target"]
     draft = w["draft"]
@@ -40,11 +53,12 @@ def run_chain(w, uniform_override=None, return_residual=False, seed=None, pad_to
     res = sv.verify_chain(
         t_dev, d_dev, torch.from_numpy(w["tokens"]).cuda(),
         w["target_temperature"], w["draft_temperature"],
-        target_top_k=w.get("target_top_k"), draft_top_k=w.get("draft_top_k"),
+        target_top_k=top_k_arg(w.get("target_top_k"), w["target"].shape[-1], force_resident),
+        draft_top_k=top_k_arg(w.get("draft_top_k"), w["target"].shape[-1], force_resident),
         seed=w["seed"] if seed is None else seed,
         uniform_override=None if uniform_override is None else torch.from_numpy(
             np.ascontiguousarray(uniform_override, dtype=np.float32)).cuda(),
-        return_residual=return_residual)
+        return_residual=return_residual, workspace_tensor=workspace_tensor)
     torch.cuda.synchronize()
     return res
 
@@ -101,26 +115,32 @@ def excuse_margin_chain(j_gpu, toks_gpu, r):
     return r["draw_margin"]
 
 
-def run_tree(w, uniform_override=None, return_residual=False, seed=None):
+def run_tree(w, uniform_override=None, return_residual=False, seed=None, workspace_tensor=None,
+             force_resident=False):
     dt = w["dtype"]
     res = sv.verify_tree(
         to_dev(w["target"], dt), to_dev(w["draft"], dt), torch.from_numpy(w["tokens"]).cuda(),
         torch.from_numpy(w["parent"]).cuda(), w["max_depth"], w["target_temperature"],
-        w["draft_temperature"], target_top_k=w.get("target_top_k"),
-        draft_top_k=w.get("draft_top_k"), seed=w["seed"] if seed is None else seed,
+        w["draft_temperature"],
+        target_top_k=top_k_arg(w.get("target_top_k"), w["target"].shape[-1], force_resident),
+        draft_top_k=top_k_arg(w.get("draft_top_k"), w["target"].shape[-1], force_resident),
+        seed=w["seed"] if seed is None else seed,
         uniform_override=None if uniform_override is None else torch.from_numpy(
             np.ascontiguousarray(uniform_override, dtype=np.float32)).cuda(),
-        return_residual=return_residual)
+        return_residual=return_residual, workspace_tensor=workspace_tensor)
     torch.cuda.synchronize()
     return res
 
 
 def oracle_tree(w, uniform_override=None, seed=None, trees=None):
-    return ov.verify_tree(w["target"], w["draft"], w["tokens"], w["parent"], w["max_depth"],
+    want = ov.verify_tree(w["target"], w["draft"], w["tokens"], w["parent"], w["max_depth"],
                           w["target_temperature"], w["draft_temperature"],
                           w.get("target_top_k"), w.get("draft_top_k"),
                           seed=w["seed"] if seed is None else seed,
                           uniform_override=uniform_override, trees=trees)
+    for r in want:
+        r["rows"] = w["parent"].shape[1]  # a tree is N target rows
+    return want
 
 
 def compare_tree(res, want, log, label, dtype="bf16", check_residual=False):
@@ -132,7 +152,7 @@ def compare_tree(res, want, log, label, dtype="bf16", check_residual=False):
     failures = []
     for r in want:
         t = r["tree"]
-        log.add_rows(1)
+        log.add_rows(r.get("rows", 1))
         same = (n[t] == r["num_accepted"] and list(path[t]) == r["path"]
                 and list(toks[t]) == r["tokens"] and flags[t] == r["flags"])
         if same:

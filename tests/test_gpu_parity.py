@@ -34,18 +34,25 @@ def built():
 # the five workloads at full size (the bench's launch configuration)
 # ---------------------------------------------------------------------------
 
+# "stream": no top-k array, the streaming kernel runs; "resident": an all-off
+# top-k array selects the resident cluster kernel on the same inputs.
+PATHS = ["stream", "resident"]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3])
-def test_chain_workload_full_size(cfg, exception_log):
+def test_chain_workload_full_size(cfg, path, exception_log):
     w = workloads.config(cfg)
-    res = run_chain(w)
-    compare_chain(res, oracle_chain(w), exception_log, f"config{cfg}", w["dtype"])
+    res = run_chain(w, force_resident=path == "resident")
+    compare_chain(res, oracle_chain(w), exception_log, f"config{cfg}-{path}", w["dtype"])
 
 
-def test_tree_workload_full_size(exception_log):
+@pytest.mark.parametrize("path", PATHS)
+def test_tree_workload_full_size(path, exception_log):
     w = workloads.config(4)
     assert w["parent"].shape == (32, 60) and w["max_depth"] == 6
-    res = run_tree(w)
-    compare_tree(res, oracle_tree(w), exception_log, "config4", w["dtype"])
+    res = run_tree(w, force_resident=path == "resident")
+    compare_tree(res, oracle_tree(w), exception_log, f"config4-{path}", w["dtype"])
 
 
 def test_tree_mask_workload(exception_log):
@@ -106,6 +113,24 @@ def test_repeated_calls_share_workspace():
     run_chain(w2)
     a2 = run_chain(w1)
     assert torch.equal(a1.tokens, a2.tokens) and torch.equal(a1.flags, a2.flags)
+
+
+def test_workspace_needs_no_initialisation(exception_log):
+    """Every call clears what must start at zero: a workspace full of 0xFF
+    bytes, shared by calls of different shapes (whose layouts overlap each
+    other's regions), still gives the oracle's results."""
+    ws = torch.full((64 << 20,), 0xFF, dtype=torch.uint8, device="cuda")
+    tw = workloads.make_tree(8, 30, 8192, dtype="bf16", seed=11, branching=(4, 3, 2, 1))
+    c1 = workloads.make_chain(96, 7, 32000, dtype="bf16", seed=12, greedy_seqs=4)
+    c2 = workloads.make_chain(8, 2, 32000, dtype="bf16", seed=13)
+    c3 = workloads.make_chain(8, 3, 3001, dtype="f32", seed=14, top_k=20)
+    for w in (tw, c1, c2, tw, c3, c1):
+        if w["kind"] == "tree":
+            compare_tree(run_tree(w, workspace_tensor=ws), oracle_tree(w), exception_log,
+                         "dirty-ws-tree", w["dtype"])
+        else:
+            compare_chain(run_chain(w, workspace_tensor=ws), oracle_chain(w), exception_log,
+                          "dirty-ws-chain", w["dtype"])
 
 
 # ---------------------------------------------------------------------------

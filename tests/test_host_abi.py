@@ -41,6 +41,12 @@ def test_status_strings(lib):
     assert "unknown" in _abi.status_string(42)
 
 
+def test_workspace_size_rejects_bad_shapes(lib):
+    assert lib.spec_verify_chain_workspace_size(4, 4, 0, 0) == 0
+    assert lib.spec_verify_chain_workspace_size(4, 4, 100, 9) == 0
+    assert lib.spec_verify_tree_workspace_size(4, 4, 100, 9) == 0
+
+
 def test_workspace_sizes(lib):
     a = lib.spec_verify_chain_workspace_size(4, 4, 32000, 0)
     b = lib.spec_verify_chain_workspace_size(256, 7, 128256, 1)
