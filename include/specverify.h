@@ -137,6 +137,45 @@ spec_status spec_verify_chain(
     uint32_t *out_flags, float *out_residual,
     void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
+/* Size of the scratch array spec_verify_chain_static works in (16 MiB). */
+#define SPEC_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* spec_verify_chain without a caller workspace: the call allocates nothing.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory at the call site: a decode loop whose
+ * device memory is reserved up front by its own pool (the KV cache takes the
+ * rest, so a per-shape workspace has nowhere to come from), or a plain C host
+ * without a device allocator of its own.  Arguments, outputs, limits and
+ * results are those of spec_verify_chain (it forwards to it).
+ *
+ * Workspace: a file-scope device array of SPEC_STATIC_SCRATCH_BYTES inside
+ *   this library, one per device.  The call uses no cudaMalloc, cudaFree or
+ *   any other allocating routine.
+ * Size limit: shapes with spec_verify_chain_workspace_size(B, gamma, V, dtype)
+ *   > SPEC_STATIC_SCRATCH_BYTES return SPEC_ERR_UNSUPPORTED before any CUDA
+ *   call; use spec_verify_chain there.  For V = 128256 bf16 and gamma = 7,
+ *   B = 512 fits (8.6 MiB) and B = 1024 does not (17.1 MiB).
+ * First call on each device (with that device current): looks the array's
+ *   address up once with cudaGetSymbolAddress, which may load this library's
+ *   device code for that device; a failure returns SPEC_ERR_CUDA.  Make that
+ *   first call outside any stream capture.
+ * Zero state: none is needed; like spec_verify_chain, every call clears the
+ *   counters and task queue it uses (one cudaMemsetAsync on `stream`).
+ * Concurrency: all calls on one device share the one array, so calls whose
+ *   GPU work could overlap (different streams without ordering between them)
+ *   race on it and give undefined results; order them on one stream.
+ */
+spec_status spec_verify_chain_static(
+    const void *target_logits, int64_t ld_target,
+    const void *draft_logits, int64_t ld_draft,
+    spec_dtype dtype, int B, int gamma, int V,
+    const int32_t *draft_tokens,
+    spec_policy target_policy, spec_policy draft_policy,
+    uint64_t seed, const float *uniform_override,
+    int32_t *out_num_accepted, int32_t *out_tokens,
+    uint32_t *out_flags, float *out_residual, spec_stream_t stream);
+
 /* Bytes of workspace spec_verify_tree needs for T trees of N nodes (0 as above). */
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype);
 

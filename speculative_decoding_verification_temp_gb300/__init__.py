@@ -17,7 +17,8 @@ from ._abi import (FLAG_BAD_TOKEN, FLAG_BAD_TREE, FLAG_DEGENERATE_RESIDUAL, FLAG
 def __getattr__(name):
     # the torch binding is imported on first use, so the workload generator
     # and the build step do not need torch
-    if name in ("verify_chain", "verify_tree", "tree_mask", "SpecVerifyError", "workspace",
+    if name in ("verify_chain", "verify_chain_static", "verify_tree", "tree_mask",
+                "SpecVerifyError", "workspace",
                 "ChainResult", "TreeResult", "MaskResult", "api"):
         import importlib
         api = importlib.import_module(__name__ + ".api")

@@ -14,6 +14,8 @@ SPEC_ERR_INVALID_ARG = 1
 SPEC_ERR_CUDA = 2
 SPEC_ERR_UNSUPPORTED = 3
 
+SPEC_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
+
 SPEC_F32 = 0
 SPEC_BF16 = 1
 
@@ -28,6 +30,7 @@ FLAG_BAD_TREE = 64
 EXPORTS = (
     "spec_verify_chain_workspace_size",
     "spec_verify_chain",
+    "spec_verify_chain_static",
     "spec_verify_tree_workspace_size",
     "spec_verify_tree",
     "spec_tree_mask",
@@ -71,6 +74,10 @@ def load():
         _p, _i64, _p, _i64, _i, _i, _i, _i, _p, spec_policy, spec_policy, _u64, _p,
         _p, _p, _p, _p, _p, _sz, _p]
     lib.spec_verify_chain.restype = _i
+    lib.spec_verify_chain_static.argtypes = [
+        _p, _i64, _p, _i64, _i, _i, _i, _i, _p, spec_policy, spec_policy, _u64, _p,
+        _p, _p, _p, _p, _p]
+    lib.spec_verify_chain_static.restype = _i
     lib.spec_verify_tree.argtypes = [
         _p, _i64, _p, _i64, _i, _i, _i, _i, _i, _p, _p, spec_policy, spec_policy, _u64, _p,
         _p, _p, _p, _p, _p, _p, _sz, _p]

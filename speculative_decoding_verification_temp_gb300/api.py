@@ -190,6 +190,55 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
     return TreeResult(num, path, out, flags, resid)
 
 
+def verify_chain_static(target_logits, draft_logits, draft_tokens, target_temperature,
+                        draft_temperature, target_top_k=None, draft_top_k=None, seed=0,
+                        uniform_override=None, return_residual=False):
+    """verify_chain on the library's fixed scratch (see spec_verify_chain_static).
+
+    Same arguments and result as verify_chain, without a workspace: the C call
+    allocates nothing (this wrapper still allocates the output tensors).  Calls
+    on one device must not overlap on the GPU; shapes whose workspace exceeds
+    SPEC_STATIC_SCRATCH_BYTES raise SpecVerifyError (SPEC_ERR_UNSUPPORTED).
+    """
+    _cuda_tensor(target_logits, "target_logits")
+    dev = target_logits.device
+    if target_logits.dtype not in _DTYPES:
+        raise ValueError("logits must be float32 or bfloat16")
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    tl, ld_t = _rows(target_logits, "target_logits")
+    if gamma > 0:
+        _cuda_tensor(draft_logits, "draft_logits")
+        if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, gamma, V):
+            raise ValueError("draft_logits must be [B, gamma, V] with the target's dtype")
+        dl, ld_d = _rows(draft_logits, "draft_logits")
+        toks = _vec(draft_tokens, B * gamma, torch.int32, "draft_tokens", dev).view(B, gamma)
+    else:
+        dl, ld_d, toks = None, 0, None
+    tp = _vec(target_temperature, B, torch.float32, "target_temperature", dev)
+    tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
+    kp = None if target_top_k is None else _vec(target_top_k, B, torch.int32, "target_top_k", dev)
+    kq = None if draft_top_k is None else _vec(draft_top_k, B, torch.int32, "draft_top_k", dev)
+    uov = None
+    if uniform_override is not None:
+        uov = _vec(uniform_override, B * G1 * 2, torch.float32, "uniform_override", dev)
+    num = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    flags = torch.empty(B, dtype=torch.int32, device=dev)
+    resid = torch.empty((B, V), dtype=torch.float32, device=dev) if return_residual else None
+    lib = _abi.load()
+    with torch.cuda.device(dev):
+        code = lib.spec_verify_chain_static(
+            _ptr(tl), ld_t, _ptr(dl), ld_d, _DTYPES[target_logits.dtype], B, gamma, V,
+            _ptr(toks),
+            _abi.spec_policy(tp.data_ptr(), None if kp is None else kp.data_ptr()),
+            _abi.spec_policy(tq.data_ptr(), None if kq is None else kq.data_ptr()),
+            int(seed) & ((1 << 64) - 1), _ptr(uov), _ptr(num), _ptr(out), _ptr(flags),
+            _ptr(resid), _stream(dev))
+    _check(code)
+    return ChainResult(num, out, flags, resid)
+
+
 def tree_mask(parent, max_depth):
     """Ancestor-or-self masks and depth positions (see spec_tree_mask).
 

@@ -100,6 +100,26 @@ def test_chain_unsupported_vocabulary(lib):
     assert chain(lib, V=100_000_000) == _abi.SPEC_ERR_UNSUPPORTED
 
 
+def test_static_chain_refuses_before_any_cuda_call(lib):
+    # B = 1024, gamma = 7 needs more workspace than the fixed scratch holds
+    assert lib.spec_verify_chain_workspace_size(1024, 7, 128256, 1) > _abi.SPEC_STATIC_SCRATCH_BYTES
+    assert lib.spec_verify_chain_workspace_size(256, 7, 128256, 1) < _abi.SPEC_STATIC_SCRATCH_BYTES
+    pol = policy()
+    args = (FAKE, 128256, FAKE, 128256, 1, 1024, 7, 128256, FAKE, pol, pol, 1, None,
+            FAKE, FAKE, None, None, None)
+    assert lib.spec_verify_chain_static(*args) == _abi.SPEC_ERR_UNSUPPORTED
+    empty = (None, 0, None, 0, 1, 0, 7, 128256, None, pol, pol, 1, None, None, None, None, None,
+             None)
+    assert lib.spec_verify_chain_static(*empty) == _abi.SPEC_OK
+    neg = (FAKE, 10, FAKE, 10, 1, -1, 7, 10, FAKE, pol, pol, 1, None, FAKE, FAKE, None, None, None)
+    assert lib.spec_verify_chain_static(*neg) == _abi.SPEC_ERR_INVALID_ARG
+
+
+def test_static_scratch_size_matches_header():
+    assert "#define SPEC_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)" in open(HEADER).read()
+    assert _abi.SPEC_STATIC_SCRATCH_BYTES == 16 * 1024 * 1024
+
+
 def tree(lib, T=2, N=5, V=100, max_depth=3, parent=FAKE, tokens=FAKE, out=FAKE, ws_bytes=0):
     pol = policy()
     return lib.spec_verify_tree(FAKE, V, FAKE, V, 1, T, N, V, max_depth, tokens, parent, pol, pol,
