@@ -1,8 +1,10 @@
 // C ABI of libspecverify: argument checks, workspace layout, launch planning.
 // The operations themselves are documented in include/specverify.h.
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
+#include "precise.cuh"
 #include "specverify.h"
 #include "verify_units.cuh"
 
@@ -15,6 +17,7 @@ cudaError_t launch_tree_mask(const int32_t *parent, int T, int N, int max_depth,
 cudaError_t launch_stream(const Params &P, int esize, size_t smem, cudaStream_t stream);
 cudaError_t launch_first_child(const int32_t *parent, int T, int N, int32_t *first_child,
                                cudaStream_t stream);
+cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream);
 }  // namespace sv
 
 namespace {
@@ -93,7 +96,7 @@ bool make_stream_plan(long long V, int esize, StreamPlan &sp) {
 // read within a call.
 struct Layout {
   size_t wq_ctr, counters, unit_done, w_done, wq, zero_bytes;
-  size_t outs, stats, final_unit, first_child, partials, dstate, wpart, wblk, total;
+  size_t outs, stats, final_unit, first_child, refine, partials, dstate, wpart, wblk, total;
   long long wq_cap;
 };
 
@@ -109,7 +112,7 @@ Layout layout(long long nseq, long long units, long long slices) {
     off = align_up(off + bytes, 256);
     return at;
   };
-  L.wq_ctr = take(4 * sizeof(uint32_t));
+  L.wq_ctr = take(4 * sizeof(uint32_t));  // [0] queue head, [1] tail, [2] units done, [3] refines
   L.counters = take(static_cast<size_t>(nseq) * sizeof(uint32_t));
   L.unit_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
   L.w_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
@@ -123,6 +126,7 @@ Layout layout(long long nseq, long long units, long long slices) {
   L.stats = take(static_cast<size_t>(units) * sizeof(sv::UnitStats));
   L.final_unit = take(static_cast<size_t>(nseq) * sizeof(int32_t));
   L.first_child = take(static_cast<size_t>(units) * sizeof(int32_t));
+  L.refine = take(static_cast<size_t>(nseq) * sizeof(int4));
   L.partials = take(static_cast<size_t>(units * slices * 2) * sizeof(sv::SlicePartial));
   L.dstate = take(static_cast<size_t>(slices ? units : 0) * sizeof(sv::DrawState));
   L.wpart = take(static_cast<size_t>(units * slices) * sizeof(float));
@@ -138,6 +142,20 @@ long long stream_slices(long long V, int esize) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2^(j/64) as double-float pairs, for the precise redraw.
+const sv::Exp2Table &exp2_table() {
+  static const sv::Exp2Table tab = [] {
+    sv::Exp2Table t;
+    for (int j = 0; j < 64; ++j) {
+      const double v = std::exp2(j / 64.0);
+      t.hi[j] = static_cast<float>(v);
+      t.lo[j] = static_cast<float>(v - static_cast<double>(t.hi[j]));
+    }
+    return t;
+  }();
+  return tab;
+}
 
 spec_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
@@ -164,6 +182,8 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   P.outs = reinterpret_cast<sv::UnitOut *>(ws + L.outs);
   P.stats = reinterpret_cast<sv::UnitStats *>(ws + L.stats);
   P.final_unit = reinterpret_cast<int32_t *>(ws + L.final_unit);
+  P.refine = reinterpret_cast<int4 *>(ws + L.refine);
+  P.refine_ctr = reinterpret_cast<uint32_t *>(ws + L.wq_ctr) + 3;
   P.n_units = static_cast<int>(n_units);
   if (streaming) {
     P.slice = sp.slice;
@@ -201,6 +221,8 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.hist_off = static_cast<int>(pl.hist_off);
     e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
   }
+  if (e != cudaSuccess) return map_cuda(e);
+  e = sv::launch_refine(P, esize, exp2_table(), stream);
   if (e != cudaSuccess) return map_cuda(e);
   if (out_residual) {
     e = sv::launch_residual(P, esize, out_residual, stream);

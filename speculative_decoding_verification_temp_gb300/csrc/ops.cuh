@@ -620,6 +620,7 @@ __device__ int cta_search(const RowDesc &dp, const RowDesc &dq, int residual, fl
     const int ocs = warp * L, oce = min(len, ocs + L);
     float base_sum = 0.f;
     int result = -1;
+    float margin = 0.f;
     for (int rb = ocs; rb < oce && result < 0; rb += 256) {
       const int base = rb + lane * 8;
       float zp[8], zq[8];
@@ -647,21 +648,33 @@ __device__ int cta_search(const RowDesc &dp, const RowDesc &dq, int residual, fl
       if (hit) {
         const int first = __ffs(hit) - 1;
         int found = -1;
+        float mg = 0.f;
         if (lane == first) {
           float run = base_sum + excl;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
+            const float prev = run;
             run += w[e];
-            if (found < 0 && w[e] > 0.f && run > trel) found = base + e;
+            if (found < 0 && w[e] > 0.f && run > trel) {
+              found = base + e;
+              mg = fminf(trel - prev, run - trel);
+            }
           }
           if (found < 0) found = lp;
         }
         result = __shfl_sync(0xFFFFFFFFu, found, first);
+        margin = __shfl_sync(0xFFFFFFFFu, mg, first);
       }
       base_sum += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    if (result < 0) result = ctl.rs.red_i[0][warp];
-    if (lane == 0) ctl.token_local = v0 + result;
+    if (result < 0) {
+      result = ctl.rs.red_i[0][warp];
+      margin = 0.f;
+    }
+    if (lane == 0) {
+      ctl.token_local = v0 + result;
+      ctl.margin = trel == INFINITY ? 0.f : margin;
+    }
   }
   csync();
   const int tok = ctl.token_local;
@@ -702,6 +715,16 @@ static __device__ int next_child(const Params &P, int seq, int node, int after, 
 __device__ __forceinline__ int child_token(const Params &P, int seq, int node, int child) {
   if (P.mode == kModeChain) return __ldg(P.tokens + static_cast<long long>(seq) * P.gamma + node);
   return __ldg(P.tokens + static_cast<long long>(seq) * P.ups + child);
+}
+
+// Queue the final unit of a sequence for the precise redraw when its draw
+// fell within the refine guard of a CDF boundary (single thread).
+__device__ __forceinline__ void queue_refine(const Params &P, int seq, long long unit, int pos,
+                                             int near) {
+  if (!near || !P.refine) return;
+  const uint32_t i = atomicAdd(P.refine_ctr, 1u);
+  if (static_cast<int>(i) < P.nseq)
+    P.refine[i] = make_int4(seq, static_cast<int>(unit), pos, 0);
 }
 
 __device__ __forceinline__ float unit_uniform(const Params &P, int seq, int pos, int draw) {

@@ -130,12 +130,12 @@ __device__ __forceinline__ void block_range(const Params &P, int r, int b, int e
 
 __device__ void publish_unit(const Params &P, int unit, int node, int next, int token,
                              uint32_t flags, const RowDesc &dp, const RowDesc &dq, float c,
-                             float total, int kind) {
+                             float total, int kind, int near = 0, int n_res = 0) {
   UnitOut o;
   o.next = next;
   o.token = token;
   o.flags = flags;
-  o.pad = 0;
+  o.near = near;
   P.outs[unit] = o;
   UnitStats st;
   st.p = dp;
@@ -144,6 +144,8 @@ __device__ void publish_unit(const Params &P, int unit, int node, int next, int 
   st.total = total;
   st.kind = kind;
   st.node = node;
+  st.n_res = n_res;
+  st.pad = 0;
   P.stats[unit] = st;
   P.unit_done[unit] = 0u;  // leave the counters zeroed for the next call
   P.w_done[unit] = 0u;
@@ -222,10 +224,11 @@ __device__ int test_children(const Params &P, const UnitInfo &u, DrawState &ds, 
 // rounding miss, the last positive entry.  Returns the index in every lane.
 template <typename TE>
 __device__ int block_search(const RowDesc &dp, const RowDesc &dq, int residual, float c,
-                            const TE *gp, const TE *gq, int bs, int be, float t) {
+                            const TE *gp, const TE *gq, int bs, int be, float t, float &margin) {
   const int lane = threadIdx.x & 31;
   float base_sum = 0.f;
   int result = -1, lastpos = -1;
+  margin = 0.f;
   for (int rb = bs; rb < be && result < 0; rb += 256) {
     const int base = rb + lane * 8;
     float w[8];
@@ -257,19 +260,26 @@ __device__ int block_search(const RowDesc &dp, const RowDesc &dq, int residual, 
     if (hit) {
       const int first = __ffs(hit) - 1;
       int found = -1;
+      float mg = 0.f;
       if (lane == first) {
         float run = base_sum + excl;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
+          const float prev = run;
           run += w[e];
-          if (found < 0 && w[e] > 0.f && run > t) found = base + e;
+          if (found < 0 && w[e] > 0.f && run > t) {
+            found = base + e;
+            mg = fminf(t - prev, run - t);
+          }
         }
         if (found < 0) found = lp;
       }
       result = __shfl_sync(0xFFFFFFFFu, found, first);
+      margin = __shfl_sync(0xFFFFFFFFu, mg, first);
     }
     base_sum += __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
+  if (result < 0 || t == INFINITY) margin = 0.f;
   return result >= 0 ? result : lastpos;
 }
 
@@ -277,7 +287,7 @@ __device__ int block_search(const RowDesc &dp, const RowDesc &dq, int residual, 
 // (warp 0; returns the token in every lane of warp 0).
 template <typename TE>
 __device__ int draw_from_blocks(const Params &P, const UnitInfo &u, const DrawState &ds,
-                                float Z) {
+                                float Z, float &margin) {
   const int lane = threadIdx.x & 31;
   const int C = P.cluster, sb = P.slice_blocks;
   const int nb = C * sb;
@@ -337,7 +347,7 @@ __device__ int draw_from_blocks(const Params &P, const UnitInfo &u, const DrawSt
   const TE *gq = static_cast<const TE *>(row_ptr(P.draft, u.qrow, P.ld_d, sizeof(TE)));
   const int residual = ds.c_cur > 0.f;
   return block_search<TE>(ds.dp, ds.dq, residual, residual ? ds.c_cur : 0.f, gp, gq, bs, be,
-                          trel);
+                          trel, margin);
 }
 
 // ---------------------------------------------------------------------------
@@ -388,7 +398,7 @@ __device__ void decide_unit(const Params &P, int unit, Ctl3 &ctl) {
   int need_fallback[2] = {0, 0};
   for (int row = 0; row < 2; ++row) {
     RowDesc d;
-    d.pad = 0;
+    d.m = 0.f;
     d.flags = 0u;
     d.thr = -INFINITY;
     if (row == 1 && !u.load_q) {
@@ -415,6 +425,7 @@ __device__ void decide_unit(const Params &P, int unit, Ctl3 &ctl) {
       d.onehot = 0;
       d.a = 0;
       d.k = kk;
+      d.m = M;
       d.nmk = -M * kk;
       d.invS = 1.f / S;
       if (bad) {
@@ -446,7 +457,7 @@ __device__ void decide_unit(const Params &P, int unit, Ctl3 &ctl) {
     ds.W_cur = 0.f;
     ds.round = 0;
     ds.blocks_c_valid = 0;
-    ds.pad = 0;
+    ds.n_res = 0;
     int child = u.has_children
                     ? (P.mode == kModeChain ? u.node + 1 : __ldg(P.first_child + unit))
                     : -1;
@@ -499,6 +510,7 @@ __device__ void finish_round(const Params &P, int unit, Ctl3 &ctl) {
         ds.c_cur = ds.c;
         ds.W_cur = W;
         ds.blocks_c_valid = 1;
+        ds.n_res += 1;
       } else {
         ds.flags |= SPEC_FLAG_DEGENERATE_RESIDUAL;
         ds.blocks_c_valid = 0;
@@ -538,11 +550,14 @@ __device__ void finish_round(const Params &P, int unit, Ctl3 &ctl) {
   csync();
   if (ctl.decision && tid < 32) {
     const DrawState dsw = ctl.ds_share;
-    const int tok = draw_from_blocks<TE>(P, u, dsw, ctl.trel);
+    float margin;
+    const int tok = draw_from_blocks<TE>(P, u, dsw, ctl.trel, margin);
     if (tid == 0) {
       const int residual = dsw.c_cur > 0.f;
-      publish_unit(P, unit, u.node, -1, tok, dsw.flags, dsw.dp, dsw.dq,
-                   residual ? dsw.c_cur : 0.f, ctl.trel, u.has_children ? 2 : 0);
+      const float c = residual ? dsw.c_cur : 0.f;
+      publish_unit(P, unit, u.node, -1, tok, dsw.flags, dsw.dp, dsw.dq, c, ctl.trel,
+                   u.has_children ? 2 : 0, margin < kRefineGuard * (1.f + c) ? 1 : 0,
+                   residual ? dsw.n_res : 0);
     }
   }
   csync();
@@ -894,6 +909,7 @@ __global__ void __launch_bounds__(kThreads) chain_combine_kernel(const Params P)
     P.out_num[seq] = j;
     if (P.out_flags) P.out_flags[seq] = f;
     P.final_unit[seq] = static_cast<int>(ubase + j);
+    queue_refine(P, seq, ubase + j, j, P.outs[ubase + j].near);
   }
 }
 
@@ -987,6 +1003,7 @@ __global__ void __launch_bounds__(kThreads) tree_combine_kernel(const Params P) 
     P.out_num[seq] = k;
     if (P.out_flags) P.out_flags[seq] = f;
     P.final_unit[seq] = static_cast<int>(ubase + cur);
+    queue_refine(P, seq, ubase + cur, k, P.outs[ubase + cur].near);
   }
 }
 

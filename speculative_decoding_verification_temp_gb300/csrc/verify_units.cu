@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
 #pragma unroll
   for (int row = 0; row < 2; ++row) {
     RowDesc d;
-    d.pad = 0;
+    d.m = 0.f;
     d.flags = 0u;
     d.thr = row == 0 ? thr_p : thr_q;
     const bool arg = row == 0 ? p_arg : q_arg;
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       d.onehot = 0;
       d.a = 0;
       d.k = kk;
+      d.m = M;
       d.nmk = -M * kk;
       d.invS = 1.f / S;
       if (bad) {
@@ -304,6 +305,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
   int next = -1, token = -1;
   int residual = 0;
   float c = 0.f, Wcur = 0.f;
+  int n_res = 0;
   bool have_parts = false;
   int xround = 0;
   int kind = 0;
@@ -369,6 +371,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
         residual = 1;
         c = cn;
         Wcur = W;
+        ++n_res;
         have_parts = true;
       } else {
         uflags |= SPEC_FLAG_DEGENERATE_RESIDUAL;
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       o.next = next;
       o.token = token;
       o.flags = uflags;
-      o.pad = 0;
+      o.near = draw && ctl.margin < kRefineGuard * (1.f + (residual ? c : 0.f)) ? 1 : 0;
       P.outs[unit] = o;
       UnitStats st;
       st.p = dp;
@@ -441,6 +444,8 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
       st.total = total;
       st.kind = kind;
       st.node = node;
+      st.n_res = residual ? n_res : 0;
+      st.pad = 0;
       P.stats[unit] = st;
       __threadfence();
       const unsigned prev = atomicAdd(P.counters + seq, 1u);
@@ -475,6 +480,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
             if (P.out_flags) P.out_flags[seq] = f;
             P.final_unit[seq] = static_cast<int>(ubase + j);
             P.counters[seq] = 0u;
+            queue_refine(P, seq, ubase + j, j, __ldcg(&P.outs[ubase + j].near));
           }
         }
       } else {
@@ -558,6 +564,7 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
           P.out_num[seq] = k;
           if (P.out_flags) P.out_flags[seq] = f;
           P.final_unit[seq] = static_cast<int>(ubase + cur);
+          queue_refine(P, seq, ubase + cur, k, __ldcg(&P.outs[ubase + cur].near));
         }
         if (tid == 0) P.counters[seq] = 0u;
       }

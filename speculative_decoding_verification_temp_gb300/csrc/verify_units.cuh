@@ -51,7 +51,7 @@ struct RowDesc {
   float invS;  // 1 / sum
   float thr;   // top-k threshold (-inf: none)
   uint32_t flags;
-  int pad;
+  float m;     // row maximum (the precise redraw recomputes the weights from it)
 };
 
 // What a unit's final draw was taken from (read by the residual-output kernel).
@@ -61,14 +61,21 @@ struct UnitStats {
   float total;  // sum of the draw weights
   int kind;     // 0: no draw (a child was accepted) or bonus draw, 1: one-hot, 2: weights
   int node;
+  int n_res;    // residual rounds that set the multiplier: c = c_{n_res} (0: p itself)
+  int pad;
 };
 
 struct UnitOut {
   int next;   // accepted child node id, -1 when the unit drew `token`
   int token;
   uint32_t flags;
-  int pad;
+  int near;   // 1: the draw fell within the refine guard of a CDF boundary
 };
+
+// A final draw whose single-precision running sum came within this distance
+// (in probability units, times 1 + c for a residual [p - c q]_+) of a CDF
+// boundary is redrawn in double-float arithmetic by the refine kernel.
+constexpr float kRefineGuard = 4e-6f;
 
 struct Params {
   const void *target;
@@ -118,6 +125,9 @@ struct Params {
   uint32_t *wq_ctr;               // [0] head, [1] tail, [2] units completed
   uint32_t epoch;                 // tags this call's queue entries
   int wq_cap;
+  // precise redraw of final draws near a CDF boundary
+  int4 *refine;                   // [nseq] (seq, unit, output position, 0)
+  uint32_t *refine_ctr;           // entries in `refine`
 };
 
 
@@ -158,6 +168,7 @@ struct __align__(16) Ctl {
   int decision;  // broadcast of thread 0's per-child verdict
   int owner;
   float trel;
+  float margin;  // distance of the draw from the nearer CDF boundary
   RedScratch rs;
 };
 
@@ -190,7 +201,7 @@ struct __align__(16) DrawState {
   uint32_t flags;
   int round;
   int blocks_c_valid;  // 1 when the stored block totals belong to the held distribution
-  int pad;
+  int n_res;           // residual rounds that set c_cur
 };
 
 // What the producer warp tells the compute threads about a task.
