@@ -18,6 +18,8 @@ cudaError_t launch_stream(const Params &P, int esize, size_t smem, cudaStream_t 
 cudaError_t launch_first_child(const int32_t *parent, int T, int N, int32_t *first_child,
                                cudaStream_t stream);
 cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream);
+cudaError_t launch_pass(const Params &P, int esize, size_t smem, cudaStream_t stream);
+size_t pass_ctl_bytes();
 }  // namespace sv
 
 namespace {
@@ -94,8 +96,43 @@ bool make_stream_plan(long long V, int esize, StreamPlan &sp) {
 // (arrival counters, the weight-task queue and its counters) come first and
 // are cleared by every call; everything after them is written before it is
 // read within a call.
+// Chain pass kernel (sequence-level decide): 32 KB chunks through a ring of
+// three slots (two CTAs per SM); every row's chunks leave one record per
+// consumer warp.
+struct PassPlan {
+  int chunk_elems;
+  int cpr;
+  int steps;
+  int ring;
+  int slot_bytes;
+  size_t data_off;
+  size_t smem;
+};
+
+constexpr int kPassMaxGamma = 31;
+
+bool make_pass_plan(long long V, int esize, int gamma, PassPlan &pp) {
+  if (gamma > kPassMaxGamma || esize <= 0) return false;
+  pp.slot_bytes = 32 * 1024;
+  pp.ring = 3;
+  pp.chunk_elems = pp.slot_bytes / esize;
+  pp.cpr = static_cast<int>((V + pp.chunk_elems - 1) / pp.chunk_elems);
+  pp.steps = static_cast<int>((V + 255) / 256);
+  pp.data_off = align_up(sv::pass_ctl_bytes(), 128);
+  pp.smem = pp.data_off + static_cast<size_t>(pp.ring) * pp.slot_bytes +
+            align_up(static_cast<size_t>(pp.steps) * sizeof(float), 16);
+  return pp.smem <= kSmemHard;
+}
+
+// 64-bit records the pass kernel writes for B sequences of gamma drafts.
+long long pass_records(long long B, int gamma, long long V, int esize) {
+  PassPlan pp;
+  if (!make_pass_plan(V, esize, gamma, pp)) return 0;
+  return B * (2 * gamma + 1) * static_cast<long long>(pp.cpr) * 8;
+}
+
 struct Layout {
-  size_t wq_ctr, counters, unit_done, w_done, wq, zero_bytes;
+  size_t wq_ctr, counters, unit_done, w_done, wq, seq_cnt, srec, err, zero_bytes;
   size_t outs, stats, final_unit, first_child, refine, partials, dstate, wpart, wblk, total;
   long long wq_cap;
 };
@@ -103,8 +140,8 @@ struct Layout {
 constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
 // slices: slices per unit of the streaming kernel, 0 when only the resident
-// kernel can run the shape.
-Layout layout(long long nseq, long long units, long long slices) {
+// kernel can run the shape; recs: records of the chain pass kernel.
+Layout layout(long long nseq, long long units, long long slices, long long recs) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -121,6 +158,9 @@ Layout layout(long long nseq, long long units, long long slices) {
   // final draw at each node), one entry per slice
   L.wq_cap = 3 * units * slices;
   L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
+  L.seq_cnt = take(static_cast<size_t>(recs ? nseq : 0) * sizeof(uint32_t));
+  L.srec = take(static_cast<size_t>(recs) * sizeof(unsigned long long));  // zero = not written
+  L.err = take(sizeof(uint32_t));
   L.zero_bytes = off;
   L.outs = take(static_cast<size_t>(units) * sizeof(sv::UnitOut));
   L.stats = take(static_cast<size_t>(units) * sizeof(sv::UnitStats));
@@ -161,8 +201,10 @@ spec_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_E
 
 int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0); }
 
-// Shared launch path of the chain and tree verifiers: the streaming kernel for
-// 16-byte aligned rows without top-k filtering, the resident kernel otherwise.
+// Shared launch path of the chain and tree verifiers.  16-byte aligned rows
+// without top-k filtering take the chain pass kernel (chains of gamma <= 31)
+// or the streaming kernel (trees, longer chains); everything else the
+// resident kernel.
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                       float *out_residual, void *workspace, size_t workspace_bytes,
                       cudaStream_t stream, bool need_draft_rows) {
@@ -170,10 +212,22 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   const bool vec = aligned16(P.target) && (P.ld_t * esize) % 16 == 0 &&
                    (!need_draft_rows || (aligned16(P.draft) && (P.ld_d * esize) % 16 == 0));
   StreamPlan sp;
+  PassPlan pp;
   Plan pl;
-  const bool streaming = vec && !topk && make_stream_plan(P.V, esize, sp);
-  if (!streaming && !make_plan(P.V, esize, extra, topk, pl)) return SPEC_ERR_UNSUPPORTED;
-  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0);
+  const bool pass = vec && !topk && P.mode == sv::kModeChain &&
+                    make_pass_plan(P.V, esize, P.gamma, pp) &&
+                    static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr < 0x7FFFFFFFll;
+  const bool streaming = !pass && vec && !topk && make_stream_plan(P.V, esize, sp);
+  if (!pass && !streaming && !make_plan(P.V, esize, extra, topk, pl))
+    return SPEC_ERR_UNSUPPORTED;
+  // the caller's workspace must hold what the size query promised for the shape
+  const size_t promised =
+      layout(P.nseq, n_units, stream_slices(P.V, esize),
+             P.mode == sv::kModeChain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0)
+          .total;
+  if (workspace_bytes < promised) return SPEC_ERR_INVALID_ARG;
+  const long long recs = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr * 8 : 0;
+  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
   cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, stream);
@@ -185,7 +239,18 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   P.refine = reinterpret_cast<int4 *>(ws + L.refine);
   P.refine_ctr = reinterpret_cast<uint32_t *>(ws + L.wq_ctr) + 3;
   P.n_units = static_cast<int>(n_units);
-  if (streaming) {
+  if (pass) {
+    P.ring = pp.ring;
+    P.slot_bytes = pp.slot_bytes;
+    P.data_off = static_cast<int>(pp.data_off);
+    P.chunk_elems = pp.chunk_elems;
+    P.cpr = pp.cpr;
+    P.steps = pp.steps;
+    P.srec = reinterpret_cast<unsigned long long *>(ws + L.srec);
+    P.seq_cnt = reinterpret_cast<uint32_t *>(ws + L.seq_cnt);
+    P.err = reinterpret_cast<uint32_t *>(ws + L.err);
+    e = sv::launch_pass(P, esize, pp.smem, stream);
+  } else if (streaming) {
     P.slice = sp.slice;
     P.cluster = sp.slices;
     P.data_off = static_cast<int>(sp.data_off);
@@ -248,13 +313,15 @@ const char *spec_status_string(spec_status status) {
 size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (B < 0 || gamma < 0 || V < 1 || esize == 0) return 0;
-  return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize)).total;
+  return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize),
+                pass_records(B, gamma, V, esize))
+      .total;
 }
 
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
-  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize)).total;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0).total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

@@ -10,7 +10,7 @@
 // (relative error below 1e-11) and double-precision sums, and overwrites the
 // token.
 //
-// One thread-block cluster of 8 CTAs per queued draw, in a loop over the
+// One thread-block cluster of 16 CTAs per queued draw, in a loop over the
 // queue.  For a residual [p - c q]_+ the passes over the row pair are:
 //   1. S_p, S_q: the softmax normalisers;
 //   2. for a tree node whose held residual came after n > 1 rejections, the
@@ -19,7 +19,8 @@
 //   3. the weights of the final distribution, per-warp and per-CTA totals;
 // then the inverse-CDF search: CTA, warp, then one warp scans its range.
 // A draw from p itself needs only pass 3.  Rows are read from global memory
-// (L2) with scalar loads: this path runs for a few percent of the draws.
+// in groups of 8 entries (16-byte loads when the rows are aligned): this path
+// runs for a few percent of the draws.
 #include <cooperative_groups.h>
 
 #include "ops.cuh"
@@ -30,7 +31,7 @@ namespace sv {
 
 namespace cg = cooperative_groups;
 
-constexpr int kRefineCluster = 8;
+constexpr int kRefineCluster = 16;
 
 struct HpRow {
   float m;         // row maximum
@@ -108,32 +109,65 @@ struct RefineRows {
   const TE *gp, *gq;
   HpRow rp, rq;
   int residual;
-  Df rho;  // c S_p / S_q: the weight is [e_p - rho e_q]_+
+  int vec;  // both rows start on 16-byte boundaries
+  Df rho;   // c S_p / S_q: the weight is [e_p - rho e_q]_+
 };
 
+// Logits of the 8 entries from `base` (a multiple of 8); -inf at or past `end`.
 template <typename TE>
-__device__ __forceinline__ Df hp_weight(const RefineRows<TE> &R, int v, const RefineSmem &sm) {
-  const Df ep = hp_exp(R.rp, to_f32(R.gp[v]), sm.tab_hi, sm.tab_lo);
-  if (!R.residual) return ep;
-  if (ep.hi == 0.f) return Df{0.f, 0.f};
-  const Df eq = hp_exp(R.rq, to_f32(R.gq[v]), sm.tab_hi, sm.tab_lo);
-  const Df d = df_sub(ep, df_mul(R.rho, eq));
-  return d.hi > 0.f ? d : Df{0.f, 0.f};
+__device__ __forceinline__ void load8z(const TE *g, int base, int end, bool vec, float z[8]) {
+  if (vec && base + 8 <= end) {
+    if (sizeof(TE) == 2) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(g + base);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        z[2 * i] = __uint_as_float(ws[i] << 16);
+        z[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+      }
+    } else {
+      const float4 a = *reinterpret_cast<const float4 *>(g + base);
+      const float4 b = *reinterpret_cast<const float4 *>(g + base + 4);
+      z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
+      z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) z[e] = base + e < end ? to_f32(g[base + e]) : -INFINITY;
 }
 
-// Sum of 8 consecutive weights from `base` (entries at or past `end` are 0).
+// Weights of the 8 entries from `base` (0 at or past `end`).
+template <typename TE>
+__device__ __forceinline__ void hp_weight8(const RefineRows<TE> &R, int base, int end,
+                                           const RefineSmem &sm, Df w[8]) {
+  float zp[8], zq[8];
+  load8z<TE>(R.gp, base, end, R.vec, zp);
+  if (R.residual) load8z<TE>(R.gq, base, end, R.vec, zq);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const Df ep = hp_exp(R.rp, zp[e], sm.tab_hi, sm.tab_lo);
+    if (!R.residual || ep.hi == 0.f) {
+      w[e] = ep;
+      continue;
+    }
+    const Df eq = hp_exp(R.rq, zq[e], sm.tab_hi, sm.tab_lo);
+    const Df d = df_sub(ep, df_mul(R.rho, eq));
+    w[e] = d.hi > 0.f ? d : Df{0.f, 0.f};
+  }
+}
+
+// Sum of the 8 weights from `base` (entries at or past `end` are 0).
 template <typename TE>
 __device__ __forceinline__ double step_sum(const RefineRows<TE> &R, int base, int end,
                                            const RefineSmem &sm, int &lastpos) {
+  Df w[8];
+  hp_weight8(R, base, end, sm, w);
   Df s{0.f, 0.f};
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const int v = base + e;
-    if (v < end) {
-      const Df w = hp_weight(R, v, sm);
-      if (w.hi > 0.f) lastpos = v;
-      s = df_add(s, w);
-    }
+    if (w[e].hi > 0.f) lastpos = base + e;
+    s = df_add(s, w[e]);
   }
   return df_to_double(s);
 }
@@ -178,19 +212,20 @@ __global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kThread
     R.gq = static_cast<const TE *>(row_ptr(P.draft, qrow, P.ld_d, sizeof(TE)));
     R.rp = hp_row(st.p, __ldg(P.Tp + seq));
     R.residual = st.c > 0.f && st.n_res > 0;
+    R.vec = ((reinterpret_cast<uintptr_t>(R.gp) | reinterpret_cast<uintptr_t>(R.gq)) & 15u) == 0;
     R.rho = Df{0.f, 0.f};
     if (R.residual) {
       R.rq = hp_row(st.q, __ldg(P.Tq + seq));
       // pass 1: the normalisers
       Df sp{0.f, 0.f}, sq{0.f, 0.f};
       for (int base = ws + lane * 8; base < we; base += 256) {
+        float zp[8], zq[8];
+        load8z<TE>(R.gp, base, we, R.vec, zp);
+        load8z<TE>(R.gq, base, we, R.vec, zq);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int v = base + e;
-          if (v < we) {
-            sp = df_add(sp, hp_exp(R.rp, to_f32(R.gp[v]), sm.tab_hi, sm.tab_lo));
-            sq = df_add(sq, hp_exp(R.rq, to_f32(R.gq[v]), sm.tab_hi, sm.tab_lo));
-          }
+          sp = df_add(sp, hp_exp(R.rp, zp[e], sm.tab_hi, sm.tab_lo));
+          sq = df_add(sq, hp_exp(R.rq, zq[e], sm.tab_hi, sm.tab_lo));
         }
       }
       double Sp, Sq;
@@ -295,15 +330,16 @@ __global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kThread
         int result = -1;
         for (int rb = ws; rb < we && result < 0; rb += 256) {
           const int base = rb + lane * 8;
+          Df wd[8];
+          hp_weight8(R, base, we, sm, wd);
           double w[8];
           double s = 0.0;
           int lpos = -1;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int v = base + e;
-            w[e] = v < we ? df_to_double(hp_weight(R, v, sm)) : 0.0;
+            w[e] = df_to_double(wd[e]);
             s += w[e];
-            if (w[e] > 0.0) lpos = v;
+            if (w[e] > 0.0) lpos = base + e;
           }
           double incl = s;
 #pragma unroll
@@ -343,12 +379,23 @@ __global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kThread
   }
 }
 
-cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream) {
-  const int G = P.nseq < 19 ? P.nseq : 19;  // one CTA per SM across 152 SMs
-  const dim3 grid(G * kRefineCluster);
-  if (esize == 2) refine_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(P, tab);
-  else refine_kernel<float><<<grid, kThreads, 0, stream>>>(P, tab);
+template <typename TE>
+cudaError_t launch_refine_t(const Params &P, const Exp2Table &tab, cudaStream_t stream) {
+  static bool attr_set = false;  // clusters of 16 need the non-portable size opt-in
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        refine_kernel<TE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int G = P.nseq < 9 ? P.nseq : 9;  // 144 CTAs: one wave on 152 SMs
+  refine_kernel<TE><<<dim3(G * kRefineCluster), kThreads, 0, stream>>>(P, tab);
   return cudaGetLastError();
+}
+
+cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream) {
+  return esize == 2 ? launch_refine_t<uint16_t>(P, tab, stream)
+                    : launch_refine_t<float>(P, tab, stream);
 }
 
 }  // namespace sv

@@ -128,6 +128,13 @@ struct Params {
   // precise redraw of final draws near a CDF boundary
   int4 *refine;                   // [nseq] (seq, unit, output position, 0)
   uint32_t *refine_ctr;           // entries in `refine`
+  // chain pass kernel
+  unsigned long long *srec;       // [rows][chunks][8] per-warp records, 0 = not yet written
+  uint32_t *seq_cnt;              // [nseq] chunks of the sequence with stored records (a hint)
+  uint32_t *err;                  // bit 0: a bounded wait gave up
+  int chunk_elems;                // entries per chunk
+  int cpr;                        // chunks per row
+  int steps;                      // draw search steps per row (256 entries each)
 };
 
 
