@@ -584,13 +584,19 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const Params P, floa
   const int u = P.final_unit[seq];
   float *o = out + static_cast<long long>(seq) * V;
   const int vbeg = blockIdx.x * kThreads * 8;
-  if (u < 0) {
+  // a sequence without a final unit (invalid tree, or a wait that gave up)
+  // has no residual; an index outside the sequence's units is treated alike
+  if (u < 0 || u >= P.n_units || u / P.ups != seq) {
     for (int v = vbeg + threadIdx.x; v < min(V, vbeg + kThreads * 8); v += kThreads) o[v] = 0.f;
     return;
   }
   const UnitStats st = P.stats[u];
   const int node = st.node;
   const int s2 = u / P.ups;
+  if (node < 0 || node >= P.ups) {
+    for (int v = vbeg + threadIdx.x; v < min(V, vbeg + kThreads * 8); v += kThreads) o[v] = 0.f;
+    return;
+  }
   long long prow, qrow;
   if (P.mode == kModeChain) {
     prow = static_cast<long long>(s2) * (P.gamma + 1) + node;
