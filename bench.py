@@ -34,7 +34,12 @@ sys.path.insert(0, ROOT)
 WORKLOAD = 2
 METRIC = "verified vocab rows/s (B*(gamma+1))"
 CSRC = os.path.join(ROOT, "speculative_decoding_verification_temp_gb300", "csrc")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "unit_kernel_traffic.json")
+# the ncu summary of the dominant kernel on this workload: its DRAM traffic per
+# launch, valid while the kernel sources hash to the recorded value
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "pass_kernel_b256_g7_v128256_bf16.md")
+# kernels the library launches per chain call on this workload: the pass
+# kernel and the precise-redraw kernel
+LAUNCHES_PER_STEP = 2
 
 
 def dist_env():
@@ -63,15 +68,26 @@ def measured_peak():
 
 
 def recorded_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged."""
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged.
+
+    The summary holds lines "- source_hash: H" and "- dram_bytes_per_launch: N".
+    """
+    rec = {}
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
-    except Exception:
+            for line in f:
+                line = line.strip()
+                if line.startswith("- ") and ":" in line:
+                    key, val = line[2:].split(":", 1)
+                    rec[key.strip()] = val.strip()
+    except OSError:
         return None
     if rec.get("source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    try:
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
@@ -143,7 +159,7 @@ def config_entry(w):
                         "(temperature 1, Zipf logits, draft sigma 0.4)",
             "B": w["B"], "gamma": w["gamma"], "V": w["V"],
             "logit_bytes_per_step": logit_bytes(w),
-            "l2": "inputs larger than L2 (985 MB of logits per step)"}
+            "l2": f"inputs larger than L2 ({logit_bytes(w) / 1e6:.0f} MB of logits per step)"}
 
 
 def logit_bytes(w):
@@ -151,12 +167,24 @@ def logit_bytes(w):
     return (w["B"] * (w["gamma"] + 1) + w["B"] * w["gamma"]) * w["V"] * esize
 
 
+def bench_workload(args):
+    """The timed workload: B = 256, gamma = 7, V = 128256 bf16, or the same
+    recipe with --batch sequences (smaller cases for profiling)."""
+    from speculative_decoding_verification_temp_gb300 import workloads
+    if not args.batch:
+        return workloads.config(WORKLOAD)
+    c = dict(workloads.CONFIGS[WORKLOAD])
+    c.pop("kind")
+    c["B"] = args.batch
+    return workloads.make_chain(seed=1000 + WORKLOAD, **c)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
     from speculative_decoding_verification_temp_gb300 import workloads
-    w = workloads.config(WORKLOAD)
+    w = bench_workload(args)
     n_seqs = args.reference_seqs
     rows_per_step = n_seqs * (w["gamma"] + 1)
     for _ in range(args.warmup):
@@ -194,7 +222,7 @@ def run_ours(args):
     import speculative_decoding_verification_temp_gb300 as sv
     from speculative_decoding_verification_temp_gb300 import workloads
 
-    w = workloads.config(WORKLOAD)
+    w = bench_workload(args)
     B, gamma, V = w["B"], w["gamma"], w["V"]
     seed = w["seed"] + rank  # each rank verifies its own batch
     rows = B * (gamma + 1)
@@ -280,11 +308,13 @@ def run_ours(args):
         "clocks": clk.summary(),
         "e2e": {"value": world * rows / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "unit_kernel", "launch_ms_avg": avg_launch_ms,
+                     "kernel": "pass_kernel (timed per call: pass_kernel + refine_kernel + "
+                               "workspace clear, so achieved is a lower bound)",
+                     "launch_ms_avg": avg_launch_ms,
                      "launch_ms_median": statistics.median(launch_ms)},
         "hbm_gbs_vs_8tbs_nominal": achieved / 8000.0,
     }
@@ -308,6 +338,8 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=256)
     ap.add_argument("--reference-seqs", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per batch (default: the B = 256 workload); for profiling")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
