@@ -1,5 +1,6 @@
 // C ABI of libspecverify: argument checks, workspace layout, launch planning.
 // The operations themselves are documented in include/specverify.h.
+#include <algorithm>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -18,7 +19,8 @@ cudaError_t launch_stream(const Params &P, int esize, size_t smem, cudaStream_t 
 cudaError_t launch_first_child(const int32_t *parent, int T, int N, int32_t *first_child,
                                cudaStream_t stream);
 cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream);
-cudaError_t launch_pass(const Params &P, int esize, size_t smem, cudaStream_t stream);
+cudaError_t launch_pass(const Params &P, int esize, const Exp2Table &tab, size_t smem,
+                        cudaStream_t stream);
 size_t pass_ctl_bytes();
 }  // namespace sv
 
@@ -124,6 +126,12 @@ bool make_pass_plan(long long V, int esize, int gamma, PassPlan &pp) {
   return pp.smem <= kSmemHard;
 }
 
+// Draw-search steps per row of the pass kernel (0: it cannot run the shape).
+long long pass_steps(long long V, int esize, int gamma) {
+  PassPlan pp;
+  return make_pass_plan(V, esize, gamma, pp) ? pp.steps : 0;
+}
+
 // 64-bit records the pass kernel writes for B sequences of gamma drafts.
 long long pass_records(long long B, int gamma, long long V, int esize) {
   PassPlan pp;
@@ -132,16 +140,21 @@ long long pass_records(long long B, int gamma, long long V, int esize) {
 }
 
 struct Layout {
-  size_t wq_ctr, counters, unit_done, w_done, wq, seq_cnt, srec, err, zero_bytes;
-  size_t outs, stats, final_unit, first_child, refine, partials, dstate, wpart, wblk, total;
+  size_t wq_ctr, counters, unit_done, w_done, wq, seq_cnt, srec, err, sctr, near_list, pctr,
+      zero_bytes;
+  size_t pseq, fstep, pstep, ppart;
+  size_t outs, stats, final_unit, first_child, refine, rpart, rc, partials, dstate, wpart, wblk, total;
   long long wq_cap;
 };
 
 constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
 // slices: slices per unit of the streaming kernel, 0 when only the resident
-// kernel can run the shape; recs: records of the chain pass kernel.
-Layout layout(long long nseq, long long units, long long slices, long long recs) {
+// kernel can run the shape; recs: records of the chain pass kernel; psteps:
+// its draw-search steps per row (0 when the pass kernel cannot run the shape).
+Layout layout(long long nseq, long long units, long long slices, long long recs,
+              long long psteps) {
+  const long long pseqs = psteps ? nseq : 0;
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -149,29 +162,55 @@ Layout layout(long long nseq, long long units, long long slices, long long recs)
     off = align_up(off + bytes, 256);
     return at;
   };
-  L.wq_ctr = take(4 * sizeof(uint32_t));  // [0] queue head, [1] tail, [2] units done, [3] refines
+  // A call runs either the streaming kernel or the pass kernel (or neither):
+  // their own regions share addresses, the workspace holds the larger set.
+  // zero prefix, common part
+  // [0] queue head, [1] tail, [2] units done, [3] refines, [4] redraw barrier
+  L.wq_ctr = take(8 * sizeof(uint32_t));
   L.counters = take(static_cast<size_t>(nseq) * sizeof(uint32_t));
-  L.unit_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
-  L.w_done = take(static_cast<size_t>(units) * sizeof(uint32_t));
+  L.err = take(sizeof(uint32_t));
+  const size_t zero_base = off;
+  // zero prefix, streaming kernel
+  L.unit_done = take(static_cast<size_t>(slices ? units : 0) * sizeof(uint32_t));
+  L.w_done = take(static_cast<size_t>(slices ? units : 0) * sizeof(uint32_t));
   // weight-task queue: a tree of N nodes runs at most (N - 1) + 2N weight
   // rounds in all (one per rejected child, plus a degenerate fallback and the
   // final draw at each node), one entry per slice
   L.wq_cap = 3 * units * slices;
   L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
+  const size_t zero_stream = off;
+  // zero prefix, pass kernel
+  off = zero_base;
   L.seq_cnt = take(static_cast<size_t>(recs ? nseq : 0) * sizeof(uint32_t));
   L.srec = take(static_cast<size_t>(recs) * sizeof(unsigned long long));  // zero = not written
-  L.err = take(sizeof(uint32_t));
+  L.sctr = take(static_cast<size_t>(pseqs) * 4 * sizeof(uint32_t));
+  L.near_list = take(static_cast<size_t>(pseqs) * sizeof(int32_t));
+  L.pseq = take(static_cast<size_t>(pseqs) * (sizeof(sv::PassSeq) / 4) * 8);
+  L.fstep = take(static_cast<size_t>(pseqs * psteps) * 8);
+  L.pctr = take(4 * sizeof(uint32_t));
+  off = std::max(off, zero_stream);
   L.zero_bytes = off;
+  // common
   L.outs = take(static_cast<size_t>(units) * sizeof(sv::UnitOut));
   L.stats = take(static_cast<size_t>(units) * sizeof(sv::UnitStats));
   L.final_unit = take(static_cast<size_t>(nseq) * sizeof(int32_t));
   L.first_child = take(static_cast<size_t>(units) * sizeof(int32_t));
   L.refine = take(static_cast<size_t>(nseq) * sizeof(int4));
+  L.rpart = take(static_cast<size_t>(std::max<long long>(sv::kRefineMaxGrid, nseq)) *
+                 sizeof(sv::RefinePart));
+  L.rc = take(static_cast<size_t>(nseq) * sizeof(double));
+  const size_t base = off;
+  // streaming kernel
   L.partials = take(static_cast<size_t>(units * slices * 2) * sizeof(sv::SlicePartial));
   L.dstate = take(static_cast<size_t>(slices ? units : 0) * sizeof(sv::DrawState));
   L.wpart = take(static_cast<size_t>(units * slices) * sizeof(float));
   L.wblk = take(static_cast<size_t>(units * slices * kMaxSliceBlocks) * sizeof(float));
-  L.total = off;
+  const size_t end_stream = off;
+  // pass kernel
+  off = base;
+  L.pstep = take(static_cast<size_t>(pseqs * psteps) * sizeof(double));
+  L.ppart = take(static_cast<size_t>(pseqs) * sv::kPassPreciseJobs * 2 * sizeof(double));
+  L.total = std::max(off, end_stream);
   return L;
 }
 
@@ -223,11 +262,12 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   // the caller's workspace must hold what the size query promised for the shape
   const size_t promised =
       layout(P.nseq, n_units, stream_slices(P.V, esize),
-             P.mode == sv::kModeChain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0)
+             P.mode == sv::kModeChain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0,
+             P.mode == sv::kModeChain ? pass_steps(P.V, esize, P.gamma) : 0)
           .total;
   if (workspace_bytes < promised) return SPEC_ERR_INVALID_ARG;
   const long long recs = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr * 8 : 0;
-  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs);
+  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs, pass ? pp.steps : 0);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
   cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, stream);
@@ -238,6 +278,10 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   P.final_unit = reinterpret_cast<int32_t *>(ws + L.final_unit);
   P.refine = reinterpret_cast<int4 *>(ws + L.refine);
   P.refine_ctr = reinterpret_cast<uint32_t *>(ws + L.wq_ctr) + 3;
+  P.rbar = reinterpret_cast<uint32_t *>(ws + L.wq_ctr) + 4;
+  P.rpart = reinterpret_cast<sv::RefinePart *>(ws + L.rpart);
+  P.rc = reinterpret_cast<double *>(ws + L.rc);
+  P.err = reinterpret_cast<uint32_t *>(ws + L.err);
   P.n_units = static_cast<int>(n_units);
   if (pass) {
     P.ring = pp.ring;
@@ -248,8 +292,14 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.steps = pp.steps;
     P.srec = reinterpret_cast<unsigned long long *>(ws + L.srec);
     P.seq_cnt = reinterpret_cast<uint32_t *>(ws + L.seq_cnt);
-    P.err = reinterpret_cast<uint32_t *>(ws + L.err);
-    e = sv::launch_pass(P, esize, pp.smem, stream);
+    P.pseqw = reinterpret_cast<unsigned long long *>(ws + L.pseq);
+    P.sctr = reinterpret_cast<uint32_t *>(ws + L.sctr);
+    P.fstep = reinterpret_cast<unsigned long long *>(ws + L.fstep);
+    P.pstep = reinterpret_cast<double *>(ws + L.pstep);
+    P.ppart = reinterpret_cast<double *>(ws + L.ppart);
+    P.near_list = reinterpret_cast<int32_t *>(ws + L.near_list);
+    P.pctr = reinterpret_cast<uint32_t *>(ws + L.pctr);
+    e = sv::launch_pass(P, esize, exp2_table(), pp.smem, stream);
   } else if (streaming) {
     P.slice = sp.slice;
     P.cluster = sp.slices;
@@ -287,8 +337,10 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
   }
   if (e != cudaSuccess) return map_cuda(e);
-  e = sv::launch_refine(P, esize, exp2_table(), stream);
-  if (e != cudaSuccess) return map_cuda(e);
+  if (!pass) {  // the pass kernel redraws near-boundary draws itself
+    e = sv::launch_refine(P, esize, exp2_table(), stream);
+    if (e != cudaSuccess) return map_cuda(e);
+  }
   if (out_residual) {
     e = sv::launch_residual(P, esize, out_residual, stream);
     if (e != cudaSuccess) return map_cuda(e);
@@ -314,14 +366,14 @@ size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtyp
   const int esize = esize_of(dtype);
   if (B < 0 || gamma < 0 || V < 1 || esize == 0) return 0;
   return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize),
-                pass_records(B, gamma, V, esize))
+                pass_records(B, gamma, V, esize), pass_steps(V, esize, gamma))
       .total;
 }
 
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
-  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0).total;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0, 0).total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

@@ -5,164 +5,112 @@
 // the normalisers and the running sums moves every boundary of that inverse
 // CDF by up to a few 1e-7 of the probability mass, so when u * Z lands that
 // close to a boundary the single-precision token can differ from the exact
-// one.  Those draws are flagged (UnitOut::near) and queued by the path
-// stitching; this kernel recomputes each queued draw with double-float weights
-// (relative error below 1e-11) and double-precision sums, and overwrites the
-// token.
+// one.  Those draws are flagged (UnitOut::near) and queued; this kernel
+// recomputes each queued draw with double-float weights (relative error below
+// 1e-11) and double-precision sums, and overwrites the token.
 //
-// One thread-block cluster of 16 CTAs per queued draw, in a loop over the
-// queue.  For a residual [p - c q]_+ the passes over the row pair are:
-//   1. S_p, S_q: the softmax normalisers;
-//   2. for a tree node whose held residual came after n > 1 rejections, the
-//      multipliers c_1 = 1, c_{s+1} = c_s + W_s with W_s the total of
-//      [p - c_s q]_+ (one pass each);
-//   3. the weights of the final distribution, per-warp and per-CTA totals;
-// then the inverse-CDF search: CTA, warp, then one warp scans its range.
-// A draw from p itself needs only pass 3.  Rows are read from global memory
-// in groups of 8 entries (16-byte loads when the rows are aligned): this path
-// runs for a few percent of the draws.
-#include <cooperative_groups.h>
-
+// The whole grid works on the queue at once: with `count` queued draws and G
+// CTAs, each draw's vocabulary is cut into S = max(1, G / count) slices and
+// work unit u (draw u / S, slice u % S) goes to CTA u mod G.  Phases are
+// separated by a grid barrier (the launch is cooperative, so every CTA is
+// resident; each wait is bounded):
+//   A. for a residual [p - c q]_+: each unit's share of the softmax
+//      normalisers S_p, S_q;
+//   R. for a tree node whose held residual came after n > 1 rejections, the
+//      multipliers c_1 = 1, c_{s+1} = c_s + W_s / S_p with W_s the total of
+//      [e_p - c_s (S_p / S_q) e_q]_+ (two barriers per round);
+//   B. the final weights: per-warp totals and last positive entries of each
+//      unit, published in the workspace;
+//   C. every unit sums its draw's slice totals in the same fixed order (so all
+//      of them see the same Z), finds the owning slice and, if it owns it,
+//      the owning warp, which scans its range with a warp prefix sum.
+// A draw from p itself needs only B and C.  Rows are read from global memory
+// in groups of 8 entries (16-byte loads when the rows are aligned).
 #include "ops.cuh"
-#include "precise.cuh"
-#include "verify_units.cuh"
+#include "precise_row.cuh"
 
 namespace sv {
 
-namespace cg = cooperative_groups;
-
-constexpr int kRefineCluster = 16;
-
-struct HpRow {
-  float m;         // row maximum
-  float khi, klo;  // log2(e) / T as a double-float
-  float thr;       // top-k threshold (-inf: none)
-};
-
-__device__ __forceinline__ HpRow hp_row(const RowDesc &d, float T) {
-  HpRow r;
-  r.m = d.m;
-  const Df k = df_from_double(1.44269504088896340735992468100189 / static_cast<double>(T));
-  r.khi = k.hi;
-  r.klo = k.lo;
-  r.thr = d.thr;
-  return r;
-}
-
-// exp((z - max) / T) as a double-float; 0 below the top-k threshold.
-__device__ __forceinline__ Df hp_exp(const HpRow &r, float z, const float *th, const float *tl) {
-  if (!(z > -INFINITY) || z < r.thr) return Df{0.f, 0.f};
-  float dh, dl;
-  two_sum(z, -r.m, dh, dl);  // z - max exactly
-  const float t_hi = __fmul_rn(dh, r.khi);
-  const float t_lo =
-      __fadd_rn(fmaf(dh, r.khi, -t_hi), fmaf(dh, r.klo, __fmul_rn(dl, r.khi)));
-  return df_exp2(df_norm(t_hi, t_lo), th, tl);
-}
+constexpr long long kRefineWaitNs = 2000000000ll;  // give up a barrier after about 2 s
 
 struct RefineSmem {
   float tab_hi[64], tab_lo[64];
-  double wsum[2][kWarps];
-  int wlast[kWarps];
-  double cta[2];   // this CTA's totals, read by the cluster
-  int cta_last;    // this CTA's last positive index (-1: none)
+  double red[2][kWarps];
+  int redi[kWarps];
   int count;
+  int nres_max;
+  int any_residual;
+  int abort;
   int token;
+  int owner_warp;
+  double wt;
 };
 
-// Sum of (a, b) over the cluster; every thread gets the same values.
-__device__ void cluster_sum2(double a, double b, double &A, double &B, RefineSmem &sm,
-                             cg::cluster_group &cl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    a += __shfl_xor_sync(0xFFFFFFFFu, a, off);
-    b += __shfl_xor_sync(0xFFFFFFFFu, b, off);
-  }
-  if (lane == 0) {
-    sm.wsum[0][warp] = a;
-    sm.wsum[1][warp] = b;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double ta = 0.0, tb = 0.0;
-    for (int w = 0; w < kWarps; ++w) {
-      ta += sm.wsum[0][w];
-      tb += sm.wsum[1][w];
-    }
-    sm.cta[0] = ta;
-    sm.cta[1] = tb;
-  }
-  cl.sync();
-  A = 0.0;
-  B = 0.0;
-  for (int r = 0; r < kRefineCluster; ++r) {
-    const double *x = cl.map_shared_rank(sm.cta, r);
-    A += x[0];
-    B += x[1];
-  }
-  cl.sync();
-}
-
+// One queued draw and the rows it is taken from.
 template <typename TE>
-struct RefineRows {
+struct RefineItem {
+  int seq, unit, pos;
+  int node;      // the node drawn at (its id keys the draw uniform)
+  int residual;  // weights [e_p - rho e_q]_+ (else e_p)
+  int n_res;
   const TE *gp, *gq;
   HpRow rp, rq;
-  int residual;
-  int vec;  // both rows start on 16-byte boundaries
-  Df rho;   // c S_p / S_q: the weight is [e_p - rho e_q]_+
+  int vec;       // both rows start on 16-byte boundaries
 };
 
-// Logits of the 8 entries from `base` (a multiple of 8); -inf at or past `end`.
 template <typename TE>
-__device__ __forceinline__ void load8z(const TE *g, int base, int end, bool vec, float z[8]) {
-  if (vec && base + 8 <= end) {
-    if (sizeof(TE) == 2) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(g + base);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        z[2 * i] = __uint_as_float(ws[i] << 16);
-        z[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
-      }
-    } else {
-      const float4 a = *reinterpret_cast<const float4 *>(g + base);
-      const float4 b = *reinterpret_cast<const float4 *>(g + base + 4);
-      z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
-      z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
-    }
-    return;
+__device__ RefineItem<TE> load_item(const Params &P, int item) {
+  const int4 q = P.refine[item];
+  RefineItem<TE> it;
+  it.seq = q.x;
+  it.unit = q.y;
+  it.pos = q.z;
+  const UnitStats st = P.stats[it.unit];
+  const int node = st.node;
+  it.node = node;
+  long long prow, qrow;
+  if (P.mode == kModeChain) {
+    prow = static_cast<long long>(it.seq) * (P.gamma + 1) + node;
+    qrow = static_cast<long long>(it.seq) * P.gamma + node;
+  } else {
+    prow = qrow = static_cast<long long>(it.seq) * P.ups + node;
   }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) z[e] = base + e < end ? to_f32(g[base + e]) : -INFINITY;
+  it.gp = static_cast<const TE *>(row_ptr(P.target, prow, P.ld_t, sizeof(TE)));
+  it.gq = static_cast<const TE *>(row_ptr(P.draft, qrow, P.ld_d, sizeof(TE)));
+  it.rp = hp_row(st.p, __ldg(P.Tp + it.seq));
+  it.residual = st.c > 0.f && st.n_res > 0;
+  it.n_res = it.residual ? st.n_res : 0;
+  it.rq = it.residual ? hp_row(st.q, __ldg(P.Tq + it.seq)) : it.rp;
+  it.vec = ((reinterpret_cast<uintptr_t>(it.gp) | reinterpret_cast<uintptr_t>(it.gq)) & 15u) == 0;
+  return it;
 }
 
-// Weights of the 8 entries from `base` (0 at or past `end`).
+// Weights of the 8 entries from `base` (0 at or past `end`); rho = c S_p / S_q.
 template <typename TE>
-__device__ __forceinline__ void hp_weight8(const RefineRows<TE> &R, int base, int end,
+__device__ __forceinline__ void hp_weight8(const RefineItem<TE> &it, Df rho, int base, int end,
                                            const RefineSmem &sm, Df w[8]) {
   float zp[8], zq[8];
-  load8z<TE>(R.gp, base, end, R.vec, zp);
-  if (R.residual) load8z<TE>(R.gq, base, end, R.vec, zq);
+  hp_load8<TE>(it.gp, base, end, it.vec, zp);
+  if (it.residual) hp_load8<TE>(it.gq, base, end, it.vec, zq);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const Df ep = hp_exp(R.rp, zp[e], sm.tab_hi, sm.tab_lo);
-    if (!R.residual || ep.hi == 0.f) {
+    const Df ep = hp_exp(it.rp, zp[e], sm.tab_hi, sm.tab_lo);
+    if (!it.residual || ep.hi == 0.f) {
       w[e] = ep;
       continue;
     }
-    const Df eq = hp_exp(R.rq, zq[e], sm.tab_hi, sm.tab_lo);
-    const Df d = df_sub(ep, df_mul(R.rho, eq));
+    const Df eq = hp_exp(it.rq, zq[e], sm.tab_hi, sm.tab_lo);
+    const Df d = df_sub(ep, df_mul(rho, eq));
     w[e] = d.hi > 0.f ? d : Df{0.f, 0.f};
   }
 }
 
-// Sum of the 8 weights from `base` (entries at or past `end` are 0).
+// Sum of the 8 weights from `base`; `lastpos` becomes the last positive entry.
 template <typename TE>
-__device__ __forceinline__ double step_sum(const RefineRows<TE> &R, int base, int end,
+__device__ __forceinline__ double step_sum(const RefineItem<TE> &it, Df rho, int base, int end,
                                            const RefineSmem &sm, int &lastpos) {
   Df w[8];
-  hp_weight8(R, base, end, sm, w);
+  hp_weight8(it, rho, base, end, sm, w);
   Df s{0.f, 0.f};
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -172,14 +120,104 @@ __device__ __forceinline__ double step_sum(const RefineRows<TE> &R, int base, in
   return df_to_double(s);
 }
 
+// Vocabulary range of slice k of S, and warp w's contiguous part of it (whole
+// groups of 256 entries, so each lane's groups of 8 stay aligned).
+struct SliceRange {
+  int v0, v1, ws, we;
+};
+
+__device__ __forceinline__ SliceRange slice_range(int V, int S, int k, int warp) {
+  SliceRange r;
+  const int Ls = ((V + S - 1) / S + 7) / 8 * 8;
+  r.v0 = min(V, k * Ls);
+  r.v1 = min(V, r.v0 + Ls);
+  const int Lw = ((Ls + kWarps - 1) / kWarps + 255) / 256 * 256;
+  r.ws = min(r.v1, r.v0 + warp * Lw);
+  r.we = min(r.v1, r.ws + Lw);
+  return r;
+}
+
+// Sum over the block of two doubles (thread 0 gets the totals).
+__device__ __forceinline__ void block_sum2(double &a, double &b, RefineSmem &sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_xor_sync(0xFFFFFFFFu, a, off);
+    b += __shfl_xor_sync(0xFFFFFFFFu, b, off);
+  }
+  if (lane == 0) {
+    sm.red[0][warp] = a;
+    sm.red[1][warp] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a = 0.0;
+    b = 0.0;
+    for (int w = 0; w < kWarps; ++w) {
+      a += sm.red[0][w];
+      b += sm.red[1][w];
+    }
+  }
+  __syncthreads();
+}
+
+// Grid barrier number `idx` (0, 1, ...): every CTA adds one to the counter and
+// waits until all G have added for this barrier.  Bounded: a wait that runs out
+// sets error bit 1 and makes the CTA stop working on the queue.
+__device__ bool grid_barrier(const Params &P, RefineSmem &sm, int idx) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.rbar) : "memory");
+    const uint32_t target = static_cast<uint32_t>(gridDim.x) * static_cast<uint32_t>(idx + 1);
+    long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    int ok = 1;
+    while (true) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.rbar) : "memory");
+      if (v >= target) break;
+      long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > kRefineWaitNs) {
+        ok = 0;
+        atomicOr(P.err, 2u);
+        break;
+      }
+      __nanosleep(64);
+    }
+    sm.abort = ok ? 0 : 1;
+  }
+  __syncthreads();
+  return sm.abort == 0;
+}
+
+// Sum over the S units of a draw of one field: lane-strided partial sums and a
+// shuffle tree, then lane 0's value for every lane, so each warp of each CTA
+// gets the same bits.
+template <typename F>
+__device__ __forceinline__ double units_sum(int S, F field) {
+  const int lane = threadIdx.x & 31;
+  double s = 0.0;
+  for (int k = lane; k < S; k += 32) s += field(k);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  return __shfl_sync(0xFFFFFFFFu, s, 0);
+}
+
+// (S_p, S_q) of a draw: the sum of its units' phase-A partials.
+__device__ __forceinline__ void item_normalisers(const Params &P, int item, int S, double &Sp,
+                                                 double &Sq) {
+  const RefinePart *x = P.rpart + static_cast<long long>(item) * S;
+  Sp = units_sum(S, [&](int k) { return __ldcg(&x[k].a); });
+  Sq = units_sum(S, [&](int k) { return __ldcg(&x[k].b); });
+}
+
 template <typename TE>
-__global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kThreads)
-    refine_kernel(const Params P, const Exp2Table tab) {
+__global__ void __launch_bounds__(kThreads) refine_kernel(const Params P, const Exp2Table tab) {
   __shared__ RefineSmem sm;
-  cg::cluster_group cl = cg::this_cluster();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rank = static_cast<int>(cl.block_rank());
-  const int cid = blockIdx.x / kRefineCluster, G = gridDim.x / kRefineCluster;
+  const int G = gridDim.x;
   for (int i = tid; i < 64; i += kThreads) {
     sm.tab_hi[i] = tab.hi[i];
     sm.tab_lo[i] = tab.lo[i];
@@ -188,192 +226,271 @@ __global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kThread
                               P.nseq);
   __syncthreads();
   const int count = sm.count;
+  if (count <= 0) return;  // the same decision in every CTA
   const int V = P.V;
-  // this CTA's range, and each warp's contiguous part of it
-  const int Ls = ((V + kRefineCluster - 1) / kRefineCluster + 7) / 8 * 8;
-  const int v0 = min(V, rank * Ls), v1 = min(V, v0 + Ls);
-  const int Lw = ((Ls + kWarps - 1) / kWarps + 255) / 256 * 256;
-  const int ws = min(v1, v0 + warp * Lw), we = min(v1, ws + Lw);
-
-  for (int item = cid; item < count; item += G) {
-    const int4 it = P.refine[item];
-    const int seq = it.x, unit = it.y, pos = it.z;
-    const UnitStats st = P.stats[unit];
-    const int node = st.node;
-    long long prow, qrow;
-    if (P.mode == kModeChain) {
-      prow = static_cast<long long>(seq) * (P.gamma + 1) + node;
-      qrow = static_cast<long long>(seq) * P.gamma + node;
-    } else {
-      prow = qrow = static_cast<long long>(seq) * P.ups + node;
+  const int S = max(1, G / count);
+  const int U = count * S;
+  // the largest residual round count and whether any draw is a residual
+  {
+    int nr = 0, anyr = 0;
+    for (int item = tid; item < count; item += kThreads) {
+      const UnitStats st = P.stats[P.refine[item].y];
+      if (st.c > 0.f && st.n_res > 0) {
+        anyr = 1;
+        nr = max(nr, st.n_res);
+      }
     }
-    RefineRows<TE> R;
-    R.gp = static_cast<const TE *>(row_ptr(P.target, prow, P.ld_t, sizeof(TE)));
-    R.gq = static_cast<const TE *>(row_ptr(P.draft, qrow, P.ld_d, sizeof(TE)));
-    R.rp = hp_row(st.p, __ldg(P.Tp + seq));
-    R.residual = st.c > 0.f && st.n_res > 0;
-    R.vec = ((reinterpret_cast<uintptr_t>(R.gp) | reinterpret_cast<uintptr_t>(R.gq)) & 15u) == 0;
-    R.rho = Df{0.f, 0.f};
-    if (R.residual) {
-      R.rq = hp_row(st.q, __ldg(P.Tq + seq));
-      // pass 1: the normalisers
+    nr = warp_max_i(nr);
+    anyr = warp_max_i(anyr);
+    if (lane == 0) {
+      sm.redi[warp] = nr;
+      sm.red[0][warp] = anyr;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int a = 0, b = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        a = max(a, sm.redi[w]);
+        b = max(b, static_cast<int>(sm.red[0][w]));
+      }
+      sm.nres_max = a;
+      sm.any_residual = b;
+    }
+    __syncthreads();
+  }
+  const int nres_max = sm.nres_max;
+  int bar = 0;
+  // A: shares of the softmax normalisers of residual draws
+  if (sm.any_residual) {
+    for (int u = blockIdx.x; u < U; u += G) {
+      const int item = u / S, k = u - item * S;
+      const RefineItem<TE> it = load_item<TE>(P, item);
+      if (!it.residual) continue;
+      const SliceRange r = slice_range(V, S, k, warp);
       Df sp{0.f, 0.f}, sq{0.f, 0.f};
-      for (int base = ws + lane * 8; base < we; base += 256) {
+#pragma unroll 4
+      for (int base = r.ws + lane * 8; base < r.we; base += 256) {
         float zp[8], zq[8];
-        load8z<TE>(R.gp, base, we, R.vec, zp);
-        load8z<TE>(R.gq, base, we, R.vec, zq);
+        hp_load8<TE>(it.gp, base, r.we, it.vec, zp);
+        hp_load8<TE>(it.gq, base, r.we, it.vec, zq);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          sp = df_add(sp, hp_exp(R.rp, zp[e], sm.tab_hi, sm.tab_lo));
-          sq = df_add(sq, hp_exp(R.rq, zq[e], sm.tab_hi, sm.tab_lo));
+          sp = df_add(sp, hp_exp(it.rp, zp[e], sm.tab_hi, sm.tab_lo));
+          sq = df_add(sq, hp_exp(it.rq, zq[e], sm.tab_hi, sm.tab_lo));
         }
       }
-      double Sp, Sq;
-      cluster_sum2(df_to_double(sp), df_to_double(sq), Sp, Sq, sm, cl);
-      // pass 2: the multiplier of the held residual
-      double c = 1.0;
-      for (int s = 1; s < st.n_res; ++s) {
-        R.rho = df_from_double(c * Sp / Sq);
-        double part = 0.0;
-        int lp = -1;
-        for (int base = ws + lane * 8; base < we; base += 256) part += step_sum(R, base, we, sm, lp);
-        double W, unused;
-        cluster_sum2(part, 0.0, W, unused, sm, cl);
-        c += W / Sp;
+      double a = df_to_double(sp), b = df_to_double(sq);
+      block_sum2(a, b, sm);
+      if (tid == 0) {
+        P.rpart[u].a = a;
+        P.rpart[u].b = b;
+        if (k == 0) P.rc[item] = 1.0;
       }
-      R.rho = df_from_double(c * Sp / Sq);
     }
-    // pass 3: weights of the final distribution, per-warp and per-CTA totals
+    if (!grid_barrier(P, sm, bar++)) return;
+  }
+  // R: multipliers of residuals held after several rejections (trees)
+  for (int s = 1; s < nres_max; ++s) {
+    for (int u = blockIdx.x; u < U; u += G) {
+      const int item = u / S, k = u - item * S;
+      const RefineItem<TE> it = load_item<TE>(P, item);
+      if (!it.residual || s >= it.n_res) continue;
+      double Sp, Sq;
+      item_normalisers(P, item, S, Sp, Sq);
+      const Df rho = df_from_double(__ldcg(P.rc + item) * Sp / Sq);
+      const SliceRange r = slice_range(V, S, k, warp);
+      double part = 0.0, unused = 0.0;
+      int lp = -1;
+#pragma unroll 4
+      for (int base = r.ws + lane * 8; base < r.we; base += 256)
+        part += step_sum(it, rho, base, r.we, sm, lp);
+      block_sum2(part, unused, sm);
+      if (tid == 0) P.rpart[u].rw = part;
+    }
+    if (!grid_barrier(P, sm, bar++)) return;
+    for (int item = blockIdx.x; item < count && warp == 0; item += G) {
+      const UnitStats st = P.stats[P.refine[item].y];
+      if (!(st.c > 0.f && st.n_res > 0) || s >= st.n_res) continue;
+      double Sp, Sq;
+      item_normalisers(P, item, S, Sp, Sq);
+      const RefinePart *x = P.rpart + static_cast<long long>(item) * S;
+      const double W = units_sum(S, [&](int k) { return __ldcg(&x[k].rw); });
+      if (lane == 0) P.rc[item] = __ldcg(P.rc + item) + W / Sp;
+    }
+    if (!grid_barrier(P, sm, bar++)) return;
+  }
+  // B: final weights, per-warp totals of each unit
+  for (int u = blockIdx.x; u < U; u += G) {
+    const int item = u / S, k = u - item * S;
+    const RefineItem<TE> it = load_item<TE>(P, item);
+    Df rho{0.f, 0.f};
+    if (it.residual) {
+      double Sp, Sq;
+      item_normalisers(P, item, S, Sp, Sq);
+      rho = df_from_double(__ldcg(P.rc + item) * Sp / Sq);
+    }
+    const SliceRange r = slice_range(V, S, k, warp);
     double part = 0.0;
     int lp = -1;
-    for (int base = ws + lane * 8; base < we; base += 256) part += step_sum(R, base, we, sm, lp);
+#pragma unroll 4
+    for (int base = r.ws + lane * 8; base < r.we; base += 256)
+      part += step_sum(it, rho, base, r.we, sm, lp);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
       lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, off));
     }
     if (lane == 0) {
-      sm.wsum[0][warp] = part;
-      sm.wlast[warp] = lp;
+      P.rpart[u].warp[warp] = part;
+      P.rpart[u].wlast[warp] = lp;
+      sm.red[0][warp] = part;
+      sm.redi[warp] = lp;
     }
     __syncthreads();
     if (tid == 0) {
       double t = 0.0;
       int l = -1;
       for (int w = 0; w < kWarps; ++w) {
-        t += sm.wsum[0][w];
-        l = max(l, sm.wlast[w]);
+        t += sm.red[0][w];
+        l = max(l, sm.redi[w]);
       }
-      sm.cta[0] = t;
-      sm.cta_last = l;
+      P.rpart[u].w = t;
+      P.rpart[u].last = l;
     }
-    cl.sync();
-    // the owning CTA: the same prefix in every CTA
-    const double u = static_cast<double>(unit_uniform(P, seq, node, 1));
-    double Z = 0.0;
-    double totals[kRefineCluster];
-    int lasts[kRefineCluster];
-    for (int r = 0; r < kRefineCluster; ++r) {
-      RefineSmem *o = cl.map_shared_rank(&sm, r);
-      totals[r] = o->cta[0];
-      lasts[r] = o->cta_last;
-      Z += totals[r];
-    }
-    const double t = u * Z;
-    int owner = -1;
-    double trel = 0.0;
-    {
-      double acc = 0.0;
-      for (int r = 0; r < kRefineCluster; ++r) {
-        if (acc + totals[r] > t) {
-          owner = r;
-          trel = t - acc;
-          break;
-        }
-        acc += totals[r];
+    __syncthreads();
+  }
+  if (!grid_barrier(P, sm, bar++)) return;
+  // C: the owning slice, warp and entry
+  for (int u = blockIdx.x; u < U; u += G) {
+    const int item = u / S, k = u - item * S;
+    const RefineItem<TE> it = load_item<TE>(P, item);
+    if (warp == 0) {
+      // the owning slice: lanes hold contiguous runs of slices, a warp scan
+      // of the run totals finds the lane, that lane walks its run
+      const RefinePart *parts = P.rpart + static_cast<long long>(item) * S;
+      const int per = (S + 31) / 32;
+      const int s0 = min(S, lane * per), s1 = min(S, s0 + per);
+      double seg = 0.0;
+      int lastslice = -1;
+      for (int x = s0; x < s1; ++x) {
+        seg += __ldcg(&parts[x].w);
+        if (__ldcg(&parts[x].last) >= 0) lastslice = x;
       }
-    }
-    bool fallback = false;
-    if (owner < 0) {
-      fallback = true;
-      for (int r = kRefineCluster - 1; r >= 0; --r)
-        if (lasts[r] >= 0) {
-          owner = r;
-          break;
-        }
-    }
-    cl.sync();  // every DSMEM read of this item is done
-    if (rank == owner) {
-      if (tid == 0) {
-        int tok = sm.cta_last;
-        int ow = -1;
-        double wt = 0.0;
-        if (!fallback) {
-          double acc = 0.0;
-          for (int w = 0; w < kWarps; ++w) {
-            if (acc + sm.wsum[0][w] > trel) {
-              ow = w;
-              wt = trel - acc;
+      double incl = seg;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const double Z = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      const double t = static_cast<double>(unit_uniform(P, it.seq, it.node, 1)) * Z;
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > t && seg > 0.0);
+      int owner = -1;
+      double trel = 0.0;
+      if (hit) {
+        const int first = __ffs(hit) - 1;
+        if (lane == first) {
+          double acc = incl - seg;
+          for (int x = s0; x < s1; ++x) {
+            const double tx = __ldcg(&parts[x].w);
+            if (acc + tx > t && tx > 0.0) {
+              owner = x;
+              trel = t - acc;
               break;
             }
-            acc += sm.wsum[0][w];
+            acc += tx;
           }
         }
-        sm.token = ow < 0 ? tok : -1 - ow;  // >= 0: decided; else the warp to scan
-        sm.wsum[1][0] = wt;
+        owner = __shfl_sync(0xFFFFFFFFu, owner, first);
+        trel = __shfl_sync(0xFFFFFFFFu, trel, first);
       }
-      __syncthreads();
-      const int code = sm.token;
-      if (code < 0 && warp == -1 - code) {
-        const double wt = sm.wsum[1][0];
-        double base_sum = 0.0;
-        int result = -1;
-        for (int rb = ws; rb < we && result < 0; rb += 256) {
-          const int base = rb + lane * 8;
-          Df wd[8];
-          hp_weight8(R, base, we, sm, wd);
-          double w[8];
-          double s = 0.0;
-          int lpos = -1;
+      int token = -2;  // -2: not this unit's; -1: scan warp sm.owner_warp
+      if (owner < 0) {
+        // rounding left no entry above u * Z: the last slice with a positive entry
+        const int fb = warp_max_i(lastslice);
+        if (fb == k) token = __ldcg(&parts[k].last);
+      } else if (owner == k) {
+        // the owning warp: a scan of the unit's eight warp totals
+        const double x = lane < kWarps ? __ldcg(&parts[k].warp[lane]) : 0.0;
+        double wi = x;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            w[e] = df_to_double(wd[e]);
-            s += w[e];
-            if (w[e] > 0.0) lpos = base + e;
+        for (int off = 1; off < 32; off <<= 1) {
+          const double y = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+          if (lane >= off) wi += y;
+        }
+        const unsigned wh = __ballot_sync(0xFFFFFFFFu, lane < kWarps && wi > trel);
+        if (wh) {
+          const int ow = __ffs(wh) - 1;
+          const double wt = trel - __shfl_sync(0xFFFFFFFFu, wi - x, ow);
+          token = -1;
+          if (lane == 0) {
+            sm.owner_warp = ow;
+            sm.wt = wt;
           }
-          double incl = s;
+        } else {
+          token = __ldcg(&parts[k].last);
+        }
+      }
+      if (lane == 0) sm.token = token;
+    }
+    __syncthreads();
+    if (sm.token == -1 && warp == sm.owner_warp) {
+      const double wt = sm.wt;
+      const SliceRange r = slice_range(V, S, k, warp);
+      Df rho{0.f, 0.f};
+      if (it.residual) {
+        double Sp, Sq;
+        item_normalisers(P, item, S, Sp, Sq);
+        rho = df_from_double(__ldcg(P.rc + item) * Sp / Sq);
+      }
+      double base_sum = 0.0;
+      int result = -1;
+      for (int rb = r.ws; rb < r.we && result < 0; rb += 256) {
+        const int base = rb + lane * 8;
+        Df wd[8];
+        hp_weight8(it, rho, base, r.we, sm, wd);
+        double w[8];
+        double s = 0.0;
+        int lpos = -1;
 #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const double x = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-            if (lane >= off) incl += x;
-          }
-          double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-          if (lane == 0) excl = 0.0;
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, base_sum + incl > wt);
-          if (hit) {
-            const int first = __ffs(hit) - 1;
-            int found = -1;
-            if (lane == first) {
-              double run = base_sum + excl;
+        for (int e = 0; e < 8; ++e) {
+          w[e] = df_to_double(wd[e]);
+          s += w[e];
+          if (w[e] > 0.0) lpos = base + e;
+        }
+        double incl = s;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                run += w[e];
-                if (found < 0 && w[e] > 0.0 && run > wt) found = base + e;
-              }
-              if (found < 0) found = lpos;
+        for (int off = 1; off < 32; off <<= 1) {
+          const double x = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += x;
+        }
+        double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+        if (lane == 0) excl = 0.0;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, base_sum + incl > wt);
+        if (hit) {
+          const int first = __ffs(hit) - 1;
+          int found = -1;
+          if (lane == first) {
+            double run = base_sum + excl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              run += w[e];
+              if (found < 0 && w[e] > 0.0 && run > wt) found = base + e;
             }
-            result = __shfl_sync(0xFFFFFFFFu, found, first);
+            if (found < 0) found = lpos;
           }
-          base_sum += __shfl_sync(0xFFFFFFFFu, incl, 31);
+          result = __shfl_sync(0xFFFFFFFFu, found, first);
         }
-        if (lane == 0) sm.token = result >= 0 ? result : sm.wlast[warp];
+        base_sum += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
-      __syncthreads();
-      if (tid == 0 && sm.token >= 0) {
-        const int width = P.mode == kModeChain ? P.gamma + 1 : P.max_depth + 1;
-        P.outs[unit].token = sm.token;
-        P.out_tokens[static_cast<long long>(seq) * width + pos] = sm.token;
-      }
+      if (lane == 0)
+        sm.token = result >= 0 ? result : __ldcg(&P.rpart[u].wlast[warp]);
+    }
+    __syncthreads();
+    if (tid == 0 && sm.token >= 0) {
+      const int width = P.mode == kModeChain ? P.gamma + 1 : P.max_depth + 1;
+      P.outs[it.unit].token = sm.token;
+      P.out_tokens[static_cast<long long>(it.seq) * width + it.pos] = sm.token;
     }
     __syncthreads();
   }
@@ -381,16 +498,23 @@ __global__ void __cluster_dims__(kRefineCluster, 1, 1) __launch_bounds__(kThread
 
 template <typename TE>
 cudaError_t launch_refine_t(const Params &P, const Exp2Table &tab, cudaStream_t stream) {
-  static bool attr_set = false;  // clusters of 16 need the non-portable size opt-in
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        refine_kernel<TE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  static int cached_dev = -1, cached_blocks = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != cached_dev) {
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, refine_kernel<TE>, kThreads, 0);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cached_blocks = min(kRefineMaxGrid, min(per_sm, 2) * sms);
+    cached_dev = dev;
   }
-  const int G = P.nseq < 9 ? P.nseq : 9;  // 144 CTAs: one wave on 152 SMs
-  refine_kernel<TE><<<dim3(G * kRefineCluster), kThreads, 0, stream>>>(P, tab);
-  return cudaGetLastError();
+  void *args[] = {const_cast<Params *>(&P), const_cast<Exp2Table *>(&tab)};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(refine_kernel<TE>),
+                                     dim3(cached_blocks), dim3(kThreads), args, 0, stream);
 }
 
 cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream) {

@@ -16,30 +16,34 @@
 //     record, the (max, sum of 2^((z - max) log2(e) / T)) of a sampling row or
 //     the (finite max, lowest index + 1) of a greedy row, and stores it in one
 //     access (a record is never seen half written; zero means not written);
-//   warps 9-12 (the decide/draw group): owns sequences b, b + grid, ...; waits
-//     until the sequence's counter reaches its chunk count, merges the
-//     records (retrying while any still reads zero)
-//     into each row's softmax normaliser (or argmax), runs the acceptance
-//     tests of all gamma positions at once (one lane each: u < min(1, p/q)
-//     with Philox uniforms, or the greedy rule), finds the first rejection j
-//     with a warp ballot, and draws the token at j: the correction from
-//     [p_j - q_j]_+ or the bonus from p_gamma.  The draw re-reads the two
-//     rows of position j, streamed a few microseconds earlier and still in
-//     L2: one pass sums the weights in steps of 256 entries, a double-
-//     precision prefix over the step totals finds the step, one warp scans it.
+//   warps 9-12 (the draw group): a small scheduler that takes, in order of
+//     priority, (1) the search of its owned sequence once the sequence's
+//     weight jobs are all counted, (2) the decision of its next owned sequence
+//     (b, b + grid, ...) once the sequence's chunk counter is complete, (3)
+//     its next weight job once that job's draw descriptor is published, and
+//     (4) precise-redraw jobs once it has nothing else left.  All of this is
+//     described with the distributed draws below.
 //
-// HBM therefore sees every logit byte once; the draw traffic hits L2.  Draws
-// that land within the refine guard of a CDF boundary are queued for the
-// precise redraw.  No fence or atomic sits on the streaming path: the records
-// validate themselves.  The decide/draw groups wait on other CTAs' progress,
-// so the grid is launched cooperatively (all CTAs resident, two per SM); every
-// wait is bounded.
+// A decision merges the records (retrying while any still reads zero) into
+// each row's softmax normaliser (or argmax), runs the acceptance tests of all
+// gamma positions at once (one lane each: u < min(1, p/q) with Philox
+// uniforms, or the greedy rule), finds the first rejection j with a warp
+// ballot and publishes the draw at j: the correction from [p_j - q_j]_+ or the
+// bonus from p_gamma.  The draw's two rows, streamed a few microseconds
+// earlier, are re-read from L2 by weight jobs spread over many CTAs.
+//
+// No fence sits on the streaming path or on the draw path: records, draw
+// descriptors and step totals are 64-bit entries that validate themselves
+// (zero means not yet written), and counters are relaxed hints.  The draw
+// groups wait on other CTAs' progress, so the grid is launched cooperatively
+// (all CTAs resident, two per SM); every wait is bounded.
 //
 // Exponent arithmetic: 2^((z - m) k) with z - m computed exactly (one
 // rounding in the product), in the records, the merge, the acceptance test
 // and the draw alike, so the normalisers and the draw weights share their
 // scale.
 #include "ops.cuh"
+#include "precise_row.cuh"
 
 namespace sv {
 
@@ -53,6 +57,8 @@ constexpr int kPMaxRing = 8;
 constexpr int kPMaxGamma = 31;
 constexpr int kPMaxRows = 2 * kPMaxGamma + 1;
 constexpr int kPStep = 256;                        // entries per draw-search step
+constexpr int kPWeightJobs = 32;                   // weight jobs per draw (at most)
+constexpr int kPPreciseJobs = kPassPreciseJobs;    // precise jobs per phase (at most)
 constexpr long long kPPollLimitNs = 2000000000ll;  // give up waiting after about 2 s
 constexpr uint32_t kNoIndex = 0x3FFFFFFFu;         // record index: no finite entry
 constexpr uint32_t kBadBit = 0x80000000u;          // record index bit: NaN or +inf seen
@@ -90,6 +96,18 @@ struct PassCtl {
   int redo;
   int red_i[kPDrawWarps];
   float red_v[kPDrawWarps];
+  // job scheduling
+  PassSeq ps;
+  double pred[2][kPDrawWarps];
+  float tab_hi[64], tab_lo[64];
+  long long idle_t0;
+  int act, next_dec, next_f, next_k, job_v, job_s;
+  int tokx[kPMaxGamma + 1];
+  int fj_s[32], fj_k[32];  // the group's weight-job residues, ascending
+  int fj_i, fj_m;
+  int next_srch;   // owned sequence whose weight jobs are awaited (-1: none)
+  int held_v;      // claimed precise job id not yet run (-1: none)
+  PassSeq ps_own;  // its descriptor
 };
 
 __device__ __forceinline__ void draw_sync() {
@@ -483,68 +501,94 @@ __device__ void producer_loop(const Params &P, PassCtl &ctl, unsigned char *ring
 // decide / draw group
 // ---------------------------------------------------------------------------
 
-// Merge row r's records (one warp).  Returns false while a record still
+// Merge the records of all 2 gamma + 1 rows of a sequence (draw group):
+// row r goes to tpr consecutive threads of one warp (tpr a power of two,
+// tpr (2 gamma + 1) <= 128), each loading its records eight at a time
+// before merging them.  Returns false (in every thread) while a record still
 // reads zero (not yet stored).
-__device__ bool merge_row(const Params &P, int seq, int r, bool arg, float k, PassRow &out) {
-  const int lane = threadIdx.x & 31;
+__device__ bool merge_rows(const Params &P, PassCtl &ctl, int seq, bool p_arg, bool q_arg,
+                           float kp, float kq) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32, w = t >> 5;
+  const int gamma = P.gamma, rps = 2 * gamma + 1;
   const int R = P.cpr * kPConsumerWarps;
-  const unsigned long long *rec =
-      P.srec + (static_cast<long long>(seq) * (2 * P.gamma + 1) + r) * R;
+  int tpr = 32;
+  while (tpr * rps > kPDrawThreads) tpr >>= 1;
+  const int r = t / tpr, sub = t - r * tpr;
+  const bool active = r < rps;
+  const bool draft = r > gamma;
+  const bool arg = draft ? q_arg : p_arg;
+  const float k = draft ? kq : kp;
   bool missing = false;
-  if (arg) {
-    float bv = -INFINITY;
-    uint32_t bi = kNoIndex, bad = 0u;
-    for (int x = lane; x < R; x += 32) {
-      const unsigned long long bits = __ldcg(rec + x);
-      missing |= bits == 0ull;
-      const float2 q = make_float2(__uint_as_float(static_cast<uint32_t>(bits)),
-                                   __uint_as_float(static_cast<uint32_t>(bits >> 32)));
-      const uint32_t b = __float_as_uint(q.y);
-      bad |= b >> 31;
-      const uint32_t idx = (b & ~kBadBit) - 1u;
-      if (q.x > bv || (q.x == bv && idx < bi)) {
-        bv = q.x;
-        bi = idx;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const uint32_t i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
-      if (v2 > bv || (v2 == bv && i2 < bi)) {
-        bv = v2;
-        bi = i2;
-      }
-    }
-    out.m = bv;
-    out.S = 0.f;
-    out.a = bi == kNoIndex ? 0 : static_cast<int>(bi);
-    out.bad = (bad || bi == kNoIndex) ? 1 : 0;
-    return !__any_sync(0xFFFFFFFFu, missing);
-  }
   float m = -INFINITY, S = 0.f;
   int bad = 0;
-  for (int x = lane; x < R; x += 32) {
-    const unsigned long long bits = __ldcg(rec + x);
-    missing |= bits == 0ull;
-    const float2 q = make_float2(__uint_as_float(static_cast<uint32_t>(bits)),
-                                 __uint_as_float(static_cast<uint32_t>(bits >> 32)));
-    if (q.y != q.y || q.x == INFINITY) bad = 1;
-    else online_merge(m, S, q.x, q.y, k);
-  }
+  float bv = -INFINITY;
+  uint32_t bi = kNoIndex;
+  if (active) {
+    const unsigned long long *rec =
+        P.srec + (static_cast<long long>(seq) * rps + r) * static_cast<long long>(R);
+    for (int x0 = sub; x0 < R; x0 += 8 * tpr) {
+      unsigned long long b[8];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
+      for (int i = 0; i < 8; ++i) {
+        const int x = x0 + i * tpr;
+        b[i] = x < R ? __ldcg(rec + x) : 0ull;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (x0 + i * tpr >= R) continue;
+        missing |= b[i] == 0ull;
+        const float qx = __uint_as_float(static_cast<uint32_t>(b[i]));
+        const uint32_t qy = static_cast<uint32_t>(b[i] >> 32);
+        if (arg) {
+          bad |= static_cast<int>(qy >> 31);
+          const uint32_t idx = (qy & ~kBadBit) - 1u;
+          if (qx > bv || (qx == bv && idx < bi)) {
+            bv = qx;
+            bi = idx;
+          }
+        } else {
+          const float qs = __uint_as_float(qy);
+          if (qs != qs || qx == INFINITY) bad = 1;
+          else online_merge(m, S, qx, qs, k);
+        }
+      }
+    }
+  }
+  // reduce over the row's tpr threads (every lane of the warp shuffles)
+  for (int off = tpr >> 1; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
     const float S2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+    const float v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+    const uint32_t i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
     bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
-    online_merge(m, S, m2, S2, k);
+    if (!arg) online_merge(m, S, m2, S2, k);
+    if (v2 > bv || (v2 == bv && i2 < bi)) {
+      bv = v2;
+      bi = i2;
+    }
   }
-  out.m = m;
-  out.S = S;
-  out.a = 0;
-  out.bad = (bad || !(m > -INFINITY) || !(S > 0.f) || S == INFINITY) ? 1 : 0;
-  return !__any_sync(0xFFFFFFFFu, missing);
+  if (active && sub == 0) {
+    PassRow pr;
+    if (arg) {
+      pr.m = bv;
+      pr.S = 0.f;
+      pr.a = bi == kNoIndex ? 0 : static_cast<int>(bi);
+      pr.bad = (bad || bi == kNoIndex) ? 1 : 0;
+    } else {
+      pr.m = m;
+      pr.S = S;
+      pr.a = 0;
+      pr.bad = (bad || !(m > -INFINITY) || !(S > 0.f) || S == INFINITY) ? 1 : 0;
+    }
+    ctl.row[r] = pr;
+  }
+  const bool any_missing = __any_sync(0xFFFFFFFFu, missing);
+  if ((t & 31) == 0) ctl.red_i[w] = any_missing ? 0 : 1;
+  draw_sync();
+  bool all = true;
+  for (int x = 0; x < kPDrawWarps; ++x) all &= ctl.red_i[x] != 0;
+  draw_sync();
+  return all;
 }
 
 // Finite argmax of a whole row (draw group; rows whose sampling statistics
@@ -826,225 +870,941 @@ __device__ int pass_draw(const Params &P, PassCtl &ctl, float *step_tot, const T
   return token;
 }
 
+// ---------------------------------------------------------------------------
+// distributed draws
+// ---------------------------------------------------------------------------
+//
+// A sequence's final draw is split into weight jobs: job k of wj sums the
+// draw weights of steps [k wj_steps, (k + 1) wj_steps) (256 entries each) into
+// the sequence's step-total array.  Job (s, k) belongs to the draw group of
+// CTA (s + 1 + k wj_stride) mod G, so one group's jobs come from sequences
+// far apart and the jobs of one draw run side by side in wj groups.  The
+// sequence's owner searches once the job count is complete: a double-
+// precision prefix over the step totals finds the step, one warp scans it.
+// Draws whose single-precision search lands within the refine guard of a
+// boundary are queued for the precise redraw: per queued draw, pj normaliser
+// jobs (double-float shares of S_p and S_q) and pj weight jobs (double-float
+// step totals), claimed by groups with no other work left; the last weight
+// job searches in double precision and overwrites the token.
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_i32(int *p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+constexpr int kSeqWords = sizeof(PassSeq) / 4;
+static_assert(kSeqWords <= 32, "a descriptor is published by one warp");
+constexpr unsigned long long kTag = 1ull << 32;  // marks a written 64-bit entry
+
+// Publish ctl.ps as sequence s's descriptor: one 32-bit word per tagged
+// 64-bit entry, so a reader can tell a complete descriptor without a fence
+// (draw group; ctl.ps must be visible to the group).
+__device__ __forceinline__ void publish_seq(const Params &P, PassCtl &ctl, int s) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32;
+  if (t < kSeqWords) {
+    const uint32_t v = reinterpret_cast<const uint32_t *>(&ctl.ps)[t];
+    P.pseqw[static_cast<long long>(s) * kSeqWords + t] = static_cast<unsigned long long>(v) | kTag;
+  }
+}
+
+// Copy sequence s's descriptor into shared memory (draw group), reading again
+// while any entry is still unset.
+__device__ void load_seq(const Params &P, PassCtl &ctl, int s) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32;
+  if (t < 32) {
+    const unsigned long long *src = P.pseqw + static_cast<long long>(s) * kSeqWords;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&ctl.ps);
+    const long long t0 = pass_ns();
+    while (true) {
+      bool ok = true;
+      if (t < kSeqWords) {
+        const unsigned long long v = __ldcg(src + t);
+        ok = (v >> 32) != 0ull;
+        dst[t] = static_cast<uint32_t>(v);
+      }
+      if (__all_sync(0xFFFFFFFFu, ok)) break;
+      if (pass_ns() - t0 > kPPollLimitNs) {
+        if (t == 0) atomicOr(P.err, 1u);
+        break;
+      }
+      __nanosleep(100);
+    }
+  }
+  draw_sync();
+}
+
+// Rows of a sequence's draw position j.
 template <typename TE>
-__device__ void draw_loop(const Params &P, PassCtl &ctl, float *step_tot) {
+__device__ __forceinline__ void draw_rows(const Params &P, int s, int j, const TE *&gp,
+                                          const TE *&gq) {
+  gp = static_cast<const TE *>(
+      row_ptr(P.target, static_cast<long long>(s) * (P.gamma + 1) + j, P.ld_t, sizeof(TE)));
+  gq = static_cast<const TE *>(row_ptr(
+      P.draft, static_cast<long long>(s) * P.gamma + (j < P.gamma ? j : 0), P.ld_d, sizeof(TE)));
+}
+
+// Outputs of a finished draw and the unit record the residual output reads.
+__device__ void write_final(const Params &P, int s, const PassSeq &ps, int token, double W,
+                            int near) {
+  const long long obase = static_cast<long long>(s) * (P.gamma + 1);
+  const long long unit = obase + ps.j;
+  uint32_t flags = ps.flags;
+  flags |= *reinterpret_cast<const volatile uint32_t *>(P.err) ? SPEC_FLAG_TIMEOUT : 0u;
+  P.out_tokens[obase + ps.j] = token;
+  P.out_num[s] = ps.j;
+  if (P.out_flags) P.out_flags[s] = flags;
+  UnitOut o;
+  o.next = -1;
+  o.token = token;
+  o.flags = flags;
+  o.near = near;
+  P.outs[unit] = o;
+  UnitStats st;
+  st.p = ps.dp;
+  st.q = ps.dq;
+  st.c = ps.residual ? 1.f : 0.f;
+  st.total = static_cast<float>(W);
+  st.kind = ps.kind;
+  st.node = ps.j;
+  st.n_res = ps.residual;
+  st.pad = 0;
+  P.stats[unit] = st;
+  P.final_unit[s] = static_cast<int>(unit);
+}
+
+// One more sequence is final (single thread; a count only, the outputs are
+// read after the kernel).
+__device__ __forceinline__ void count_final(const Params &P) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.pctr + 2) : "memory");
+}
+
+// Decide sequence s: merge its records into the row statistics, run the
+// acceptance tests, and publish the draw (or finish the sequence when the
+// token needs no draw).
+template <typename TE>
+__device__ void decide(const Params &P, PassCtl &ctl, int seq) {
   const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
   const int gamma = P.gamma, rps = 2 * gamma + 1, V = P.V;
-  const uint32_t need = static_cast<uint32_t>(rps * P.cpr);
-  for (int seq = blockIdx.x; seq < P.nseq; seq += gridDim.x) {
-    // wait until the sequence's counter says all its chunks are in
-    int ok = 1;
-    if (t == 0) {
-      const long long t0 = pass_ns();
-      while (ld_volatile_pass(P.seq_cnt + seq) < need) {
-        if (pass_ns() - t0 > kPPollLimitNs) {
-          ok = 0;
-          break;
-        }
-        __nanosleep(1000);
+  const float Tp = __ldg(P.Tp + seq), Tq = __ldg(P.Tq + seq);
+  const bool p_arg = row_is_arg(Tp), q_arg = row_is_arg(Tq);
+  const bool tp_bad = !(Tp >= 0.f) || Tp == INFINITY, tq_bad = !(Tq >= 0.f) || Tq == INFINITY;
+  const float kp = p_arg ? 0.f : kLog2e / Tp, kq = q_arg ? 0.f : kLog2e / Tq;
+  // 1. row statistics (the progress count can run ahead of the records:
+  // merge again while any still reads zero)
+  {
+    const long long t0 = pass_ns();
+    // the draft tokens, loaded beside the records
+    const int xtok = t < gamma ? __ldg(P.tokens + static_cast<long long>(seq) * gamma + t) : 0;
+    while (true) {
+      if (merge_rows(P, ctl, seq, p_arg, q_arg, kp, kq)) {
+        if (t < gamma) ctl.tokx[t] = xtok;
+        break;
       }
-      ctl.redo = ok;
-    }
-    draw_sync();
-    ok = ctl.redo;
-    const float Tp = __ldg(P.Tp + seq), Tq = __ldg(P.Tq + seq);
-    const bool p_arg = row_is_arg(Tp), q_arg = row_is_arg(Tq);
-    const bool tp_bad = !(Tp >= 0.f) || Tp == INFINITY, tq_bad = !(Tq >= 0.f) || Tq == INFINITY;
-    const float kp = p_arg ? 0.f : kLog2e / Tp, kq = q_arg ? 0.f : kLog2e / Tq;
-    if (!ok) {
-      // a wait gave up: report the sequence as timed out
-      if (t == 0) {
-        P.out_num[seq] = 0;
-        if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
-        P.final_unit[seq] = -1;
+      if (pass_ns() - t0 > kPPollLimitNs) {
+        if (t == 0) atomicOr(P.err, 1u);
+        break;
       }
-      for (int i = t; i <= gamma; i += kPDrawThreads)
-        P.out_tokens[static_cast<long long>(seq) * (gamma + 1) + i] = -1;
-      draw_sync();
-      continue;
+      __nanosleep(200);
     }
-    // 1. row statistics (the progress hint can run ahead of the records:
-    // merge again while any still reads zero)
-    {
-      const long long t0 = pass_ns();
-      while (true) {
-        bool complete = true;
-        for (int r = w; r < rps; r += kPDrawWarps) {
-          const bool draft = r > gamma;
-          PassRow pr;
-          complete &= merge_row(P, seq, r, draft ? q_arg : p_arg, draft ? kq : kp, pr);
-          if (lane == 0) ctl.row[r] = pr;
-        }
-        if (lane == 0) ctl.red_i[w] = complete ? 1 : 0;
-        draw_sync();
-        bool all = true;
-        for (int x = 0; x < kPDrawWarps; ++x) all &= ctl.red_i[x] != 0;
-        draw_sync();
-        if (all) break;
-        if (pass_ns() - t0 > kPPollLimitNs) {
-          if (t == 0) atomicOr(P.err, 1u);
-          break;
-        }
-        __nanosleep(200);
-      }
+  }
+  for (int r = 0; r < rps; ++r) {
+    const bool draft = r > gamma;
+    const bool arg = draft ? q_arg : p_arg;
+    const bool tbad = draft ? tq_bad : tp_bad;
+    const PassRow pr = ctl.row[r];
+    RowDesc d;
+    d.thr = -INFINITY;
+    d.flags = 0u;
+    d.m = 0.f;
+    d.k = d.nmk = d.invS = 0.f;
+    d.a = 0;
+    if (arg) {
+      d.onehot = 1;
+      d.a = pr.a;
+      if (tbad || pr.bad) d.flags = SPEC_FLAG_NONFINITE;
+    } else if (pr.bad) {
+      const long long row = draft ? static_cast<long long>(seq) * gamma + (r - gamma - 1)
+                                  : static_cast<long long>(seq) * (gamma + 1) + r;
+      const TE *g = static_cast<const TE *>(
+          row_ptr(draft ? P.draft : P.target, row, draft ? P.ld_d : P.ld_t, sizeof(TE)));
+      d.onehot = 1;
+      d.a = finite_argmax_row<TE>(g, V, ctl);
+      d.flags = SPEC_FLAG_NONFINITE;
+    } else {
+      const float kk = draft ? kq : kp;
+      d.onehot = 0;
+      d.k = kk;
+      d.m = pr.m;
+      d.nmk = -pr.m * kk;
+      d.invS = 1.f / pr.S;
     }
-    for (int r = 0; r < rps; ++r) {
-      const bool draft = r > gamma;
-      const bool arg = draft ? q_arg : p_arg;
-      const bool tbad = draft ? tq_bad : tp_bad;
-      const PassRow pr = ctl.row[r];
-      RowDesc d;
-      d.thr = -INFINITY;
-      d.flags = 0u;
-      d.m = 0.f;
-      d.k = d.nmk = d.invS = 0.f;
-      d.a = 0;
-      if (arg) {
-        d.onehot = 1;
-        d.a = pr.a;
-        if (tbad || pr.bad) d.flags = SPEC_FLAG_NONFINITE;
-      } else if (pr.bad) {
-        const long long row = draft ? static_cast<long long>(seq) * gamma + (r - gamma - 1)
-                                    : static_cast<long long>(seq) * (gamma + 1) + r;
-        const TE *g = static_cast<const TE *>(
-            row_ptr(draft ? P.draft : P.target, row, draft ? P.ld_d : P.ld_t, sizeof(TE)));
-        d.onehot = 1;
-        d.a = finite_argmax_row<TE>(g, V, ctl);
-        d.flags = SPEC_FLAG_NONFINITE;
+    if (t == 0) ctl.desc[r] = d;
+  }
+  draw_sync();
+  // 2. acceptance tests, one lane per draft position
+  if (w == 0) {
+    int i = lane;
+    uint32_t f = 0u;
+    bool reject = true;
+    if (i < gamma) {
+      const RowDesc dp = ctl.desc[i];
+      const RowDesc dq = ctl.desc[gamma + 1 + i];
+      const int x = ctl.tokx[i];
+      f = dp.flags;
+      const bool valid = x >= 0 && x < V;
+      if (!valid) f |= SPEC_FLAG_BAD_TOKEN;
+      if (dp.onehot) {
+        reject = !(valid && x == dp.a);
       } else {
-        const float kk = draft ? kq : kp;
-        d.onehot = 0;
-        d.k = kk;
-        d.m = pr.m;
-        d.nmk = -pr.m * kk;
-        d.invS = 1.f / pr.S;
+        f |= dq.flags;
+        if (valid) {
+          const TE *gp = static_cast<const TE *>(
+              row_ptr(P.target, static_cast<long long>(seq) * (gamma + 1) + i, P.ld_t,
+                      sizeof(TE)));
+          const TE *gq = static_cast<const TE *>(
+              row_ptr(P.draft, static_cast<long long>(seq) * gamma + i, P.ld_d, sizeof(TE)));
+          const float px = pprob(dp, dp.onehot ? 0.f : to_f32(gp[x]), x);
+          const float qx = pprob(dq, dq.onehot ? 0.f : to_f32(gq[x]), x);
+          if (!(qx > 0.f)) {
+            f |= SPEC_FLAG_ZERO_Q;
+          } else {
+            const float uu = unit_uniform(P, seq, i, 0);
+            reject = !(uu < fminf(1.f, px / qx));
+          }
+        }
       }
-      if (t == 0) ctl.desc[r] = d;
+      ctl.pos_flags[i] = static_cast<int>(f);
     }
-    draw_sync();
-    // 2. acceptance tests, one lane per draft position
-    if (w == 0) {
-      int i = lane;
-      uint32_t f = 0u;
-      bool reject = true;
-      if (i < gamma) {
-        const RowDesc dp = ctl.desc[i];
-        const RowDesc dq = ctl.desc[gamma + 1 + i];
-        const int x = __ldg(P.tokens + static_cast<long long>(seq) * gamma + i);
-        f = dp.flags;
-        const bool valid = x >= 0 && x < V;
-        if (!valid) f |= SPEC_FLAG_BAD_TOKEN;
-        if (dp.onehot) {
-          reject = !(valid && x == dp.a);
-        } else {
-          f |= dq.flags;
-          if (valid) {
-            const TE *gp = static_cast<const TE *>(
-                row_ptr(P.target, static_cast<long long>(seq) * (gamma + 1) + i, P.ld_t,
-                        sizeof(TE)));
-            const TE *gq = static_cast<const TE *>(
-                row_ptr(P.draft, static_cast<long long>(seq) * gamma + i, P.ld_d, sizeof(TE)));
-            const float px = pprob(dp, dp.onehot ? 0.f : to_f32(gp[x]), x);
-            const float qx = pprob(dq, dq.onehot ? 0.f : to_f32(gq[x]), x);
-            if (!(qx > 0.f)) {
-              f |= SPEC_FLAG_ZERO_Q;
-            } else {
-              const float uu = unit_uniform(P, seq, i, 0);
-              reject = !(uu < fminf(1.f, px / qx));
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, reject && i < gamma);
+    const int j = rej ? __ffs(rej) - 1 : gamma;
+    uint32_t fo = (i < j) ? f : 0u;
+    fo = warp_or(fo);
+    if (lane == 0) {
+      if (j < gamma) fo |= static_cast<uint32_t>(ctl.pos_flags[j]);
+      else fo |= ctl.desc[gamma].flags;
+      ctl.j = j;
+      ctl.flags = fo;
+    }
+  }
+  draw_sync();
+  const int j = ctl.j;
+  const long long obase = static_cast<long long>(seq) * (gamma + 1);
+  for (int i = t; i <= gamma; i += kPDrawThreads) {
+    if (i < j) P.out_tokens[obase + i] = __ldg(P.tokens + static_cast<long long>(seq) * gamma + i);
+    else if (i > j) P.out_tokens[obase + i] = -1;
+  }
+  // 3. the draw at j
+  if (t == 0) {
+    PassSeq ps;
+    ps.dp = ctl.desc[j];
+    ps.residual = j < gamma ? 1 : 0;
+    if (ps.residual) {
+      ps.dq = ctl.desc[gamma + 1 + j];
+    } else {
+      ps.dq = ps.dp;
+      ps.dq.onehot = 1;
+      ps.dq.a = 0;
+    }
+    ps.j = j;
+    ps.flags = ctl.flags;
+    ps.W = 0.f;
+    ps.u = 0.f;
+    if (ps.dp.onehot) {
+      ps.kind = j < gamma ? 1 : 0;
+      ps.residual = 0;
+      ps.draw = 0;
+      write_final(P, seq, ps, ps.dp.a, 0.0, 0);
+      count_final(P);
+    } else {
+      ps.kind = j < gamma ? 2 : 0;
+      ps.u = unit_uniform(P, seq, j, 1);
+      ps.draw = 1;
+    }
+    ctl.ps = ps;
+  }
+  draw_sync();
+  publish_seq(P, ctl, seq);  // the weight jobs read it (and skip when no draw)
+  if (t == 0) {
+    ctl.ps_own = ctl.ps;
+    ctl.next_srch = ctl.ps.draw ? seq : -1;
+  }
+  draw_sync();
+}
+
+// Single-precision inverse-CDF search over sequence s's published step
+// totals, then the scan of the owning step (draw group; ctl.ps holds the
+// descriptor).  Finishes the sequence or queues it for the precise redraw.
+template <typename TE>
+__device__ void fsearch(const Params &P, PassCtl &ctl, float *step_tot, int s) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
+  const int nsteps = P.steps, V = P.V;
+  const unsigned long long *fst = P.fstep + static_cast<long long>(s) * nsteps;
+  PassSeq ps = ctl.ps_own;
+  const TE *gp, *gq;
+  draw_rows<TE>(P, s, ps.j, gp, gq);
+  if (w == 0) {
+    const int per = (nsteps + 31) / 32;
+    const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
+    double seg = 0.0;
+    int lastpos = -1;
+    const long long t0 = pass_ns();
+    while (true) {  // read again while a job's totals are not all visible
+      bool miss = false;
+      seg = 0.0;
+      lastpos = -1;
+      for (int b0 = s0; b0 < s1; b0 += 16) {  // sixteen loads in flight
+        unsigned long long x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = b0 + i < s1 ? __ldcg(fst + b0 + i) : kTag;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          miss |= (x[i] >> 32) == 0ull;
+          const float v = __uint_as_float(static_cast<uint32_t>(x[i]));
+          seg += static_cast<double>(v);
+          if (v > 0.f) lastpos = b0 + i;
+        }
+      }
+      if (!__any_sync(0xFFFFFFFFu, miss)) break;
+      if (pass_ns() - t0 > kPPollLimitNs) {
+        if (lane == 0) atomicOr(P.err, 1u);
+        break;
+      }
+      __nanosleep(100);
+    }
+    double incl = seg;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const double W = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const double tt = static_cast<double>(ps.u) * W;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > tt && seg > 0.0);
+    int step = -1;
+    double trel = 0.0;
+    if (hit) {
+      const int first = __ffs(hit) - 1;
+      if (lane == first) {
+        double acc = incl - seg;
+        for (int b0 = s0; b0 < s1 && step < 0; b0 += 16) {
+          float xs[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            xs[i] = b0 + i < s1 ? __uint_as_float(static_cast<uint32_t>(__ldcg(fst + b0 + i))) : 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const double x = static_cast<double>(xs[i]);
+            if (step < 0 && b0 + i < s1) {
+              if (acc + x > tt && x > 0.0) {
+                step = b0 + i;
+                trel = tt - acc;
+              }
+              acc += x;
             }
           }
         }
-        ctl.pos_flags[i] = static_cast<int>(f);
+        if (step < 0) {
+          step = lastpos;
+          trel = INFINITY;
+        }
       }
-      const unsigned rej = __ballot_sync(0xFFFFFFFFu, reject && i < gamma);
-      const int j = rej ? __ffs(rej) - 1 : gamma;
-      uint32_t fo = (i < j) ? f : 0u;
-      fo = warp_or(fo);
+      step = __shfl_sync(0xFFFFFFFFu, step, first);
+      trel = __shfl_sync(0xFFFFFFFFu, trel, first);
+    } else {
+      step = warp_max_i(lastpos);
+      trel = INFINITY;
+    }
+    int token = -1;
+    float margin = 0.f;
+    if (step >= 0) {
+      const bool exact = trel != INFINITY;
+      const float tr = static_cast<float>(trel);
+      const int base = step * kPStep + lane * 8;
+      float x[8];
+      step_weights<TE>(gp, gq, ps.dp, ps.dq, ps.residual, base, V, x);
+      float sm = 0.f;
+      int lp = -1;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sm += x[e];
+        if (x[e] > 0.f) lp = base + e;
+      }
+      float fin = sm;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, fin, off);
+        if (lane >= off) fin += y;
+      }
+      const float excl = fin - sm;
+      const unsigned h2 = exact ? __ballot_sync(0xFFFFFFFFu, fin > tr && sm > 0.f) : 0u;
+      if (h2) {
+        const int first = __ffs(h2) - 1;
+        int found = -1;
+        float mg = 0.f;
+        if (lane == first) {
+          float run = excl;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float prev = run;
+            run += x[e];
+            if (found < 0 && x[e] > 0.f && run > tr) {
+              found = base + e;
+              mg = fminf(tr - prev, run - tr);
+            }
+          }
+          if (found < 0) found = lp;
+        }
+        token = __shfl_sync(0xFFFFFFFFu, found, first);
+        margin = __shfl_sync(0xFFFFFFFFu, mg, first);
+      } else {
+        token = warp_max_i(lp);
+        margin = 0.f;
+      }
+    }
+    if (lane == 0) {
+      ctl.W = W;
+      ctl.step = token;
+      ctl.red_v[0] = margin;
+    }
+  }
+  draw_sync();
+  int token = ctl.step;
+  double W = ctl.W;
+  float margin = ctl.red_v[0];
+  draw_sync();
+  if (ps.residual && !(W > 0.0)) {
+    // degenerate residual: draw from p itself (this group alone)
+    ps.flags |= SPEC_FLAG_DEGENERATE_RESIDUAL;
+    ps.residual = 0;
+    ps.dq = ps.dp;
+    ps.dq.onehot = 1;
+    ps.dq.a = 0;
+    token = pass_draw<TE>(P, ctl, step_tot, gp, gq, ps.dp, ps.dq, 0, ps.u, margin, W);
+  }
+  // redraw precisely when the draw came within 1e-6 of the draw mass of a
+  // boundary (the single-precision boundary error measured on 128K-entry rows
+  // stays below 3e-7 of it)
+  const int near = margin < 1e-6f * static_cast<float>(W) ? 1 : 0;
+  if (t == 0) {
+    ps.W = static_cast<float>(W);
+    write_final(P, s, ps, token, W, near);
+    if (!near) count_final(P);
+    ctl.ps = ps;
+    ctl.redo = near;
+  }
+  draw_sync();
+  if (ctl.redo) {
+    // the precise redraw reads the final descriptor (a rare path: fenced)
+    publish_seq(P, ctl, s);
+    draw_sync();
+    if (t == 0) {
+      __threadfence();
+      const uint32_t i = atomicAdd(P.pctr, 1u);
+      st_release_i32(P.near_list + i, s + 1);
+    }
+    draw_sync();
+  }
+}
+
+// Weight job (s, k): step totals of steps [k kf_steps, (k + 1) kf_steps).
+template <typename TE>
+__device__ void fjob(const Params &P, PassCtl &ctl, float *step_tot, int s, int k) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
+  const PassSeq &ps = ctl.ps;  // read by the scheduler
+  const TE *gp, *gq;
+  draw_rows<TE>(P, s, ps.j, gp, gq);
+  const RowDesc dp = ps.dp, dq = ps.dq;
+  const int residual = ps.residual;
+  const int V = P.V;
+  const int b0 = k * P.wj_steps, b1 = min(P.steps, b0 + P.wj_steps);
+  unsigned long long *fst = P.fstep + static_cast<long long>(s) * P.steps;
+  // full steps four per warp at a time, their loads issued before any is used
+  constexpr int kU = 4;
+  const int nfull = min(b1, V / kPStep);
+  int st0 = b0 + w;
+  for (; st0 + (kU - 1) * kPDrawWarps < nfull; st0 += kPDrawWarps * kU) {
+    Raw8<TE> rp[kU], rq[kU];
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const int base = (st0 + q * kPDrawWarps) * kPStep + lane * 8;
+      rp[q].load(gp + base);
+      if (residual) rq[q].load(gq + base);
+    }
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const int base = (st0 + q * kPDrawWarps) * kPStep + lane * 8;
+      float zp[8], zq[8], x[8];
+      rp[q].get(zp);
+      rq[q].get(zq);
+      weights8(dp, dq, residual, base, zp, zq, x);
+      float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+      sm = warp_sum(sm);
+      if (lane == 0) fst[st0 + q * kPDrawWarps] = static_cast<unsigned long long>(__float_as_uint(sm)) | kTag;
+    }
+  }
+  for (int st = st0; st < b1; st += kPDrawWarps) {
+    float x[8];
+    step_weights<TE>(gp, gq, dp, dq, residual, st * kPStep + lane * 8, V, x);
+    float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+    sm = warp_sum(sm);
+    if (lane == 0) fst[st] = static_cast<unsigned long long>(__float_as_uint(sm)) | kTag;
+  }
+  draw_sync();
+  // count the job (relaxed): the sequence's owner searches once the count is
+  // complete, reading the totals again until every job's entries are visible
+  if (t == 0) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.sctr + 4ll * s + 1)
+                           : "memory");
+}
+
+// Double-float weights of the 8 entries from `base` (precise redraw).
+template <typename TE>
+__device__ __forceinline__ void pweights8(const TE *gp, const TE *gq, const HpRow &rp,
+                                          const HpRow &rq, int residual, Df rho, int base, int V,
+                                          bool vec, const PassCtl &ctl, Df w[8]) {
+  float zp[8], zq[8];
+  hp_load8<TE>(gp, base, V, vec, zp);
+  if (residual) hp_load8<TE>(gq, base, V, vec, zq);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const Df ep = hp_exp(rp, zp[e], ctl.tab_hi, ctl.tab_lo);
+    if (!residual || ep.hi == 0.f) {
+      w[e] = ep;
+      continue;
+    }
+    const Df eq = hp_exp(rq, zq[e], ctl.tab_hi, ctl.tab_lo);
+    const Df d = df_sub(ep, df_mul(rho, eq));
+    w[e] = d.hi > 0.f ? d : Df{0.f, 0.f};
+  }
+}
+
+// Sum over the pj normaliser shares of sequence s (the same bits in every
+// lane and every group: lane-strided sums, a butterfly, lane 0's value).
+__device__ __forceinline__ double pshare_sum(const Params &P, int s, int which) {
+  const int lane = threadIdx.x & 31;
+  const double *x = P.ppart + static_cast<long long>(s) * P.pj * 2 + which;
+  double v = 0.0;
+  for (int k = lane; k < P.pj; k += 32) v += __ldcg(x + 2 * k);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  return __shfl_sync(0xFFFFFFFFu, v, 0);
+}
+
+// Double-precision search of a precise redraw over its step totals, then the
+// scan of the owning step with double-float weights; overwrites the token.
+template <typename TE>
+__device__ void psearch(const Params &P, PassCtl &ctl, int s, const TE *gp, const TE *gq,
+                        const HpRow &rp, const HpRow &rq, Df rho, bool vec) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
+  const PassSeq &ps = ctl.ps;
+  const int nsteps = P.steps;
+  if (w == 0) {
+    const double *pst = P.pstep + static_cast<long long>(s) * nsteps;
+    const int per = (nsteps + 31) / 32;
+    const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
+    double seg = 0.0;
+    int lastpos = -1;
+    for (int b0 = s0; b0 < s1; b0 += 8) {  // eight loads in flight
+      double x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = b0 + i < s1 ? __ldcg(pst + b0 + i) : 0.0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        seg += x[i];
+        if (x[i] > 0.0) lastpos = b0 + i;
+      }
+    }
+    double incl = seg;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const double Z = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const double tt = static_cast<double>(ps.u) * Z;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > tt && seg > 0.0);
+    int step = -1;
+    double trel = 0.0;
+    if (hit) {
+      const int first = __ffs(hit) - 1;
+      if (lane == first) {
+        double acc = incl - seg;
+        for (int b0 = s0; b0 < s1 && step < 0; b0 += 8) {
+          double xs[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xs[i] = b0 + i < s1 ? __ldcg(pst + b0 + i) : 0.0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (step < 0 && b0 + i < s1) {
+              if (acc + xs[i] > tt && xs[i] > 0.0) {
+                step = b0 + i;
+                trel = tt - acc;
+              }
+              acc += xs[i];
+            }
+          }
+        }
+        if (step < 0) {
+          step = lastpos;
+          trel = INFINITY;
+        }
+      }
+      step = __shfl_sync(0xFFFFFFFFu, step, first);
+      trel = __shfl_sync(0xFFFFFFFFu, trel, first);
+    } else {
+      step = warp_max_i(lastpos);
+      trel = INFINITY;
+    }
+    int token = -1;
+    if (step >= 0) {
+      const int base = step * kPStep + lane * 8;
+      Df wd[8];
+      pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, base, P.V, vec, ctl, wd);
+      double x[8];
+      double sm = 0.0;
+      int lp = -1;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[e] = df_to_double(wd[e]);
+        sm += x[e];
+        if (x[e] > 0.0) lp = base + e;
+      }
+      double fin = sm;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, fin, off);
+        if (lane >= off) fin += y;
+      }
+      const unsigned h2 =
+          trel != INFINITY ? __ballot_sync(0xFFFFFFFFu, fin > trel && sm > 0.0) : 0u;
+      if (h2) {
+        const int first = __ffs(h2) - 1;
+        int found = -1;
+        if (lane == first) {
+          double run = fin - sm;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            run += x[e];
+            if (found < 0 && x[e] > 0.0 && run > trel) found = base + e;
+          }
+          if (found < 0) found = lp;
+        }
+        token = __shfl_sync(0xFFFFFFFFu, found, first);
+      } else {
+        token = warp_max_i(lp);
+      }
+    }
+    if (lane == 0) {
+      if (token >= 0) {
+        const long long obase = static_cast<long long>(s) * (P.gamma + 1);
+        P.out_tokens[obase + ps.j] = token;
+        P.outs[obase + ps.j].token = token;
+      }
+      count_final(P);
+    }
+  }
+  draw_sync();
+}
+
+// Precise job v: redraw item v / (2 pj); normaliser share (phase 0) or step
+// totals (phase 1) of slice v % pj.
+template <typename TE>
+__device__ void pjob(const Params &P, PassCtl &ctl, int v) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
+  const int kp = P.pj;
+  const int item = v / (2 * kp), r = v - item * 2 * kp;
+  const int phase = r < kp ? 0 : 1, k = r < kp ? r : r - kp;
+  if (t == 0) {
+    const long long t0 = pass_ns();
+    int sv1;
+    while ((sv1 = *reinterpret_cast<const volatile int *>(P.near_list + item)) == 0) {
+      if (pass_ns() - t0 > kPPollLimitNs) {
+        atomicOr(P.err, 1u);
+        break;
+      }
+      __nanosleep(100);
+    }
+    __threadfence();
+    ctl.job_s = sv1 - 1;
+  }
+  draw_sync();
+  const int s = ctl.job_s;
+  if (s < 0) return;
+  load_seq(P, ctl, s);
+  const PassSeq &ps = ctl.ps;
+  const TE *gp, *gq;
+  draw_rows<TE>(P, s, ps.j, gp, gq);
+  const bool vec = ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(gq)) & 15u) == 0;
+  const HpRow rp = hp_row(ps.dp, __ldg(P.Tp + s));
+  const HpRow rq = ps.residual ? hp_row(ps.dq, __ldg(P.Tq + s)) : rp;
+  const int V = P.V;
+  const int b0 = k * P.pj_steps, b1 = min(P.steps, b0 + P.pj_steps);
+  uint32_t *cnt = P.sctr + 4ll * s;
+  if (phase == 0) {
+    if (ps.residual) {
+      double a = 0.0, b = 0.0;
+      for (int st = b0 + w; st < b1; st += kPDrawWarps) {
+        const int base = st * kPStep + lane * 8;
+        float zp[8], zq[8];
+        hp_load8<TE>(gp, base, V, vec, zp);
+        hp_load8<TE>(gq, base, V, vec, zq);
+        Df sp{0.f, 0.f}, sq{0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sp = df_add(sp, hp_exp(rp, zp[e], ctl.tab_hi, ctl.tab_lo));
+          sq = df_add(sq, hp_exp(rq, zq[e], ctl.tab_hi, ctl.tab_lo));
+        }
+        a += df_to_double(sp);
+        b += df_to_double(sq);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, off);
+        b += __shfl_xor_sync(0xFFFFFFFFu, b, off);
+      }
       if (lane == 0) {
-        if (j < gamma) fo |= static_cast<uint32_t>(ctl.pos_flags[j]);
-        else fo |= ctl.desc[gamma].flags;
-        ctl.j = j;
-        ctl.flags = fo;
+        ctl.pred[0][w] = a;
+        ctl.pred[1][w] = b;
+      }
+      draw_sync();
+      if (t == 0) {
+        double A = 0.0, B = 0.0;
+        for (int x = 0; x < kPDrawWarps; ++x) {
+          A += ctl.pred[0][x];
+          B += ctl.pred[1][x];
+        }
+        double *dst = P.ppart + (static_cast<long long>(s) * kp + k) * 2;
+        dst[0] = A;
+        dst[1] = B;
+      }
+    }
+    if (t == 0) {
+      __threadfence();
+      atomicAdd(cnt + 2, 1u);
+    }
+    draw_sync();
+    return;
+  }
+  // phase 1: wait for every normaliser share of the draw
+  if (t == 0) {
+    const long long t0 = pass_ns();
+    while (ld_acquire_u32(cnt + 2) < static_cast<uint32_t>(kp)) {
+      if (pass_ns() - t0 > kPPollLimitNs) {
+        atomicOr(P.err, 1u);
+        break;
+      }
+      __nanosleep(100);
+    }
+  }
+  draw_sync();
+  Df rho{0.f, 0.f};
+  if (ps.residual) {
+    const double Sp = pshare_sum(P, s, 0), Sq = pshare_sum(P, s, 1);
+    rho = df_from_double(Sp / Sq);
+  }
+  double *pst = P.pstep + static_cast<long long>(s) * P.steps;
+  for (int st = b0 + w; st < b1; st += kPDrawWarps) {
+    const int base = st * kPStep + lane * 8;
+    Df wd[8];
+    pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, base, V, vec, ctl, wd);
+    Df acc{0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = df_add(acc, wd[e]);
+    double x = df_to_double(acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+    if (lane == 0) pst[st] = x;
+  }
+  draw_sync();
+  if (t == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(cnt + 3, 1u);
+    ctl.redo = old + 1 == static_cast<uint32_t>(kp) ? 1 : 0;
+    if (ctl.redo) __threadfence();
+  }
+  draw_sync();
+  if (ctl.redo) psearch<TE>(P, ctl, s, gp, gq, rp, rq, rho, vec);
+}
+
+// Weight jobs of group g: job (s, k) belongs to group (s + 1 + k stride) mod G,
+// so the group's jobs are the sequences s = (g - 1 - k stride) mod G + m G.
+// The wj residues are sorted once (ctl.fj_s / fj_k, warp 0); the m-th pass
+// over them gives the jobs in sequence order.
+__device__ void init_fjobs(const Params &P, PassCtl &ctl, int g, int G) {
+  const int lane = threadIdx.x & 31;
+  int r = INT_MAX, k = lane;
+  if (lane < P.wj) {
+    r = (g - 1 - lane * P.wj_stride) % G;
+    if (r < 0) r += G;
+  }
+  // rank of each residue among the lanes (residues are distinct)
+  int rank = 0;
+  for (int x = 0; x < 32; ++x) {
+    const int rx = __shfl_sync(0xFFFFFFFFu, r, x);
+    rank += rx < r ? 1 : 0;
+  }
+  if (lane < P.wj) {
+    ctl.fj_s[rank] = r;
+    ctl.fj_k[rank] = k;
+  }
+  if (lane == 0) {
+    ctl.fj_i = 0;
+    ctl.fj_m = 0;
+  }
+  __syncwarp();
+}
+
+// Advance to the group's next weight job (thread 0): ctl.next_f / next_k, or
+// next_f = nseq when none is left.
+__device__ void advance_fjob(const Params &P, PassCtl &ctl, int G) {
+  int i = ctl.fj_i, m = ctl.fj_m;
+  while (true) {
+    if (i >= P.wj) {
+      i = 0;
+      ++m;
+    }
+    const long long s = ctl.fj_s[i] + static_cast<long long>(m) * G;
+    if (s >= P.nseq && i == 0) {  // residues are sorted: this pass and later are empty
+      ctl.next_f = P.nseq;
+      break;
+    }
+    if (s < P.nseq) {
+      ctl.next_f = static_cast<int>(s);
+      ctl.next_k = ctl.fj_k[i];
+      ++i;
+      break;
+    }
+    i = P.wj;  // the rest of this pass is past the batch
+  }
+  ctl.fj_i = i;
+  ctl.fj_m = m;
+}
+
+// Timed-out sequence: no tokens, SPEC_FLAG_TIMEOUT (single thread).
+__device__ void write_timeout(const Params &P, int seq) {
+  P.out_num[seq] = 0;
+  if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
+  P.final_unit[seq] = -1;
+  for (int i = 0; i <= P.gamma; ++i) P.out_tokens[static_cast<long long>(seq) * (P.gamma + 1) + i] = -1;
+}
+
+enum { kActIdle = 0, kActDecide = 1, kActWeights = 2, kActPrecise = 3, kActExit = 4, kActSearch = 5 };
+
+// The draw group's scheduler: decide owned sequences as their chunks complete,
+// run weight jobs as their descriptors appear, and otherwise take precise
+// jobs; leave when every sequence of the batch is final.
+template <typename TE>
+__device__ void draw_loop(const Params &P, PassCtl &ctl, float *step_tot, const Exp2Table &tab) {
+  const int t = threadIdx.x - kPDrawWarp0 * 32;
+  const int G = gridDim.x, g = blockIdx.x;
+  const uint32_t need = static_cast<uint32_t>((2 * P.gamma + 1) * P.cpr);
+  if (t < 32) init_fjobs(P, ctl, g, G);
+  if (t == 0) {
+    ctl.next_dec = g;
+    ctl.next_srch = -1;
+    ctl.held_v = -1;
+    advance_fjob(P, ctl, G);
+    ctl.idle_t0 = pass_ns();
+  }
+  for (int i = t; i < 64; i += kPDrawThreads) {
+    ctl.tab_hi[i] = tab.hi[i];
+    ctl.tab_lo[i] = tab.lo[i];
+  }
+  draw_sync();
+  unsigned sleep_ns = 64;
+  while (true) {
+    if (t < 32) {
+      // one round trip: the next weight job's descriptor (tagged words), the
+      // progress count of the next owned sequence, the precise-job counters
+      const int lane = t;
+      const int nd = ctl.next_dec, nf = ctl.next_f;
+      unsigned long long dw = kTag;
+      uint32_t c = 0u;
+      if (lane < kSeqWords && nf < P.nseq) dw = __ldcg(P.pseqw + static_cast<long long>(nf) * kSeqWords + lane);
+      if (lane == 31 && nd < P.nseq) c = ld_volatile_pass(P.seq_cnt + nd);
+      if (lane == 30) c = ld_volatile_pass(P.pctr);
+      if (lane == 29) c = ld_volatile_pass(P.pctr + 1);
+      if (lane == 28) c = ld_volatile_pass(P.pctr + 2);
+      if (lane == 27 && ctl.next_srch >= 0) c = ld_volatile_pass(P.sctr + 4ll * ctl.next_srch + 1);
+      const bool desc_ok = __all_sync(0xFFFFFFFFu, (dw >> 32) != 0ull) && nf < P.nseq;
+      const uint32_t cnt = __shfl_sync(0xFFFFFFFFu, c, 31);
+      const uint32_t nq = __shfl_sync(0xFFFFFFFFu, c, 30);
+      const uint32_t claimed = __shfl_sync(0xFFFFFFFFu, c, 29);
+      const uint32_t nfinal = __shfl_sync(0xFFFFFFFFu, c, 28);
+      const uint32_t jobs_done = __shfl_sync(0xFFFFFFFFu, c, 27);
+      const int ns = ctl.next_srch;
+      int act = kActIdle;
+      if (ns >= 0 && jobs_done >= static_cast<uint32_t>(P.wj)) {
+        act = kActSearch;
+      } else if (ns < 0 && nd < P.nseq && cnt >= need) {
+        act = kActDecide;
+      } else if (desc_ok) {
+        act = kActWeights;
+        if (lane < kSeqWords) reinterpret_cast<uint32_t *>(&ctl.ps)[lane] = static_cast<uint32_t>(dw);
+      } else if (lane == 0) {
+        // precise jobs once this group's own decides and weight jobs are done:
+        // claim a job id (fetch-and-add), run it once its redraw is queued
+        const bool free = ns < 0 && nd >= P.nseq && nf >= P.nseq;
+        const uint32_t per_item = 2u * static_cast<uint32_t>(P.pj);
+        if (free && ctl.held_v < 0 && claimed < nq * per_item)
+          ctl.held_v = static_cast<int>(atomicAdd(P.pctr + 1, 1u));
+        if (free && ctl.held_v >= 0 && static_cast<uint32_t>(ctl.held_v) < nq * per_item) {
+          act = kActPrecise;
+          ctl.job_v = ctl.held_v;
+          ctl.held_v = -1;
+        } else if (free && nfinal >= static_cast<uint32_t>(P.nseq)) {
+          act = kActExit;  // every sequence is final: a held id has no job
+        } else if (pass_ns() - ctl.idle_t0 > kPPollLimitNs) {
+          // nothing moved for too long: give up, marking what this group owns
+          atomicOr(P.err, 1u);
+          for (int x = nd; x < P.nseq; x += G) write_timeout(P, x);
+          act = kActExit;
+        }
+      }
+      if (lane == 0) {
+        if (act != kActIdle) ctl.idle_t0 = pass_ns();
+        ctl.act = act;
       }
     }
     draw_sync();
-    const int j = ctl.j;
-    uint32_t flags = ctl.flags;
-    const long long obase = static_cast<long long>(seq) * (gamma + 1);
-    for (int i = t; i <= gamma; i += kPDrawThreads) {
-      if (i < j) P.out_tokens[obase + i] = __ldg(P.tokens + static_cast<long long>(seq) * gamma + i);
-      else if (i > j) P.out_tokens[obase + i] = -1;
+    const int act = ctl.act;
+    if (act == kActExit) break;
+    if (act == kActIdle) {
+      if (t == 0) __nanosleep(sleep_ns);
+      sleep_ns = min(sleep_ns * 2u, 2048u);
+      continue;
     }
-    // 3. the token at j
-    const RowDesc dp = ctl.desc[j];
-    RowDesc dq;
-    int residual = j < gamma ? 1 : 0;
-    if (residual) {
-      dq = ctl.desc[gamma + 1 + j];
+    sleep_ns = 64;
+    if (act == kActSearch) {
+      const int s = ctl.next_srch;
+      draw_sync();
+      fsearch<TE>(P, ctl, step_tot, s);
+      if (t == 0) ctl.next_srch = -1;
+    } else if (act == kActDecide) {
+      const int s = ctl.next_dec;
+      draw_sync();
+      decide<TE>(P, ctl, s);
+      if (t == 0) ctl.next_dec = s + G;
+    } else if (act == kActWeights) {
+      const int s = ctl.next_f, k = ctl.next_k;
+      draw_sync();
+      if (ctl.ps.draw) fjob<TE>(P, ctl, step_tot, s, k);
+      if (t == 0) advance_fjob(P, ctl, G);
     } else {
-      dq = dp;
-      dq.onehot = 1;
-      dq.a = 0;
-    }
-    const long long unit = obase + j;
-    int token;
-    float margin = 0.f;
-    double W = 0.0;
-    int kind;
-    if (dp.onehot) {
-      token = dp.a;
-      kind = j < gamma ? 1 : 0;
-      residual = 0;
-    } else {
-      const TE *gp = static_cast<const TE *>(row_ptr(P.target, unit, P.ld_t, sizeof(TE)));
-      const TE *gq = static_cast<const TE *>(
-          row_ptr(P.draft, static_cast<long long>(seq) * gamma + (j < gamma ? j : 0), P.ld_d,
-                  sizeof(TE)));
-      const float u = unit_uniform(P, seq, j, 1);
-      token = pass_draw<TE>(P, ctl, step_tot, gp, gq, dp, dq, residual, u, margin, W);
-      if (residual && !(W > 0.0)) {
-        // degenerate residual: draw from p itself
-        flags |= SPEC_FLAG_DEGENERATE_RESIDUAL;
-        residual = 0;
-        token = pass_draw<TE>(P, ctl, step_tot, gp, gq, dp, dq, 0, u, margin, W);
-      }
-      kind = j < gamma ? 2 : 0;
-    }
-    if (t == 0) {
-      const float c = residual ? 1.f : 0.f;
-      // redraw precisely when the draw came within 1e-6 of the draw mass of a
-      // boundary (the single-precision boundary error measured on 128K-entry
-      // rows stays below 3e-7 of it)
-      const int near = (!dp.onehot && margin < 1e-6f * static_cast<float>(W)) ? 1 : 0;
-      flags |= *reinterpret_cast<const volatile uint32_t *>(P.err) ? SPEC_FLAG_TIMEOUT : 0u;
-      P.out_tokens[obase + j] = token;
-      P.out_num[seq] = j;
-      if (P.out_flags) P.out_flags[seq] = flags;
-      UnitOut o;
-      o.next = -1;
-      o.token = token;
-      o.flags = flags;
-      o.near = near;
-      P.outs[unit] = o;
-      UnitStats st;
-      st.p = dp;
-      st.q = dq;
-      st.c = c;
-      st.total = static_cast<float>(W);
-      st.kind = kind;
-      st.node = j;
-      st.n_res = residual;
-      st.pad = 0;
-      P.stats[unit] = st;
-      P.final_unit[seq] = static_cast<int>(unit);
-      queue_refine(P, seq, unit, j, near);
+      const int v = ctl.job_v;
+      draw_sync();
+      pjob<TE>(P, ctl, v);
     }
     draw_sync();
   }
 }
 
 template <typename TE>
-__global__ void __launch_bounds__(kPThreads, 2) pass_kernel(const Params P) {
+__global__ void __launch_bounds__(kPThreads, 2) pass_kernel(const Params P, const Exp2Table tab) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   PassCtl &ctl = *reinterpret_cast<PassCtl *>(smem_raw);
   unsigned char *ring = smem_raw + P.data_off;
@@ -1066,12 +1826,26 @@ __global__ void __launch_bounds__(kPThreads, 2) pass_kernel(const Params P) {
   } else if (warp == kPProducerWarp) {
     if (lane == 0) producer_loop<TE>(P, ctl, ring, total);
   } else {
-    draw_loop<TE>(P, ctl, step_tot);
+    draw_loop<TE>(P, ctl, step_tot, tab);
   }
 }
 
+// Job split of the draws for a grid of G CTAs: about 32 weight jobs and 32
+// precise jobs per draw, whole 256-entry steps each, at most G weight jobs.
+void set_job_split(Params &P, int G) {
+  const int steps = P.steps;
+  int kf = steps < kPWeightJobs ? steps : kPWeightJobs;
+  if (kf > G) kf = G;
+  P.wj_steps = (steps + kf - 1) / kf;
+  P.wj = (steps + P.wj_steps - 1) / P.wj_steps;
+  P.wj_stride = G / P.wj;
+  const int kp = steps < kPPreciseJobs ? steps : kPPreciseJobs;
+  P.pj_steps = (steps + kp - 1) / kp;
+  P.pj = (steps + P.pj_steps - 1) / P.pj_steps;
+}
+
 template <typename TE>
-cudaError_t launch_pass_t(const Params &P, size_t smem, cudaStream_t stream) {
+cudaError_t launch_pass_t(Params P, const Exp2Table &tab, size_t smem, cudaStream_t stream) {
   static int cached_dev = -1, cached_smem = -1, cached_blocks = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1090,14 +1864,16 @@ cudaError_t launch_pass_t(const Params &P, size_t smem, cudaStream_t stream) {
     cached_dev = dev;
     cached_smem = static_cast<int>(smem);
   }
-  void *args[] = {const_cast<Params *>(&P)};
+  set_job_split(P, cached_blocks);
+  void *args[] = {&P, const_cast<Exp2Table *>(&tab)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(pass_kernel<TE>),
                                      dim3(cached_blocks), dim3(kPThreads), args, smem, stream);
 }
 
-cudaError_t launch_pass(const Params &P, int esize, size_t smem, cudaStream_t stream) {
-  return esize == 2 ? launch_pass_t<uint16_t>(P, smem, stream)
-                    : launch_pass_t<float>(P, smem, stream);
+cudaError_t launch_pass(const Params &P, int esize, const Exp2Table &tab, size_t smem,
+                        cudaStream_t stream) {
+  return esize == 2 ? launch_pass_t<uint16_t>(P, tab, smem, stream)
+                    : launch_pass_t<float>(P, tab, smem, stream);
 }
 
 size_t pass_ctl_bytes() { return sizeof(PassCtl); }

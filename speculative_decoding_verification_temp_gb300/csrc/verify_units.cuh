@@ -77,6 +77,37 @@ struct UnitOut {
 // boundary is redrawn in double-float arithmetic by the refine kernel.
 constexpr float kRefineGuard = 4e-6f;
 
+// The precise redraw runs on at most this many CTAs.
+constexpr int kRefineMaxGrid = 1024;
+
+// Precise-redraw jobs per phase of one chain draw in the pass kernel (at most).
+constexpr int kPassPreciseJobs = 64;
+
+// One work unit of the precise redraw (a slice of one queued draw's
+// vocabulary): its partial sums, published for the other units of the draw.
+// A chain's final draw, published by the sequence's deciding group for the
+// groups that run its weight jobs (chain pass kernel).
+struct __align__(16) PassSeq {
+  RowDesc dp, dq;  // the draw distribution: [p - q]_+ (residual) or p
+  float u;         // draw uniform
+  float W;         // single-precision total of the draw weights
+  int residual;
+  int j;           // draw position
+  uint32_t flags;
+  int kind;        // 0: bonus draw, 1: one-hot, 2: residual draw (UnitStats::kind)
+  int draw;        // 1: weight jobs run the draw; 0: the token needed no draw
+};
+
+struct __align__(16) RefinePart {
+  double a, b;           // shares of the softmax normalisers S_p, S_q
+  double rw;             // share of a residual round's total W_s
+  double w;              // share of the final draw's total
+  double warp[kWarps];   // per-warp totals of the final weights
+  int wlast[kWarps];     // per-warp last entry with positive weight (-1: none)
+  int last;              // the unit's last entry with positive weight
+  int pad[3];
+};
+
 struct Params {
   const void *target;
   long long ld_t;
@@ -128,6 +159,9 @@ struct Params {
   // precise redraw of final draws near a CDF boundary
   int4 *refine;                   // [nseq] (seq, unit, output position, 0)
   uint32_t *refine_ctr;           // entries in `refine`
+  RefinePart *rpart;              // [max(kRefineMaxGrid, nseq)] work-unit partials
+  double *rc;                     // [nseq] residual multiplier of each queued draw
+  uint32_t *rbar;                 // grid-barrier arrivals of the redraw kernel
   // chain pass kernel
   unsigned long long *srec;       // [rows][chunks][8] per-warp records, 0 = not yet written
   uint32_t *seq_cnt;              // [nseq] chunks of the sequence with stored records (a hint)
@@ -135,6 +169,19 @@ struct Params {
   int chunk_elems;                // entries per chunk
   int cpr;                        // chunks per row
   int steps;                      // draw search steps per row (256 entries each)
+  // chain pass kernel: draws split into jobs
+  unsigned long long *pseqw;      // [nseq][sizeof(PassSeq) / 4] draw descriptors, one 32-bit
+                                  //   word per 64-bit entry with a nonzero tag (0: unset)
+  uint32_t *sctr;                 // [nseq][4] weight jobs started, precise normaliser jobs
+                                  //   done, precise weight jobs done (entry 0 unused)
+  unsigned long long *fstep;      // [nseq][steps] single-precision step totals, tagged (0: unset)
+  double *pstep;                  // [nseq][steps] double-float step totals
+  double *ppart;                  // [nseq][pj][2] shares of S_p, S_q
+  int *near_list;                 // [nseq] sequence + 1 of each precise redraw (0: unset)
+  uint32_t *pctr;                 // [0] precise redraws queued, [1] precise jobs claimed,
+                                  // [2] sequences final
+  int wj, wj_steps, wj_stride;    // weight jobs per draw, steps per job, group stride
+  int pj, pj_steps;               // precise jobs per phase, steps per job
 };
 
 
