@@ -14,7 +14,7 @@ Pages followed
   tannlonggtaoo.github.io "Speculative Decoding", § Greedy Sampling:
   temperature 0 reduces verification to comparing against the argmax.
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
   * greedy / argmax tie-break: the lowest index among the maxima;
   * top-k selects on the raw logits (before temperature); the threshold is the
     k-th largest raw value and every entry >= threshold is kept, so ties at the
