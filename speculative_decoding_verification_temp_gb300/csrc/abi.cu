@@ -208,7 +208,7 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
   const size_t end_stream = off;
   // pass kernel
   off = base;
-  L.pstep = take(static_cast<size_t>(pseqs * psteps) * sizeof(double));
+  L.pstep = take(static_cast<size_t>(pseqs * psteps) * 2 * sizeof(double));
   L.ppart = take(static_cast<size_t>(pseqs) * sv::kPassPreciseJobs * 2 * sizeof(double));
   L.total = std::max(off, end_stream);
   return L;

@@ -882,10 +882,10 @@ __device__ int pass_draw(const Params &P, PassCtl &ctl, float *step_tot, const T
 // sequence's owner searches once the job count is complete: a double-
 // precision prefix over the step totals finds the step, one warp scans it.
 // Draws whose single-precision search lands within the refine guard of a
-// boundary are queued for the precise redraw: per queued draw, pj normaliser
-// jobs (double-float shares of S_p and S_q) and pj weight jobs (double-float
-// step totals), claimed by groups with no other work left; the last weight
-// job searches in double precision and overwrites the token.
+// boundary are queued for the precise redraw: per queued draw, pj jobs of
+// double-float step sums and normaliser shares, claimed by groups with no
+// other work left; the last job searches in double precision and overwrites
+// the token.
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
   uint32_t v;
@@ -1394,28 +1394,71 @@ __device__ __forceinline__ double pshare_sum(const Params &P, int s, int which) 
   return __shfl_sync(0xFFFFFFFFu, v, 0);
 }
 
-// Double-precision search of a precise redraw over its step totals, then the
-// scan of the owning step with double-float weights; overwrites the token.
+// Double-precision search of a precise redraw (the group that completed the
+// draw's jobs).  The step totals are A - rho B with rho = S_p / S_q from the
+// normaliser shares (A alone for a draw from p); steps a job marked
+// uncertain are first recomputed entry by entry.  One warp then finds the
+// step by a prefix over its lanes' runs of steps and scans it with double-
+// float weights; the token is overwritten.
 template <typename TE>
 __device__ void psearch(const Params &P, PassCtl &ctl, int s, const TE *gp, const TE *gq,
-                        const HpRow &rp, const HpRow &rq, Df rho, bool vec) {
+                        const HpRow &rp, const HpRow &rq, bool vec) {
   const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
   const PassSeq &ps = ctl.ps;
   const int nsteps = P.steps;
+  double *pa = P.pstep + static_cast<long long>(s) * 2 * nsteps;
+  double *pb = pa + nsteps;
+  double rhod = 0.0;
+  Df rho{0.f, 0.f};
+  if (ps.residual) {
+    const double Sp = pshare_sum(P, s, 0), Sq = pshare_sum(P, s, 1);
+    rhod = Sp / Sq;
+    rho = df_from_double(rhod);
+  }
+  if (t == 0) ctl.redo = static_cast<int>(__ldcg(P.sctr + 4ll * s + 3));
+  draw_sync();
+  if (ctl.redo) {
+    // uncertain steps: their exact totals, one warp per step
+    for (int base = w * 32; base < nsteps; base += kPDrawWarps * 32) {
+      const int st = base + lane;
+      unsigned todo = __ballot_sync(0xFFFFFFFFu, st < nsteps && __ldcg(pb + st) < 0.0);
+      while (todo) {
+        const int x = base + __ffs(todo) - 1;
+        todo &= todo - 1;
+        Df wd[8];
+        pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, x * kPStep + lane * 8, P.V, vec, ctl, wd);
+        Df acc{0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = df_add(acc, wd[e]);
+        double v = df_to_double(acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        if (lane == 0) {
+          pa[x] = v;
+          pb[x] = 0.0;
+        }
+      }
+    }
+    __threadfence_block();
+    draw_sync();
+  }
   if (w == 0) {
-    const double *pst = P.pstep + static_cast<long long>(s) * nsteps;
     const int per = (nsteps + 31) / 32;
     const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
     double seg = 0.0;
     int lastpos = -1;
-    for (int b0 = s0; b0 < s1; b0 += 8) {  // eight loads in flight
-      double x[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = b0 + i < s1 ? __ldcg(pst + b0 + i) : 0.0;
+    for (int b0 = s0; b0 < s1; b0 += 8) {  // eight pairs of loads in flight
+      double xa[8], xb[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        seg += x[i];
-        if (x[i] > 0.0) lastpos = b0 + i;
+        xa[i] = b0 + i < s1 ? __ldcg(pa + b0 + i) : 0.0;
+        xb[i] = b0 + i < s1 ? __ldcg(pb + b0 + i) : 0.0;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const double x = xa[i] - rhod * xb[i];
+        seg += x;
+        if (x > 0.0) lastpos = b0 + i;
       }
     }
     double incl = seg;
@@ -1436,7 +1479,8 @@ __device__ void psearch(const Params &P, PassCtl &ctl, int s, const TE *gp, cons
         for (int b0 = s0; b0 < s1 && step < 0; b0 += 8) {
           double xs[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) xs[i] = b0 + i < s1 ? __ldcg(pst + b0 + i) : 0.0;
+          for (int i = 0; i < 8; ++i)
+            xs[i] = b0 + i < s1 ? __ldcg(pa + b0 + i) - rhod * __ldcg(pb + b0 + i) : 0.0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             if (step < 0 && b0 + i < s1) {
@@ -1510,14 +1554,19 @@ __device__ void psearch(const Params &P, PassCtl &ctl, int s, const TE *gp, cons
   draw_sync();
 }
 
-// Precise job v: redraw item v / (2 pj); normaliser share (phase 0) or step
-// totals (phase 1) of slice v % pj.
+// Precise job v: redraw item v / pj, slice v % pj of its steps.  For each
+// 256-entry step of the slice it stores the double-float sums A of e_p and B
+// of e_q over the entries whose weight e_p - rho e_q is certainly positive,
+// classified with the single-precision rho of the row statistics (within
+// 1e-6 of the exact one; an entry is certain when |e_p - rho e_q| > 1e-5 e_p),
+// or B = -1 when an entry of the step is uncertain; and the slice's shares of
+// S_p and S_q.  A draw from p stores A = the sum of e_p, B = 0.  The job that
+// completes the item's count searches.
 template <typename TE>
 __device__ void pjob(const Params &P, PassCtl &ctl, int v) {
   const int t = threadIdx.x - kPDrawWarp0 * 32, lane = t & 31, w = t >> 5;
   const int kp = P.pj;
-  const int item = v / (2 * kp), r = v - item * 2 * kp;
-  const int phase = r < kp ? 0 : 1, k = r < kp ? r : r - kp;
+  const int item = v / kp, k = v - item * kp;
   if (t == 0) {
     const long long t0 = pass_ns();
     int sv1;
@@ -1541,93 +1590,85 @@ __device__ void pjob(const Params &P, PassCtl &ctl, int v) {
   const bool vec = ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(gq)) & 15u) == 0;
   const HpRow rp = hp_row(ps.dp, __ldg(P.Tp + s));
   const HpRow rq = ps.residual ? hp_row(ps.dq, __ldg(P.Tq + s)) : rp;
+  const int residual = ps.residual;
+  const float rho_a = residual ? ps.dq.invS / ps.dp.invS : 0.f;  // S_p / S_q, single precision
   const int V = P.V;
   const int b0 = k * P.pj_steps, b1 = min(P.steps, b0 + P.pj_steps);
+  double *pa = P.pstep + static_cast<long long>(s) * 2 * P.steps;
+  double *pb = pa + P.steps;
   uint32_t *cnt = P.sctr + 4ll * s;
-  if (phase == 0) {
-    if (ps.residual) {
-      double a = 0.0, b = 0.0;
-      for (int st = b0 + w; st < b1; st += kPDrawWarps) {
-        const int base = st * kPStep + lane * 8;
-        float zp[8], zq[8];
-        hp_load8<TE>(gp, base, V, vec, zp);
-        hp_load8<TE>(gq, base, V, vec, zq);
-        Df sp{0.f, 0.f}, sq{0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          sp = df_add(sp, hp_exp(rp, zp[e], ctl.tab_hi, ctl.tab_lo));
-          sq = df_add(sq, hp_exp(rq, zq[e], ctl.tab_hi, ctl.tab_lo));
-        }
-        a += df_to_double(sp);
-        b += df_to_double(sq);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, off);
-        b += __shfl_xor_sync(0xFFFFFFFFu, b, off);
-      }
-      if (lane == 0) {
-        ctl.pred[0][w] = a;
-        ctl.pred[1][w] = b;
-      }
-      draw_sync();
-      if (t == 0) {
-        double A = 0.0, B = 0.0;
-        for (int x = 0; x < kPDrawWarps; ++x) {
-          A += ctl.pred[0][x];
-          B += ctl.pred[1][x];
-        }
-        double *dst = P.ppart + (static_cast<long long>(s) * kp + k) * 2;
-        dst[0] = A;
-        dst[1] = B;
-      }
-    }
-    if (t == 0) {
-      __threadfence();
-      atomicAdd(cnt + 2, 1u);
-    }
-    draw_sync();
-    return;
-  }
-  // phase 1: wait for every normaliser share of the draw
-  if (t == 0) {
-    const long long t0 = pass_ns();
-    while (ld_acquire_u32(cnt + 2) < static_cast<uint32_t>(kp)) {
-      if (pass_ns() - t0 > kPPollLimitNs) {
-        atomicOr(P.err, 1u);
-        break;
-      }
-      __nanosleep(100);
-    }
-  }
-  draw_sync();
-  Df rho{0.f, 0.f};
-  if (ps.residual) {
-    const double Sp = pshare_sum(P, s, 0), Sq = pshare_sum(P, s, 1);
-    rho = df_from_double(Sp / Sq);
-  }
-  double *pst = P.pstep + static_cast<long long>(s) * P.steps;
+  double sp_tot = 0.0, sq_tot = 0.0;
+  bool unc_any = false;
   for (int st = b0 + w; st < b1; st += kPDrawWarps) {
     const int base = st * kPStep + lane * 8;
-    Df wd[8];
-    pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, base, V, vec, ctl, wd);
-    Df acc{0.f, 0.f};
+    float zp[8], zq[8];
+    hp_load8<TE>(gp, base, V, vec, zp);
+    if (residual) hp_load8<TE>(gq, base, V, vec, zq);
+    Df sp{0.f, 0.f}, sq{0.f, 0.f}, a{0.f, 0.f}, b{0.f, 0.f};
+    bool unc = false;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = df_add(acc, wd[e]);
-    double x = df_to_double(acc);
+    for (int e = 0; e < 8; ++e) {
+      const Df ep = hp_exp(rp, zp[e], ctl.tab_hi, ctl.tab_lo);
+      sp = df_add(sp, ep);
+      if (!residual) continue;
+      const Df eq = hp_exp(rq, zq[e], ctl.tab_hi, ctl.tab_lo);
+      sq = df_add(sq, eq);
+      if (ep.hi > 0.f) {
+        const float d = fmaf(-rho_a, eq.hi, ep.hi);
+        if (d > 1e-5f * ep.hi) {
+          a = df_add(a, ep);
+          b = df_add(b, eq);
+        } else if (d >= -1e-5f * ep.hi) {
+          unc = true;
+        }
+      }
+    }
+    double A = residual ? df_to_double(a) : df_to_double(sp);
+    double Bq = df_to_double(b);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
-    if (lane == 0) pst[st] = x;
+    for (int off = 16; off > 0; off >>= 1) {
+      A += __shfl_xor_sync(0xFFFFFFFFu, A, off);
+      Bq += __shfl_xor_sync(0xFFFFFFFFu, Bq, off);
+    }
+    unc = __any_sync(0xFFFFFFFFu, unc);
+    if (lane == 0) {
+      pa[st] = A;
+      pb[st] = unc ? -1.0 : Bq;
+    }
+    unc_any |= unc;
+    sp_tot += df_to_double(sp);
+    sq_tot += df_to_double(sq);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sp_tot += __shfl_xor_sync(0xFFFFFFFFu, sp_tot, off);
+    sq_tot += __shfl_xor_sync(0xFFFFFFFFu, sq_tot, off);
+  }
+  if (lane == 0) {
+    ctl.pred[0][w] = sp_tot;
+    ctl.pred[1][w] = sq_tot;
+    ctl.red_i[w] = unc_any ? 1 : 0;
   }
   draw_sync();
   if (t == 0) {
+    double A = 0.0, B = 0.0;
+    int u = 0;
+    for (int x = 0; x < kPDrawWarps; ++x) {
+      A += ctl.pred[0][x];
+      B += ctl.pred[1][x];
+      u |= ctl.red_i[x];
+    }
+    double *dst = P.ppart + (static_cast<long long>(s) * kp + k) * 2;
+    dst[0] = A;
+    dst[1] = B;
+    if (u) atomicAdd(cnt + 3, 1u);
     __threadfence();
-    const uint32_t old = atomicAdd(cnt + 3, 1u);
+    const uint32_t old = atomicAdd(cnt + 2, 1u);
     ctl.redo = old + 1 == static_cast<uint32_t>(kp) ? 1 : 0;
     if (ctl.redo) __threadfence();
   }
   draw_sync();
-  if (ctl.redo) psearch<TE>(P, ctl, s, gp, gq, rp, rq, rho, vec);
+  if (ctl.redo) psearch<TE>(P, ctl, s, gp, gq, rp, rq, vec);
 }
 
 // Weight jobs of group g: job (s, k) belongs to group (s + 1 + k stride) mod G,
@@ -1749,7 +1790,7 @@ __device__ void draw_loop(const Params &P, PassCtl &ctl, float *step_tot, const 
         // precise jobs once this group's own decides and weight jobs are done:
         // claim a job id (fetch-and-add), run it once its redraw is queued
         const bool free = ns < 0 && nd >= P.nseq && nf >= P.nseq;
-        const uint32_t per_item = 2u * static_cast<uint32_t>(P.pj);
+        const uint32_t per_item = static_cast<uint32_t>(P.pj);
         if (free && ctl.held_v < 0 && claimed < nq * per_item)
           ctl.held_v = static_cast<int>(atomicAdd(P.pctr + 1, 1u));
         if (free && ctl.held_v >= 0 && static_cast<uint32_t>(ctl.held_v) < nq * per_item) {

@@ -172,10 +172,10 @@ struct Params {
   // chain pass kernel: draws split into jobs
   unsigned long long *pseqw;      // [nseq][sizeof(PassSeq) / 4] draw descriptors, one 32-bit
                                   //   word per 64-bit entry with a nonzero tag (0: unset)
-  uint32_t *sctr;                 // [nseq][4] weight jobs started, precise normaliser jobs
-                                  //   done, precise weight jobs done (entry 0 unused)
+  uint32_t *sctr;                 // [nseq][4] [1] weight jobs done, [2] precise jobs done,
+                                  //   [3] precise jobs that met an uncertain step
   unsigned long long *fstep;      // [nseq][steps] single-precision step totals, tagged (0: unset)
-  double *pstep;                  // [nseq][steps] double-float step totals
+  double *pstep;                  // [nseq][2][steps] precise step sums A (e_p) and B (e_q)
   double *ppart;                  // [nseq][pj][2] shares of S_p, S_q
   int *near_list;                 // [nseq] sequence + 1 of each precise redraw (0: unset)
   uint32_t *pctr;                 // [0] precise redraws queued, [1] precise jobs claimed,

@@ -140,3 +140,47 @@ def test_tree_draws_at_boundaries(path, exception_log):
     n = check(toks, res.num_accepted.cpu().numpy(), want, "tree", exception_log,
               f"boundary-tree-{path}")
     assert n >= 12
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_chain_draws_at_boundaries_with_equal_entries(path, exception_log):
+    """Draft rows that are the target rows with a few entries swapped: S_p =
+    S_q, so p = q on every other entry and [p - q]_+ lives on the swapped
+    entries alone.  Every entry with p = q sits on the edge of the residual's
+    support, which the precise redraw must treat exactly (its fast
+    classification of entries cannot decide them)."""
+    B, gamma, V = 12, 2, 4096
+    rng = np.random.default_rng(11)
+    target = workloads.round_bf16_inplace(
+        (2.0 * rng.standard_normal((B, gamma + 1, V))).astype(np.float32))
+    draft = target[:, :gamma].copy()
+    tokens = np.zeros((B, gamma), np.int32)
+    for b in range(B):
+        for i in range(gamma):
+            row = draft[b, i]
+            order = np.argsort(row)
+            # swap eight pairs of entries far apart in value (p and q differ there)
+            lo, hi = order[:8], order[-8:]
+            row[lo], row[hi] = target[b, i, hi], target[b, i, lo]
+            tokens[b, i] = lo[0]  # now q(x) > p(x): a likely rejection
+    w = dict(kind="chain", B=B, gamma=gamma, V=V, dtype="bf16", target=target, draft=draft,
+             tokens=tokens, target_temperature=np.ones(B, np.float32),
+             draft_temperature=np.ones(B, np.float32), target_top_k=None, draft_top_k=None,
+             seed=77)
+    uo = philox_override(w["seed"], B, gamma + 1)
+    uo[:, :, 0] = np.float32(0.99999)  # reject at the first position
+    prng = np.random.default_rng(12)
+    for r in oracle_chain(w, uniform_override=uo):
+        wt = chain_draw_weights(w, r)
+        if wt is None:
+            continue
+        u = near_boundary(wt, prng, above=r["seq"] % 2 == 0)
+        if u is not None:
+            uo[r["seq"], r["num_accepted"], 1] = u
+    want = oracle_chain(w, uniform_override=uo)
+    assert sum(r["num_accepted"] < gamma for r in want) >= B // 2
+    exception_log.add_rows(len(want) * (gamma + 1))
+    res = run_chain(w, uniform_override=uo, force_resident=path == "resident")
+    n = check(res.tokens.cpu().numpy(), res.num_accepted.cpu().numpy(), want, "seq",
+              exception_log, f"boundary-equal-entries-{path}")
+    assert n >= B - 2
