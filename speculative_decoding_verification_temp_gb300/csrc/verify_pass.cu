@@ -58,6 +58,7 @@ constexpr int kPMaxGamma = 31;
 constexpr int kPMaxRows = 2 * kPMaxGamma + 1;
 constexpr int kPStep = 256;                        // entries per draw-search step
 constexpr int kPWeightJobs = 32;                   // weight jobs per draw (at most)
+static_assert(kPWeightJobs <= 32, "a group's weight-job residues are sorted by one warp");
 constexpr int kPPreciseJobs = kPassPreciseJobs;    // precise jobs per phase (at most)
 constexpr long long kPPollLimitNs = 2000000000ll;  // give up waiting after about 2 s
 constexpr uint32_t kNoIndex = 0x3FFFFFFFu;         // record index: no finite entry
@@ -103,6 +104,7 @@ struct PassCtl {
   long long idle_t0;
   int act, next_dec, next_f, next_k, job_v, job_s;
   int tokx[kPMaxGamma + 1];
+  float u_draw;  // the draw uniform at the decided position
   int fj_s[32], fj_k[32];  // the group's weight-job residues, ascending
   int fj_i, fj_m;
   int next_srch;   // owned sequence whose weight jobs are awaited (-1: none)
@@ -913,9 +915,11 @@ __device__ __forceinline__ void publish_seq(const Params &P, PassCtl &ctl, int s
 }
 
 // Copy sequence s's descriptor into shared memory (draw group), reading again
-// while any entry is still unset.
-__device__ void load_seq(const Params &P, PassCtl &ctl, int s) {
+// while any entry is still unset.  Returns false (in every thread) when the
+// bounded wait gave up: the scratch then holds no usable descriptor.
+__device__ bool load_seq(const Params &P, PassCtl &ctl, int s) {
   const int t = threadIdx.x - kPDrawWarp0 * 32;
+  if (t == 0) ctl.redo = 1;
   if (t < 32) {
     const unsigned long long *src = P.pseqw + static_cast<long long>(s) * kSeqWords;
     uint32_t *dst = reinterpret_cast<uint32_t *>(&ctl.ps);
@@ -929,13 +933,19 @@ __device__ void load_seq(const Params &P, PassCtl &ctl, int s) {
       }
       if (__all_sync(0xFFFFFFFFu, ok)) break;
       if (pass_ns() - t0 > kPPollLimitNs) {
-        if (t == 0) atomicOr(P.err, 1u);
+        if (t == 0) {
+          atomicOr(P.err, 1u);
+          ctl.redo = 0;
+        }
         break;
       }
       __nanosleep(100);
     }
   }
   draw_sync();
+  const bool good = ctl.redo != 0;
+  draw_sync();
+  return good;
 }
 
 // Rows of a sequence's draw position j.
@@ -1012,7 +1022,8 @@ __device__ void decide(const Params &P, PassCtl &ctl, int seq) {
       __nanosleep(200);
     }
   }
-  for (int r = 0; r < rps; ++r) {
+  if (t < rps) {  // one thread per row
+    const int r = t;
     const bool draft = r > gamma;
     const bool arg = draft ? q_arg : p_arg;
     const bool tbad = draft ? tq_bad : tp_bad;
@@ -1028,12 +1039,7 @@ __device__ void decide(const Params &P, PassCtl &ctl, int seq) {
       d.a = pr.a;
       if (tbad || pr.bad) d.flags = SPEC_FLAG_NONFINITE;
     } else if (pr.bad) {
-      const long long row = draft ? static_cast<long long>(seq) * gamma + (r - gamma - 1)
-                                  : static_cast<long long>(seq) * (gamma + 1) + r;
-      const TE *g = static_cast<const TE *>(
-          row_ptr(draft ? P.draft : P.target, row, draft ? P.ld_d : P.ld_t, sizeof(TE)));
-      d.onehot = 1;
-      d.a = finite_argmax_row<TE>(g, V, ctl);
+      d.onehot = 1;  // the finite argmax is filled in below
       d.flags = SPEC_FLAG_NONFINITE;
     } else {
       const float kk = draft ? kq : kp;
@@ -1043,7 +1049,18 @@ __device__ void decide(const Params &P, PassCtl &ctl, int seq) {
       d.nmk = -pr.m * kk;
       d.invS = 1.f / pr.S;
     }
-    if (t == 0) ctl.desc[r] = d;
+    ctl.desc[r] = d;
+  }
+  draw_sync();
+  for (int r = 0; r < rps; ++r) {  // rows whose sampling statistics were not finite (rare)
+    const bool draft = r > gamma;
+    if ((draft ? q_arg : p_arg) || !ctl.row[r].bad) continue;
+    const long long row = draft ? static_cast<long long>(seq) * gamma + (r - gamma - 1)
+                                : static_cast<long long>(seq) * (gamma + 1) + r;
+    const TE *g = static_cast<const TE *>(
+        row_ptr(draft ? P.draft : P.target, row, draft ? P.ld_d : P.ld_t, sizeof(TE)));
+    const int a = finite_argmax_row<TE>(g, V, ctl);
+    if (t == 0) ctl.desc[r].a = a;
   }
   draw_sync();
   // 2. acceptance tests, one lane per draft position
@@ -1082,6 +1099,9 @@ __device__ void decide(const Params &P, PassCtl &ctl, int seq) {
     }
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, reject && i < gamma);
     const int j = rej ? __ffs(rej) - 1 : gamma;
+    // the draw uniform at every position, computed beside the tests
+    const float ud = i <= gamma ? unit_uniform(P, seq, i, 1) : 0.f;
+    const float u_draw = __shfl_sync(0xFFFFFFFFu, ud, j);
     uint32_t fo = (i < j) ? f : 0u;
     fo = warp_or(fo);
     if (lane == 0) {
@@ -1089,6 +1109,7 @@ __device__ void decide(const Params &P, PassCtl &ctl, int seq) {
       else fo |= ctl.desc[gamma].flags;
       ctl.j = j;
       ctl.flags = fo;
+      ctl.u_draw = u_draw;
     }
   }
   draw_sync();
@@ -1122,7 +1143,7 @@ __device__ void decide(const Params &P, PassCtl &ctl, int seq) {
       count_final(P);
     } else {
       ps.kind = j < gamma ? 2 : 0;
-      ps.u = unit_uniform(P, seq, j, 1);
+      ps.u = ctl.u_draw;
       ps.draw = 1;
     }
     ctl.ps = ps;
@@ -1582,9 +1603,9 @@ __device__ void pjob(const Params &P, PassCtl &ctl, int v) {
   }
   draw_sync();
   const int s = ctl.job_s;
-  if (s < 0) return;
-  load_seq(P, ctl, s);
+  if (s < 0 || s >= P.nseq || !load_seq(P, ctl, s)) return;
   const PassSeq &ps = ctl.ps;
+  if (ps.j < 0 || ps.j > P.gamma) return;  // not a drawn position: never use it as a row
   const TE *gp, *gq;
   draw_rows<TE>(P, s, ps.j, gp, gq);
   const bool vec = ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(gq)) & 15u) == 0;
@@ -1816,7 +1837,7 @@ __device__ void draw_loop(const Params &P, PassCtl &ctl, float *step_tot, const 
     if (act == kActExit) break;
     if (act == kActIdle) {
       if (t == 0) __nanosleep(sleep_ns);
-      sleep_ns = min(sleep_ns * 2u, 2048u);
+      sleep_ns = min(sleep_ns * 2u, 512u);
       continue;
     }
     sleep_ns = 64;
