@@ -10,12 +10,13 @@
 //   warp 8 (producer): streams the CTA's chunks into a ring of shared-memory
 //     slots with bulk asynchronous copies (cp.async.bulk, one "full" and one
 //     "empty" mbarrier per slot), with each chunk's description beside it.
-//     When the consumers hand a slot back it refills it and adds the finished
-//     chunk to its sequence's counter (a relaxed add, no fence: only a hint);
+//     When the consumers hand a slot back it refills it;
 //   warps 0-7 (consumers): each reduces its eighth of the chunk to one 64-bit
 //     record, the (max, sum of 2^((z - max) log2(e) / T)) of a sampling row or
 //     the (finite max, lowest index + 1) of a greedy row, and stores it in one
 //     access (a record is never seen half written; zero means not written);
+//     the last warp done with a chunk adds it to its sequence's counter (a
+//     relaxed add, no fence: only a hint);
 //   warps 9-12 (the draw group): a small scheduler that takes, in order of
 //     priority, (1) the search of its owned sequence once the sequence's
 //     weight jobs are all counted, (2) the decision of its next owned sequence
@@ -57,7 +58,7 @@ constexpr int kPMaxRing = 8;
 constexpr int kPMaxGamma = 31;
 constexpr int kPMaxRows = 2 * kPMaxGamma + 1;
 constexpr int kPStep = 256;                        // entries per draw-search step
-constexpr int kPWeightJobs = 32;                   // weight jobs per draw (at most)
+constexpr int kPWeightJobs = 16;                   // weight jobs per draw (at most)
 static_assert(kPWeightJobs <= 32, "a group's weight-job residues are sorted by one warp");
 constexpr int kPPreciseJobs = kPassPreciseJobs;    // precise jobs per phase (at most)
 constexpr long long kPPollLimitNs = 2000000000ll;  // give up waiting after about 2 s
@@ -73,7 +74,7 @@ struct SlotInfo {
   float k;         // log2(e) / T, 0 for a greedy row
   int arg;         // greedy row: argmax record
   int v0;          // vocabulary index of the chunk's first entry
-  int pad;
+  int seq;         // sequence of the chunk
 };
 
 struct PassRow {
@@ -86,6 +87,7 @@ struct PassCtl {
   unsigned long long full[kPMaxRing];
   unsigned long long empty[kPMaxRing];
   SlotInfo info[kPMaxRing];
+  int slot_done[kPMaxRing];  // consumer warps finished with the slot's chunk
   PassRow row[kPMaxRows];
   RowDesc desc[kPMaxRows];
   double W;
@@ -435,6 +437,13 @@ __device__ void consumer_loop(const Params &P, PassCtl &ctl, unsigned char *ring
           static_cast<unsigned long long>(__float_as_uint(rec.x)) |
           (static_cast<unsigned long long>(__float_as_uint(rec.y)) << 32);
       P.srec[si.rec + warp] = bits;  // one 64-bit store
+      // the last warp done with the chunk counts it for its sequence (relaxed,
+      // no fence: the records validate themselves, the count only says when
+      // to look); it resets the slot's tally before handing the slot back
+      if (atomicAdd(&ctl.slot_done[slot], 1) == kPConsumerWarps - 1) {
+        ctl.slot_done[slot] = 0;
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.seq_cnt + si.seq) : "memory");
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive1(&ctl.empty[slot]);
@@ -444,14 +453,6 @@ __device__ void consumer_loop(const Params &P, PassCtl &ctl, unsigned char *ring
 // ---------------------------------------------------------------------------
 // producer: bulk copies into the ring, chunk completion to the counters
 // ---------------------------------------------------------------------------
-
-// One more chunk of a sequence has its records stored (relaxed: the records
-// validate themselves, the count only says when to look).
-__device__ __forceinline__ void count_chunk(const Params &P, long long k) {
-  const int per_seq = (2 * P.gamma + 1) * P.cpr;
-  const int seq = static_cast<int>(k) / per_seq;
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.seq_cnt + seq) : "memory");
-}
 
 template <typename TE>
 __device__ void producer_loop(const Params &P, PassCtl &ctl, unsigned char *ring,
@@ -468,10 +469,7 @@ __device__ void producer_loop(const Params &P, PassCtl &ctl, unsigned char *ring
   int i = 0;
   for (long long k = blockIdx.x; k < total; k += G, ++i) {
     const int slot = i % NS;
-    if (i >= NS) {
-      wait_done(i - NS);
-      count_chunk(P, k - NS * G);
-    }
+    if (i >= NS) wait_done(i - NS);
     const ChunkInfo ci = chunk_info(P, k);
     const float T = __ldg((ci.draft ? P.Tq : P.Tp) + ci.seq);
     const bool arg = row_is_arg(T);
@@ -488,15 +486,13 @@ __device__ void producer_loop(const Params &P, PassCtl &ctl, unsigned char *ring
     si.k = arg ? 0.f : kLog2e / T;
     si.arg = arg ? 1 : 0;
     si.v0 = ci.c * CE;
+    si.seq = ci.seq;
     mbar_arrive_expect_tx(&ctl.full[slot], bytes);
     if (bytes) bulk_g2s_plain(ring + static_cast<size_t>(slot) * P.slot_bytes, gl, bytes,
                               &ctl.full[slot]);
   }
   const int issued = i;
-  for (int d = max(0, issued - NS); d < issued; ++d) {
-    wait_done(d);
-    count_chunk(P, blockIdx.x + d * G);
-  }
+  for (int d = max(0, issued - NS); d < issued; ++d) wait_done(d);
 }
 
 // ---------------------------------------------------------------------------
@@ -1878,6 +1874,7 @@ __global__ void __launch_bounds__(kPThreads, 2) pass_kernel(const Params P, cons
     for (int s = 0; s < P.ring; ++s) {
       mbar_init(&ctl.full[s], 1);
       mbar_init(&ctl.empty[s], kPConsumerWarps);
+      ctl.slot_done[s] = 0;
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
