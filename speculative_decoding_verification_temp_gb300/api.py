@@ -40,11 +40,12 @@ _WORKSPACES = {}
 
 
 def workspace(device, nbytes):
-    """A zero-filled device workspace of at least nbytes, cached per device.
+    """A device workspace of at least nbytes, cached per device.
 
-    The library leaves a workspace zeroed after every completed call, so the
-    cached buffer can be reused by successive calls on one stream.  Calls that
-    run concurrently on different streams need workspaces of their own.
+    The library needs no initialised workspace: every call first clears the
+    part it relies on, so the cached buffer serves successive calls on one
+    stream.  Calls that run concurrently on different streams need workspaces
+    of their own.
     """
     dev = torch.device(device)
     key = dev.index if dev.index is not None else torch.cuda.current_device()
