@@ -218,6 +218,41 @@ def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
 # tree
 # ---------------------------------------------------------------------------
 
+def overlap(p, q):
+    """beta = sum_x min(p(x), q(x)): the acceptance rate of one position.
+
+    whoami-wesleyyou.top "Speculative Decoding" notes, § Correction 为什么用正
+    残差 (beta := sum_x min{p(x), q(x)}, Z := 1 - beta = sum_x [p(x) - q(x)]_+;
+    beta = 1 when p = q) and § 手稿中的数值例子 (beta = 0.7).
+
+    Works on float64 and on Fraction arrays.  Parity: pinned (the page's
+    worked examples, the identity beta + Z = 1 against positive_residual,
+    p = q, disjoint supports).
+    """
+    return np.minimum(p, q).sum()
+
+
+def chain_overlap(target_logits, draft_logits, target_temperature, draft_temperature,
+                  target_top_k=None, draft_top_k=None):
+    """beta_i for every draft position i of every sequence: [B, gamma] float64.
+
+    Each side's policy is applied as in verify_chain (oracle.policy), then
+    overlap(p_i, q_i).  Rows whose policy flags them non-finite use their
+    one-hot fallback, as the verifier does.
+    """
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    out = np.zeros((B, gamma))
+    for b in range(B):
+        kp = 0 if target_top_k is None else int(target_top_k[b])
+        kq = 0 if draft_top_k is None else int(draft_top_k[b])
+        for i in range(gamma):
+            p = policy_distribution(target_logits[b, i], float(target_temperature[b]), kp).dense(V)
+            q = policy_distribution(draft_logits[b, i], float(draft_temperature[b]), kq).dense(V)
+            out[b, i] = overlap(p, q)
+    return out
+
+
 def tree_check(parent, max_depth):
     """Validate a parent array; returns (flags, depth list or None).
 

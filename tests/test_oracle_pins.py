@@ -662,3 +662,43 @@ def test_tree_mask_invalid_links():
     assert list(pos) == [0, 1, -1, -1]
     mask, pos, flags = verify.tree_mask([-1, 0, 1, 2], max_depth=2)
     assert flags == verify.FLAG_DEPTH and list(pos) == [0, 1, 2, 3]
+
+
+def test_overlap_page_examples():
+    g = load_golden("worked_examples.json")
+    a = g["example_a"]
+    p, q = frac_array(a["p"]), frac_array(a["q"])
+    assert verify.overlap(p, q) == F(a["beta"])
+    # the second example: the accepted mass (0.4, 0.2, 0.1) sums to 0.7
+    b = g["example_b"]
+    p, q = frac_array(b["p"]), frac_array(b["q"])
+    assert verify.overlap(p, q) == sum(F(v) for v in b["accepted_mass"])
+
+
+def test_overlap_identities():
+    rng = np.random.default_rng(21)
+    for V in (2, 3, 5, 8):
+        for _ in range(20):
+            p, q = random_rational_dist(rng, V), random_rational_dist(rng, V)
+            _, Z, _ = verify.positive_residual(p, q)
+            assert verify.overlap(p, q) + Z == 1
+            assert verify.overlap(p, p) == 1
+            assert verify.overlap(p, q) == verify.overlap(q, p)
+    # disjoint supports share no mass
+    assert verify.overlap(frac_array(["1", "0"]), frac_array(["0", "1"])) == 0
+
+
+def test_chain_overlap_matches_per_row_policy():
+    rng = np.random.default_rng(22)
+    B, gamma, V = 3, 2, 40
+    zt = rng.normal(size=(B, gamma + 1, V))
+    zd = zt[:, :gamma] + 0.5 * rng.normal(size=(B, gamma, V))
+    t = np.array([1.0, 0.0, 0.7])
+    beta = verify.chain_overlap(zt, zd, t, t)
+    # sequence 1 is greedy on both sides: beta is 1 where the argmaxes agree
+    for i in range(gamma):
+        assert beta[1, i] == float(np.argmax(zt[1, i]) == np.argmax(zd[1, i]))
+    # a softmax pair: beta is the expected acceptance probability under q
+    p = np.exp(zt[0, 0] - zt[0, 0].max()); p /= p.sum()
+    q = np.exp(zd[0, 0] - zd[0, 0].max()); q /= q.sum()
+    assert abs(beta[0, 0] - np.sum(q * np.minimum(1.0, p / q))) < 1e-12
