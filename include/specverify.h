@@ -225,6 +225,32 @@ spec_status spec_tree_mask(const int32_t *parent, int T, int N, int max_depth,
                            uint64_t *out_mask, int32_t *out_position,
                            uint32_t *out_flags, spec_stream_t stream);
 
+/* Per-position overlap of a draft chain: beta_i = sum_v min(p_i(v), q_i(v)),
+ * the acceptance rate of draft position i (1 - beta_i is the mass of the
+ * residual [p_i - q_i]_+).  whoami-wesleyyou.top "Speculative Decoding"
+ * notes, section "Correction 为什么用正残差" (beta := sum_x min{p(x), q(x)}).
+ *
+ * Inputs as for spec_verify_chain (target rows [B, gamma+1, V], draft rows
+ * [B, gamma, V]; target row i and draft row i are compared for i < gamma).
+ * Policies: temperature per sequence (0: greedy, the one-hot at the argmax);
+ * the top_k pointers must be NULL (SPEC_ERR_UNSUPPORTED otherwise).  A row
+ * whose temperature or logits are not finite is the one-hot at its finite
+ * argmax and sets SPEC_FLAG_NONFINITE in out_flags.
+ *
+ * out_beta [B, gamma] float: beta_i of sequence b at b * gamma + i.
+ * out_flags [B] (nullable): cleared by the call, then SPEC_FLAG_NONFINITE.
+ * No workspace.  B = 0 or gamma = 0 is a no-op; B * gamma above 2^28 - 1 is
+ * SPEC_ERR_INVALID_ARG (one cluster of 8 CTAs per position).  Arguments are
+ * checked on the host before any launch; a CUDA launch error is
+ * SPEC_ERR_CUDA and leaves out_beta undefined.
+ */
+spec_status spec_overlap(
+    const void *target_logits, int64_t ld_target,
+    const void *draft_logits, int64_t ld_draft,
+    spec_dtype dtype, int B, int gamma, int V,
+    spec_policy target_policy, spec_policy draft_policy,
+    float *out_beta, uint32_t *out_flags, spec_stream_t stream);
+
 /* Static description of a status code. */
 const char *spec_status_string(spec_status status);
 

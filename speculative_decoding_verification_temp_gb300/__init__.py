@@ -8,6 +8,7 @@ in include/specverify.h); ``api`` is a thin torch binding over it.
                  token from p
   verify_tree    recursive rejection over sibling candidates of token trees
   tree_mask      ancestor-or-self attention masks and depth position ids
+  overlap        per-position acceptance rate beta_i = sum_v min(p_i, q_i)
 """
 
 from ._abi import (FLAG_BAD_TOKEN, FLAG_BAD_TREE, FLAG_DEGENERATE_RESIDUAL, FLAG_DEPTH,  # noqa: F401
@@ -17,9 +18,9 @@ from ._abi import (FLAG_BAD_TOKEN, FLAG_BAD_TREE, FLAG_DEGENERATE_RESIDUAL, FLAG
 def __getattr__(name):
     # the torch binding is imported on first use, so the workload generator
     # and the build step do not need torch
-    if name in ("verify_chain", "verify_chain_static", "verify_tree", "tree_mask",
+    if name in ("verify_chain", "verify_chain_static", "verify_tree", "tree_mask", "overlap",
                 "SpecVerifyError", "workspace",
-                "ChainResult", "TreeResult", "MaskResult", "api"):
+                "ChainResult", "TreeResult", "MaskResult", "OverlapResult", "api"):
         import importlib
         api = importlib.import_module(__name__ + ".api")
         return api if name == "api" else getattr(api, name)

@@ -34,6 +34,7 @@ EXPORTS = (
     "spec_verify_tree_workspace_size",
     "spec_verify_tree",
     "spec_tree_mask",
+    "spec_overlap",
     "spec_status_string",
 )
 
@@ -84,6 +85,9 @@ def load():
     lib.spec_verify_tree.restype = _i
     lib.spec_tree_mask.argtypes = [_p, _i, _i, _i, _p, _p, _p, _p]
     lib.spec_tree_mask.restype = _i
+    lib.spec_overlap.argtypes = [_p, _i64, _p, _i64, _i, _i, _i, _i, spec_policy, spec_policy,
+                                 _p, _p, _p]
+    lib.spec_overlap.restype = _i
     lib.spec_status_string.argtypes = [_i]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib

@@ -258,3 +258,37 @@ def tree_mask(parent, max_depth):
                                       _ptr(flags), _stream(dev))
     _check(code)
     return MaskResult(mask, pos, flags)
+
+
+OverlapResult = namedtuple("OverlapResult", "beta flags")
+
+
+def overlap(target_logits, draft_logits, target_temperature, draft_temperature):
+    """Per-position overlap beta_i = sum_v min(p_i(v), q_i(v)) (see spec_overlap).
+
+    target_logits [B, gamma+1, V] and draft_logits [B, gamma, V] (float32 or
+    bfloat16, CUDA); temperatures per sequence (scalars broadcast).  Returns
+    OverlapResult with beta [B, gamma] float32 and flags [B] int32.
+    """
+    _cuda_tensor(target_logits, "target_logits")
+    _cuda_tensor(draft_logits, "draft_logits")
+    dev = target_logits.device
+    if target_logits.dtype not in _DTYPES or draft_logits.dtype != target_logits.dtype:
+        raise ValueError("logits must both be float32 or both bfloat16")
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    if tuple(draft_logits.shape) != (B, gamma, V):
+        raise ValueError("draft_logits must be [B, gamma, V]")
+    tl, ld_t = _rows(target_logits, "target_logits")
+    dl, ld_d = _rows(draft_logits, "draft_logits")
+    tp = _vec(target_temperature, B, torch.float32, "target_temperature", dev)
+    tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
+    beta = torch.empty((B, gamma), dtype=torch.float32, device=dev)
+    flags = torch.empty(B, dtype=torch.int32, device=dev)
+    lib = _abi.load()
+    code = lib.spec_overlap(_ptr(tl), ld_t, _ptr(dl), ld_d, _DTYPES[target_logits.dtype], B,
+                            gamma, V, _abi.spec_policy(tp.data_ptr(), None),
+                            _abi.spec_policy(tq.data_ptr(), None), _ptr(beta), _ptr(flags),
+                            _stream(dev))
+    _check(code)
+    return OverlapResult(beta, flags)

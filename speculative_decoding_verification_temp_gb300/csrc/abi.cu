@@ -19,6 +19,9 @@ cudaError_t launch_stream(const Params &P, int esize, size_t smem, cudaStream_t 
 cudaError_t launch_first_child(const int32_t *parent, int T, int N, int32_t *first_child,
                                cudaStream_t stream);
 cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream);
+cudaError_t launch_overlap(const void *target, long long ld_t, const void *draft, long long ld_d,
+                           int esize, int B, int gamma, int V, const float *Tp, const float *Tq,
+                           float *out_beta, uint32_t *out_flags, cudaStream_t stream);
 cudaError_t launch_pass(const Params &P, int esize, const Exp2Table &tab, size_t smem,
                         cudaStream_t stream);
 size_t pass_ctl_bytes();
@@ -468,6 +471,28 @@ spec_status spec_tree_mask(const int32_t *parent, int T, int N, int max_depth, u
   if (!parent || !out_mask || !out_position) return SPEC_ERR_INVALID_ARG;
   return map_cuda(sv::launch_tree_mask(parent, T, N, max_depth, out_mask, out_position, out_flags,
                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spec_status spec_overlap(const void *target_logits, int64_t ld_target, const void *draft_logits,
+                         int64_t ld_draft, spec_dtype dtype, int B, int gamma, int V,
+                         spec_policy target_policy, spec_policy draft_policy, float *out_beta,
+                         uint32_t *out_flags, spec_stream_t stream) {
+  const int esize = esize_of(dtype);
+  if (esize == 0 || B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * gamma == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits || !out_beta || !target_policy.temperature ||
+      !draft_policy.temperature || ld_target < V || ld_draft < V)
+    return SPEC_ERR_INVALID_ARG;
+  if (target_policy.top_k || draft_policy.top_k) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * gamma > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (out_flags) {
+    const cudaError_t e = cudaMemsetAsync(out_flags, 0, static_cast<size_t>(B) * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return map_cuda(e);
+  }
+  return map_cuda(sv::launch_overlap(target_logits, ld_target, draft_logits, ld_draft, esize, B,
+                                     gamma, V, target_policy.temperature,
+                                     draft_policy.temperature, out_beta, out_flags, st));
 }
 
 }  // extern "C"

@@ -169,3 +169,31 @@ def test_library_links_no_torch(lib):
                          text=True).stdout
     needed = re.findall(r"\(NEEDED\).*\[(.*)\]", out)
     assert needed and not any("torch" in n or "c10" in n for n in needed)
+
+
+def overlap_call(lib, B=2, gamma=3, V=100, dtype=1, target=FAKE, draft=FAKE, out=FAKE, pol=None,
+                 polq=None, ld=None):
+    pol = pol or policy()
+    polq = polq or pol
+    return lib.spec_overlap(target, ld if ld is not None else V, draft,
+                            ld if ld is not None else V, dtype, B, gamma, V, pol, polq, out, None,
+                            None)
+
+
+def test_overlap_rejects_bad_arguments(lib):
+    INV = _abi.SPEC_ERR_INVALID_ARG
+    assert overlap_call(lib, B=-1) == INV
+    assert overlap_call(lib, gamma=-1) == INV
+    assert overlap_call(lib, V=0) == INV
+    assert overlap_call(lib, dtype=7) == INV
+    assert overlap_call(lib, target=None) == INV
+    assert overlap_call(lib, draft=None) == INV
+    assert overlap_call(lib, out=None) == INV
+    assert overlap_call(lib, ld=99) == INV
+    assert overlap_call(lib, pol=_abi.spec_policy(None, None)) == INV
+    # top-k policies are not supported by the overlap kernel
+    topk = _abi.spec_policy(FAKE.value, FAKE.value)
+    assert overlap_call(lib, polq=topk) == _abi.SPEC_ERR_UNSUPPORTED
+    # nothing to compare: a no-op
+    assert overlap_call(lib, B=0, target=None, draft=None, out=None) == _abi.SPEC_OK
+    assert overlap_call(lib, gamma=0, target=None, draft=None, out=None) == _abi.SPEC_OK
