@@ -240,7 +240,7 @@ spec_status spec_tree_mask(const int32_t *parent, int T, int N, int max_depth,
  * out_beta [B, gamma] float: beta_i of sequence b at b * gamma + i.
  * out_flags [B] (nullable): cleared by the call, then SPEC_FLAG_NONFINITE.
  * No workspace.  B = 0 or gamma = 0 is a no-op; B * gamma above 2^28 - 1 is
- * SPEC_ERR_INVALID_ARG (one cluster of 8 CTAs per position).  Arguments are
+ * SPEC_ERR_INVALID_ARG (one cluster of up to 4 CTAs per position).  Arguments are
  * checked on the host before any launch; a CUDA launch error is
  * SPEC_ERR_CUDA and leaves out_beta undefined.
  */

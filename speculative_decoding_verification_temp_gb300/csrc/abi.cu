@@ -484,7 +484,7 @@ spec_status spec_overlap(const void *target_logits, int64_t ld_target, const voi
       !draft_policy.temperature || ld_target < V || ld_draft < V)
     return SPEC_ERR_INVALID_ARG;
   if (target_policy.top_k || draft_policy.top_k) return SPEC_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * gamma > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * gamma > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;  // headroom for clusters
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (out_flags) {
     const cudaError_t e = cudaMemsetAsync(out_flags, 0, static_cast<size_t>(B) * sizeof(uint32_t), st);

@@ -5,12 +5,13 @@
 // position (Z = 1 - beta is the mass of the residual [p - q]_+); beta = 1
 // when p = q.
 //
-// A cluster of C CTAs per (sequence, position), C in {1, 2, 4, 8}; CTA r owns
+// A cluster of C CTAs per (sequence, position), C in {1, 2, 4}; CTA r owns
 // the slice [r S, (r + 1) S) of the vocabulary, S a multiple of 8.  C is the
-// smallest size whose slices of the row pair take at most 64 KB, raised while
-// the grid would hold fewer than three CTAs per SM.  The slices of the CTAs in
-// flight (a few tens of MB) stay in the L2 between the two passes, so the pair
-// leaves HBM once.
+// smallest size whose slices of the row pair take at most 64 KB (4 when none
+// does), raised while the grid would hold fewer than three CTAs per SM.  The
+// slices of the CTAs in flight (at most about 80 MB) stay in the L2 between
+// the two passes, so the pair leaves HBM once.  (Clusters of 8 measured slower:
+// the per-CTA merges and barriers then outweigh the work.)
 //
 // Pass 1, per row with temperature T > 0: each thread loads four groups of 8
 // at a time, takes their max (packed bf16x2 max), rescales its running sum
@@ -38,7 +39,7 @@ namespace sv {
 
 namespace {
 
-constexpr int kOvCluster = 8;
+constexpr int kOvCluster = 4;
 constexpr size_t kSliceTarget = 64 * 1024;  // both rows' slices, per CTA
 
 // Eight consecutive entries of a row as raw words (-inf outside the slice).

@@ -100,7 +100,7 @@ def test_overlap_nonfinite_rows_are_flagged():
 
 @pytest.mark.parametrize("V", [1, 5, 37])
 def test_overlap_tiny_vocab_with_empty_slices(V):
-    # a vocabulary shorter than the cluster leaves the later slices empty
+    # a vocabulary shorter than the cluster's slices leaves the later slices empty
     rng = np.random.default_rng(43 + V)
     B, gamma = 3, 2
     t = rng.standard_normal((B, gamma + 1, V)).astype(np.float32)
@@ -135,7 +135,7 @@ def test_overlap_greedy_ties_across_slices():
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_overlap_large_vocab(dtype):
-    # 262147 entries: slices of 32776 entries per CTA of a cluster of 8, a
+    # 262147 entries: slices of 65544 entries per CTA of a cluster of 4, a
     # ragged last slice, rows that are not 16-byte aligned (element loads)
     rng = np.random.default_rng(45)
     B, gamma, V = 2, 2, 262147
