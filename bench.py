@@ -13,6 +13,9 @@ Arms:
   --impl reference  the CPU oracle (the plain float64 restatement of the
                     method) on this host's cores, on a bounded sample
 
+--op overlap times the per-position overlap beta_i = sum min(p_i, q_i) of
+the same workload instead (metric: positions per second, B * gamma per step).
+
 Under torchrun each rank verifies its own batch on its own GPU (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
 """
@@ -40,6 +43,9 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "pass_kernel_b256_g7_v128256_bf16.
 # kernels the library launches per chain call on this workload: the pass
 # kernel (it redraws near-boundary draws itself)
 LAUNCHES_PER_STEP = 1
+OVERLAP_METRIC = "overlap positions/s (B*gamma)"
+L2_BYTES = 129e6
+OVERLAP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "overlap_kernel_b256_g7_v128256_bf16.md")
 
 
 def dist_env():
@@ -65,12 +71,12 @@ def job_rate(world, rows_per_rank_step, steps, seconds):
     return world * rows_per_rank_step * steps / seconds
 
 
-def kernel_source_hash():
-    """Hash of the pass kernel's sources: its translation unit (which also
-    holds its launch function) and the device headers it includes."""
+def kernel_source_hash(unit="verify_pass.cu"):
+    """Hash of a kernel's sources: its translation unit (which also holds its
+    launch function) and the device headers."""
     h = hashlib.sha256()
     for name in sorted(os.listdir(CSRC)):
-        if name != "verify_pass.cu" and not name.endswith(".cuh"):
+        if name != unit and not name.endswith(".cuh"):
             continue
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
@@ -87,14 +93,14 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def recorded_traffic():
+def recorded_traffic(path=TRAFFIC_FILE, unit="verify_pass.cu"):
     """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged.
 
     The summary holds lines "- source_hash: H" and "- dram_bytes_per_launch: N".
     """
     rec = {}
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             for line in f:
                 line = line.strip()
                 if line.startswith("- ") and ":" in line:
@@ -102,7 +108,7 @@ def recorded_traffic():
                     rec[key.strip()] = val.strip()
     except OSError:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(unit):
         return None
     try:
         return int(rec["dram_bytes_per_launch"])
@@ -185,7 +191,12 @@ def config_entry(w):
                         "(temperature 1, Zipf logits, draft sigma 0.4)",
             "B": w["B"], "gamma": w["gamma"], "V": w["V"],
             "logit_bytes_per_step": logit_bytes(w),
-            "l2": f"inputs larger than L2 ({logit_bytes(w) / 1e6:.0f} MB of logits per step)"}
+            "l2": l2_note(logit_bytes(w), "logits")}
+
+
+def l2_note(nbytes, what):
+    side = "larger" if nbytes > L2_BYTES else "smaller"
+    return f"inputs {side} than L2 ({nbytes / 1e6:.0f} MB of {what} per step)"
 
 
 def logit_bytes(w):
@@ -348,6 +359,153 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def overlap_bytes(w):
+    """Algorithmic bytes of one overlap call: each (target, draft) row pair of
+    the gamma draft positions read once (the bonus row is not read)."""
+    esize = 2 if w["dtype"] == "bf16" else 4
+    return 2 * w["B"] * w["gamma"] * w["V"] * esize
+
+
+def overlap_config(w):
+    c = config_entry(w)
+    c["workload"] = (f"overlap beta B={w['B']} gamma={w['gamma']} V={w['V']} {w['dtype']} "
+                     "(temperature 1, Zipf logits, draft sigma 0.4)")
+    c["row_pair_bytes_per_step"] = overlap_bytes(w)
+    c["l2"] = l2_note(overlap_bytes(w), "row pairs")
+    return c
+
+
+def oracle_overlap_rate(w, n_seqs):
+    """The CPU oracle's beta on the first n_seqs sequences: (positions/s, seconds)."""
+    from oracle import verify as ov
+    t0 = time.perf_counter()
+    ov.chain_overlap(w["target"][:n_seqs], w["draft"][:n_seqs], w["target_temperature"][:n_seqs],
+                     w["draft_temperature"][:n_seqs])
+    dt = time.perf_counter() - t0
+    return n_seqs * w["gamma"] / dt, dt
+
+
+def run_overlap_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = bench_workload(args)
+    # one sequence per step: a bounded sample of the same workload
+    oracle_overlap_rate(w, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_overlap_rate(w, 1)
+    dt = time.perf_counter() - t0
+    value = w["gamma"] * args.steps / dt
+    line = {
+        "impl": "reference", "metric": OVERLAP_METRIC, "value": value, "unit": "positions/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": overlap_config(w),
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                         "sample": f"the first sequence of {w['B']} per step"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_overlap(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verification_temp_gb300 as sv
+
+    w = bench_workload(args)
+    B, gamma = w["B"], w["gamma"]
+    units = B * gamma
+    nbytes = overlap_bytes(w)
+    target_h = torch.from_numpy(w["target"]).to(torch.bfloat16).pin_memory()
+    draft_h = torch.from_numpy(w["draft"]).to(torch.bfloat16).pin_memory()
+    target, draft = target_h.to(dev), draft_h.to(dev)
+    tp = torch.from_numpy(w["target_temperature"]).to(dev)
+    tq = torch.from_numpy(w["draft_temperature"]).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        sv.overlap(target, draft, tp, tq)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            sv.overlap(target, draft, tp, tq)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    elapsed_ms = max_over_ranks(t_begin.elapsed_time(t_end), world, dev)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        r = sv.overlap(target_h.to(dev, non_blocking=True), draft_h.to(dev, non_blocking=True),
+                       tp, tq)
+        beta = r.beta.to("cpu")
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    avg_launch_ms = statistics.mean(launch_ms)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
+    line = {
+        "metric": OVERLAP_METRIC, "value": job_rate(world, units, args.steps, elapsed_ms / 1e3),
+        "unit": "positions/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": overlap_config(w),
+        "clocks": clk.summary(),
+        "e2e": {"value": job_rate(world, units, 1, e2e_s), "unit": "positions/s",
+                "h2d_bytes_per_step": (target_h.numel() + draft_h.numel()) * 2,
+                "d2h_bytes_per_step": beta.numel() * 4},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(OVERLAP_TRAFFIC_FILE, "overlap.cu"),
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "overlap_kernel (timed per call)",
+                     "launch_ms_avg": avg_launch_ms,
+                     "launch_ms_median": statistics.median(launch_ms)},
+    }
+    if not args.no_cpu_baseline:
+        n = min(B, max(1, args.cpu_seqs // 32))
+        rate, dt = oracle_overlap_rate(w, n)
+        line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"the first {n} of {B} sequences, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -360,8 +518,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per batch (default: the B = 256 workload); for profiling")
+    ap.add_argument("--op", default="verify", choices=["verify", "overlap"],
+                    help="verify: the chain verifier (default); overlap: beta_i per position")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.op == "overlap":
+        if args.impl == "reference":
+            run_overlap_reference(args)
+        else:
+            run_overlap(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
