@@ -14,7 +14,7 @@ Flag bits are the interface values of the library's per-sequence flag word.
 import numpy as np
 
 from . import philox
-from .policy import Dist, policy_distribution
+from .policy import Dist, finite_argmax, policy_distribution
 
 FLAG_BAD_TOKEN = 1
 FLAG_ZERO_Q = 2
@@ -251,6 +251,91 @@ def chain_overlap(target_logits, draft_logits, target_temperature, draft_tempera
             q = policy_distribution(draft_logits[b, i], float(draft_temperature[b]), kq).dense(V)
             out[b, i] = overlap(p, q)
     return out
+
+
+# ---------------------------------------------------------------------------
+# typical acceptance (approximate, not distribution-exact)
+# ---------------------------------------------------------------------------
+
+def entropy(p):
+    """H(p) = -sum_x p(x) ln p(x), natural log, with 0 ln 0 = 0."""
+    p = np.asarray(p, dtype=np.float64)
+    nz = p > 0
+    return float(-(p[nz] * np.log(p[nz])).sum())
+
+
+def typical_threshold(p, epsilon, delta):
+    """min(epsilon, delta * exp(-H(p))): the probability a draft token must exceed.
+
+    whoami-wesleyyou.top "Speculative Decoding" notes, § Medusa-1 与 typical
+    acceptance (the criterion p(x_i | x_<i) > min{epsilon, delta
+    exp[-H(p(. | x_<i))]}, H the entropy; epsilon a fixed threshold, delta
+    scaling the entropy-dependent one).
+    """
+    return min(float(epsilon), float(delta) * float(np.exp(-entropy(p))))
+
+
+def walk_typical(gamma, V, get_p, get_z, tokens, epsilon, delta):
+    """Typical acceptance of one draft chain.
+
+    whoami-wesleyyou.top "Speculative Decoding" notes, § Medusa-1 与 typical
+    acceptance: each draft token x_i is tested against the target's own
+    distribution at its position with p(x_i) > min(epsilon, delta exp(-H)),
+    the longest prefix that passes is kept, and the token that follows it is
+    the target's greedy choice, accepted without a test.  The rule trades the
+    exactness of the min(1, p/q) test for speed: its output law is not the
+    target's (also jennyma11.github.io "11.3 Self-Draft: Medusa、EAGLE-2/3 与
+    Draft Tree", § 11.3.1: typical acceptance is an approximate acceptance
+    mode).
+
+    get_p(i) -> Dist of target position i after its policy; get_z(i) -> raw
+    logits of that row (for the greedy token).  A draft token outside [0, V)
+    fails its test and sets FLAG_BAD_TOKEN.  Returns a dict: num_accepted,
+    tokens (gamma + 1, -1 padded), flags, decisions [(i, p(x_i) - threshold)].
+    """
+    flags = 0
+    out = []
+    decisions = []
+    for i in range(gamma + 1):
+        p = get_p(i)
+        flags |= p.flags
+        if i < gamma:
+            x = int(tokens[i])
+            if 0 <= x < V:
+                dense = p.dense(V)
+                px = float(dense[x])
+                thr = typical_threshold(dense, epsilon, delta)
+                decisions.append((i, px - thr))
+                if px > thr:
+                    out.append(x)
+                    continue
+            else:
+                flags |= FLAG_BAD_TOKEN
+        greedy = p.index if p.onehot else finite_argmax(get_z(i))
+        toks = out + [greedy]
+        toks += [-1] * (gamma + 1 - len(toks))
+        return dict(num_accepted=len(out), tokens=toks, flags=flags, decisions=decisions)
+    raise AssertionError("unreachable")
+
+
+def typical_chain(target_logits, draft_tokens, target_temperature, epsilon, delta, seqs=None):
+    """Typical acceptance for a batch: target_logits [B, gamma+1, V], draft_tokens
+    [B, gamma], a temperature per sequence (top-k is not part of this rule's
+    interface).  Rows are read lazily, up to the first failed test."""
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    results = []
+    for b in (range(B) if seqs is None else seqs):
+        def get_z(i, b=b):
+            return np.asarray(target_logits[b, i], np.float64)
+
+        def get_p(i, b=b):
+            return policy_distribution(get_z(i), target_temperature[b], 0)
+
+        res = walk_typical(gamma, V, get_p, get_z, draft_tokens[b], epsilon, delta)
+        res["seq"] = b
+        results.append(res)
+    return results
 
 
 def tree_check(parent, max_depth):

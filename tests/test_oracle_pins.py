@@ -702,3 +702,89 @@ def test_chain_overlap_matches_per_row_policy():
     p = np.exp(zt[0, 0] - zt[0, 0].max()); p /= p.sum()
     q = np.exp(zd[0, 0] - zd[0, 0].max()); q /= q.sum()
     assert abs(beta[0, 0] - np.sum(q * np.minimum(1.0, p / q))) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# typical acceptance: whoami-wesleyyou.top "Speculative Decoding" notes,
+# § Medusa-1 与 typical acceptance
+# ---------------------------------------------------------------------------
+
+def test_entropy_closed_forms_and_library():
+    import math
+    from scipy.stats import entropy as scipy_entropy
+    for V in (1, 2, 7, 128):
+        assert abs(verify.entropy(np.full(V, 1.0 / V)) - math.log(V)) < 1e-12
+    assert verify.entropy(np.array([0.0, 1.0, 0.0])) == 0.0
+    rng = np.random.default_rng(31)
+    for _ in range(20):
+        p = rng.dirichlet(np.full(50, 0.3))
+        p[rng.integers(0, 50, 5)] = 0.0  # zero entries contribute nothing
+        p /= p.sum()
+        assert abs(verify.entropy(p) - scipy_entropy(p)) < 1e-12
+
+
+def test_typical_threshold_branches():
+    u = np.full(4, 0.25)  # exp(-H) = 1/4
+    assert abs(verify.typical_threshold(u, 1.0, 0.5) - 0.125) < 1e-15
+    assert abs(verify.typical_threshold(u, 0.1, 0.5) - 0.1) < 1e-15
+    # p(x) = 1/4 passes 1/8 and fails 3/8
+    assert 0.25 > verify.typical_threshold(u, 1.0, 0.5)
+    assert not 0.25 > verify.typical_threshold(u, 1.0, 1.5)
+    # a one-hot row has H = 0: the threshold is min(epsilon, delta)
+    assert verify.typical_threshold(np.array([0.0, 1.0]), 0.3, 0.9) == 0.3
+    # a more spread target lowers the entropy-dependent threshold
+    rng = np.random.default_rng(32)
+    z = rng.normal(size=64)
+    thr = []
+    for T in (0.3, 0.6, 1.0, 2.0, 4.0):
+        p = np.exp((z - z.max()) / T)
+        thr.append(verify.typical_threshold(p / p.sum(), 1.0, 0.8))
+    assert all(a > b for a, b in zip(thr, thr[1:]))
+
+
+def _rows(*dists):
+    return [Dist(False, probs=np.asarray(d, np.float64)) for d in dists]
+
+
+def test_walk_typical_longest_prefix_then_greedy_token():
+    V = 4
+    # thresholds min(0.2, 0.5 exp(-H)): 0.195 for (.7, .1, .1, .1) (H = 0.9405),
+    # 0.125 for the uniform row; every draft passes, the bonus is argmax 1
+    rows = _rows([0.7, 0.1, 0.1, 0.1],
+                 [0.25, 0.25, 0.25, 0.25],
+                 [0.1, 0.1, 0.1, 0.7],
+                 [0.1, 0.6, 0.2, 0.1])
+    logits = [np.log(r.probs) for r in rows]
+    get_p = lambda i: rows[i]
+    get_z = lambda i: logits[i]
+    res = verify.walk_typical(3, V, get_p, get_z, [0, 1, 3], 0.2, 0.5)
+    assert res["num_accepted"] == 3 and res["tokens"] == [0, 1, 3, 1]
+    # a failed test ends the prefix even when later drafts would pass: under
+    # (.97, .01, .01, .01) the threshold is 0.2 and token 1 has 0.01
+    rows2 = _rows([0.7, 0.1, 0.1, 0.1], [0.97, 0.01, 0.01, 0.01], [0.1, 0.1, 0.1, 0.7],
+                  [0.1, 0.6, 0.2, 0.1])
+    logits2 = [np.log(r.probs) for r in rows2]
+    res = verify.walk_typical(3, V, lambda i: rows2[i], lambda i: logits2[i], [0, 1, 3], 0.2, 0.5)
+    assert res["num_accepted"] == 1 and res["tokens"] == [0, 0, -1, -1]
+    # a draft outside the vocabulary fails and is flagged
+    res = verify.walk_typical(3, V, get_p, get_z, [0, 9, 3], 0.2, 0.5)
+    assert res["num_accepted"] == 1 and res["tokens"] == [0, 0, -1, -1]
+    assert res["flags"] == verify.FLAG_BAD_TOKEN
+
+
+def test_typical_chain_greedy_and_threshold_one():
+    rng = np.random.default_rng(33)
+    B, gamma, V = 2, 3, 30
+    z = rng.normal(size=(B, gamma + 1, V))
+    arg = z.argmax(-1)
+    toks = arg[:, :gamma].copy()
+    toks[1, 1] = (arg[1, 1] + 1) % V
+    t0 = np.zeros(B)
+    # greedy rows: the test passes exactly for the argmax (threshold min(eps, delta) < 1)
+    r = verify.typical_chain(z, toks, t0, 0.3, 0.5)
+    assert r[0]["num_accepted"] == gamma and r[0]["tokens"] == list(arg[0])
+    assert r[1]["num_accepted"] == 1 and r[1]["tokens"] == [arg[1, 0], arg[1, 1], -1, -1]
+    # with epsilon = delta = 1 no probability exceeds the threshold
+    r = verify.typical_chain(z, toks, t0, 1.0, 1.0)
+    assert all(x["num_accepted"] == 0 for x in r)
+    assert [x["tokens"][0] for x in r] == list(arg[:, 0])
