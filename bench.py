@@ -14,7 +14,9 @@ Arms:
                     method) on this host's cores, on a bounded sample
 
 --op overlap times the per-position overlap beta_i = sum min(p_i, q_i) of
-the same workload instead (metric: positions per second, B * gamma per step).
+the same workload instead (metric: positions per second, B * gamma per step);
+--op typical times typical acceptance (epsilon 0.0625, delta 0.5; metric:
+target rows per second, B * (gamma + 1) per step).
 
 Under torchrun each rank verifies its own batch on its own GPU (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
@@ -46,6 +48,9 @@ LAUNCHES_PER_STEP = 1
 OVERLAP_METRIC = "overlap positions/s (B*gamma)"
 L2_BYTES = 129e6
 OVERLAP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "overlap_kernel_b256_g7_v128256_bf16.md")
+TYPICAL_METRIC = "typical-acceptance target rows/s (B*(gamma+1))"
+TYPICAL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "typical_rows_b256_g7_v128256_bf16.md")
+TYPICAL_EPS, TYPICAL_DELTA = 0.0625, 0.5
 
 
 def dist_env():
@@ -73,11 +78,22 @@ def job_rate(world, rows_per_rank_step, steps, seconds):
 
 def kernel_source_hash(unit="verify_pass.cu"):
     """Hash of a kernel's sources: its translation unit (which also holds its
-    launch function) and the device headers."""
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name != unit and not name.endswith(".cuh"):
+    launch function) and the local headers it includes, transitively."""
+    seen, todo = set(), [unit]
+    while todo:
+        name = todo.pop()
+        if name in seen:
             continue
+        seen.add(name)
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            for line in f:
+                line = line.strip()
+                if line.startswith('#include "'):
+                    inc = line.split('"')[1]
+                    if os.path.exists(os.path.join(CSRC, inc)):
+                        todo.append(inc)
+    h = hashlib.sha256()
+    for name in sorted(seen):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -385,33 +401,76 @@ def oracle_overlap_rate(w, n_seqs):
     return n_seqs * w["gamma"] / dt, dt
 
 
-def run_overlap_reference(args):
+def typical_bytes(w):
+    """Algorithmic bytes of one typical-acceptance call: every target row once."""
+    esize = 2 if w["dtype"] == "bf16" else 4
+    return w["B"] * (w["gamma"] + 1) * w["V"] * esize
+
+
+def typical_config(w):
+    c = config_entry(w)
+    c["workload"] = (f"typical acceptance B={w['B']} gamma={w['gamma']} V={w['V']} {w['dtype']} "
+                     f"(epsilon {TYPICAL_EPS}, delta {TYPICAL_DELTA}, temperature 1, Zipf logits)")
+    c["target_bytes_per_step"] = typical_bytes(w)
+    c["l2"] = l2_note(typical_bytes(w), "target rows")
+    return c
+
+
+def oracle_typical_rate(w, n_seqs):
+    """The CPU oracle's typical acceptance on the first n_seqs sequences: (rows/s, seconds)."""
+    from oracle import verify as ov
+    t0 = time.perf_counter()
+    ov.typical_chain(w["target"], w["tokens"], w["target_temperature"], TYPICAL_EPS,
+                     TYPICAL_DELTA, seqs=range(n_seqs))
+    dt = time.perf_counter() - t0
+    return n_seqs * (w["gamma"] + 1) / dt, dt
+
+
+# what --op overlap / --op typical measure: metric, unit, units per call,
+# algorithmic bytes, configuration, traffic record and kernel source, kernel
+# launches per call, the oracle's rate and a label for the roofline kernel
+ROW_OPS = {
+    "overlap": dict(metric=OVERLAP_METRIC, unit="positions/s",
+                    units=lambda w: w["B"] * w["gamma"], nbytes=overlap_bytes,
+                    config=overlap_config, traffic=(OVERLAP_TRAFFIC_FILE, "overlap.cu"),
+                    launches=1, oracle=oracle_overlap_rate,
+                    kernel="overlap_kernel (timed per call)"),
+    "typical": dict(metric=TYPICAL_METRIC, unit="rows/s",
+                    units=lambda w: w["B"] * (w["gamma"] + 1), nbytes=typical_bytes,
+                    config=typical_config, traffic=(TYPICAL_TRAFFIC_FILE, "typical.cu"),
+                    launches=2, oracle=oracle_typical_rate,
+                    kernel="typical_row_kernel + typical_decide_kernel (timed per call)"),
+}
+
+
+def run_rowop_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    op = ROW_OPS[args.op]
     w = bench_workload(args)
     # one sequence per step: a bounded sample of the same workload
-    oracle_overlap_rate(w, 1)
+    op["oracle"](w, 1)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_overlap_rate(w, 1)
+        op["oracle"](w, 1)
     dt = time.perf_counter() - t0
-    value = w["gamma"] * args.steps / dt
+    per_seq = op["units"](w) // w["B"]
+    value = per_seq * args.steps / dt
     line = {
-        "impl": "reference", "metric": OVERLAP_METRIC, "value": value, "unit": "positions/s",
+        "impl": "reference", "metric": op["metric"], "value": value, "unit": op["unit"],
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": overlap_config(w),
-        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": 1, "kind": "oracle",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": op["config"](w),
+        "cpu_baseline": {"value": value, "unit": op["unit"], "cores": 1, "kind": "oracle",
                          "sample": f"the first sequence of {w['B']} per step"},
-        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": op["unit"], "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_overlap(args):
+def run_rowop(args):
     import torch
     import torch.distributed as dist
 
@@ -425,19 +484,28 @@ def run_overlap(args):
     __graft_entry__.build()
     import speculative_decoding_verification_temp_gb300 as sv
 
+    op = ROW_OPS[args.op]
     w = bench_workload(args)
-    B, gamma = w["B"], w["gamma"]
-    units = B * gamma
-    nbytes = overlap_bytes(w)
+    B = w["B"]
+    units = op["units"](w)
+    nbytes = op["nbytes"](w)
     target_h = torch.from_numpy(w["target"]).to(torch.bfloat16).pin_memory()
     draft_h = torch.from_numpy(w["draft"]).to(torch.bfloat16).pin_memory()
-    target, draft = target_h.to(dev), draft_h.to(dev)
+    tokens_h = torch.from_numpy(w["tokens"]).pin_memory()
+    target, draft, tokens = target_h.to(dev), draft_h.to(dev), tokens_h.to(dev)
     tp = torch.from_numpy(w["target_temperature"]).to(dev)
     tq = torch.from_numpy(w["draft_temperature"]).to(dev)
     stream = torch.cuda.current_stream(dev)
 
+    def call(t, d, k):
+        if args.op == "overlap":
+            r = sv.overlap(t, d, tp, tq)
+            return r.beta
+        r = sv.typical_accept(t, k, tp, TYPICAL_EPS, TYPICAL_DELTA)
+        return r.tokens
+
     for _ in range(max(args.warmup, 3)):
-        sv.overlap(target, draft, tp, tq)
+        call(target, draft, tokens)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -450,7 +518,7 @@ def run_overlap(args):
         t_begin.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
-            sv.overlap(target, draft, tp, tq)
+            call(target, draft, tokens)
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -459,15 +527,21 @@ def run_overlap(args):
     elapsed_ms = max_over_ranks(t_begin.elapsed_time(t_end), world, dev)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
+    # end to end: the inputs the op reads copied from pinned host memory, the
+    # result read back
     e2e_steps = max(1, args.e2e_steps)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        r = sv.overlap(target_h.to(dev, non_blocking=True), draft_h.to(dev, non_blocking=True),
-                       tp, tq)
-        beta = r.beta.to("cpu")
+        t_d = target_h.to(dev, non_blocking=True)
+        if args.op == "overlap":
+            out = call(t_d, draft_h.to(dev, non_blocking=True), None).to("cpu")
+        else:
+            out = call(t_d, None, tokens_h.to(dev, non_blocking=True)).to("cpu")
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, dev)
+    h2d = target_h.numel() * 2 + (draft_h.numel() * 2 if args.op == "overlap"
+                                  else tokens_h.numel() * 4)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -477,29 +551,24 @@ def run_overlap(args):
     peak, peak_kind = measured_peak()
     achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
     line = {
-        "metric": OVERLAP_METRIC, "value": job_rate(world, units, args.steps, elapsed_ms / 1e3),
-        "unit": "positions/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": op["metric"], "value": job_rate(world, units, args.steps, elapsed_ms / 1e3),
+        "unit": op["unit"], "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": overlap_config(w),
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": op["config"](w),
         "clocks": clk.summary(),
-        "e2e": {"value": job_rate(world, units, 1, e2e_s), "unit": "positions/s",
-                "h2d_bytes_per_step": (target_h.numel() + draft_h.numel()) * 2,
-                "d2h_bytes_per_step": beta.numel() * 4},
-        "gpu_launches": args.steps,
+        "e2e": {"value": job_rate(world, units, 1, e2e_s), "unit": op["unit"],
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4},
+        "gpu_launches": op["launches"] * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     "traffic": recorded_traffic(OVERLAP_TRAFFIC_FILE, "overlap.cu"),
+                     "frac": achieved / peak, "traffic": recorded_traffic(*op["traffic"]),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "overlap_kernel (timed per call)",
-                     "launch_ms_avg": avg_launch_ms,
+                     "kernel": op["kernel"], "launch_ms_avg": avg_launch_ms,
                      "launch_ms_median": statistics.median(launch_ms)},
     }
     if not args.no_cpu_baseline:
-        n = min(B, max(1, args.cpu_seqs // 32))
-        rate, dt = oracle_overlap_rate(w, n)
-        line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": 1,
-                                "kind": "oracle",
+        n = min(B, args.cpu_seqs)
+        rate, dt = op["oracle"](w, n)
+        line["cpu_baseline"] = {"value": rate, "unit": op["unit"], "cores": 1, "kind": "oracle",
                                 "sample": f"the first {n} of {B} sequences, {dt:.1f} s"}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -518,14 +587,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per batch (default: the B = 256 workload); for profiling")
-    ap.add_argument("--op", default="verify", choices=["verify", "overlap"],
-                    help="verify: the chain verifier (default); overlap: beta_i per position")
+    ap.add_argument("--op", default="verify", choices=["verify", "overlap", "typical"],
+                    help="verify: the chain verifier (default); overlap: beta_i per position; "
+                         "typical: typical acceptance")
     args = ap.parse_args()
-    if args.op == "overlap":
+    if args.op in ROW_OPS:
         if args.impl == "reference":
-            run_overlap_reference(args)
+            run_rowop_reference(args)
         else:
-            run_overlap(args)
+            run_rowop(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -254,6 +254,44 @@ spec_status spec_overlap(
 /* Static description of a status code. */
 const char *spec_status_string(spec_status status);
 
+/* Bytes of workspace spec_typical_accept needs: 8 per target row,
+ * B * (gamma + 1) rows (0 for a negative size). */
+size_t spec_typical_workspace_size(int B, int gamma);
+
+/* Typical acceptance of a draft chain (an approximate rule: the output is not
+ * distributed as the target's).  whoami-wesleyyou.top "Speculative Decoding"
+ * notes, section "Medusa-1 与 typical acceptance": draft token x_i passes when
+ * p_i(x_i) > min(epsilon, delta * exp(-H(p_i))), H the entropy (natural log)
+ * of the target's distribution at position i; the longest passing prefix is
+ * kept and the target's greedy token follows it.
+ *
+ * target_logits [B, gamma+1, V]: as for spec_verify_chain; every row is read
+ *                                once (rows past the first failure too).
+ * draft_tokens  [B, gamma] int32 (may be NULL when gamma == 0).
+ * target_policy: temperature per sequence (0: greedy, the one-hot at the
+ *                argmax, H = 0); top_k must be NULL (SPEC_ERR_UNSUPPORTED).
+ * epsilon, delta: finite, >= 0.
+ * Outputs (device):
+ *   out_num_accepted [B]: length n of the passing prefix (0..gamma).
+ *   out_tokens [B, gamma+1]: the n passing drafts, then the greedy token of row
+ *                            n (the lowest index of the largest logit), then -1.
+ *   out_flags [B] (nullable): OR over rows 0..n of SPEC_FLAG_NONFINITE (a NaN or
+ *                            +inf logit, no finite logit, or a bad temperature:
+ *                            the row is the one-hot at its finite argmax) and
+ *                            SPEC_FLAG_BAD_TOKEN (x_n outside [0, V): it fails).
+ * workspace: device, >= spec_typical_workspace_size(B, gamma) bytes, 8-byte
+ *            aligned; no contents carried between calls.
+ * Errors: SPEC_ERR_INVALID_ARG (bad sizes, NULL pointers, ld_target < V, a
+ * short or misaligned workspace, epsilon or delta negative or not finite),
+ * before any launch; SPEC_ERR_CUDA for a failed launch.  Two launches.
+ */
+spec_status spec_typical_accept(
+    const void *target_logits, int64_t ld_target, spec_dtype dtype,
+    int B, int gamma, int V, spec_policy target_policy,
+    const int32_t *draft_tokens, float epsilon, float delta,
+    int32_t *out_num_accepted, int32_t *out_tokens, uint32_t *out_flags,
+    void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

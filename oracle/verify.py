@@ -291,7 +291,7 @@ def walk_typical(gamma, V, get_p, get_z, tokens, epsilon, delta):
     get_p(i) -> Dist of target position i after its policy; get_z(i) -> raw
     logits of that row (for the greedy token).  A draft token outside [0, V)
     fails its test and sets FLAG_BAD_TOKEN.  Returns a dict: num_accepted,
-    tokens (gamma + 1, -1 padded), flags, decisions [(i, p(x_i) - threshold)].
+    tokens (gamma + 1, -1 padded), flags, decisions [(i, p(x_i), threshold)].
     """
     flags = 0
     out = []
@@ -305,7 +305,7 @@ def walk_typical(gamma, V, get_p, get_z, tokens, epsilon, delta):
                 dense = p.dense(V)
                 px = float(dense[x])
                 thr = typical_threshold(dense, epsilon, delta)
-                decisions.append((i, px - thr))
+                decisions.append((i, px, thr))
                 if px > thr:
                     out.append(x)
                     continue

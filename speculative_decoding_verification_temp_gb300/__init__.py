@@ -9,6 +9,8 @@ in include/specverify.h); ``api`` is a thin torch binding over it.
   verify_tree    recursive rejection over sibling candidates of token trees
   tree_mask      ancestor-or-self attention masks and depth position ids
   overlap        per-position acceptance rate beta_i = sum_v min(p_i, q_i)
+  typical_accept typical acceptance (entropy threshold; approximate, not
+                 distribution-exact)
 """
 
 from ._abi import (FLAG_BAD_TOKEN, FLAG_BAD_TREE, FLAG_DEGENERATE_RESIDUAL, FLAG_DEPTH,  # noqa: F401
@@ -19,8 +21,9 @@ def __getattr__(name):
     # the torch binding is imported on first use, so the workload generator
     # and the build step do not need torch
     if name in ("verify_chain", "verify_chain_static", "verify_tree", "tree_mask", "overlap",
-                "SpecVerifyError", "workspace",
-                "ChainResult", "TreeResult", "MaskResult", "OverlapResult", "api"):
+                "typical_accept", "SpecVerifyError", "workspace",
+                "ChainResult", "TreeResult", "MaskResult", "OverlapResult", "TypicalResult",
+                "api"):
         import importlib
         api = importlib.import_module(__name__ + ".api")
         return api if name == "api" else getattr(api, name)

@@ -292,3 +292,42 @@ def overlap(target_logits, draft_logits, target_temperature, draft_temperature):
                             _stream(dev))
     _check(code)
     return OverlapResult(beta, flags)
+
+
+TypicalResult = namedtuple("TypicalResult", "num_accepted tokens flags")
+
+
+def typical_accept(target_logits, draft_tokens, target_temperature, epsilon, delta,
+                   workspace_tensor=None):
+    """Typical acceptance (see spec_typical_accept): an approximate rule, not
+    distribution-exact.
+
+    target_logits [B, gamma+1, V] (float32 or bfloat16, CUDA), draft_tokens
+    [B, gamma] integer, temperatures per sequence (scalars broadcast), epsilon
+    and delta floats.  Returns TypicalResult with num_accepted [B] int32,
+    tokens [B, gamma+1] int32 (-1 padded) and flags [B] int32.
+    """
+    _cuda_tensor(target_logits, "target_logits")
+    dev = target_logits.device
+    if target_logits.dtype not in _DTYPES:
+        raise ValueError("target_logits must be float32 or bfloat16")
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    tl, ld_t = _rows(target_logits, "target_logits")
+    toks = None
+    if gamma > 0:
+        toks = _vec(draft_tokens, B * gamma, torch.int32, "draft_tokens", dev).view(B, gamma)
+    tp = _vec(target_temperature, B, torch.float32, "target_temperature", dev)
+    num = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    flags = torch.empty(B, dtype=torch.int32, device=dev)
+    lib = _abi.load()
+    nbytes = lib.spec_typical_workspace_size(B, gamma)
+    ws = workspace(dev, nbytes) if workspace_tensor is None else workspace_tensor
+    code = lib.spec_typical_accept(_ptr(tl), ld_t, _DTYPES[target_logits.dtype], B, gamma, V,
+                                   _abi.spec_policy(tp.data_ptr(), None),
+                                   None if toks is None else _ptr(toks), float(epsilon),
+                                   float(delta), _ptr(num), _ptr(out), _ptr(flags), _ptr(ws),
+                                   ws.numel(), _stream(dev))
+    _check(code)
+    return TypicalResult(num, out, flags)

@@ -22,6 +22,11 @@ cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cuda
 cudaError_t launch_overlap(const void *target, long long ld_t, const void *draft, long long ld_d,
                            int esize, int B, int gamma, int V, const float *Tp, const float *Tq,
                            float *out_beta, uint32_t *out_flags, cudaStream_t stream);
+size_t typical_workspace_bytes(int B, int gamma);
+cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B, int gamma, int V,
+                           const float *Tp, const int32_t *tokens, float epsilon, float delta,
+                           int32_t *out_num, int32_t *out_tokens, uint32_t *out_flags,
+                           void *workspace, cudaStream_t stream);
 cudaError_t launch_pass(const Params &P, int esize, const Exp2Table &tab, size_t smem,
                         cudaStream_t stream);
 size_t pass_ctl_bytes();
@@ -493,6 +498,36 @@ spec_status spec_overlap(const void *target_logits, int64_t ld_target, const voi
   return map_cuda(sv::launch_overlap(target_logits, ld_target, draft_logits, ld_draft, esize, B,
                                      gamma, V, target_policy.temperature,
                                      draft_policy.temperature, out_beta, out_flags, st));
+}
+
+size_t spec_typical_workspace_size(int B, int gamma) {
+  if (B < 0 || gamma < 0 || gamma > kMaxGamma) return 0;
+  return sv::typical_workspace_bytes(B, gamma);
+}
+
+spec_status spec_typical_accept(const void *target_logits, int64_t ld_target, spec_dtype dtype,
+                                int B, int gamma, int V, spec_policy target_policy,
+                                const int32_t *draft_tokens, float epsilon, float delta,
+                                int32_t *out_num_accepted, int32_t *out_tokens,
+                                uint32_t *out_flags, void *workspace, size_t workspace_bytes,
+                                spec_stream_t stream) {
+  const int esize = esize_of(dtype);
+  if (esize == 0 || B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!(epsilon >= 0.f) || !(delta >= 0.f) || epsilon == INFINITY || delta == INFINITY)
+    return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !target_policy.temperature || (gamma > 0 && !draft_tokens) ||
+      !out_num_accepted || !out_tokens || !workspace || ld_target < V)
+    return SPEC_ERR_INVALID_ARG;
+  if (target_policy.top_k) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * (gamma + 1) > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;
+  if (workspace_bytes < sv::typical_workspace_bytes(B, gamma) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 7u) != 0)
+    return SPEC_ERR_INVALID_ARG;
+  return map_cuda(sv::launch_typical(target_logits, ld_target, esize, B, gamma, V,
+                                     target_policy.temperature, draft_tokens, epsilon, delta,
+                                     out_num_accepted, out_tokens, out_flags, workspace,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

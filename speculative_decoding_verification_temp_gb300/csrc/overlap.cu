@@ -34,6 +34,7 @@
 #include "common.cuh"
 #include "ops.cuh"
 #include "precise.cuh"
+#include "slice_rows.cuh"
 
 namespace sv {
 
@@ -41,73 +42,6 @@ namespace {
 
 constexpr int kOvCluster = 4;
 constexpr size_t kSliceTarget = 64 * 1024;  // both rows' slices, per CTA
-
-// Eight consecutive entries of a row as raw words (-inf outside the slice).
-template <typename TE> struct Group;
-template <> struct Group<uint16_t> {
-  uint32_t w[4];
-};
-template <> struct Group<float> {
-  float f[8];
-};
-
-template <typename TE>
-__device__ __forceinline__ Group<TE> load_group(const TE *g, int base, int n, bool fast);
-
-template <>
-__device__ __forceinline__ Group<uint16_t> load_group<uint16_t>(const uint16_t *g, int base, int n,
-                                                                bool fast) {
-  Group<uint16_t> r;
-  if (fast) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(g + base);
-    r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
-    return r;
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = base + 2 * i < n ? g[base + 2 * i] : 0xFF80u;
-    const uint32_t hi = base + 2 * i + 1 < n ? g[base + 2 * i + 1] : 0xFF80u;
-    r.w[i] = lo | (hi << 16);
-  }
-  return r;
-}
-
-template <>
-__device__ __forceinline__ Group<float> load_group<float>(const float *g, int base, int n,
-                                                          bool fast) {
-  Group<float> r;
-  if (fast) {
-    const float4 a = *reinterpret_cast<const float4 *>(g + base);
-    const float4 b = *reinterpret_cast<const float4 *>(g + base + 4);
-    r.f[0] = a.x; r.f[1] = a.y; r.f[2] = a.z; r.f[3] = a.w;
-    r.f[4] = b.x; r.f[5] = b.y; r.f[6] = b.z; r.f[7] = b.w;
-    return r;
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) r.f[e] = base + e < n ? g[base + e] : -INFINITY;
-  return r;
-}
-
-// The group's entries i and i + 1 (i even) as an fp32 pair, and its max.
-__device__ __forceinline__ uint64_t pair_of(const Group<uint16_t> &x, int i) {
-  return bf16x2_to_pair(x.w[i / 2]);
-}
-__device__ __forceinline__ uint64_t pair_of(const Group<float> &x, int i) {
-  return pack2(x.f[i], x.f[i + 1]);
-}
-__device__ __forceinline__ float group_max(const Group<uint16_t> &x) {
-  const uint32_t h = bf16x2_max(bf16x2_max(x.w[0], x.w[1]), bf16x2_max(x.w[2], x.w[3]));
-  return fmaxf(__uint_as_float(h << 16), __uint_as_float(h & 0xFFFF0000u));
-}
-__device__ __forceinline__ float group_max(const Group<float> &x) {
-  return fmaxf(fmaxf(fmaxf(x.f[0], x.f[1]), fmaxf(x.f[2], x.f[3])),
-               fmaxf(fmaxf(x.f[4], x.f[5]), fmaxf(x.f[6], x.f[7])));
-}
-__device__ __forceinline__ float entry(const Group<uint16_t> &x, int e) {
-  const uint32_t w = x.w[e / 2];
-  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
-}
-__device__ __forceinline__ float entry(const Group<float> &x, int e) { return x.f[e]; }
 
 // Statistics of one row: for T > 0, mk = (max finite-or-inf logit) * k and
 // S = sum 2^(z k - mk) (NaN when a NaN was summed); for the argmax, the finite
@@ -176,25 +110,14 @@ __device__ RowStat thread_sum(const TE *g, int n, float k, bool vec) {
   return r;
 }
 
-// One thread's finite argmax and non-finite flag over its groups of a slice
-// whose first entry is vocabulary index lo.
+// One thread's finite argmax and non-finite flag (slice_argmax) as a RowStat.
 template <typename TE>
 __device__ RowStat thread_argmax(const TE *g, int n, int lo, bool vec) {
+  const ArgStat a = slice_argmax<TE>(g, n, lo, vec);
   RowStat r = empty_stat();
-  const int ngroups = (n + 7) / 8;
-  for (int j = threadIdx.x; j < ngroups; j += kThreads) {
-    const Group<TE> x = load_group<TE>(g, 8 * j, n, vec && 8 * j + 8 <= n);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float z = entry(x, e);
-      if (z != z || z == INFINITY) {
-        r.bad = 1;  // padding is -inf, never NaN or +inf
-      } else if (z > r.av) {
-        r.av = z;
-        r.ai = lo + 8 * j + e;
-      }
-    }
-  }
+  r.av = a.av;
+  r.ai = a.ai;
+  r.bad = a.bad;
   return r;
 }
 
@@ -263,17 +186,6 @@ struct OverlapSmem {
   Side side[2];              // the two rows' distributions
 };
 
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  cluster_wait();
-}
-
 // Merges the threads' statistics of both rows over the block, stores each
 // rank's result into every rank's shared memory (slot `round`), waits on the
 // cluster barrier and merges the C slices in rank order into sm.row.  The
@@ -305,7 +217,7 @@ __device__ void cluster_merge(RowStat r[2], OverlapSmem &sm, cg::cluster_group &
     for (int w = 0; w < kWarps; ++w) merge_into(a, sm.warp[x][w]);
     for (int d = 0; d < C; ++d) cluster.map_shared_rank(&sm.slice[round][rank][x], d)[0] = a;
   }
-  cluster_barrier();
+  cluster_sync_all();
   if (threadIdx.x < 2) {
     const int x = threadIdx.x;
     RowStat a = empty_stat();
@@ -415,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) overlap_kernel(
     for (int w = 0; w < kWarps; ++w) b += df_to_double(sm.part[w]);
     cluster.map_shared_rank(&sm.bpart[rank], 0)[0] = b;
   }
-  cluster_barrier();
+  cluster_sync_all();
   if (rank == 0 && threadIdx.x == 0) {
     double beta = 0.0;
     for (int d = 0; d < C; ++d) beta += sm.bpart[d];

@@ -1,0 +1,138 @@
+"""Typical acceptance on the GPU against the oracle, sequence by sequence.
+
+The bar: accepted counts, tokens and flags are bit-exact, except in a sequence
+where some test has |p(x) - threshold| <= 1e-5 threshold on the oracle's side
+(float32 logits and exponentials against float64 can decide such a test
+either way).  Such sequences are counted and must stay at most 1e-5 of the
+sequences checked, i.e. none in these tests.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import to_dev
+from oracle import verify as ov
+from speculative_decoding_verification_temp_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+EPS, DELTA = 0.0625, 0.5  # exact in float32; the epsilon branch is active on low-entropy rows
+REL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def run(w, eps=EPS, delta=DELTA, pad_to=None):
+    import speculative_decoding_verification_temp_gb300 as sv
+    t = w["target"]
+    if pad_to is not None:
+        V = t.shape[-1]
+        tp = np.zeros(t.shape[:-1] + (pad_to,), np.float32)
+        tp[..., :V] = t
+        td = to_dev(tp, w["dtype"])[..., :V]
+    else:
+        td = to_dev(t, w["dtype"])
+    toks = torch.from_numpy(np.ascontiguousarray(w["tokens"], np.int32)).cuda()
+    r = sv.typical_accept(td, toks, w["target_temperature"], eps, delta)
+    torch.cuda.synchronize()
+    return r.num_accepted.cpu().numpy(), r.tokens.cpu().numpy(), r.flags.cpu().numpy()
+
+
+def check(w, seqs, eps=EPS, delta=DELTA, pad_to=None):
+    num, toks, flags = run(w, eps, delta, pad_to)
+    ref = ov.typical_chain(w["target"], w["tokens"], w["target_temperature"], eps, delta, seqs=seqs)
+    excused = 0
+    for r in ref:
+        b = r["seq"]
+        if any(abs(px - thr) <= REL * thr for _, px, thr in r["decisions"]):
+            excused += 1
+            continue
+        assert num[b] == r["num_accepted"], (b, num[b], r)
+        assert list(toks[b]) == r["tokens"], (b, toks[b], r["tokens"])
+        assert flags[b] == r["flags"], (b, flags[b], r["flags"])
+    assert excused <= REL * len(ref)
+    return num, ref
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2])
+def test_typical_workloads(cfg):
+    w = workloads.config(cfg)
+    seqs = range(min(w["B"], 24))
+    num, _ = check(w, seqs)
+    assert len(set(num.tolist())) > 1  # a mix of prefix lengths
+
+
+def test_typical_threshold_extremes():
+    w = workloads.config(0)
+    seqs = range(w["B"])
+    # epsilon = delta = 0: every draft with p(x) > 0 passes
+    num, _ = check(w, seqs, eps=0.0, delta=0.0)
+    assert (num == w["gamma"]).all()
+    # a threshold of 1: nothing passes, the greedy token of row 0 follows
+    num, _ = check(w, seqs, eps=1.0, delta=float(2 ** 20))
+    assert (num == 0).all()
+
+
+def make(rng, B, gamma, V, dtype, temps, spread=2.0):
+    t = (spread * rng.standard_normal((B, gamma + 1, V))).astype(np.float32)
+    if dtype == "bf16":
+        workloads.round_bf16_inplace(t)
+    # drafts: half the argmax, half random tokens
+    toks = np.where(rng.random((B, gamma)) < 0.5, t[:, :gamma].argmax(-1),
+                    rng.integers(0, V, (B, gamma))).astype(np.int32)
+    return dict(target=t, tokens=toks, target_temperature=np.asarray(temps, np.float32),
+                dtype=dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_typical_greedy_mixed_temperatures_ragged_vocab(dtype):
+    rng = np.random.default_rng(51)
+    w = make(rng, 8, 4, 1001, dtype, [1.0, 0.0, 0.5, 2.0, 0.0, 1.3, 0.7, 1.0])
+    check(w, range(8))
+    check(w, range(8), pad_to=1004)  # unaligned rows take element loads
+
+
+def test_typical_nonfinite_rows_and_bad_tokens():
+    rng = np.random.default_rng(52)
+    w = make(rng, 6, 3, 700, "f32", [1.0] * 6)
+    t, toks = w["target"], w["tokens"]
+    t[0, 0, 11] = np.nan
+    t[1, 0, 5] = np.inf           # row 0 is the one-hot at its finite argmax, which passes
+    toks[1, 0] = np.where(np.arange(700) == 5, -np.inf, t[1, 0]).argmax()
+    t[2, 0, :] = -np.inf          # no finite logit
+    w["target_temperature"][3] = -1.0
+    toks[4, 0] = -1               # outside the vocabulary
+    toks[5, 1] = 700
+    toks[5, 0] = t[5, 0].argmax()
+    num, ref = check(w, range(6))
+    assert num[1] >= 1 and num[4] == 0 and num[5] <= 1
+
+
+@pytest.mark.parametrize("V", [1, 5, 37])
+def test_typical_tiny_vocab(V):
+    rng = np.random.default_rng(53 + V)
+    w = make(rng, 4, 3, V, "f32", [1.0, 0.0, 0.6, 3.0])
+    check(w, range(4))
+
+
+def test_typical_gamma_zero_and_ties_across_slices():
+    rng = np.random.default_rng(54)
+    w = make(rng, 3, 0, 4099, "f32", [1.0, 0.0, 0.8])
+    w["target"][:, 0, [7, 4090]] = 50.0  # equal maxima in the first and last slice
+    num, toks, _ = run(w)
+    assert (num == 0).all() and (toks[:, 0] == 7).all()
+    check(w, range(3))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_typical_large_vocab(dtype):
+    rng = np.random.default_rng(55)
+    w = make(rng, 2, 3, 262147, dtype, [1.0, 0.4])
+    check(w, range(2))

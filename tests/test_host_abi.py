@@ -197,3 +197,41 @@ def test_overlap_rejects_bad_arguments(lib):
     # nothing to compare: a no-op
     assert overlap_call(lib, B=0, target=None, draft=None, out=None) == _abi.SPEC_OK
     assert overlap_call(lib, gamma=0, target=None, draft=None, out=None) == _abi.SPEC_OK
+
+
+def typical_call(lib, B=2, gamma=3, V=100, dtype=1, target=FAKE, tokens=FAKE, out=FAKE, pol=None,
+                 ld=None, eps=0.1, delta=0.5, ws=FAKE, ws_bytes=None):
+    pol = pol or policy()
+    if ws_bytes is None:
+        ws_bytes = lib.spec_typical_workspace_size(B, gamma)
+    return lib.spec_typical_accept(target, ld if ld is not None else V, dtype, B, gamma, V, pol,
+                                   tokens, eps, delta, out, out, None, ws, ws_bytes, None)
+
+
+def test_typical_workspace_size(lib):
+    assert lib.spec_typical_workspace_size(3, 4) == 3 * 5 * 8
+    assert lib.spec_typical_workspace_size(-1, 4) == 0
+    assert lib.spec_typical_workspace_size(3, -1) == 0
+
+
+def test_typical_rejects_bad_arguments(lib):
+    INV = _abi.SPEC_ERR_INVALID_ARG
+    assert typical_call(lib, B=-1) == INV
+    assert typical_call(lib, gamma=-1) == INV
+    assert typical_call(lib, V=0) == INV
+    assert typical_call(lib, dtype=7) == INV
+    assert typical_call(lib, target=None) == INV
+    assert typical_call(lib, tokens=None) == INV
+    assert typical_call(lib, out=None) == INV
+    assert typical_call(lib, ld=99) == INV
+    assert typical_call(lib, pol=_abi.spec_policy(None, None)) == INV
+    assert typical_call(lib, eps=-0.1) == INV
+    assert typical_call(lib, delta=float("nan")) == INV
+    assert typical_call(lib, eps=float("inf")) == INV
+    assert typical_call(lib, ws=None) == INV
+    assert typical_call(lib, ws_bytes=8) == INV
+    assert typical_call(lib, ws=ctypes.c_void_p(FAKE.value + 4)) == INV  # misaligned
+    topk = _abi.spec_policy(FAKE.value, FAKE.value)
+    assert typical_call(lib, pol=topk) == _abi.SPEC_ERR_UNSUPPORTED
+    # nothing to verify: a no-op
+    assert typical_call(lib, B=0, target=None, tokens=None, out=None, ws=None) == _abi.SPEC_OK
