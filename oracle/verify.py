@@ -542,3 +542,65 @@ def tree_mask(parent, max_depth):
         else:
             flags |= FLAG_BAD_TREE
     return mask, position, flags
+
+
+# ---------------------------------------------------------------------------
+# EAGLE-2 rerank of a draft tree
+# ---------------------------------------------------------------------------
+
+def tree_values(parent, confidence):
+    """value(t_n) = product of the confidences c_j on the path root..t_n.
+
+    zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE：特征空间草稿",
+    § 10.3 扩展 + 重排 (value(t_i) = prod over Path(root, t_i) of c_j).
+    Computed in float32 from the root down, value[n] = value[parent[n]] *
+    c[n] with value[0] = c[0]: the ranking below is decided on these floats,
+    in the same precision and order as the kernel's.  parent must be valid
+    (tree_check).
+    """
+    c = np.asarray(confidence, dtype=np.float32)
+    value = np.zeros(len(parent), dtype=np.float32)
+    for n in range(len(parent)):
+        value[n] = c[0] if n == 0 else np.float32(value[int(parent[n])] * c[n])
+    return value
+
+
+def clamp_confidence(confidence):
+    """Confidences clamped into [0, 1] (NaN -> 0) and whether any was changed.
+
+    The pages' properties (value(child) <= value(parent), a connected top-m)
+    need c in [0, 1]; this entry point's reading is to clamp and flag."""
+    c = np.asarray(confidence, dtype=np.float32)
+    out = np.where(c > 0, np.minimum(c, np.float32(1)), np.float32(0)).astype(np.float32)
+    changed = bool(np.isnan(c).any() or (c < 0).any() or (c > 1).any())
+    return out, changed
+
+
+def tree_rerank(parent, confidence, m):
+    """EAGLE-2 rerank: the top-m nodes of a draft tree by value.
+
+    zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE：特征空间草稿",
+    § 10.3 扩展 + 重排 (rerank: the m nodes of highest value over the whole
+    tree, flattened into one sequence for verification; ties go to the
+    shallower node; because c <= 1 a child's value never exceeds its parent's,
+    so the chosen set is a connected tree) and § 题 5.  Reading: remaining
+    ties go to the lower node index.
+
+    Returns (nodes, new_parent, values, flags): the chosen node ids in
+    ascending order (so parents precede children), each one's parent as a
+    position in that list (-1 for the root), their values, and flags
+    (FLAG_BAD_TREE for an invalid parent array: nothing chosen;
+    FLAG_NONFINITE when a confidence was clamped into [0, 1]).
+    """
+    N = len(parent)
+    flags, depth = tree_check(parent, N)
+    if flags & FLAG_BAD_TREE:
+        return [], [], [], FLAG_BAD_TREE
+    c, changed = clamp_confidence(confidence)
+    flags = FLAG_NONFINITE if changed else 0
+    value = tree_values(parent, c)
+    order = sorted(range(N), key=lambda n: (-float(value[n]), depth[n], n))
+    chosen = sorted(order[:min(m, N)])
+    pos = {n: i for i, n in enumerate(chosen)}
+    new_parent = [-1 if n == 0 else pos[int(parent[n])] for n in chosen]
+    return chosen, new_parent, [float(value[n]) for n in chosen], flags

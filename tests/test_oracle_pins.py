@@ -788,3 +788,75 @@ def test_typical_chain_greedy_and_threshold_one():
     r = verify.typical_chain(z, toks, t0, 1.0, 1.0)
     assert all(x["num_accepted"] == 0 for x in r)
     assert [x["tokens"][0] for x in r] == list(arg[:, 0])
+
+
+# ---------------------------------------------------------------------------
+# EAGLE-2 rerank: zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE", § 10.3
+# and § 题 5
+# ---------------------------------------------------------------------------
+
+def random_tree(rng, N):
+    return np.array([-1] + [int(rng.integers(0, n)) for n in range(1, N)], np.int32)
+
+
+def test_tree_values_are_path_products():
+    import math
+    rng = np.random.default_rng(61)
+    for _ in range(20):
+        N = int(rng.integers(1, 40))
+        par = random_tree(rng, N)
+        c = rng.random(N).astype(np.float32)
+        val = verify.tree_values(par, c)
+        for n in range(N):
+            path, a = [], n
+            while a != -1:
+                path.append(float(c[a]))
+                a = int(par[a])
+            assert abs(float(val[n]) - math.prod(path)) <= 1e-6 * max(math.prod(path), 1e-30)
+            if n:  # value(child) <= value(parent)
+                assert val[n] <= val[par[n]]
+
+
+def test_rerank_is_connected_and_top_m():
+    rng = np.random.default_rng(62)
+    for _ in range(50):
+        N = int(rng.integers(1, 30))
+        par = random_tree(rng, N)
+        c = rng.random(N).astype(np.float32)
+        c[0] = 1.0
+        c[rng.random(N) < 0.2] = 1.0  # ties along paths
+        for m in (1, 3, N, N + 2):
+            nodes, newp, vals, flags = verify.tree_rerank(par, c, m)
+            assert flags == 0 and len(nodes) == min(m, N) and nodes[0] == 0
+            chosen = set(nodes)
+            for n in nodes:  # every chosen node's parent is chosen
+                assert n == 0 or int(par[n]) in chosen
+            for i, n in enumerate(nodes):  # the re-indexed parents match
+                assert newp[i] == (-1 if n == 0 else nodes.index(int(par[n])))
+            # no unchosen node beats a chosen one
+            val = verify.tree_values(par, c)
+            if len(nodes) < N:
+                worst = min(val[list(chosen)])
+                assert all(val[n] <= worst for n in range(N) if n not in chosen)
+
+
+def test_rerank_page_properties_by_hand():
+    # root 0 -> 1 (c .9) -> 2 (c .9) -> 3 (c .5); root -> 4 (c .6)
+    par = np.array([-1, 0, 1, 2, 0], np.int32)
+    c = np.array([1.0, 0.9, 0.9, 0.5, 0.6], np.float32)
+    # values 1, .9, .81, .405, .6: with m = 4 the shallow unexpanded node 4
+    # (.6) is kept and the deep node 3 (.405) is dropped
+    nodes, newp, vals, _ = verify.tree_rerank(par, c, 4)
+    assert nodes == [0, 1, 2, 4] and newp == [-1, 0, 1, 0]
+    # a tie between a depth-1 and a depth-2 node goes to the shallower one
+    par = np.array([-1, 0, 1, 0], np.int32)
+    c = np.array([1.0, 1.0, 0.5, 0.5], np.float32)  # values 1, 1, .5, .5
+    assert verify.tree_rerank(par, c, 3)[0] == [0, 1, 3]
+
+
+def test_rerank_bad_inputs():
+    assert verify.tree_rerank(np.array([0, 0], np.int32), np.ones(2), 2)[3] == verify.FLAG_BAD_TREE
+    assert verify.tree_rerank(np.array([-1, 1], np.int32), np.ones(2), 2)[3] == verify.FLAG_BAD_TREE
+    nodes, _, vals, flags = verify.tree_rerank(np.array([-1, 0, 0], np.int32),
+                                               np.array([1.0, np.nan, 2.0]), 2)
+    assert flags == verify.FLAG_NONFINITE and nodes == [0, 2] and vals == [1.0, 1.0]
