@@ -16,7 +16,9 @@ Arms:
 --op overlap times the per-position overlap beta_i = sum min(p_i, q_i) of
 the same workload instead (metric: positions per second, B * gamma per step);
 --op typical times typical acceptance (epsilon 0.0625, delta 0.5; metric:
-target rows per second, B * (gamma + 1) per step).
+target rows per second, B * (gamma + 1) per step); --op rerank times the
+EAGLE-2 rerank of 256 draft trees of 1024 nodes (top 64; metric: trees per
+second).
 
 Under torchrun each rank verifies its own batch on its own GPU (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
@@ -575,6 +577,138 @@ def run_rowop(args):
         dist.destroy_process_group()
 
 
+RERANK_METRIC = "reranked draft trees/s"
+RERANK_T, RERANK_N, RERANK_M = 256, 1024, 64
+
+
+def rerank_workload():
+    from speculative_decoding_verification_temp_gb300 import workloads
+    return workloads.make_rerank(RERANK_T, RERANK_N, seed=1100)
+
+
+def rerank_config():
+    return {"workload": f"EAGLE-2 rerank: {RERANK_T} trees of {RERANK_N} nodes, top m = {RERANK_M}",
+            "T": RERANK_T, "N": RERANK_N, "m": RERANK_M,
+            "input_bytes_per_step": RERANK_T * RERANK_N * 8,
+            "l2": "L2 flushed (a 256 MB write) before every call; value from the calls' own "
+                  "event times"}
+
+
+def oracle_rerank_rate(w, n_trees):
+    from oracle import verify as ov
+    t0 = time.perf_counter()
+    for t in range(n_trees):
+        ov.tree_rerank(w["parent"][t], w["confidence"][t], RERANK_M)
+    dt = time.perf_counter() - t0
+    return n_trees / dt, dt
+
+
+def run_rerank(args):
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = rerank_workload()
+        oracle_rerank_rate(w, 1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_rerank_rate(w, 1)
+        dt = time.perf_counter() - t0
+        value = args.steps / dt
+        print(json.dumps({
+            "impl": "reference", "metric": RERANK_METRIC, "value": value, "unit": "trees/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": rerank_config(),
+            "cpu_baseline": {"value": value, "unit": "trees/s", "cores": 1, "kind": "oracle",
+                             "sample": "one tree per step"},
+            "e2e": {"value": value, "unit": "trees/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verification_temp_gb300 as sv
+
+    w = rerank_workload()
+    par_h = torch.from_numpy(w["parent"]).pin_memory()
+    conf_h = torch.from_numpy(w["confidence"]).pin_memory()
+    par, conf = par_h.to(dev), conf_h.to(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        sv.tree_rerank(par, conf, RERANK_M)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            sv.tree_rerank(par, conf, RERANK_M)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    elapsed_ms = max_over_ranks(sum(launch_ms), world, dev)
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        r = sv.tree_rerank(par_h.to(dev, non_blocking=True), conf_h.to(dev, non_blocking=True),
+                           RERANK_M)
+        out = r.nodes.to("cpu")
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    avg_launch_ms = statistics.mean(launch_ms)
+    peak, peak_kind = measured_peak()
+    nbytes = RERANK_T * RERANK_N * 8 + RERANK_T * RERANK_M * 12 + RERANK_T * 8
+    achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
+    line = {
+        "metric": RERANK_METRIC, "value": job_rate(world, RERANK_T, args.steps, elapsed_ms / 1e3),
+        "unit": "trees/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": rerank_config(),
+        "clocks": clk.summary(),
+        "e2e": {"value": job_rate(world, RERANK_T, 1, e2e_s), "unit": "trees/s",
+                "h2d_bytes_per_step": (par_h.numel() + conf_h.numel()) * 4,
+                "d2h_bytes_per_step": out.numel() * 4},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "tree_rerank_kernel (latency-bound: one CTA per tree, "
+                               "log-depth and per-level passes, a bitonic sort)",
+                     "launch_ms_avg": avg_launch_ms,
+                     "launch_ms_median": statistics.median(launch_ms)},
+    }
+    if not args.no_cpu_baseline:
+        n = min(RERANK_T, args.cpu_seqs)
+        rate, dt = oracle_rerank_rate(w, n)
+        line["cpu_baseline"] = {"value": rate, "unit": "trees/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of {RERANK_T} trees, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,11 +721,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per batch (default: the B = 256 workload); for profiling")
-    ap.add_argument("--op", default="verify", choices=["verify", "overlap", "typical"],
+    ap.add_argument("--op", default="verify", choices=["verify", "overlap", "typical", "rerank"],
                     help="verify: the chain verifier (default); overlap: beta_i per position; "
-                         "typical: typical acceptance")
+                         "typical: typical acceptance; rerank: EAGLE-2 tree rerank")
     args = ap.parse_args()
-    if args.op in ROW_OPS:
+    if args.op == "rerank":
+        run_rerank(args)
+    elif args.op in ROW_OPS:
         if args.impl == "reference":
             run_rowop_reference(args)
         else:

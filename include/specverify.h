@@ -292,6 +292,34 @@ spec_status spec_typical_accept(
     int32_t *out_num_accepted, int32_t *out_tokens, uint32_t *out_flags,
     void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
+/* EAGLE-2 rerank of T draft trees of N nodes: keep the m nodes of highest
+ * value.  zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE：特征空间草稿",
+ * section 10.3: value(t_i) is the product of the confidences c_j on the path
+ * from the root to t_i; the m nodes of highest value over the whole tree are
+ * kept, ties to the shallower node (then to the lower index).  Since c <= 1
+ * the kept set is a connected tree; it is returned in ascending node order
+ * with re-indexed parents, ready for spec_tree_mask.
+ *
+ * parent [T, N] int32: node 0 is the root (parent -1), 0 <= parent[n] < n.
+ * confidence [T, N] float: c_n in [0, 1]; values outside (or NaN) are
+ *                clamped into [0, 1] (NaN -> 0) and flag SPEC_FLAG_NONFINITE.
+ *                value[n] = value[parent[n]] * c[n] in float32, value[0] = c[0].
+ * 1 <= N <= 4096, m >= 1.
+ * Outputs (device):
+ *   out_nodes [T, m] int32: the kept node ids, ascending, then -1.
+ *   out_parent [T, m] int32: each kept node's parent as a position in
+ *                            out_nodes (-1 for the root), then -1.
+ *   out_value [T, m] float (nullable): their values, then 0.
+ *   out_count [T] int32: min(m, N), or 0 for an invalid tree.
+ *   out_flags [T] (nullable): SPEC_FLAG_BAD_TREE (invalid parent array:
+ *                             nothing kept), SPEC_FLAG_NONFINITE (clamped).
+ * Errors: SPEC_ERR_INVALID_ARG (bad sizes or NULL pointers) before any launch;
+ * SPEC_ERR_CUDA for a failed launch.  T = 0 is a no-op.  One launch.
+ */
+spec_status spec_tree_rerank(const int32_t *parent, const float *confidence, int T, int N, int m,
+                             int32_t *out_nodes, int32_t *out_parent, float *out_value,
+                             int32_t *out_count, uint32_t *out_flags, spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

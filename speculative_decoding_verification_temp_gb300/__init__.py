@@ -11,6 +11,7 @@ in include/specverify.h); ``api`` is a thin torch binding over it.
   overlap        per-position acceptance rate beta_i = sum_v min(p_i, q_i)
   typical_accept typical acceptance (entropy threshold; approximate, not
                  distribution-exact)
+  tree_rerank    EAGLE-2 rerank: the top-m nodes of a draft tree by path value
 """
 
 from ._abi import (FLAG_BAD_TOKEN, FLAG_BAD_TREE, FLAG_DEGENERATE_RESIDUAL, FLAG_DEPTH,  # noqa: F401
@@ -21,9 +22,9 @@ def __getattr__(name):
     # the torch binding is imported on first use, so the workload generator
     # and the build step do not need torch
     if name in ("verify_chain", "verify_chain_static", "verify_tree", "tree_mask", "overlap",
-                "typical_accept", "SpecVerifyError", "workspace",
+                "typical_accept", "tree_rerank", "SpecVerifyError", "workspace",
                 "ChainResult", "TreeResult", "MaskResult", "OverlapResult", "TypicalResult",
-                "api"):
+                "RerankResult", "api"):
         import importlib
         api = importlib.import_module(__name__ + ".api")
         return api if name == "api" else getattr(api, name)

@@ -37,6 +37,7 @@ EXPORTS = (
     "spec_overlap",
     "spec_typical_workspace_size",
     "spec_typical_accept",
+    "spec_tree_rerank",
     "spec_status_string",
 )
 
@@ -95,6 +96,8 @@ def load():
     lib.spec_typical_accept.argtypes = [_p, _i64, _i, _i, _i, _i, spec_policy, _p,
                                         ctypes.c_float, ctypes.c_float, _p, _p, _p, _p, _sz, _p]
     lib.spec_typical_accept.restype = _i
+    lib.spec_tree_rerank.argtypes = [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p]
+    lib.spec_tree_rerank.restype = _i
     lib.spec_status_string.argtypes = [_i]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib

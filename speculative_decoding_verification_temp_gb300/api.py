@@ -331,3 +331,33 @@ def typical_accept(target_logits, draft_tokens, target_temperature, epsilon, del
                                    ws.numel(), _stream(dev))
     _check(code)
     return TypicalResult(num, out, flags)
+
+
+RerankResult = namedtuple("RerankResult", "nodes parent value count flags")
+
+
+def tree_rerank(parent, confidence, m):
+    """EAGLE-2 rerank (see spec_tree_rerank): the m nodes of highest path
+    product of confidences per tree, ascending, with re-indexed parents.
+
+    parent [T, N] integer and confidence [T, N] float (CUDA tensors or
+    arrays).  Returns RerankResult with nodes, parent [T, m] int32, value
+    [T, m] float32, count [T] int32 and flags [T] int32.
+    """
+    par = torch.as_tensor(parent)
+    if par.dim() == 1:
+        par = par.unsqueeze(0)
+    T, N = par.shape
+    dev = par.device if par.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    par = par.to(device=dev, dtype=torch.int32).contiguous()
+    conf = torch.as_tensor(confidence).to(device=dev, dtype=torch.float32).reshape(T, N).contiguous()
+    m = int(m)
+    nodes = torch.empty((T, max(m, 1)), dtype=torch.int32, device=dev)
+    newp = torch.empty_like(nodes)
+    value = torch.empty((T, max(m, 1)), dtype=torch.float32, device=dev)
+    count = torch.empty(T, dtype=torch.int32, device=dev)
+    flags = torch.empty(T, dtype=torch.int32, device=dev)
+    code = _abi.load().spec_tree_rerank(_ptr(par), _ptr(conf), T, N, m, _ptr(nodes), _ptr(newp),
+                                        _ptr(value), _ptr(count), _ptr(flags), _stream(dev))
+    _check(code)
+    return RerankResult(nodes, newp, value, count, flags)

@@ -22,6 +22,9 @@ cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cuda
 cudaError_t launch_overlap(const void *target, long long ld_t, const void *draft, long long ld_d,
                            int esize, int B, int gamma, int V, const float *Tp, const float *Tq,
                            float *out_beta, uint32_t *out_flags, cudaStream_t stream);
+cudaError_t launch_tree_rerank(const int32_t *parent, const float *confidence, int T, int N, int m,
+                               int32_t *out_nodes, int32_t *out_parent, float *out_value,
+                               int32_t *out_count, uint32_t *out_flags, cudaStream_t stream);
 size_t typical_workspace_bytes(int B, int gamma);
 cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B, int gamma, int V,
                            const float *Tp, const int32_t *tokens, float epsilon, float delta,
@@ -528,6 +531,18 @@ spec_status spec_typical_accept(const void *target_logits, int64_t ld_target, sp
                                      target_policy.temperature, draft_tokens, epsilon, delta,
                                      out_num_accepted, out_tokens, out_flags, workspace,
                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+spec_status spec_tree_rerank(const int32_t *parent, const float *confidence, int T, int N, int m,
+                             int32_t *out_nodes, int32_t *out_parent, float *out_value,
+                             int32_t *out_count, uint32_t *out_flags, spec_stream_t stream) {
+  if (T < 0 || N < 1 || N > kMaxNodes || m < 1) return SPEC_ERR_INVALID_ARG;
+  if (T == 0) return SPEC_OK;
+  if (!parent || !confidence || !out_nodes || !out_parent || !out_count)
+    return SPEC_ERR_INVALID_ARG;
+  return map_cuda(sv::launch_tree_rerank(parent, confidence, T, N, m, out_nodes, out_parent,
+                                         out_value, out_count, out_flags,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

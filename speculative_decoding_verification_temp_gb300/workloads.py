@@ -175,6 +175,27 @@ def make_tree(T, N, V, dtype="bf16", scale=2.5, zipf=1.2, sigma=0.5, temperature
                 target_top_k=topk.copy(), draft_top_k=topk.copy(), seed=PHILOX_SEED)
 
 
+def make_rerank(T, N, seed=0, width=8, levels=256, deep=False):
+    """Draft trees for the rerank: parent [T, N] int32 and confidence [T, N]
+    float32.
+
+    Node n > 0 hangs under a node drawn uniformly from the previous `width`
+    ids (bushy trees a few levels deep; deep=True: a single chain).
+    Confidences are a draft's top probabilities, Beta(2, 1)-shaped, on a grid
+    of `levels` steps so that equal values (and equal path products) occur;
+    the root's is 1.
+    """
+    rng = np.random.default_rng(seed)
+    parent = np.empty((T, N), np.int32)
+    parent[:, 0] = -1
+    for n in range(1, N):
+        parent[:, n] = n - 1 if deep else rng.integers(max(0, n - width), n, size=T)
+    conf = np.sqrt(rng.random((T, N)))
+    conf = (np.ceil(conf * levels) / levels).astype(np.float32)
+    conf[:, 0] = 1.0
+    return dict(parent=parent, confidence=conf)
+
+
 def config(i):
     """Inputs of workload i (0-4), generator seed 1000 + i."""
     c = dict(CONFIGS[i])

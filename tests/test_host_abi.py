@@ -235,3 +235,19 @@ def test_typical_rejects_bad_arguments(lib):
     assert typical_call(lib, pol=topk) == _abi.SPEC_ERR_UNSUPPORTED
     # nothing to verify: a no-op
     assert typical_call(lib, B=0, target=None, tokens=None, out=None, ws=None) == _abi.SPEC_OK
+
+
+def test_tree_rerank_rejects_bad_arguments(lib):
+    INV = _abi.SPEC_ERR_INVALID_ARG
+
+    def call(T=2, N=10, m=3, par=FAKE, conf=FAKE, out=FAKE):
+        return lib.spec_tree_rerank(par, conf, T, N, m, out, out, None, out, None, None)
+
+    assert call(T=-1) == INV
+    assert call(N=0) == INV
+    assert call(N=4097) == INV
+    assert call(m=0) == INV
+    assert call(par=None) == INV
+    assert call(conf=None) == INV
+    assert call(out=None) == INV
+    assert call(T=0, par=None, conf=None, out=None) == _abi.SPEC_OK
