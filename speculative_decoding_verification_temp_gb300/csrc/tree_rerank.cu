@@ -13,9 +13,9 @@
 //      flagged); an invalid parent array (parent[0] != -1 or parent[n] not in
 //      [0, n)) ends the tree with nothing kept;
 //   2. depths by pointer jumping (about log2 N rounds);
-//   3. nodes bucketed by depth (counting sort), then values level by level,
-//      value[n] = value[parent[n]] * c[n] in float32, so every product is
-//      taken in the same order as the path from the root;
+//   3. nodes bucketed by depth (counting sort), then values level by level
+//      by one warp, value[n] = value[parent[n]] * c[n] in float32, so every
+//      product is taken in the same order as the path from the root;
 //   4. one 64-bit key per node, (~value bits, depth, index), ascending in the
 //      wanted order, bitonic-sorted; the key of rank m - 1 is the cut;
 //   5. kept nodes in ascending index (parents before children) through an
@@ -161,14 +161,19 @@ __global__ void __launch_bounds__(kRrThreads) tree_rerank_kernel(
   block_exclusive_scan(lvl, D + 1, warp_tot);
   for (int n = threadIdx.x; n < N; n += kRrThreads) order[atomicAdd(&lvl[dep[n]], 1)] = n;
   __syncthreads();  // lvl[d] is now the end of level d
-  for (int d = 1; d <= D; ++d) {
-    const int b = lvl[d - 1], e = lvl[d];
-    for (int i = b + threadIdx.x; i < e; i += kRrThreads) {
-      const int n = order[i];
-      val[n] = __fmul_rn(val[par[n]], val[n]);
+  // one warp walks the levels (a level holds a few nodes in a draft tree, so
+  // a warp barrier per level beats a block barrier)
+  if (threadIdx.x < 32) {
+    for (int d = 1; d <= D; ++d) {
+      const int b = lvl[d - 1], e = lvl[d];
+      for (int i = b + static_cast<int>(threadIdx.x); i < e; i += 32) {
+        const int n = order[i];
+        val[n] = __fmul_rn(val[par[n]], val[n]);
+      }
+      __syncwarp();
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // 4. keys, bitonic sort, the cut
   for (int i = threadIdx.x; i < P; i += kRrThreads)
