@@ -24,6 +24,17 @@ Readings where the pages are silent:
     flagged and replaced by the one-hot distribution at the finite argmax
     (index 0 when nothing is finite).  The pages only say such inputs are
     errors (verify_candidate raises ValueError on non-finite probabilities).
+  * top-p and min-p: the pages list them among the processors p and q must
+    share (wineandchord.com, § 与 Logit Processor 的组合) but define neither.  The plain published
+    definitions are used: top-p (nucleus sampling, Holtzman et al., "The
+    Curious Case of Neural Text Degeneration", ICLR 2020) keeps the smallest
+    set of most probable tokens whose mass reaches p; min-p keeps the tokens
+    whose probability is at least min_p times the largest.  Order: temperature
+    and top-k, then top-p on that distribution, then min-p on the result, each
+    renormalised.  Ties at a boundary value are all kept, as for top-k.
+    top_p >= 1 and min_p <= 0 mean no filtering.  Where float rounding puts
+    a cumulative mass within 1e-12 of p the decision is the float64 one here;
+    a GPU decision in float32 may differ there (a parity excuse, not a pin).
 """
 
 import numpy as np
@@ -91,3 +102,43 @@ def policy_distribution(z, temperature, top_k=0):
     m = kept.max()
     weights = np.exp((kept - m) / T)
     return Dist(False, probs=weights / weights.sum())
+
+
+def topp_threshold(probs, top_p):
+    """Smallest probability kept by top-p: the value at which the descending
+    cumulative mass first reaches top_p (None for no filter)."""
+    if top_p >= 1.0:
+        return None
+    ordered = np.sort(np.asarray(probs, dtype=np.float64))[::-1]
+    i = int(np.searchsorted(np.cumsum(ordered), top_p, side="left"))
+    return ordered[min(i, len(ordered) - 1)]
+
+
+def topp_filter(probs, top_p):
+    """Nucleus (top-p) filtering of a probability vector, renormalised; every
+    entry tied with the boundary value is kept."""
+    probs = np.asarray(probs, dtype=np.float64)
+    thr = topp_threshold(probs, top_p)
+    if thr is None:
+        return probs
+    kept = np.where(probs >= thr, probs, 0.0)
+    return kept / kept.sum()
+
+
+def minp_filter(probs, min_p):
+    """Min-p filtering: keep p(x) >= min_p * max p, renormalised."""
+    probs = np.asarray(probs, dtype=np.float64)
+    if min_p <= 0.0:
+        return probs
+    kept = np.where(probs >= min_p * probs.max(), probs, 0.0)
+    return kept / kept.sum()
+
+
+def policy_distribution_ext(z, temperature, top_k=0, top_p=1.0, min_p=0.0):
+    """policy_distribution followed by top-p and then min-p (see the module
+    readings); a greedy or non-finite row stays one-hot."""
+    d = policy_distribution(z, temperature, top_k)
+    if d.onehot:
+        return d
+    probs = minp_filter(topp_filter(d.probs, top_p), min_p)
+    return Dist(False, probs=probs, flags=d.flags)

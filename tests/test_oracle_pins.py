@@ -860,3 +860,86 @@ def test_rerank_bad_inputs():
     nodes, _, vals, flags = verify.tree_rerank(np.array([-1, 0, 0], np.int32),
                                                np.array([1.0, np.nan, 2.0]), 2)
     assert flags == verify.FLAG_NONFINITE and nodes == [0, 2] and vals == [1.0, 1.0]
+
+
+# ---------------------------------------------------------------------------
+# top-p and min-p (the published definitions; the pages only name them)
+# ---------------------------------------------------------------------------
+
+def test_topp_hand_cases():
+    from oracle import policy as pol
+    p = np.array([0.05, 0.5, 0.15, 0.3])
+    # descending 0.5, 0.3, 0.15, 0.05: the mass reaches 0.8 at the second token
+    assert np.allclose(pol.topp_filter(p, 0.8), [0, 0.5 / 0.8, 0, 0.3 / 0.8])
+    assert np.allclose(pol.topp_filter(p, 0.81), [0, 0.5, 0.15, 0.3] / np.float64(0.95))
+    assert np.array_equal(pol.topp_filter(p, 1.0), p)
+    # the most probable token alone when top_p is below its mass
+    assert np.allclose(pol.topp_filter(p, 0.3), [0, 1, 0, 0])
+    # ties at the boundary are all kept
+    q = np.array([0.4, 0.2, 0.2, 0.2])
+    assert np.allclose(pol.topp_filter(q, 0.5), q)
+
+
+def test_topp_minimal_prefix_property():
+    from oracle import policy as pol
+    rng = np.random.default_rng(71)
+    for _ in range(200):
+        V = int(rng.integers(2, 40))
+        p = rng.dirichlet(np.full(V, 0.5))
+        tp = float(rng.uniform(0.05, 0.99))
+        f = pol.topp_filter(p, tp)
+        kept = f > 0
+        # a descending prefix, holding at least top_p of the mass ...
+        assert p[kept].min() >= p[~kept].max(initial=0.0)
+        assert p[kept].sum() >= tp - 1e-12
+        # ... and minimal: without its smallest value it falls short
+        assert p[kept].sum() - p[kept].min() * (p[kept] == p[kept].min()).sum() < tp
+        assert abs(f.sum() - 1.0) < 1e-12
+
+
+def test_minp_hand_cases_and_composition():
+    from oracle import policy as pol
+    p = np.array([0.5, 0.3, 0.15, 0.05])
+    assert np.allclose(pol.minp_filter(p, 0.2), [0.5, 0.3, 0.15, 0] / np.float64(0.95))
+    assert np.allclose(pol.minp_filter(p, 0.6), [0.5, 0.3, 0, 0] / np.float64(0.8))
+    assert np.array_equal(pol.minp_filter(p, 0.0), p)
+    # min-p at 1 keeps the maxima only; temperature first, then the filters
+    z = np.log(np.array([0.5, 0.3, 0.15, 0.05]))
+    d = pol.policy_distribution_ext(z, 1.0, 0, 1.0, 1.0)
+    assert np.allclose(d.probs, [1, 0, 0, 0])
+    d = pol.policy_distribution_ext(z, 2.0, 0, 0.8, 0.0)
+    sm = np.exp(z / 2) / np.exp(z / 2).sum()
+    assert np.allclose(d.probs, pol.topp_filter(sm, 0.8))
+    # greedy rows stay one-hot
+    assert pol.policy_distribution_ext(z, 0.0, 0, 0.5, 0.5).onehot
+
+
+def test_filtered_policies_keep_the_verifier_exact():
+    """With the same top-p / min-p on both sides the chain still returns the
+    filtered target law exactly (enumeration over uniforms, exact arithmetic)."""
+    from oracle import policy as pol
+    rng = np.random.default_rng(72)
+    for _ in range(10):
+        V = 5
+        p = pol.minp_filter(pol.topp_filter(rng.dirichlet(np.ones(V)), 0.85), 0.1)
+        q = pol.minp_filter(pol.topp_filter(rng.dirichlet(np.ones(V)), 0.85), 0.1)
+        pf = random_rational_from(p)
+        qf = random_rational_from(q)
+        law = [F(0)] * V
+        for x in range(V):
+            if qf[x] == 0:
+                continue
+            accepted, alpha, _ = verify.accept_test(pf, qf, x, F(0))
+            law[x] += qf[x] * alpha
+        r, Z, _ = verify.positive_residual(pf, qf)
+        for y in range(V):
+            law[y] += Z * r[y] if Z > 0 else 0
+        assert law == list(pf)
+
+
+def random_rational_from(p):
+    # a nearby distribution in exact rationals with the same support
+    w = [int(round(float(x) * 1000)) if x > 0 else 0 for x in p]
+    w = [max(x, 1) if px > 0 else 0 for x, px in zip(w, p)]
+    s = sum(w)
+    return np.array([F(x, s) for x in w], dtype=object)
