@@ -359,7 +359,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(),
+                     "frac": achieved / peak,
+                     # the record is for the full-size workload only
+                     "traffic": None if args.batch else recorded_traffic(),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "kernel": "pass_kernel (timed per call: workspace clear + pass_kernel, "
                                "so achieved is a lower bound)",
@@ -562,7 +564,8 @@ def run_rowop(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4},
         "gpu_launches": op["launches"] * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(*op["traffic"]),
+                     "frac": achieved / peak,
+                     "traffic": None if args.batch else recorded_traffic(*op["traffic"]),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "kernel": op["kernel"], "launch_ms_avg": avg_launch_ms,
                      "launch_ms_median": statistics.median(launch_ms)},
