@@ -41,7 +41,19 @@ def _rank_main(rank, world, port, out):
         buf = io.StringIO()
         with redirect_stdout(buf):
             bench.run_reference(args)
-        out.put((rank, w, r, local, slowest, rate, buf.getvalue()))
+        # the oracle arms of the other measured operations behave the same way
+        ops = {}
+        for op in ("overlap", "typical", "rerank"):
+            oargs = bench.argparse.Namespace(steps=1, warmup=0, gpus=w, batch=2, op=op,
+                                             impl="reference")
+            obuf = io.StringIO()
+            with redirect_stdout(obuf):
+                if op == "rerank":
+                    bench.run_rerank(oargs)
+                else:
+                    bench.run_rowop_reference(oargs)
+            ops[op] = obuf.getvalue()
+        out.put((rank, w, r, local, slowest, rate, buf.getvalue(), ops))
     finally:
         dist.destroy_process_group()
 
@@ -57,7 +69,7 @@ def test_two_ranks_take_the_slowest_time_and_count_all_rows():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    for rank, w, r, local, slowest, rate, printed in res:
+    for rank, w, r, local, slowest, rate, printed, _ in res:
         assert (w, r, local) == (2, rank, rank)
         assert slowest == 0.75
         assert rate == 2 * 2048 * 10 / 0.75
@@ -65,6 +77,11 @@ def test_two_ranks_take_the_slowest_time_and_count_all_rows():
     line = json.loads(res[0][6].strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["scaling"] == "weak"
     assert line["cpu_baseline"]["kind"] == "oracle"
+    for op in ("overlap", "typical", "rerank"):
+        assert res[1][7][op] == ""
+        line = json.loads(res[0][7][op].strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["value"] > 0
+        assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
 def test_one_rank_is_its_own_maximum():
