@@ -712,6 +712,72 @@ def run_rerank(args):
         dist.destroy_process_group()
 
 
+def run_workloads(args):
+    """Per-call times of the five verification workloads and the tree mask:
+    CUDA events around each call through the Python API, inputs resident in
+    HBM, the L2 flushed (a 256 MB write) before every call; the median of
+    --steps calls after --warmup calls.  One JSON line with every workload."""
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verification_temp_gb300 as sv
+    from speculative_decoding_verification_temp_gb300 import workloads
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def median_call_us(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    def dev_logits(x, dtype):
+        t = torch.from_numpy(x).to(dev)
+        return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+    per = {}
+    for i in range(5):
+        w = workloads.config(i)
+        t = dev_logits(w["target"], w["dtype"])
+        d = dev_logits(w["draft"], w["dtype"])
+        esize = 2 if w["dtype"] == "bf16" else 4
+        if "B" in w:
+            tok = torch.from_numpy(w["tokens"]).to(dev)
+            us = median_call_us(lambda: sv.verify_chain(
+                t, d, tok, w["target_temperature"], w["draft_temperature"],
+                w.get("target_top_k"), w.get("draft_top_k"), seed=w["seed"]))
+            rows = w["B"] * (w["gamma"] + 1)
+        else:
+            tok = torch.from_numpy(w["tokens"]).to(dev)
+            par = torch.from_numpy(w["parent"]).to(dev)
+            us = median_call_us(lambda: sv.verify_tree(
+                t, d, tok, par, w["max_depth"], w["target_temperature"],
+                w["draft_temperature"], w.get("target_top_k"), w.get("draft_top_k"),
+                seed=w["seed"]))
+            rows = w["T"] * w["N"]
+            per["tree_mask"] = {"us_per_call": median_call_us(
+                lambda: sv.tree_mask(par, w["max_depth"])), "trees": w["T"], "nodes": w["N"]}
+        per[f"workload_{i}"] = {"us_per_call": us, "rows_per_s": rows / (us / 1e6),
+                                "dtype": w["dtype"], "V": w["V"], "esize": esize}
+    print(json.dumps({"metric": "per-call time of each workload", "unit": "us",
+                      "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+                      "l2": "flushed (a 256 MB write) before every call",
+                      "workloads": per}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -724,11 +790,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per batch (default: the B = 256 workload); for profiling")
-    ap.add_argument("--op", default="verify", choices=["verify", "overlap", "typical", "rerank"],
+    ap.add_argument("--op", default="verify",
+                    choices=["verify", "overlap", "typical", "rerank", "workloads"],
                     help="verify: the chain verifier (default); overlap: beta_i per position; "
-                         "typical: typical acceptance; rerank: EAGLE-2 tree rerank")
+                         "typical: typical acceptance; rerank: EAGLE-2 tree rerank; "
+                         "workloads: per-call times of workloads 0-4 and the tree mask")
     args = ap.parse_args()
-    if args.op == "rerank":
+    if args.op == "workloads":
+        run_workloads(args)
+    elif args.op == "rerank":
         run_rerank(args)
     elif args.op in ROW_OPS:
         if args.impl == "reference":
