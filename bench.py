@@ -754,7 +754,8 @@ def run_workloads(args):
         return x if x is not None and (x > 0).any() else None
 
     per = {}
-    for i in range(5):
+    ids = [int(x) for x in args.only.split(",")] if args.only else range(5)
+    for i in ids:
         w = workloads.config(i)
         t = dev_logits(w["target"], w["dtype"])
         d = dev_logits(w["draft"], w["dtype"])
@@ -800,6 +801,8 @@ def main():
                     help="verify: the chain verifier (default); overlap: beta_i per position; "
                          "typical: typical acceptance; rerank: EAGLE-2 tree rerank; "
                          "workloads: per-call times of workloads 0-4 and the tree mask")
+    ap.add_argument("--only", default="",
+                    help="--op workloads: a comma list of workload ids (default: 0-4)")
     args = ap.parse_args()
     if args.op == "workloads":
         run_workloads(args)
