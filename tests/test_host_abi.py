@@ -251,3 +251,15 @@ def test_tree_rerank_rejects_bad_arguments(lib):
     assert call(conf=None) == INV
     assert call(out=None) == INV
     assert call(T=0, par=None, conf=None, out=None) == _abi.SPEC_OK
+
+
+def test_binding_argtypes_match_the_header(lib):
+    """Every function the header declares has as many parameters as the
+    binding passes (a drift check for the ctypes argtypes)."""
+    hdr = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for name in _abi.EXPORTS:
+        m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", hdr)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == len(params), (name, len(params))
