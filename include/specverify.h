@@ -23,6 +23,16 @@
  *   - Tree mask: each node sees itself and its ancestors; position = depth.
  *     Notes section "Token Tree Verifier: topology-aware causal mask";
  *     jennyma11.github.io "11.3 Self-Draft", section 11.3.4 Tree Attention.
+ *   - Overlap (spec_overlap): beta_i = sum_v min(p_i(v), q_i(v)), the
+ *     acceptance rate of draft position i.  Notes section "Correction 为什么
+ *     用正残差".
+ *   - Typical acceptance (spec_typical_accept): an approximate rule, not
+ *     distribution-exact; p(x_i) > min(epsilon, delta exp(-H(p_i))), longest
+ *     passing prefix, then the target's greedy token.  Notes section
+ *     "Medusa-1 与 typical acceptance".
+ *   - EAGLE-2 rerank (spec_tree_rerank): the m nodes of highest product of
+ *     confidences along the path, shallow nodes first on ties.
+ *     zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE", section 10.3.
  *
  * Readings where the pages are silent (fixed here, identical in the tests):
  *   greedy/argmax ties -> lowest index; top-k keeps every logit >= the k-th
@@ -40,8 +50,10 @@
  *   - Host-checkable problems (a NULL required pointer, a negative size, a
  *     stride shorter than the row, a size above the limits below, a workspace
  *     that is too small) return SPEC_ERR_INVALID_ARG before anything is
- *     launched.  SPEC_ERR_UNSUPPORTED means the shape cannot be run by this
- *     build (vocabulary too large for one thread-block cluster).
+ *     launched.  SPEC_ERR_UNSUPPORTED means the call cannot be run by this
+ *     build: a vocabulary too large for one thread-block cluster (the
+ *     verifiers), or a top-k policy passed to spec_overlap or
+ *     spec_typical_accept.
  *     SPEC_ERR_CUDA reports a failed launch (cudaGetLastError).
  *   - Data-dependent problems never trap the GPU: they set per-sequence flag
  *     bits (SPEC_FLAG_*) and the sequence takes the defined fallback.
@@ -52,9 +64,10 @@
  *     (arrival counters and the weight-task queue).  Calls that share one
  *     workspace must not overlap on the GPU.
  *
- * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; V >= 1 and small enough that a
- * target+draft row pair fits in 16 thread blocks' shared memory (about
- * 800k bf16 or 400k fp32 entries).
+ * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; for the verifiers V >= 1 and
+ * small enough that a target+draft row pair fits in 16 thread blocks' shared
+ * memory (about 800k bf16 or 400k fp32 entries); spec_overlap and
+ * spec_typical_accept read rows from global memory and take any V >= 1.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
