@@ -14,7 +14,7 @@ Flag bits are the interface values of the library's per-sequence flag word.
 import numpy as np
 
 from . import philox
-from .policy import Dist, finite_argmax, policy_distribution
+from .policy import Dist, finite_argmax, policy_distribution, policy_distribution_ext
 
 FLAG_BAD_TOKEN = 1
 FLAG_ZERO_Q = 2
@@ -182,30 +182,39 @@ def chain_uniforms(seed, seq, uniform_override):
             (lambda i: philox.uniform(seed, seq, i, 1)))
 
 
+def _per_seq(x, n, default):
+    return np.full(n, default, np.float64) if x is None else np.asarray(x, np.float64)
+
+
 def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
                  draft_temperature, target_top_k=None, draft_top_k=None,
-                 seed=0, uniform_override=None, seqs=None):
+                 seed=0, uniform_override=None, seqs=None, target_top_p=None,
+                 draft_top_p=None, target_min_p=None, draft_min_p=None):
     """Logit-level chain verification for a batch.
 
     target_logits [B, gamma+1, V], draft_logits [B, gamma, V] (any real
     dtype, converted exactly to float64 row by row), draft_tokens [B, gamma],
-    per-sequence temperatures and top-k.  Rows are processed lazily: only the
-    rows up to the first rejection are touched, like the pages' loop.
+    per-sequence temperatures and top-k, and optionally per-sequence top-p and
+    min-p (oracle.policy.policy_distribution_ext; None: no filter).  Rows are
+    processed lazily: only the rows up to the first rejection are touched,
+    like the pages' loop.
     Returns a list of per-sequence dicts (see ``walk_chain``).
     """
     B, G1, V = target_logits.shape
     gamma = G1 - 1
     kp = np.zeros(B, np.int64) if target_top_k is None else np.asarray(target_top_k)
     kq = np.zeros(B, np.int64) if draft_top_k is None else np.asarray(draft_top_k)
+    pp, pq = _per_seq(target_top_p, B, 1.0), _per_seq(draft_top_p, B, 1.0)
+    mp, mq = _per_seq(target_min_p, B, 0.0), _per_seq(draft_min_p, B, 0.0)
     results = []
     for b in (range(B) if seqs is None else seqs):
         def get_p(i, b=b):
-            return policy_distribution(np.asarray(target_logits[b, i], np.float64),
-                                       target_temperature[b], kp[b])
+            return policy_distribution_ext(np.asarray(target_logits[b, i], np.float64),
+                                           target_temperature[b], kp[b], pp[b], mp[b])
 
         def get_q(i, b=b):
-            return policy_distribution(np.asarray(draft_logits[b, i], np.float64),
-                                       draft_temperature[b], kq[b])
+            return policy_distribution_ext(np.asarray(draft_logits[b, i], np.float64),
+                                           draft_temperature[b], kq[b], pq[b], mq[b])
 
         ua, ud = chain_uniforms(seed, b, uniform_override)
         res = walk_chain(gamma, V, get_p, get_q, draft_tokens[b], ua, ud)
@@ -466,7 +475,8 @@ def tree_uniforms(seed, tree, uniform_override):
 
 def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
                 target_temperature, draft_temperature, target_top_k=None,
-                draft_top_k=None, seed=0, uniform_override=None, trees=None):
+                draft_top_k=None, seed=0, uniform_override=None, trees=None,
+                target_top_p=None, draft_top_p=None, target_min_p=None, draft_min_p=None):
     """Logit-level tree verification for a batch of T trees of N nodes.
 
     target_logits [T, N, V]: row n is the target's next-token logits after the
@@ -476,15 +486,17 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
     T, N, V = target_logits.shape
     kp = np.zeros(T, np.int64) if target_top_k is None else np.asarray(target_top_k)
     kq = np.zeros(T, np.int64) if draft_top_k is None else np.asarray(draft_top_k)
+    pp, pq = _per_seq(target_top_p, T, 1.0), _per_seq(draft_top_p, T, 1.0)
+    mp, mq = _per_seq(target_min_p, T, 0.0), _per_seq(draft_min_p, T, 0.0)
     results = []
     for t in (range(T) if trees is None else trees):
         def get_p(n, t=t):
-            return policy_distribution(np.asarray(target_logits[t, n], np.float64),
-                                       target_temperature[t], kp[t])
+            return policy_distribution_ext(np.asarray(target_logits[t, n], np.float64),
+                                           target_temperature[t], kp[t], pp[t], mp[t])
 
         def get_q(n, t=t):
-            return policy_distribution(np.asarray(draft_logits[t, n], np.float64),
-                                       draft_temperature[t], kq[t])
+            return policy_distribution_ext(np.asarray(draft_logits[t, n], np.float64),
+                                           draft_temperature[t], kq[t], pq[t], mq[t])
 
         ua, ud = tree_uniforms(seed, t, uniform_override)
         res = walk_tree(N, V, parent[t], node_tokens[t], get_p, get_q, ua, ud, max_depth)

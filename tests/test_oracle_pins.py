@@ -943,3 +943,29 @@ def random_rational_from(p):
     w = [max(x, 1) if px > 0 else 0 for x, px in zip(w, p)]
     s = sum(w)
     return np.array([F(x, s) for x in w], dtype=object)
+
+
+def test_verify_chain_with_topp_minp_defaults_and_filtering():
+    """The new filters are off by default (identical results) and, when on,
+    every emitted token lies in the filtered target support."""
+    from oracle import policy as pol
+    rng = np.random.default_rng(73)
+    B, gamma, V = 6, 3, 50
+    zt = rng.normal(size=(B, gamma + 1, V)) * 2
+    zd = zt[:, :gamma] + 0.5 * rng.normal(size=(B, gamma, V))
+    toks = zd.argmax(-1)
+    t = np.ones(B)
+    base = verify.verify_chain(zt, zd, toks, t, t, seed=5)
+    same = verify.verify_chain(zt, zd, toks, t, t, seed=5, target_top_p=np.ones(B),
+                               draft_top_p=np.ones(B), target_min_p=np.zeros(B),
+                               draft_min_p=np.zeros(B))
+    assert [r["tokens"] for r in base] == [r["tokens"] for r in same]
+    tp, mp = np.full(B, 0.6), np.full(B, 0.05)
+    res = verify.verify_chain(zt, zd, toks, t, t, seed=5, target_top_p=tp, draft_top_p=tp,
+                              target_min_p=mp, draft_min_p=mp)
+    for b, r in enumerate(res):
+        for i, x in enumerate(r["tokens"]):
+            if x < 0:
+                break
+            p = pol.policy_distribution_ext(zt[b, i], 1.0, 0, 0.6, 0.05).probs
+            assert p[x] > 0, (b, i, x)
