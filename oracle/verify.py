@@ -11,6 +11,8 @@ and then call them.
 Flag bits are the interface values of the library's per-sequence flag word.
 """
 
+import math
+
 import numpy as np
 
 from . import philox
@@ -560,21 +562,51 @@ def tree_mask(parent, max_depth):
 # EAGLE-2 rerank of a draft tree
 # ---------------------------------------------------------------------------
 
+def _dyadic(x):
+    """A finite float as an exact pair (num, exp) with x = num * 2**exp."""
+    m, e = math.frexp(float(x))
+    if m == 0:
+        return 0, 0
+    num, exp = int(m * (1 << 53)), e - 53
+    while num and num % 2 == 0:
+        num //= 2
+        exp += 1
+    return num, exp
+
+
 def tree_values(parent, confidence):
-    """value(t_n) = product of the confidences c_j on the path root..t_n.
+    """value(t_n) = product of the confidences c_j on the path root..t_n, exactly.
 
     zzszmyf.github.io "LLM 推测解码精读笔记 · 04 EAGLE：特征空间草稿",
-    § 10.3 扩展 + 重排 (value(t_i) = prod over Path(root, t_i) of c_j).
-    Computed in float32 from the root down, value[n] = value[parent[n]] *
-    c[n] with value[0] = c[0]: the ranking below is decided on these floats,
-    in the same precision and order as the kernel's.  parent must be valid
-    (tree_check).
+    § 10.3 扩展 + 重排 (value(t_i) = prod over Path(root, t_i) of c_j).  Each
+    confidence is taken as the exact value of its float32, and the product is
+    formed in exact integer arithmetic: value[n] = (num, exp) with
+    value = num * 2**exp.  Nothing is rounded, so the ranking below is the
+    one the page's definition gives.  parent must be valid (tree_check).
     """
     c = np.asarray(confidence, dtype=np.float32)
-    value = np.zeros(len(parent), dtype=np.float32)
+    value = []
     for n in range(len(parent)):
-        value[n] = c[0] if n == 0 else np.float32(value[int(parent[n])] * c[n])
+        num, exp = _dyadic(c[n])
+        if n:
+            pn, pe = value[int(parent[n])]
+            num, exp = num * pn, exp + pe
+        value.append((num, exp) if num else (0, 0))
     return value
+
+
+def value_float(v):
+    """The float64 nearest an exact (num, exp) value (0 when it underflows);
+    Python's integer true division rounds correctly."""
+    num, exp = v
+    return num / (1 << -exp) if exp < 0 else float(num << exp)
+
+
+def value_keys(value):
+    """Integers that order the exact values like the values themselves: each
+    value scaled to the smallest exponent present."""
+    emin = min((e for n, e in value if n), default=0)
+    return [n << (e - emin) if n else 0 for n, e in value]
 
 
 def clamp_confidence(confidence):
@@ -596,13 +628,15 @@ def tree_rerank(parent, confidence, m):
     tree, flattened into one sequence for verification; ties go to the
     shallower node; because c <= 1 a child's value never exceeds its parent's,
     so the chosen set is a connected tree) and § 题 5.  Reading: remaining
-    ties go to the lower node index.
+    ties go to the lower node index.  The ranking uses the exact path
+    products of tree_values.
 
     Returns (nodes, new_parent, values, flags): the chosen node ids in
     ascending order (so parents precede children), each one's parent as a
-    position in that list (-1 for the root), their values, and flags
-    (FLAG_BAD_TREE for an invalid parent array: nothing chosen;
-    FLAG_NONFINITE when a confidence was clamped into [0, 1]).
+    position in that list (-1 for the root), their values (the float64
+    nearest each exact product), and flags (FLAG_BAD_TREE for an invalid
+    parent array: nothing chosen; FLAG_NONFINITE when a confidence was
+    clamped into [0, 1]).
     """
     N = len(parent)
     flags, depth = tree_check(parent, N)
@@ -611,8 +645,21 @@ def tree_rerank(parent, confidence, m):
     c, changed = clamp_confidence(confidence)
     flags = FLAG_NONFINITE if changed else 0
     value = tree_values(parent, c)
-    order = sorted(range(N), key=lambda n: (-float(value[n]), depth[n], n))
+    key = value_keys(value)
+    order = sorted(range(N), key=lambda n: (-key[n], depth[n], n))
     chosen = sorted(order[:min(m, N)])
     pos = {n: i for i, n in enumerate(chosen)}
     new_parent = [-1 if n == 0 else pos[int(parent[n])] for n in chosen]
-    return chosen, new_parent, [float(value[n]) for n in chosen], flags
+    return chosen, new_parent, [value_float(value[n]) for n in chosen], flags
+
+
+def rerank_order(parent, confidence):
+    """Every node of a valid tree in rerank order (best first) with its exact
+    value and depth: the ranking tree_rerank cuts at m."""
+    N = len(parent)
+    _, depth = tree_check(parent, N)
+    c, _ = clamp_confidence(confidence)
+    value = tree_values(parent, c)
+    key = value_keys(value)
+    order = sorted(range(N), key=lambda n: (-key[n], depth[n], n))
+    return order, value, depth

@@ -800,7 +800,7 @@ def random_tree(rng, N):
 
 
 def test_tree_values_are_path_products():
-    import math
+    from fractions import Fraction
     rng = np.random.default_rng(61)
     for _ in range(20):
         N = int(rng.integers(1, 40))
@@ -808,13 +808,47 @@ def test_tree_values_are_path_products():
         c = rng.random(N).astype(np.float32)
         val = verify.tree_values(par, c)
         for n in range(N):
-            path, a = [], n
+            path, a = Fraction(1), n
             while a != -1:
-                path.append(float(c[a]))
+                path *= Fraction(float(c[a]))
                 a = int(par[a])
-            assert abs(float(val[n]) - math.prod(path)) <= 1e-6 * max(math.prod(path), 1e-30)
+            num, exp = val[n]
+            assert Fraction(num) * Fraction(2) ** exp == path  # exact, no rounding
+            assert verify.value_float(val[n]) == float(path)
             if n:  # value(child) <= value(parent)
-                assert val[n] <= val[par[n]]
+                pn, pe = val[int(par[n])]
+                assert Fraction(num) * Fraction(2) ** exp <= Fraction(pn) * Fraction(2) ** pe
+
+
+def test_rerank_ranks_exact_products_not_rounded_ones():
+    # Two nodes whose float32 path products are equal but whose exact products
+    # differ: a deep node a * b just above a shallow node d = fl32(a * b).
+    # Rounded products would tie and hand the place to the shallower node; the
+    # page's value (the exact product) puts the deeper one first.
+    a = np.float32(1 - 3 * 2.0 ** -24)
+    exact = float(a) * float(a)
+    d = np.float32(exact)
+    assert float(d) < exact and np.float32(a * a) == d
+    par = np.array([-1, 0, 1, 0], np.int32)       # 0 -> 1 -> 2 and 0 -> 3
+    c = np.array([1.0, a, a, d], np.float32)      # values 1, a, a*a, d
+    nodes, _, vals, _ = verify.tree_rerank(par, c, 3)
+    assert nodes == [0, 1, 2] and vals[2] == exact
+    # with the products exactly equal the shallower node wins the tie
+    c = np.array([1.0, 0.5, 0.5, 0.25], np.float32)
+    assert verify.tree_rerank(par, c, 3)[0] == [0, 1, 3]
+
+
+def test_tree_values_do_not_underflow():
+    # A chain of 400 nodes of confidence 0.5: the deepest value is 2^-399,
+    # below every float32 and float64 normal, yet still ordered exactly.
+    N = 400
+    par = np.arange(-1, N - 1, dtype=np.int32)
+    c = np.full(N, 0.5, np.float32)
+    c[0] = 1.0
+    val = verify.tree_values(par, c)
+    assert val[N - 1] == (1, -(N - 1))
+    order, _, _ = verify.rerank_order(par, c)
+    assert order == list(range(N))
 
 
 def test_rerank_is_connected_and_top_m():
@@ -834,10 +868,10 @@ def test_rerank_is_connected_and_top_m():
             for i, n in enumerate(nodes):  # the re-indexed parents match
                 assert newp[i] == (-1 if n == 0 else nodes.index(int(par[n])))
             # no unchosen node beats a chosen one
-            val = verify.tree_values(par, c)
+            key = verify.value_keys(verify.tree_values(par, c))
             if len(nodes) < N:
-                worst = min(val[list(chosen)])
-                assert all(val[n] <= worst for n in range(N) if n not in chosen)
+                worst = min(key[n] for n in chosen)
+                assert all(key[n] <= worst for n in range(N) if n not in chosen)
 
 
 def test_rerank_page_properties_by_hand():
