@@ -169,10 +169,13 @@ spec_status spec_verify_chain(
  *   > SPEC_STATIC_SCRATCH_BYTES return SPEC_ERR_UNSUPPORTED before any CUDA
  *   call; use spec_verify_chain there.  For V = 128256 bf16 and gamma = 7,
  *   B = 512 fits (8.6 MiB) and B = 1024 does not (17.1 MiB).
- * First call on each device (with that device current): looks the array's
- *   address up once with cudaGetSymbolAddress, which may load this library's
- *   device code for that device; a failure returns SPEC_ERR_CUDA.  Make that
- *   first call outside any stream capture.
+ * Address: every call looks the array's address up with cudaGetSymbolAddress
+ *   in the device context current on the calling thread, so a call made after
+ *   a device reset works in the new context.  The first call on each device
+ *   may load this library's device code for that device: make it outside any
+ *   stream capture.  A failed lookup returns SPEC_ERR_CUDA.
+ * Errors: the arguments are checked exactly as spec_verify_chain checks them
+ *   (SPEC_ERR_INVALID_ARG) before the size limit below is applied.
  * Zero state: none is needed; like spec_verify_chain, every call clears the
  *   counters and task queue it uses (one cudaMemsetAsync on `stream`).
  * Concurrency: all calls on one device share the one array, so calls whose

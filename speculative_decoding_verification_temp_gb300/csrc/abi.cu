@@ -1,6 +1,7 @@
 // C ABI of libspecverify: argument checks, workspace layout, launch planning.
 // The operations themselves are documented in include/specverify.h.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -329,9 +330,12 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.wq = reinterpret_cast<int4 *>(ws + L.wq);
     P.wq_ctr = reinterpret_cast<uint32_t *>(ws + L.wq_ctr);
     P.wq_cap = static_cast<int>(L.wq_cap);
-    static uint32_t epoch = 0;  // tags this call's queue entries (stale ones never match)
-    epoch = epoch + 1 == 0 ? 1 : epoch + 1;
-    P.epoch = epoch;
+    // tags this call's queue entries (stale ones never match); one counter for
+    // all host threads, never 0
+    static std::atomic<uint32_t> epoch{0};
+    uint32_t ep = epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    if (ep == 0u) ep = epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    P.epoch = ep;
     if (P.mode == sv::kModeTree) {
       int32_t *fc = reinterpret_cast<int32_t *>(ws + L.first_child);
       e = sv::launch_first_child(P.parent, P.nseq, P.ups, fc, stream);
@@ -360,6 +364,28 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
 }
 
 }  // namespace
+
+namespace sv {
+
+// Host-side argument checks of a chain verification call (everything except
+// the workspace), shared by spec_verify_chain and spec_verify_chain_static.
+// SPEC_OK with B == 0 means there is nothing to do.
+spec_status check_chain_args(const void *target_logits, int64_t ld_target,
+                             const void *draft_logits, int64_t ld_draft, spec_dtype dtype, int B,
+                             int gamma, int V, const int32_t *draft_tokens,
+                             spec_policy target_policy, spec_policy draft_policy,
+                             const int32_t *out_num_accepted, const int32_t *out_tokens) {
+  const int esize = esize_of(dtype);
+  if (esize == 0 || B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || ld_target < V || !target_policy.temperature ||
+      !draft_policy.temperature || !out_num_accepted || !out_tokens)
+    return SPEC_ERR_INVALID_ARG;
+  if (gamma > 0 && (!draft_logits || ld_draft < V || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+}  // namespace sv
 
 extern "C" {
 
@@ -394,13 +420,12 @@ spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,
                               const float *uniform_override, int32_t *out_num_accepted,
                               int32_t *out_tokens, uint32_t *out_flags, float *out_residual,
                               void *workspace, size_t workspace_bytes, spec_stream_t stream) {
+  const spec_status chk = sv::check_chain_args(target_logits, ld_target, draft_logits, ld_draft,
+                                               dtype, B, gamma, V, draft_tokens, target_policy,
+                                               draft_policy, out_num_accepted, out_tokens);
+  if (chk != SPEC_OK || B == 0) return chk;
+  if (!workspace) return SPEC_ERR_INVALID_ARG;
   const int esize = esize_of(dtype);
-  if (esize == 0 || B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1) return SPEC_ERR_INVALID_ARG;
-  if (B == 0) return SPEC_OK;
-  if (!target_logits || ld_target < V || !target_policy.temperature ||
-      !draft_policy.temperature || !out_num_accepted || !out_tokens || !workspace)
-    return SPEC_ERR_INVALID_ARG;
-  if (gamma > 0 && (!draft_logits || ld_draft < V || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
   sv::Params P = {};
   P.target = target_logits;
   P.ld_t = ld_target;

@@ -113,6 +113,16 @@ def test_static_chain_refuses_before_any_cuda_call(lib):
     assert lib.spec_verify_chain_static(*empty) == _abi.SPEC_OK
     neg = (FAKE, 10, FAKE, 10, 1, -1, 7, 10, FAKE, pol, pol, 1, None, FAKE, FAKE, None, None, None)
     assert lib.spec_verify_chain_static(*neg) == _abi.SPEC_ERR_INVALID_ARG
+    # the argument checks of spec_verify_chain come before the size limit
+    INV = _abi.SPEC_ERR_INVALID_ARG
+    for B, gamma, V, dtype in ((1024, 7, 0, 1), (1024, 4096, 128256, 1), (4, 7, 128256, 7),
+                               (4, -1, 128256, 1)):
+        a = (FAKE, max(V, 1), FAKE, max(V, 1), dtype, B, gamma, V, FAKE, pol, pol, 1, None,
+             FAKE, FAKE, None, None, None)
+        assert lib.spec_verify_chain_static(*a) == INV, (B, gamma, V, dtype)
+    missing = (FAKE, 128256, FAKE, 128256, 1, 4, 7, 128256, None, pol, pol, 1, None,
+               FAKE, FAKE, None, None, None)
+    assert lib.spec_verify_chain_static(*missing) == INV  # no draft tokens
 
 
 def test_static_scratch_size_matches_header():
