@@ -40,20 +40,37 @@ _WORKSPACES = {}
 
 
 def workspace(device, nbytes):
-    """A device workspace of at least nbytes, cached per device.
+    """A device workspace of at least nbytes, cached per (device, stream).
 
     The library needs no initialised workspace: every call first clears the
     part it relies on, so the cached buffer serves successive calls on one
-    stream.  Calls that run concurrently on different streams need workspaces
-    of their own.
+    stream.  Calls on different streams may run concurrently on the GPU, so
+    each stream gets a buffer of its own (allocated on that stream).
     """
     dev = torch.device(device)
-    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    index = dev.index if dev.index is not None else torch.cuda.current_device()
+    stream = torch.cuda.current_stream(index)
+    key = (index, stream.cuda_stream)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=torch.device("cuda", index))
         _WORKSPACES[key] = ws
     return ws
+
+
+def _top_k(x, n, V, name, device):
+    """A per-sequence top-k argument as a device array, or None when no row
+    filters.  A host value (scalar, list, numpy array, CPU tensor) whose
+    entries are all off (k <= 0 or k >= V) becomes None, so that it does not
+    send the call down the top-k path; a CUDA tensor is passed as given."""
+    if x is None:
+        return None
+    if not (isinstance(x, torch.Tensor) and x.is_cuda):
+        k = torch.as_tensor(x).to(torch.int64).flatten()
+        if not bool(((k > 0) & (k < V)).any()):
+            return None
+    return _vec(x, n, torch.int32, name, device)
 
 
 def _rows(x, name):
@@ -120,8 +137,8 @@ def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
         dl, ld_d, toks = None, 0, None
     tp = _vec(target_temperature, B, torch.float32, "target_temperature", dev)
     tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
-    kp = None if target_top_k is None else _vec(target_top_k, B, torch.int32, "target_top_k", dev)
-    kq = None if draft_top_k is None else _vec(draft_top_k, B, torch.int32, "draft_top_k", dev)
+    kp = _top_k(target_top_k, B, V, "target_top_k", dev)
+    kq = _top_k(draft_top_k, B, V, "draft_top_k", dev)
     uov = None
     if uniform_override is not None:
         uov = _vec(uniform_override, B * G1 * 2, torch.float32, "uniform_override", dev)
@@ -166,8 +183,8 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
     par = _vec(parent, T * N, torch.int32, "parent", dev)
     tp = _vec(target_temperature, T, torch.float32, "target_temperature", dev)
     tq = _vec(draft_temperature, T, torch.float32, "draft_temperature", dev)
-    kp = None if target_top_k is None else _vec(target_top_k, T, torch.int32, "target_top_k", dev)
-    kq = None if draft_top_k is None else _vec(draft_top_k, T, torch.int32, "draft_top_k", dev)
+    kp = _top_k(target_top_k, T, V, "target_top_k", dev)
+    kq = _top_k(draft_top_k, T, V, "draft_top_k", dev)
     uov = None
     if uniform_override is not None:
         uov = _vec(uniform_override, T * N * 2, torch.float32, "uniform_override", dev)
@@ -218,8 +235,8 @@ def verify_chain_static(target_logits, draft_logits, draft_tokens, target_temper
         dl, ld_d, toks = None, 0, None
     tp = _vec(target_temperature, B, torch.float32, "target_temperature", dev)
     tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
-    kp = None if target_top_k is None else _vec(target_top_k, B, torch.int32, "target_top_k", dev)
-    kq = None if draft_top_k is None else _vec(draft_top_k, B, torch.int32, "draft_top_k", dev)
+    kp = _top_k(target_top_k, B, V, "target_top_k", dev)
+    kq = _top_k(draft_top_k, B, V, "draft_top_k", dev)
     uov = None
     if uniform_override is not None:
         uov = _vec(uniform_override, B * G1 * 2, torch.float32, "uniform_override", dev)

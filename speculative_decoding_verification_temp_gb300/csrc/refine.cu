@@ -26,6 +26,8 @@
 //      the owning warp, which scans its range with a warp prefix sum.
 // A draw from p itself needs only B and C.  Rows are read from global memory
 // in groups of 8 entries (16-byte loads when the rows are aligned).
+#include <mutex>
+
 #include "ops.cuh"
 #include "precise_row.cuh"
 
@@ -498,10 +500,12 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(const Params P, const 
 
 template <typename TE>
 cudaError_t launch_refine_t(const Params &P, const Exp2Table &tab, cudaStream_t stream) {
+  static std::mutex mu;  // guards the cache below across host threads
   static int cached_dev = -1, cached_blocks = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  std::unique_lock<std::mutex> lock(mu);
   if (dev != cached_dev) {
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, refine_kernel<TE>, kThreads, 0);
@@ -512,9 +516,11 @@ cudaError_t launch_refine_t(const Params &P, const Exp2Table &tab, cudaStream_t 
     cached_blocks = min(kRefineMaxGrid, min(per_sm, 2) * sms);
     cached_dev = dev;
   }
+  const int blocks = cached_blocks;
+  lock.unlock();
   void *args[] = {const_cast<Params *>(&P), const_cast<Exp2Table *>(&tab)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(refine_kernel<TE>),
-                                     dim3(cached_blocks), dim3(kThreads), args, 0, stream);
+                                     dim3(blocks), dim3(kThreads), args, 0, stream);
 }
 
 cudaError_t launch_refine(const Params &P, int esize, const Exp2Table &tab, cudaStream_t stream) {

@@ -43,6 +43,8 @@
 // rounding in the product), in the records, the merge, the acceptance test
 // and the draw alike, so the normalisers and the draw weights share their
 // scale.
+#include <mutex>
+
 #include "ops.cuh"
 #include "precise_row.cuh"
 
@@ -1905,10 +1907,14 @@ void set_job_split(Params &P, int G) {
 
 template <typename TE>
 cudaError_t launch_pass_t(Params P, const Exp2Table &tab, size_t smem, cudaStream_t stream) {
+  // occupancy of the last (device, shared memory) pair, shared by every host
+  // thread that launches this instantiation: read and written under the lock
+  static std::mutex mu;
   static int cached_dev = -1, cached_smem = -1, cached_blocks = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  std::unique_lock<std::mutex> lock(mu);
   if (dev != cached_dev || static_cast<int>(smem) != cached_smem) {
     e = cudaFuncSetAttribute(pass_kernel<TE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
@@ -1923,10 +1929,12 @@ cudaError_t launch_pass_t(Params P, const Exp2Table &tab, size_t smem, cudaStrea
     cached_dev = dev;
     cached_smem = static_cast<int>(smem);
   }
-  set_job_split(P, cached_blocks);
+  const int blocks = cached_blocks;
+  lock.unlock();
+  set_job_split(P, blocks);
   void *args[] = {&P, const_cast<Exp2Table *>(&tab)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(pass_kernel<TE>),
-                                     dim3(cached_blocks), dim3(kPThreads), args, smem, stream);
+                                     dim3(blocks), dim3(kPThreads), args, smem, stream);
 }
 
 cudaError_t launch_pass(const Params &P, int esize, const Exp2Table &tab, size_t smem,

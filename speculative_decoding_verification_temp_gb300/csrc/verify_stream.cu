@@ -27,6 +27,8 @@
 // bounded polling of the queue once their stats tasks are done, which is why
 // the grid is launched cooperatively (all CTAs resident).  A second small
 // kernel stitches each sequence's path.
+#include <mutex>
+
 #include "ops.cuh"
 
 namespace sv {
@@ -1035,10 +1037,12 @@ cudaError_t launch_stream_t(const Params &P, size_t smem, cudaStream_t stream) {
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // resident CTAs per SM for this footprint (cached per shared-memory size)
+  static std::mutex mu;  // guards the cache below across host threads
   static int cache_key[16][2];
   static int cache_val[16];
   static int cache_n = 0;
   int per_sm = 0;
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < cache_n; ++i)
     if (cache_key[i][0] == static_cast<int>(smem) && cache_key[i][1] == static_cast<int>(sizeof(TE)))
       per_sm = cache_val[i];

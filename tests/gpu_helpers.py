@@ -20,12 +20,16 @@ RESID_TOL = {"f32": 1e-5, "bf16": 2e-3}
 
 def top_k_arg(k, V, force_resident):
     """The top-k argument of a call: None when no row filters (every k <= 0 or
-    >= V), which lets the library take its streaming kernel; the array itself
-    when force_resident (any top-k array selects the resident kernel)."""
+    >= V), which lets the library take its streaming kernels; the array itself
+    otherwise.  force_resident passes it as a CUDA tensor even when every row
+    is off: the binding forwards a device array as given, and any top-k array
+    selects the resident kernel."""
     if k is None:
         return None
     k = np.asarray(k)
-    if force_resident or np.any((k > 0) & (k < V)):
+    if force_resident:
+        return torch.from_numpy(np.ascontiguousarray(k, dtype=np.int32)).cuda()
+    if np.any((k > 0) & (k < V)):
         return k
     return None
 
