@@ -270,6 +270,23 @@ spec_status spec_overlap(
 /* Static description of a status code. */
 const char *spec_status_string(spec_status status);
 
+/* Profiling hook (the pages have no counterpart; it exists so that a benchmark
+ * can time the dominant kernel of a chain verification live, on the stream the
+ * kernel runs on).
+ *
+ * start_event, stop_event: cudaEvent_t handles (as void *) created by the
+ *   caller, or both NULL to switch the hook off.  While set, every
+ *   spec_verify_chain / spec_verify_chain_static call that takes the streaming
+ *   path (16-byte aligned rows, no top-k, gamma <= 31) records start_event
+ *   immediately before and stop_event immediately after its rows kernel (the
+ *   pass that reads every logit row once) on the call's stream.  Other calls
+ *   record nothing.
+ * The setting is process-wide, not per thread; the library does not own or
+ * destroy the events.  Returns SPEC_ERR_INVALID_ARG when exactly one of the
+ * two is NULL (the previous setting is kept), SPEC_OK otherwise.
+ */
+spec_status spec_set_profile_events(void *start_event, void *stop_event);
+
 /* Bytes of workspace spec_typical_accept needs: 8 per target row,
  * B * (gamma + 1) rows (0 for a negative size). */
 size_t spec_typical_workspace_size(int B, int gamma);

@@ -39,6 +39,7 @@ EXPORTS = (
     "spec_typical_accept",
     "spec_tree_rerank",
     "spec_status_string",
+    "spec_set_profile_events",
 )
 
 
@@ -100,6 +101,8 @@ def load():
     lib.spec_tree_rerank.restype = _i
     lib.spec_status_string.argtypes = [_i]
     lib.spec_status_string.restype = ctypes.c_char_p
+    lib.spec_set_profile_events.argtypes = [_p, _p]
+    lib.spec_set_profile_events.restype = _i
     _lib = lib
     return lib
 

@@ -19,7 +19,7 @@ LIB_NAME = "libspecverify.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["abi.cu", "verify_units.cu", "verify_stream.cu", "tree_mask.cu", "static_scratch.cu",
-           "refine.cu", "verify_pass.cu", "overlap.cu", "typical.cu", "tree_rerank.cu"]
+           "refine.cu", "chain_rows.cu", "verify_chain.cu", "overlap.cu", "typical.cu", "tree_rerank.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

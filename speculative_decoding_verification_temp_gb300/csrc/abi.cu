@@ -31,9 +31,11 @@ cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B,
                            const float *Tp, const int32_t *tokens, float epsilon, float delta,
                            int32_t *out_num, int32_t *out_tokens, uint32_t *out_flags,
                            void *workspace, cudaStream_t stream);
-cudaError_t launch_pass(const Params &P, int esize, const Exp2Table &tab, size_t smem,
-                        cudaStream_t stream);
-size_t pass_ctl_bytes();
+cudaError_t launch_chain(const Params &P, int esize, const Exp2Table &tab, size_t smem,
+                         cudaStream_t stream);
+size_t chain_rows_ctl_bytes();
+int chain_records_per_chunk();
+bool set_profile_events(void *start, void *stop);
 }  // namespace sv
 
 namespace {
@@ -110,17 +112,16 @@ bool make_stream_plan(long long V, int esize, StreamPlan &sp) {
 // (arrival counters, the weight-task queue and its counters) come first and
 // are cleared by every call; everything after them is written before it is
 // read within a call.
-// Chain pass kernel (sequence-level decide): 32 KB chunks through a ring of
-// three slots (two CTAs per SM); every row's chunks leave one record per
-// consumer warp.
+// Chain path (rows -> decide -> weights -> search -> precise kernels): 32 KB
+// chunks through a ring of two slots (three rows-kernel CTAs per SM); every
+// row's chunks leave one record per consumer warp; the draw search works in
+// 256-entry steps.
 struct PassPlan {
   int chunk_elems;
   int cpr;
   int steps;
   int ring;
   int slot_bytes;
-  size_t data_off;
-  size_t smem;
 };
 
 constexpr int kPassMaxGamma = 31;
@@ -128,32 +129,36 @@ constexpr int kPassMaxGamma = 31;
 bool make_pass_plan(long long V, int esize, int gamma, PassPlan &pp) {
   if (gamma > kPassMaxGamma || esize <= 0) return false;
   pp.slot_bytes = 32 * 1024;
-  pp.ring = 3;
+  pp.ring = 2;  // three CTAs of the rows kernel per SM
   pp.chunk_elems = pp.slot_bytes / esize;
   pp.cpr = static_cast<int>((V + pp.chunk_elems - 1) / pp.chunk_elems);
   pp.steps = static_cast<int>((V + 255) / 256);
-  pp.data_off = align_up(sv::pass_ctl_bytes(), 128);
-  pp.smem = pp.data_off + static_cast<size_t>(pp.ring) * pp.slot_bytes +
-            align_up(static_cast<size_t>(pp.steps) * sizeof(float), 16);
-  return pp.smem <= kSmemHard;
+  return true;
 }
 
-// Draw-search steps per row of the pass kernel (0: it cannot run the shape).
+// Draw-search steps per row of the chain path (0: it cannot run the shape).
 long long pass_steps(long long V, int esize, int gamma) {
-  PassPlan pp;
+  PassPlan pp{};
   return make_pass_plan(V, esize, gamma, pp) ? pp.steps : 0;
 }
 
-// 64-bit records the pass kernel writes for B sequences of gamma drafts.
+// 64-bit records the chain rows kernel writes for B sequences of gamma drafts
+// (one per consumer warp per chunk).
 long long pass_records(long long B, int gamma, long long V, int esize) {
-  PassPlan pp;
+  PassPlan pp{};
   if (!make_pass_plan(V, esize, gamma, pp)) return 0;
-  return B * (2 * gamma + 1) * static_cast<long long>(pp.cpr) * 8;
+  return B * (2 * gamma + 1) * static_cast<long long>(pp.cpr) * sv::chain_records_per_chunk();
+}
+
+// Rows of the chain path (2 gamma + 1 per sequence; 0 when it cannot run).
+long long chain_rows(long long B, int gamma, long long V, int esize) {
+  PassPlan pp{};
+  if (!make_pass_plan(V, esize, gamma, pp)) return 0;
+  return B * (2 * gamma + 1);
 }
 
 struct Layout {
-  size_t wq_ctr, counters, unit_done, w_done, wq, seq_cnt, srec, err, sctr, near_list, pctr,
-      zero_bytes;
+  size_t wq_ctr, counters, unit_done, w_done, wq, srec, err, sctr, near_list, pctr, zero_bytes;
   size_t pseq, fstep, pstep, ppart;
   size_t outs, stats, final_unit, first_child, refine, rpart, rc, partials, dstate, wpart, wblk, total;
   long long wq_cap;
@@ -162,9 +167,10 @@ struct Layout {
 constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
 // slices: slices per unit of the streaming kernel, 0 when only the resident
-// kernel can run the shape; recs: records of the chain pass kernel; psteps:
-// its draw-search steps per row (0 when the pass kernel cannot run the shape).
-Layout layout(long long nseq, long long units, long long slices, long long recs,
+// kernel can run the shape; recs, rows: records and rows of the chain path;
+// psteps: its draw-search steps per row (0 when the chain path cannot run the
+// shape).
+Layout layout(long long nseq, long long units, long long slices, long long recs, long long rows,
               long long psteps) {
   const long long pseqs = psteps ? nseq : 0;
   Layout L;
@@ -174,7 +180,7 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
     off = align_up(off + bytes, 256);
     return at;
   };
-  // A call runs either the streaming kernel or the pass kernel (or neither):
+  // A call runs either the streaming kernel or the chain path (or neither):
   // their own regions share addresses, the workspace holds the larger set.
   // zero prefix, common part
   // [0] queue head, [1] tail, [2] units done, [3] refines, [4] redraw barrier
@@ -191,14 +197,9 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
   L.wq_cap = 3 * units * slices;
   L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
   const size_t zero_stream = off;
-  // zero prefix, pass kernel
+  // zero prefix, chain path: the arrival counters
   off = zero_base;
-  L.seq_cnt = take(static_cast<size_t>(recs ? nseq : 0) * sizeof(uint32_t));
-  L.srec = take(static_cast<size_t>(recs) * sizeof(unsigned long long));  // zero = not written
   L.sctr = take(static_cast<size_t>(pseqs) * 4 * sizeof(uint32_t));
-  L.near_list = take(static_cast<size_t>(pseqs) * sizeof(int32_t));
-  L.pseq = take(static_cast<size_t>(pseqs) * (sizeof(sv::PassSeq) / 4) * 8);
-  L.fstep = take(static_cast<size_t>(pseqs * psteps) * 8);
   L.pctr = take(4 * sizeof(uint32_t));
   off = std::max(off, zero_stream);
   L.zero_bytes = off;
@@ -218,10 +219,15 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
   L.wpart = take(static_cast<size_t>(units * slices) * sizeof(float));
   L.wblk = take(static_cast<size_t>(units * slices * kMaxSliceBlocks) * sizeof(float));
   const size_t end_stream = off;
-  // pass kernel
+  // chain path: written before they are read within a call (the records by
+  // the rows kernel, read by the decide kernel after it)
   off = base;
-  L.pstep = take(static_cast<size_t>(pseqs * psteps) * 2 * sizeof(double));
-  L.ppart = take(static_cast<size_t>(pseqs) * sv::kPassPreciseJobs * 2 * sizeof(double));
+  L.srec = take(static_cast<size_t>(recs) * sizeof(unsigned long long));
+  L.pseq = take(static_cast<size_t>(pseqs) * sizeof(sv::PassSeq));
+  L.near_list = take(static_cast<size_t>(pseqs) * sizeof(int32_t));
+  L.fstep = take(static_cast<size_t>(pseqs * psteps) * sizeof(float));
+  L.pstep = take(static_cast<size_t>(pseqs * psteps) * 2 * sizeof(float2));
+  L.ppart = take(static_cast<size_t>(pseqs) * sv::kPassPreciseJobs * 2 * sizeof(float2));
   L.total = std::max(off, end_stream);
   return L;
 }
@@ -263,7 +269,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   const bool vec = aligned16(P.target) && (P.ld_t * esize) % 16 == 0 &&
                    (!need_draft_rows || (aligned16(P.draft) && (P.ld_d * esize) % 16 == 0));
   StreamPlan sp;
-  PassPlan pp;
+  PassPlan pp{};
   Plan pl;
   const bool pass = vec && !topk && P.mode == sv::kModeChain &&
                     make_pass_plan(P.V, esize, P.gamma, pp) &&
@@ -272,14 +278,18 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   if (!pass && !streaming && !make_plan(P.V, esize, extra, topk, pl))
     return SPEC_ERR_UNSUPPORTED;
   // the caller's workspace must hold what the size query promised for the shape
+  const bool chain = P.mode == sv::kModeChain;
   const size_t promised =
       layout(P.nseq, n_units, stream_slices(P.V, esize),
-             P.mode == sv::kModeChain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0,
-             P.mode == sv::kModeChain ? pass_steps(P.V, esize, P.gamma) : 0)
+             chain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0,
+             chain ? chain_rows(P.nseq, P.gamma, P.V, esize) : 0,
+             chain ? pass_steps(P.V, esize, P.gamma) : 0)
           .total;
   if (workspace_bytes < promised) return SPEC_ERR_INVALID_ARG;
-  const long long recs = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr * 8 : 0;
-  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs, pass ? pp.steps : 0);
+  const long long rows = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) : 0;
+  const long long recs = rows * pp.cpr * sv::chain_records_per_chunk();
+  const Layout L =
+      layout(P.nseq, n_units, streaming ? sp.slices : 0, recs, rows, pass ? pp.steps : 0);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
   cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, stream);
@@ -298,12 +308,10 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   if (pass) {
     P.ring = pp.ring;
     P.slot_bytes = pp.slot_bytes;
-    P.data_off = static_cast<int>(pp.data_off);
     P.chunk_elems = pp.chunk_elems;
     P.cpr = pp.cpr;
     P.steps = pp.steps;
     P.srec = reinterpret_cast<unsigned long long *>(ws + L.srec);
-    P.seq_cnt = reinterpret_cast<uint32_t *>(ws + L.seq_cnt);
     P.pseqw = reinterpret_cast<unsigned long long *>(ws + L.pseq);
     P.sctr = reinterpret_cast<uint32_t *>(ws + L.sctr);
     P.fstep = reinterpret_cast<unsigned long long *>(ws + L.fstep);
@@ -311,7 +319,11 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.ppart = reinterpret_cast<double *>(ws + L.ppart);
     P.near_list = reinterpret_cast<int32_t *>(ws + L.near_list);
     P.pctr = reinterpret_cast<uint32_t *>(ws + L.pctr);
-    e = sv::launch_pass(P, esize, exp2_table(), pp.smem, stream);
+    // rows kernel: its control block, then the ring of chunk slots
+    const size_t rows_off = align_up(sv::chain_rows_ctl_bytes(), 128);
+    P.data_off = static_cast<int>(rows_off);
+    e = sv::launch_chain(P, esize, exp2_table(), rows_off + static_cast<size_t>(pp.ring) * pp.slot_bytes,
+                         stream);
   } else if (streaming) {
     P.slice = sp.slice;
     P.cluster = sp.slices;
@@ -389,6 +401,10 @@ spec_status check_chain_args(const void *target_logits, int64_t ld_target,
 
 extern "C" {
 
+spec_status spec_set_profile_events(void *start_event, void *stop_event) {
+  return sv::set_profile_events(start_event, stop_event) ? SPEC_OK : SPEC_ERR_INVALID_ARG;
+}
+
 const char *spec_status_string(spec_status status) {
   switch (status) {
     case SPEC_OK: return "SPEC_OK";
@@ -403,14 +419,15 @@ size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtyp
   const int esize = esize_of(dtype);
   if (B < 0 || gamma < 0 || V < 1 || esize == 0) return 0;
   return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize),
-                pass_records(B, gamma, V, esize), pass_steps(V, esize, gamma))
+                pass_records(B, gamma, V, esize), chain_rows(B, gamma, V, esize),
+                pass_steps(V, esize, gamma))
       .total;
 }
 
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
-  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0, 0).total;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0, 0, 0).total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

@@ -1,0 +1,465 @@
+// The rows kernel of the chain path: the pass that reads every logit row of
+// the batch from HBM exactly once (see verify_chain.cu for the whole path).
+//
+// Every logit row of the batch - the gamma + 1 target rows and the gamma draft
+// rows of each sequence - is cut into 32 KB chunks, numbered sequence-major and
+// handed out round-robin over a persistent grid (three CTAs per SM).  In each
+// CTA one producer warp streams its chunks into a ring of two shared-memory
+// slots with bulk asynchronous copies (cp.async.bulk, one "full" and one
+// "empty" mbarrier per slot); eight consumer warps reduce each chunk to one
+// 64-bit record per warp: the (max, sum of 2^((z - max) k)) of a sampling row,
+// k = log2(e) / T, or the (finite max, lowest index + 1) of a greedy row.  Each
+// logit costs one exponential; nothing else happens on this path (no atomics,
+// no cross-CTA waits).  Every mbarrier wait is bounded (about two seconds) and
+// sets the error word, which turns into SPEC_FLAG_TIMEOUT.
+#include <mutex>
+
+#include "ops.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kRConsumerWarps = kChainRecordsPerChunk;
+constexpr int kRProducerWarp = kRConsumerWarps;
+constexpr int kRThreads = (kRConsumerWarps + 1) * 32;  // 288
+constexpr int kRMaxRing = 8;
+constexpr uint32_t kNoIndex = 0x3FFFFFFFu;  // record index: no finite entry
+constexpr uint32_t kBadBit = 0x80000000u;   // record index bit: NaN or +inf seen
+static_assert(kRConsumerWarps == 8, "the fast record paths cover 32 KB chunks with 8 warps");
+
+__device__ __forceinline__ void mbar_arrive1_c(unsigned long long *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// What the producer tells the consumers about the chunk in a slot.
+struct SlotInfo {
+  const void *gl;  // the chunk in global memory
+  long long rec;   // index of the chunk's first record
+  int n;           // entries
+  int nb;          // entries copied to shared memory
+  float k;         // log2(e) / T, 0 for a greedy row
+  int arg;         // greedy row: argmax record
+  int v0;          // vocabulary index of the chunk's first entry
+  int pad;
+};
+
+struct RowsCtl {
+  unsigned long long full[kRMaxRing];
+  unsigned long long empty[kRMaxRing];
+  SlotInfo info[kRMaxRing];
+};
+
+// Where work item k (a chunk) lives.
+struct ChunkInfo {
+  int seq, r, c, n;  // sequence, row within the sequence, chunk, entries
+  long long row;     // global row of its tensor
+  bool draft;
+};
+
+__device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
+  ChunkInfo ci;
+  const int rps = 2 * P.gamma + 1;
+  const int per_seq = rps * P.cpr;
+  const int k32 = static_cast<int>(k);  // the host keeps the chunk count below 2^31
+  ci.seq = k32 / per_seq;
+  const int rem = k32 - ci.seq * per_seq;
+  ci.r = rem / P.cpr;
+  ci.c = rem - ci.r * P.cpr;
+  ci.n = min(P.chunk_elems, P.V - ci.c * P.chunk_elems);
+  ci.draft = ci.r > P.gamma;
+  ci.row = ci.draft ? static_cast<long long>(ci.seq) * P.gamma + (ci.r - P.gamma - 1)
+                    : static_cast<long long>(ci.seq) * (P.gamma + 1) + ci.r;
+  return ci;
+}
+
+// Policy of a row: greedy (argmax) or sampling with k = log2(e) / T.
+__device__ __forceinline__ bool row_is_arg(float T) { return !(T > 0.f) || T == INFINITY; }
+
+template <typename TE>
+__device__ __forceinline__ void load_vec(const TE *s, float z[8]);
+template <>
+__device__ __forceinline__ void load_vec<uint16_t>(const uint16_t *s, float z[8]) {
+  const uint4 w = *reinterpret_cast<const uint4 *>(s);
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    z[2 * i] = __uint_as_float(ws[i] << 16);
+    z[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void load_vec<float>(const float *s, float z[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(s);
+  const float4 b = *reinterpret_cast<const float4 *>(s + 4);
+  z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
+  z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
+}
+
+// Warp merge of per-lane (max, sum) pairs; a NaN sum marks the record bad.
+__device__ __forceinline__ float2 warp_merge_ms(float m, float S, float k) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+    const float S2 = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+    if (S2 != S2 || S != S) {
+      S = __int_as_float(0x7FC00000);
+      m = fmaxf(m, m2);
+    } else if (m2 > -INFINITY) {
+      if (m == -INFINITY) {
+        m = m2;
+        S = S2;
+      } else {
+        const float M = fmaxf(m, m2);
+        S = S * fast_exp2(__fmul_rn(__fsub_rn(m, M), k)) +
+            S2 * fast_exp2(__fmul_rn(__fsub_rn(m2, M), k));
+        m = M;
+      }
+    }
+  }
+  return make_float2(m, S);
+}
+
+// Record of this warp's part [e0, e1) of a chunk, any layout: entries below nb
+// come from shared memory (groups of 8), the rest (fewer than 8) from global
+// memory.
+template <typename TE>
+__device__ float2 chunk_record(const TE *sm, const TE *gl, int e0, int e1, int nb, int v0,
+                               bool arg, float k) {
+  const int lane = threadIdx.x & 31;
+  if (arg) {
+    float bv = -INFINITY;
+    uint32_t bi = kNoIndex, bad = 0u;
+    for (int base = e0 + lane * 8; base < e1; base += 256) {
+      float z[8];
+      if (base + 8 <= nb) {
+        load_vec<TE>(sm + base, z);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[e] = base + e < e1 ? to_f32(gl[base + e]) : -INFINITY;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = z[e];
+        if (x != x || x == INFINITY) {
+          if (base + e < e1) bad = 1u;
+        } else if (x > bv) {
+          bv = x;
+          bi = static_cast<uint32_t>(v0 + base + e);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      const uint32_t i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+      bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
+      if (v2 > bv || (v2 == bv && i2 < bi)) {
+        bv = v2;
+        bi = i2;
+      }
+    }
+    return make_float2(bv, __uint_as_float((bi + 1u) | (bad ? kBadBit : 0u)));
+  }
+  // sampling row: one pass with a running max; the packed partial sums are
+  // rescaled (folded into S) whenever the max grows
+  float m = -INFINITY, S = 0.f;
+  bool nan = false;
+  const uint64_t k2 = pack2(k, k);
+  uint64_t acc0 = 0ull, acc1 = 0ull;
+  for (int base = e0 + lane * 8; base < e1; base += 256) {
+    float z[8];
+    if (base + 8 <= nb) {
+      load_vec<TE>(sm + base, z);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) z[e] = base + e < e1 ? to_f32(gl[base + e]) : -INFINITY;
+    }
+    const float gm = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
+                           fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
+    if (gm > m) {
+      if (m > -INFINITY) {
+        const float sc = fast_exp2(__fmul_rn(__fsub_rn(m, gm), k));
+        S = (S + hsum2(fadd2(acc0, acc1))) * sc;
+      }
+      acc0 = acc1 = 0ull;
+      m = gm;
+    }
+    if (m == -INFINITY) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) nan |= z[e] != z[e];
+      continue;
+    }
+    const uint64_t nm2 = pack2(-m, -m);
+    acc0 = fadd2(acc0, ex2_pair(fmul2(fadd2(pack2(z[0], z[1]), nm2), k2)));
+    acc1 = fadd2(acc1, ex2_pair(fmul2(fadd2(pack2(z[2], z[3]), nm2), k2)));
+    acc0 = fadd2(acc0, ex2_pair(fmul2(fadd2(pack2(z[4], z[5]), nm2), k2)));
+    acc1 = fadd2(acc1, ex2_pair(fmul2(fadd2(pack2(z[6], z[7]), nm2), k2)));
+  }
+  S += hsum2(fadd2(acc0, acc1));
+  if (nan) S = __int_as_float(0x7FC00000);  // NaN marks the record bad
+  return warp_merge_ms(m, S, k);
+}
+
+// Sampling-row record when every group of 8 entries of the warp's part is in
+// shared memory: each lane loads all of its groups; the warp takes one max
+// (lanes exchange their maxima first, so every lane's terms share the warp's
+// scale), then one sum of 2^((z - max) k) over independent packed chains.  A
+// NaN propagates into the sum and marks the record bad.
+template <typename TE>
+__device__ float2 sample_record_fast(const TE *sm, int e0, int e1, float k);
+
+template <>
+__device__ float2 sample_record_fast<uint16_t>(const uint16_t *sm, int e0, int e1, float k) {
+  const int lane = threadIdx.x & 31;
+  constexpr int G = 8;  // 2048 entries per warp
+  uint4 w[G];
+  if (e0 + G * 256 <= e1) {  // a full part: no per-group bounds
+#pragma unroll
+    for (int g = 0; g < G; ++g) w[g] = *reinterpret_cast<const uint4 *>(sm + e0 + g * 256 + lane * 8);
+  } else {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int base = e0 + g * 256 + lane * 8;
+      w[g] = base < e1 ? *reinterpret_cast<const uint4 *>(sm + base)
+                       : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+  }
+  uint32_t h[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) h[g] = bf16x2_max(bf16x2_max(w[g].x, w[g].y), bf16x2_max(w[g].z, w[g].w));
+  uint32_t hh = bf16x2_max(bf16x2_max(bf16x2_max(h[0], h[1]), bf16x2_max(h[2], h[3])),
+                           bf16x2_max(bf16x2_max(h[4], h[5]), bf16x2_max(h[6], h[7])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) hh = bf16x2_max(hh, __shfl_xor_sync(0xFFFFFFFFu, hh, off));
+  const float m = fmaxf(__uint_as_float(hh << 16), __uint_as_float(hh & 0xFFFF0000u));
+  float S = 0.f;
+  if (m == -INFINITY) {  // nothing but -inf and NaN in the whole part: look for NaN
+    bool nan = false;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint32_t ws[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        nan |= (ws[i] & 0x7FFFu) > 0x7F80u || (ws[i] & 0x7FFF0000u) > 0x7F800000u;
+    }
+    S = __any_sync(0xFFFFFFFFu, nan) ? __int_as_float(0x7FC00000) : 0.f;
+    return make_float2(m, S);
+  }
+  const uint64_t nm2 = pack2(-m, -m), k2 = pack2(k, k);
+  // eight independent chains (two per word slot, alternating groups)
+  uint64_t a[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) a[c] = 0ull;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int o = (g & 1) * 4;
+    a[o + 0] = fadd2(a[o + 0], ex2_pair(fmul2(fadd2(bf16x2_to_pair(w[g].x), nm2), k2)));
+    a[o + 1] = fadd2(a[o + 1], ex2_pair(fmul2(fadd2(bf16x2_to_pair(w[g].y), nm2), k2)));
+    a[o + 2] = fadd2(a[o + 2], ex2_pair(fmul2(fadd2(bf16x2_to_pair(w[g].z), nm2), k2)));
+    a[o + 3] = fadd2(a[o + 3], ex2_pair(fmul2(fadd2(bf16x2_to_pair(w[g].w), nm2), k2)));
+  }
+  S = hsum2(fadd2(fadd2(fadd2(a[0], a[1]), fadd2(a[2], a[3])),
+                  fadd2(fadd2(a[4], a[5]), fadd2(a[6], a[7]))));
+  return make_float2(m, warp_sum(S));  // every lane's terms are relative to the warp's max
+}
+
+template <>
+__device__ float2 sample_record_fast<float>(const float *sm, int e0, int e1, float k) {
+  const int lane = threadIdx.x & 31;
+  constexpr int G = 4;  // 1024 entries per warp
+  float4 a[G], b[G];
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  if (e0 + G * 256 <= e1) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      a[g] = *reinterpret_cast<const float4 *>(sm + e0 + g * 256 + lane * 8);
+      b[g] = *reinterpret_cast<const float4 *>(sm + e0 + g * 256 + lane * 8 + 4);
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int base = e0 + g * 256 + lane * 8;
+      a[g] = base < e1 ? *reinterpret_cast<const float4 *>(sm + base) : ninf;
+      b[g] = base < e1 ? *reinterpret_cast<const float4 *>(sm + base + 4) : ninf;
+    }
+  }
+  float mg[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    mg[g] = fmaxf(fmaxf(fmaxf(a[g].x, a[g].y), fmaxf(a[g].z, a[g].w)),
+                  fmaxf(fmaxf(b[g].x, b[g].y), fmaxf(b[g].z, b[g].w)));
+  float m = fmaxf(fmaxf(mg[0], mg[1]), fmaxf(mg[2], mg[3]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float S = 0.f;
+  if (m == -INFINITY) {
+    bool nan = false;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      nan |= a[g].x != a[g].x || a[g].y != a[g].y || a[g].z != a[g].z || a[g].w != a[g].w ||
+             b[g].x != b[g].x || b[g].y != b[g].y || b[g].z != b[g].z || b[g].w != b[g].w;
+    S = __any_sync(0xFFFFFFFFu, nan) ? __int_as_float(0x7FC00000) : 0.f;
+    return make_float2(m, S);
+  }
+  const uint64_t nm2 = pack2(-m, -m), k2 = pack2(k, k);
+  uint64_t s0 = 0ull, s1 = 0ull, s2 = 0ull, s3 = 0ull;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    s0 = fadd2(s0, ex2_pair(fmul2(fadd2(pack2(a[g].x, a[g].y), nm2), k2)));
+    s1 = fadd2(s1, ex2_pair(fmul2(fadd2(pack2(a[g].z, a[g].w), nm2), k2)));
+    s2 = fadd2(s2, ex2_pair(fmul2(fadd2(pack2(b[g].x, b[g].y), nm2), k2)));
+    s3 = fadd2(s3, ex2_pair(fmul2(fadd2(pack2(b[g].z, b[g].w), nm2), k2)));
+  }
+  S = hsum2(fadd2(fadd2(s0, s1), fadd2(s2, s3)));
+  return make_float2(m, warp_sum(S));
+}
+
+template <typename TE>
+__device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring,
+                              long long total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = P.ring;
+  const int EW = P.chunk_elems / kRConsumerWarps;  // entries per warp (a multiple of 256)
+  int i = 0;
+  for (long long k = blockIdx.x; k < total; k += gridDim.x, ++i) {
+    const int slot = i % NS;
+    const uint32_t phase = static_cast<uint32_t>(i / NS) & 1u;
+    if (!mbar_wait_bounded(&ctl.full[slot], phase)) {
+      if (lane == 0) atomicOr(P.err, 1u);
+      mbar_wait_bounded(&ctl.full[slot], phase);  // do not leave a copy in flight
+    }
+    const SlotInfo si = ctl.info[slot];
+    const TE *sm = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * P.slot_bytes);
+    const int e0 = min(si.n, warp * EW), e1 = min(si.n, e0 + EW);
+    const float2 rec = (!si.arg && si.nb == si.n && (si.n & 7) == 0)
+                           ? sample_record_fast<TE>(sm, e0, e1, si.k)
+                           : chunk_record<TE>(sm, static_cast<const TE *>(si.gl), e0, e1, si.nb,
+                                              si.v0, si.arg != 0, si.k);
+    if (lane == 0) {
+      const unsigned long long bits =
+          static_cast<unsigned long long>(__float_as_uint(rec.x)) |
+          (static_cast<unsigned long long>(__float_as_uint(rec.y)) << 32);
+      P.srec[si.rec + warp] = bits;  // read by the decide kernel, after this kernel
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);
+  }
+}
+
+template <typename TE>
+__device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring,
+                              long long total) {
+  const int NS = P.ring;
+  const int CE = P.chunk_elems;
+  const long long G = gridDim.x;
+  // the consumers of the id-th chunk handed its slot back
+  auto wait_done = [&](int id) {
+    const int slot = id % NS;
+    const uint32_t phase = static_cast<uint32_t>(id / NS) & 1u;
+    if (!mbar_wait_bounded(&ctl.empty[slot], phase)) atomicOr(P.err, 1u);
+  };
+  int i = 0;
+  for (long long k = blockIdx.x; k < total; k += G, ++i) {
+    const int slot = i % NS;
+    if (i >= NS) wait_done(i - NS);
+    const ChunkInfo ci = chunk_info(P, k);
+    const float T = __ldg((ci.draft ? P.Tq : P.Tp) + ci.seq);
+    const bool arg = row_is_arg(T);
+    const TE *gl = static_cast<const TE *>(row_ptr(ci.draft ? P.draft : P.target, ci.row,
+                                                   ci.draft ? P.ld_d : P.ld_t, sizeof(TE))) +
+                   static_cast<long long>(ci.c) * CE;
+    const uint32_t bytes = static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
+    SlotInfo &si = ctl.info[slot];
+    si.gl = gl;
+    si.rec = ((static_cast<long long>(ci.seq) * (2 * P.gamma + 1) + ci.r) * P.cpr + ci.c) *
+             kRConsumerWarps;
+    si.n = ci.n;
+    si.nb = static_cast<int>(bytes / sizeof(TE));
+    si.k = arg ? 0.f : kLog2e / T;
+    si.arg = arg ? 1 : 0;
+    si.v0 = ci.c * CE;
+    mbar_arrive_expect_tx(&ctl.full[slot], bytes);
+    if (bytes) bulk_g2s_plain(ring + static_cast<size_t>(slot) * P.slot_bytes, gl, bytes,
+                              &ctl.full[slot]);
+  }
+  const int issued = i;
+  for (int d = max(0, issued - NS); d < issued; ++d) wait_done(d);
+}
+
+template <typename TE>
+__global__ void __launch_bounds__(kRThreads, 3) chain_rows_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  RowsCtl &ctl = *reinterpret_cast<RowsCtl *>(smem_raw);
+  unsigned char *ring = smem_raw + P.data_off;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long total =
+      static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * static_cast<long long>(P.cpr);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.ring; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], kRConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp < kRConsumerWarps) {
+    rows_consumer<TE>(P, ctl, ring, total);
+  } else if (warp == kRProducerWarp && lane == 0) {
+    rows_producer<TE>(P, ctl, ring, total);
+  }
+  // this CTA's work is done: the next kernel in the stream may start launching
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+
+std::mutex g_occ_mu;
+int g_occ_dev = -1, g_occ_smem = -1, g_occ_blocks[2] = {0, 0};
+
+template <typename TE>
+cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
+  auto kern = chain_rows_kernel<TE>;
+  const int which = sizeof(TE) == 2 ? 0 : 1;
+  int blocks = 0;
+  {
+    // resident CTAs per SM for the last (device, shared memory) pair, shared
+    // by every host thread under the lock
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    if (dev != g_occ_dev || static_cast<int>(smem) != g_occ_smem) {
+      g_occ_blocks[0] = g_occ_blocks[1] = 0;
+      g_occ_dev = dev;
+      g_occ_smem = static_cast<int>(smem);
+    }
+    if (!g_occ_blocks[which]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRThreads, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      if (per_sm < 1) return cudaErrorInvalidConfiguration;
+      g_occ_blocks[which] = per_sm * sms;
+    }
+    blocks = g_occ_blocks[which];
+  }
+  const long long total = static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * P.cpr;
+  kern<<<static_cast<int>(total < blocks ? total : blocks), kRThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chain_rows_ctl_bytes() { return sizeof(RowsCtl); }
+int chain_records_per_chunk() { return kRConsumerWarps; }
+
+cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStream_t stream) {
+  return esize == 2 ? launch_rows_t<uint16_t>(P, smem, stream)
+                    : launch_rows_t<float>(P, smem, stream);
+}
+
+}  // namespace sv

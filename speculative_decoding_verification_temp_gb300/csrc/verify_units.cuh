@@ -80,8 +80,12 @@ constexpr float kRefineGuard = 4e-6f;
 // The precise redraw runs on at most this many CTAs.
 constexpr int kRefineMaxGrid = 1024;
 
-// Precise-redraw jobs per phase of one chain draw in the pass kernel (at most).
+// Precise-redraw jobs of one chain draw (at most).
 constexpr int kPassPreciseJobs = 64;
+
+// 64-bit records the chain rows kernel leaves per 32 KB chunk (one per
+// consumer warp).
+constexpr int kChainRecordsPerChunk = 8;
 
 // One work unit of the precise redraw (a slice of one queued draw's
 // vocabulary): its partial sums, published for the other units of the draw.

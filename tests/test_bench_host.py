@@ -45,7 +45,7 @@ def test_algorithmic_bytes_of_the_headline_workload():
 
 
 def test_committed_profiles_name_their_kernels():
-    for path, unit in ((bench.TRAFFIC_FILE, "verify_pass.cu"),
+    for path, unit in ((bench.TRAFFIC_FILE, bench.TRAFFIC_UNIT),
                        (bench.OVERLAP_TRAFFIC_FILE, "overlap.cu"),
                        (bench.TYPICAL_TRAFFIC_FILE, "typical.cu")):
         assert os.path.exists(path)
@@ -54,3 +54,13 @@ def test_committed_profiles_name_their_kernels():
             text = f.read()
         assert "- source_hash:" in text and "- dram_bytes_per_launch:" in text
         assert "--clock-control none" in text
+
+
+def test_all_core_oracle_baseline_matches_the_oracle_rows():
+    # the all-core CPU baseline: spawned processes over shared memory, the
+    # oracle's rows per second on a small chain workload
+    from speculative_decoding_verification_temp_gb300 import workloads
+    w = workloads.make_chain(3, 2, 300, dtype="f32", seed=5)
+    rate, dt, procs = bench.oracle_all_cores(w, 3)
+    assert procs == min(3, os.cpu_count() or 1)
+    assert rate > 0 and dt > 0

@@ -96,8 +96,14 @@ def test_chain_empty_batch_is_a_no_op(lib):
 
 
 def test_chain_unsupported_vocabulary(lib):
-    # a float32 row pair of 10^8 entries cannot fit one cluster's shared memory
-    assert chain(lib, V=100_000_000) == _abi.SPEC_ERR_UNSUPPORTED
+    # with top-k filtering a float32 row pair of 10^8 entries would have to fit
+    # one cluster's shared memory: refused before any launch
+    topk = _abi.spec_policy(FAKE.value, FAKE.value)
+    assert chain(lib, V=100_000_000, pol=topk) == _abi.SPEC_ERR_UNSUPPORTED
+    # without top-k the streaming chain path takes any vocabulary; this call's
+    # workspace (0 bytes) is too small for it
+    assert lib.spec_verify_chain_workspace_size(2, 3, 100_000_000, 0) > 0
+    assert chain(lib, V=100_000_000) == _abi.SPEC_ERR_INVALID_ARG
 
 
 def test_static_chain_refuses_before_any_cuda_call(lib):
