@@ -106,8 +106,12 @@ def policy_distribution(z, temperature, top_k=0):
 
 def topp_threshold(probs, top_p):
     """Smallest probability kept by top-p: the value at which the descending
-    cumulative mass first reaches top_p (None for no filter)."""
-    if top_p >= 1.0:
+    cumulative mass first reaches top_p (None for no filter).
+
+    Out-of-range readings (the pages define neither filter): top_p >= 1 or NaN
+    is no filter; top_p <= 0 keeps the most probable value (and its ties)."""
+    top_p = float(top_p)
+    if not top_p < 1.0:  # also NaN
         return None
     ordered = np.sort(np.asarray(probs, dtype=np.float64))[::-1]
     i = int(np.searchsorted(np.cumsum(ordered), top_p, side="left"))
@@ -126,10 +130,16 @@ def topp_filter(probs, top_p):
 
 
 def minp_filter(probs, min_p):
-    """Min-p filtering: keep p(x) >= min_p * max p, renormalised."""
+    """Min-p filtering: keep p(x) >= min_p * max p, renormalised.
+
+    Out-of-range readings: min_p <= 0 or NaN is no filter; min_p > 1 is taken
+    as 1 (only the most probable value and its ties are kept), so the kept
+    mass is never empty."""
     probs = np.asarray(probs, dtype=np.float64)
-    if min_p <= 0.0:
+    min_p = float(min_p)
+    if not min_p > 0.0:  # also NaN
         return probs
+    min_p = min(min_p, 1.0)
     kept = np.where(probs >= min_p * probs.max(), probs, 0.0)
     return kept / kept.sum()
 

@@ -948,6 +948,25 @@ def test_minp_hand_cases_and_composition():
     assert pol.policy_distribution_ext(z, 0.0, 0, 0.5, 0.5).onehot
 
 
+def test_topp_minp_out_of_range_readings():
+    # the pages define neither filter: NaN switches a filter off, top_p <= 0
+    # keeps the most probable value, min_p > 1 is taken as 1; the kept mass is
+    # never empty, so every result is a distribution
+    from oracle import policy as pol
+    p = np.array([0.1, 0.4, 0.4, 0.1])
+    assert np.array_equal(pol.topp_filter(p, np.nan), p)
+    assert np.array_equal(pol.minp_filter(p, np.nan), p)
+    assert np.allclose(pol.topp_filter(p, 0.0), [0, 0.5, 0.5, 0])    # ties with the top kept
+    assert np.allclose(pol.topp_filter(p, -1.0), [0, 0.5, 0.5, 0])
+    assert np.allclose(pol.minp_filter(p, 7.0), pol.minp_filter(p, 1.0))
+    assert np.allclose(pol.minp_filter(p, 7.0), [0, 0.5, 0.5, 0])
+    assert np.array_equal(pol.minp_filter(p, -0.5), p)
+    z = np.log(p)
+    for tp, mp in ((np.nan, 2.0), (-3.0, np.nan), (0.5, 1.5)):
+        d = pol.policy_distribution_ext(z, 1.0, 0, tp, mp)
+        assert np.isfinite(d.probs).all() and abs(d.probs.sum() - 1) < 1e-12
+
+
 def test_filtered_policies_keep_the_verifier_exact():
     """With the same top-p / min-p on both sides the chain still returns the
     filtered target law exactly (enumeration over uniforms, exact arithmetic)."""
