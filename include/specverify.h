@@ -95,10 +95,28 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
  *   temperature [B]: 0 -> greedy; > 0 -> softmax(z / T); NaN, < 0 or inf ->
  *                    the row is flagged SPEC_FLAG_NONFINITE.  Required.
  *   top_k [B]:       k-th largest raw logit filter; <= 0 or >= V: off.
- *                    May be NULL (no filtering). */
+ *                    May be NULL (no filtering).
+ *   top_p [B]:       nucleus filter on the distribution after temperature and
+ *                    top-k: keep the most probable values until their mass
+ *                    reaches top_p (every entry tied with the boundary value
+ *                    is kept); >= 1 or NaN: off; <= 0: the most probable
+ *                    value only.  May be NULL.
+ *   min_p [B]:       after top-p, keep p(x) >= min_p * max p; <= 0 or NaN:
+ *                    off; > 1 is taken as 1.  May be NULL.
+ *   Both sides of a verification must apply the policies they sampled with
+ *   (wineandchord.com "推测解码：接受规则、状态与收益边界", section
+ *   "与 Logit Processor 的组合" lists top-k, top-p and min-p among the
+ *   processors p and q must both reflect); each filter renormalises.  A call
+ *   with any top-k, top-p or min-p array runs on the cluster kernel that holds
+ *   each row pair in shared memory; greedy rows ignore the filters.  The
+ *   floating-point top-p boundary is decided on single-precision masses summed
+ *   exactly in fixed point, so a boundary whose cumulative mass lies within
+ *   about 1e-6 of top_p may fall on either side. */
 typedef struct {
   const float *temperature;
   const int32_t *top_k;
+  const float *top_p;
+  const float *min_p;
 } spec_policy;
 
 /* Per-sequence flag bits (uint32). */

@@ -44,7 +44,8 @@ EXPORTS = (
 
 
 class spec_policy(ctypes.Structure):
-    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p)]
+    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p),
+                ("top_p", ctypes.c_void_p), ("min_p", ctypes.c_void_p)]
 
 
 _p = ctypes.c_void_p

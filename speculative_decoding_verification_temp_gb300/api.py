@@ -93,6 +93,33 @@ def _rows(x, name):
     return x, ld
 
 
+def _filter(x, n, name, device, off):
+    """A per-sequence top-p or min-p argument as a device float array, or None
+    when no row filters: a host value whose entries are all off (off(value)
+    true) becomes None; a CUDA tensor is passed as given."""
+    if x is None:
+        return None
+    if not (isinstance(x, torch.Tensor) and x.is_cuda):
+        v = torch.as_tensor(x, dtype=torch.float64).flatten()
+        if bool(off(v).all()):
+            return None
+    return _vec(x, n, torch.float32, name, device)
+
+
+def _topp_off(v):
+    return ~(v < 1.0)  # >= 1 or NaN
+
+
+def _minp_off(v):
+    return ~(v > 0.0)  # <= 0 or NaN
+
+
+def _policy(temperature, top_k, top_p, min_p):
+    """A spec_policy over device arrays (top_k, top_p and min_p may be None)."""
+    ptr = lambda t: None if t is None else t.data_ptr()
+    return _abi.spec_policy(temperature.data_ptr(), ptr(top_k), ptr(top_p), ptr(min_p))
+
+
 def _vec(x, n, dtype, name, device):
     t = torch.as_tensor(x, device=device)
     if t.dim() == 0:
@@ -111,7 +138,8 @@ def _cuda_tensor(x, name):
 
 def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
                  draft_temperature, target_top_k=None, draft_top_k=None, seed=0,
-                 uniform_override=None, return_residual=False, workspace_tensor=None):
+                 uniform_override=None, return_residual=False, workspace_tensor=None,
+                 target_top_p=None, draft_top_p=None, target_min_p=None, draft_min_p=None):
     """Chain speculative-sampling verification on the GPU (see spec_verify_chain).
 
     target_logits [B, gamma+1, V] and draft_logits [B, gamma, V] (float32 or
@@ -139,6 +167,10 @@ def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
     tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
     kp = _top_k(target_top_k, B, V, "target_top_k", dev)
     kq = _top_k(draft_top_k, B, V, "draft_top_k", dev)
+    pp = _filter(target_top_p, B, "target_top_p", dev, _topp_off)
+    pq = _filter(draft_top_p, B, "draft_top_p", dev, _topp_off)
+    mp = _filter(target_min_p, B, "target_min_p", dev, _minp_off)
+    mq = _filter(draft_min_p, B, "draft_min_p", dev, _minp_off)
     uov = None
     if uniform_override is not None:
         uov = _vec(uniform_override, B * G1 * 2, torch.float32, "uniform_override", dev)
@@ -152,8 +184,8 @@ def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
     ws = workspace(dev, nbytes) if workspace_tensor is None else workspace_tensor
     code = lib.spec_verify_chain(
         _ptr(tl), ld_t, _ptr(dl), ld_d, dt, B, gamma, V, _ptr(toks),
-        _abi.spec_policy(tp.data_ptr(), None if kp is None else kp.data_ptr()),
-        _abi.spec_policy(tq.data_ptr(), None if kq is None else kq.data_ptr()),
+        _policy(tp, kp, pp, mp),
+        _policy(tq, kq, pq, mq),
         int(seed) & ((1 << 64) - 1), _ptr(uov), _ptr(num), _ptr(out), _ptr(flags), _ptr(resid),
         _ptr(ws), ws.numel(), _stream(dev))
     _check(code)
@@ -162,7 +194,8 @@ def verify_chain(target_logits, draft_logits, draft_tokens, target_temperature,
 
 def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
                 target_temperature, draft_temperature, target_top_k=None, draft_top_k=None,
-                seed=0, uniform_override=None, return_residual=False, workspace_tensor=None):
+                seed=0, uniform_override=None, return_residual=False, workspace_tensor=None,
+                target_top_p=None, draft_top_p=None, target_min_p=None, draft_min_p=None):
     """Tree verification by recursive rejection on the GPU (see spec_verify_tree).
 
     target_logits, draft_logits [T, N, V]; node_tokens, parent [T, N].
@@ -185,6 +218,10 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
     tq = _vec(draft_temperature, T, torch.float32, "draft_temperature", dev)
     kp = _top_k(target_top_k, T, V, "target_top_k", dev)
     kq = _top_k(draft_top_k, T, V, "draft_top_k", dev)
+    pp = _filter(target_top_p, T, "target_top_p", dev, _topp_off)
+    pq = _filter(draft_top_p, T, "draft_top_p", dev, _topp_off)
+    mp = _filter(target_min_p, T, "target_min_p", dev, _minp_off)
+    mq = _filter(draft_min_p, T, "draft_min_p", dev, _minp_off)
     uov = None
     if uniform_override is not None:
         uov = _vec(uniform_override, T * N * 2, torch.float32, "uniform_override", dev)
@@ -200,8 +237,8 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
     ws = workspace(dev, nbytes) if workspace_tensor is None else workspace_tensor
     code = lib.spec_verify_tree(
         _ptr(tl), ld_t, _ptr(dl), ld_d, dt, T, N, V, int(max_depth), _ptr(toks), _ptr(par),
-        _abi.spec_policy(tp.data_ptr(), None if kp is None else kp.data_ptr()),
-        _abi.spec_policy(tq.data_ptr(), None if kq is None else kq.data_ptr()),
+        _policy(tp, kp, pp, mp),
+        _policy(tq, kq, pq, mq),
         int(seed) & ((1 << 64) - 1), _ptr(uov), _ptr(num), _ptr(path), _ptr(out), _ptr(flags),
         _ptr(resid), _ptr(ws), ws.numel(), _stream(dev))
     _check(code)
@@ -210,7 +247,8 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, max_depth,
 
 def verify_chain_static(target_logits, draft_logits, draft_tokens, target_temperature,
                         draft_temperature, target_top_k=None, draft_top_k=None, seed=0,
-                        uniform_override=None, return_residual=False):
+                        uniform_override=None, return_residual=False, target_top_p=None,
+                        draft_top_p=None, target_min_p=None, draft_min_p=None):
     """verify_chain on the library's fixed scratch (see spec_verify_chain_static).
 
     Same arguments and result as verify_chain, without a workspace: the C call
@@ -237,6 +275,10 @@ def verify_chain_static(target_logits, draft_logits, draft_tokens, target_temper
     tq = _vec(draft_temperature, B, torch.float32, "draft_temperature", dev)
     kp = _top_k(target_top_k, B, V, "target_top_k", dev)
     kq = _top_k(draft_top_k, B, V, "draft_top_k", dev)
+    pp = _filter(target_top_p, B, "target_top_p", dev, _topp_off)
+    pq = _filter(draft_top_p, B, "draft_top_p", dev, _topp_off)
+    mp = _filter(target_min_p, B, "target_min_p", dev, _minp_off)
+    mq = _filter(draft_min_p, B, "draft_min_p", dev, _minp_off)
     uov = None
     if uniform_override is not None:
         uov = _vec(uniform_override, B * G1 * 2, torch.float32, "uniform_override", dev)
@@ -249,8 +291,8 @@ def verify_chain_static(target_logits, draft_logits, draft_tokens, target_temper
         code = lib.spec_verify_chain_static(
             _ptr(tl), ld_t, _ptr(dl), ld_d, _DTYPES[target_logits.dtype], B, gamma, V,
             _ptr(toks),
-            _abi.spec_policy(tp.data_ptr(), None if kp is None else kp.data_ptr()),
-            _abi.spec_policy(tq.data_ptr(), None if kq is None else kq.data_ptr()),
+            _policy(tp, kp, pp, mp),
+            _policy(tq, kq, pq, mq),
             int(seed) & ((1 << 64) - 1), _ptr(uov), _ptr(num), _ptr(out), _ptr(flags),
             _ptr(resid), _stream(dev))
     _check(code)

@@ -52,22 +52,25 @@ struct Plan {
   int slice;
   size_t data_off;
   size_t hist_off;
+  size_t mass_off;
   size_t smem;
 };
 
 // Smallest cluster whose CTAs hold their slice of a target+draft row pair in
 // shared memory within the occupancy target; the largest cluster otherwise.
-bool make_plan(long long V, int esize, size_t extra, bool topk, Plan &pl) {
+bool make_plan(long long V, int esize, size_t extra, bool topk, bool topp, Plan &pl) {
   pl.data_off = align_up(sizeof(sv::Ctl), 128);
   for (int C = 1; C <= sv::kMaxCluster; C *= 2) {
     const long long slice = static_cast<long long>(align_up(static_cast<size_t>((V + C - 1) / C), 8));
     const size_t data = 2 * static_cast<size_t>(slice) * esize;
     const size_t region = align_up(data > extra ? data : extra, 128);
-    const size_t smem = pl.data_off + region + (topk ? sizeof(sv::TopkScratch) : 0);
+    const size_t hist = topk ? align_up(sizeof(sv::TopkScratch), 16) : 0;
+    const size_t smem = pl.data_off + region + hist + (topp ? sizeof(sv::MassScratch) : 0);
     if (smem <= kSmemTarget || (C == sv::kMaxCluster && smem <= kSmemHard)) {
       pl.cluster = C;
       pl.slice = static_cast<int>(slice);
       pl.hist_off = topk ? pl.data_off + region : 0;
+      pl.mass_off = topp ? pl.data_off + region + hist : 0;
       pl.smem = smem;
       return true;
     }
@@ -265,7 +268,10 @@ int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0)
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                       float *out_residual, void *workspace, size_t workspace_bytes,
                       cudaStream_t stream, bool need_draft_rows) {
-  const bool topk = P.kp != nullptr || P.kq != nullptr;
+  // top-k, top-p and min-p filters all run on the resident kernel
+  const bool topp = P.pp != nullptr || P.pq != nullptr;
+  const bool topk = P.kp != nullptr || P.kq != nullptr || topp || P.mp != nullptr ||
+                    P.mq != nullptr;
   const bool vec = aligned16(P.target) && (P.ld_t * esize) % 16 == 0 &&
                    (!need_draft_rows || (aligned16(P.draft) && (P.ld_d * esize) % 16 == 0));
   StreamPlan sp;
@@ -275,7 +281,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                     make_pass_plan(P.V, esize, P.gamma, pp) &&
                     static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr < 0x7FFFFFFFll;
   const bool streaming = !pass && vec && !topk && make_stream_plan(P.V, esize, sp);
-  if (!pass && !streaming && !make_plan(P.V, esize, extra, topk, pl))
+  if (!pass && !streaming && !make_plan(P.V, esize, extra, topk, topp, pl))
     return SPEC_ERR_UNSUPPORTED;
   // the caller's workspace must hold what the size query promised for the shape
   const bool chain = P.mode == sv::kModeChain;
@@ -361,6 +367,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.cluster = pl.cluster;
     P.data_off = static_cast<int>(pl.data_off);
     P.hist_off = static_cast<int>(pl.hist_off);
+    P.mass_off = static_cast<int>(pl.mass_off);
     e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
   }
   if (e != cudaSuccess) return map_cuda(e);
@@ -460,6 +467,10 @@ spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,
   P.Tq = draft_policy.temperature;
   P.kp = target_policy.top_k;
   P.kq = draft_policy.top_k;
+  P.pp = target_policy.top_p;
+  P.pq = draft_policy.top_p;
+  P.mp = target_policy.min_p;
+  P.mq = draft_policy.min_p;
   P.seed = seed;
   P.uov = uniform_override;
   P.out_num = out_num_accepted;
@@ -504,6 +515,10 @@ spec_status spec_verify_tree(const void *target_logits, int64_t ld_target,
   P.Tq = draft_policy.temperature;
   P.kp = target_policy.top_k;
   P.kq = draft_policy.top_k;
+  P.pp = target_policy.top_p;
+  P.pq = draft_policy.top_p;
+  P.mp = target_policy.min_p;
+  P.mq = draft_policy.min_p;
   P.seed = seed;
   P.uov = uniform_override;
   P.out_num = out_num_accepted;
@@ -533,7 +548,9 @@ spec_status spec_overlap(const void *target_logits, int64_t ld_target, const voi
   if (!target_logits || !draft_logits || !out_beta || !target_policy.temperature ||
       !draft_policy.temperature || ld_target < V || ld_draft < V)
     return SPEC_ERR_INVALID_ARG;
-  if (target_policy.top_k || draft_policy.top_k) return SPEC_ERR_UNSUPPORTED;
+  if (target_policy.top_k || draft_policy.top_k || target_policy.top_p || draft_policy.top_p ||
+      target_policy.min_p || draft_policy.min_p)
+    return SPEC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * gamma > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;  // headroom for clusters
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (out_flags) {
@@ -564,7 +581,7 @@ spec_status spec_typical_accept(const void *target_logits, int64_t ld_target, sp
   if (!target_logits || !target_policy.temperature || (gamma > 0 && !draft_tokens) ||
       !out_num_accepted || !out_tokens || !workspace || ld_target < V)
     return SPEC_ERR_INVALID_ARG;
-  if (target_policy.top_k) return SPEC_ERR_UNSUPPORTED;
+  if (target_policy.top_k || target_policy.top_p || target_policy.min_p) return SPEC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * (gamma + 1) > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;
   if (workspace_bytes < sv::typical_workspace_bytes(B, gamma) ||
       (reinterpret_cast<uintptr_t>(workspace) & 7u) != 0)

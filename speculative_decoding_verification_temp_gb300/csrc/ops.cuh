@@ -495,6 +495,119 @@ __device__ void topk_thresholds(const TE *sp, const TE *sq, int len, bool do_p, 
 }
 
 // ---------------------------------------------------------------------------
+// cluster-wide top-p threshold: radix select on order keys weighted by mass
+// ---------------------------------------------------------------------------
+
+// Masses are fixed point (w * 2^40, w = 2^((z - m) k) <= 1) so that the
+// histogram sums are exact and independent of the order of the atomics.
+constexpr float kMassScale = 1099511627776.0f;  // 2^40, exact in float
+
+// w * 2^40 is exact in float (a power-of-two scale); the conversion rounds to
+// the nearest integer, an error below 2^-41 of the row maximum per entry.
+__device__ __forceinline__ unsigned long long mass_fixed(float z, float m, float k) {
+  return __float2ull_rn(fast_exp2(__fmul_rn(__fsub_rn(z, m), k)) * kMassScale);
+}
+
+// Top-p boundary of the rows p (do_p) and q (do_q): the largest logit value
+// thr such that the entries >= thr (among those >= cut, the threshold already
+// in force) hold at least top_p of the kept mass.  Every entry tied with the
+// boundary is kept.  One radix round per 8 bits of the order key; per round a
+// mass histogram of the entries under the current prefix, summed over the
+// cluster, and a scan from the top digit by one warp per row.
+template <typename TE>
+__device__ void topp_thresholds(const TE *sp, const TE *sq, int len, bool do_p, bool do_q,
+                                const float cut[2], const float m[2], const float k[2],
+                                const float top_p[2], Ctl &ctl, MassScratch &ms,
+                                cg::cluster_group &cluster, int C, float thr[2]) {
+  constexpr int R = Elem<TE>::kKeyRounds;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 2) {
+    ctl.prefix[tid] = 0u;
+    ms.remaining[tid] = 0ull;  // set from the total in round 0
+  }
+  for (int round = 0; round < R; ++round) {
+    const int buf = round & 1;
+    const int shift = (R - 1 - round) * 8;
+    for (int i = tid; i < 512; i += kThreads) (&ms.hist[buf][0][0])[i] = 0ull;
+    csync();
+    const uint32_t hmask = static_cast<uint32_t>(~0ull << (shift + 8));
+#pragma unroll
+    for (int row = 0; row < 2; ++row) {
+      if (row == 0 ? !do_p : !do_q) continue;
+      const TE *s = row == 0 ? sp : sq;
+      const uint32_t want =
+          static_cast<uint32_t>(static_cast<unsigned long long>(ctl.prefix[row]) << (shift + 8));
+      for (int v = tid; v < len; v += kThreads) {
+        const float z = to_f32(s[v]);
+        if (!(z >= cut[row])) continue;
+        const uint32_t key = order_key(s[v]);
+        if ((key & hmask) == want)
+          atomicAdd(&ms.hist[buf][row][(key >> shift) & 255u], mass_fixed(z, m[row], k[row]));
+      }
+    }
+    csync();
+    cluster_sync_all();
+    for (int i = tid; i < 512; i += kThreads) {
+      unsigned long long g = 0ull;
+      for (int r = 0; r < C; ++r) g += cluster.map_shared_rank(&ms.hist[buf][0][0], r)[i];
+      (&ms.ghist[0][0])[i] = g;
+    }
+    csync();
+    if (warp < 2 && (warp == 0 ? do_p : do_q)) {
+      const int row = warp;
+      // lane l owns digits 255 - 8 l - j, j = 0..7 (descending values)
+      unsigned long long cnt[8];
+      unsigned long long s = 0ull;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = ms.ghist[row][255 - 8 * lane - j];
+        s += cnt[j];
+      }
+      unsigned long long incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (round == 0) {
+        // the target: top_p of the kept mass (at least one unit, so that
+        // top_p = 0 keeps the largest value)
+        const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        double t = static_cast<double>(top_p[row]) * static_cast<double>(total);
+        unsigned long long tg = static_cast<unsigned long long>(t);
+        if (static_cast<double>(tg) < t) ++tg;  // ceil: the mass must reach top_p
+        if (lane == 0) ms.remaining[row] = tg > 0ull ? tg : 1ull;
+        __syncwarp();
+      }
+      const unsigned long long need = ms.remaining[row];
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, incl >= need);
+      const int first = bal ? __ffs(bal) - 1 : 31;
+      if (lane == first) {
+        unsigned long long acc = incl - s;
+        int d = 255 - 8 * lane - 7;
+        unsigned long long left = need - (acc < need ? acc : need);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc + cnt[j] >= need) {
+            d = 255 - 8 * lane - j;
+            left = need - acc;
+            break;
+          }
+          acc += cnt[j];
+        }
+        ctl.prefix[row] = (ctl.prefix[row] << 8) | static_cast<uint32_t>(d);
+        ms.remaining[row] = left;
+      }
+    }
+    csync();
+  }
+#pragma unroll
+  for (int row = 0; row < 2; ++row)
+    thr[row] = sizeof(TE) == 2 ? key_value_bf16(ctl.prefix[row]) : key_value_f32(ctl.prefix[row]);
+  csync();
+}
+
+// ---------------------------------------------------------------------------
 // draw weights: per-CTA totals and the inverse-CDF search
 // ---------------------------------------------------------------------------
 

@@ -224,6 +224,86 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
   }
   __syncthreads();
 
+  // ---- 2b. top-p / min-p: a further threshold from the merged statistics,
+  // then the statistics again over the entries it keeps.  The decision is the
+  // same in every CTA of the cluster (per-sequence parameters and merged
+  // statistics).
+  {
+    const float topp_v[2] = {P.pp ? __ldg(P.pp + seq) : 1.f, P.pq ? __ldg(P.pq + seq) : 1.f};
+    const float minp_v[2] = {P.mp ? __ldg(P.mp + seq) : 0.f, P.mq ? __ldg(P.mq + seq) : 0.f};
+    const float Tv[2] = {Tp, Tq};
+    bool filt[2], do_topp[2];
+    float cut[2] = {thr_p, thr_q}, mm[2], kk2[2] = {kpv, kqv}, nthr[2] = {thr_p, thr_q};
+#pragma unroll
+    for (int row = 0; row < 2; ++row) {
+      const bool sampled = row == 0 ? !p_arg : (load_q && !q_arg);
+      const Partial o = ctl.merged[row];
+      const bool finite = o.m > -INFINITY && o.m < INFINITY && !(o.flags & 3);
+      filt[row] = sampled && finite && (topp_v[row] < 1.f || minp_v[row] > 0.f);
+      do_topp[row] = filt[row] && topp_v[row] < 1.f;
+      mm[row] = o.m;
+      if (filt[row] && minp_v[row] > 0.f)
+        nthr[row] = fmaxf(nthr[row], o.m + Tv[row] * logf(fminf(minp_v[row], 1.f)));
+    }
+    if (filt[0] || filt[1]) {
+      if (do_topp[0] || do_topp[1]) {
+        MassScratch &ms = *reinterpret_cast<MassScratch *>(smem_raw + P.mass_off);
+        float tt[2];
+        const float tpv[2] = {fmaxf(topp_v[0], 0.f), fmaxf(topp_v[1], 0.f)};
+        topp_thresholds<TE>(sp, sq, len, do_topp[0], do_topp[1], cut, mm, kk2, tpv, ctl, ms,
+                            cluster, C, tt);
+#pragma unroll
+        for (int row = 0; row < 2; ++row)
+          if (do_topp[row]) nthr[row] = fmaxf(nthr[row], tt[row]);
+      }
+      thr_p = nthr[0];
+      thr_q = nthr[1];
+      // every CTA has read the first round's partials before they are rewritten
+      cluster_sync_all();
+#pragma unroll
+      for (int row = 0; row < 2; ++row) {
+        if (!filt[row]) continue;
+        RowAcc a;
+        acc_init(a);
+        stage_softmax_masked<TE>(row == 0 ? sp : sq, 0, len, kk2[row], nthr[row], a);
+        block_online(a.m, a.S, a.fl, kk2[row], ctl.rs);
+        Partial pt;
+        pt.m = a.m;
+        pt.S = a.S;
+        pt.av = 0.f;
+        pt.ai = 0;
+        pt.flags = a.fl | ctl.merged[row].flags;
+        if (tid == 0) ctl.part[row] = pt;
+      }
+      cluster_sync_all();
+      if (warp == 0) {
+#pragma unroll
+        for (int row = 0; row < 2; ++row) {
+          if (!filt[row]) continue;
+          Partial o;
+          if (lane < C) {
+            o = cluster.map_shared_rank(&ctl.part[row], lane)[0];
+          } else {
+            o.m = -INFINITY;
+            o.S = 0.f;
+            o.av = -INFINITY;
+            o.ai = INT_MAX;
+            o.flags = 0;
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xFFFFFFFFu, o.m, off);
+            const float S2 = __shfl_xor_sync(0xFFFFFFFFu, o.S, off);
+            o.flags |= __shfl_xor_sync(0xFFFFFFFFu, o.flags, off);
+            online_merge(o.m, o.S, m2, S2, kk2[row]);
+          }
+          if (lane == 0) ctl.merged[row] = o;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
   RowDesc dp, dq;
   bool need_fallback[2] = {false, false};
   uint32_t tmo = 0u;

@@ -129,6 +129,10 @@ struct Params {
   const float *Tq;
   const int32_t *kp;
   const int32_t *kq;
+  const float *pp;  // top-p per sequence (NULL: none)
+  const float *pq;
+  const float *mp;  // min-p per sequence (NULL: none)
+  const float *mq;
   unsigned long long seed;
   const float *uov;
   int32_t *out_num;
@@ -143,6 +147,7 @@ struct Params {
   int cluster;    // CTAs per cluster
   int data_off;   // byte offset of the data slices in dynamic shared memory
   int hist_off;   // byte offset of the top-k histograms (0: no top-k in this launch)
+  int mass_off;   // byte offset of the top-p mass histograms (0: no top-p in this launch)
   // streaming (persistent) kernel only
   const int32_t *first_child;  // [T*N] first child of each tree node, -1 for leaves
   int n_units;
@@ -208,6 +213,13 @@ struct RedScratch {
 struct TopkScratch {
   int hist[2][2][256];
   int ghist[2][256];
+};
+
+// Mass histograms of the top-p select (fixed point, see topp_thresholds).
+struct MassScratch {
+  unsigned long long hist[2][2][256];
+  unsigned long long ghist[2][256];
+  unsigned long long remaining[2];
 };
 
 struct __align__(16) Ctl {
