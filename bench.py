@@ -13,6 +13,8 @@ Arms:
   --impl reference  the CPU oracle (the plain float64 restatement of the
                     method) on this host's cores, on a bounded sample
 
+--op filters times the same chain verification with top-p 0.9 and min-p 0.05
+on both sides of every sequence (same metric);
 --op overlap times the per-position overlap beta_i = sum min(p_i, q_i) of
 the same workload instead (metric: positions per second, B * gamma per step);
 --op typical times typical acceptance (epsilon 0.0625, delta 0.5; metric:
@@ -49,6 +51,10 @@ TRAFFIC_UNIT = "chain_rows.cu"
 # kernels the library launches per chain call on this workload: rows, decide,
 # weights, search, precise jobs, precise search
 LAUNCHES_PER_STEP = 6
+# --op filters: top-p and min-p of every sequence (both sides); the resident
+# kernel and the precise redraw kernel run
+FILTER_TOP_P, FILTER_MIN_P = 0.9, 0.05
+FILTER_LAUNCHES_PER_STEP = 2
 OVERLAP_METRIC = "overlap positions/s (B*gamma)"
 L2_BYTES = 129e6
 OVERLAP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "overlap_kernel_b256_g7_v128256_bf16.md")
@@ -190,7 +196,8 @@ class ClockSampler:
 
 def oracle_sample_rate(w, n_seqs, min_s=0.0, max_passes=1):
     """The CPU oracle on the first n_seqs sequences, repeated until min_s seconds
-    (at most max_passes passes): (verified rows per second, seconds, passes)."""
+    (at most max_passes passes): (verified rows per second, seconds, passes).
+    w["filters"], when present, holds the top-p / min-p arrays of the call."""
     from oracle import verify as ov
     gamma = w["gamma"]
     t0 = time.perf_counter()
@@ -198,7 +205,7 @@ def oracle_sample_rate(w, n_seqs, min_s=0.0, max_passes=1):
     while True:
         ov.verify_chain(w["target"], w["draft"], w["tokens"], w["target_temperature"],
                         w["draft_temperature"], w["target_top_k"], w["draft_top_k"],
-                        seed=w["seed"], seqs=range(n_seqs))
+                        seed=w["seed"], seqs=range(n_seqs), **w.get("filters", {}))
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= min_s or passes >= max_passes:
@@ -206,9 +213,9 @@ def oracle_sample_rate(w, n_seqs, min_s=0.0, max_passes=1):
     return passes * n_seqs * (gamma + 1) / dt, dt, passes
 
 
-def _oracle_worker(spec, seqs):
-    """One process of the all-core CPU baseline: the oracle on `seqs`, the
-    workload's arrays attached from shared memory."""
+def _oracle_worker(spec, seqs, passes=1):
+    """One process of the all-core CPU baseline: the oracle on `seqs`, `passes`
+    times, the workload's arrays attached from shared memory."""
     from multiprocessing import shared_memory
     sys.path.insert(0, ROOT)
     from oracle import verify as ov
@@ -218,8 +225,9 @@ def _oracle_worker(spec, seqs):
         shms.append(shm)
         arrs[key] = np.ndarray(shape, dtype=dtype, buffer=shm.buf)
     t0 = time.perf_counter()
-    ov.verify_chain(arrs["target"], arrs["draft"], arrs["tokens"], arrs["tt"], arrs["td"],
-                    None, None, seed=spec["seed"], seqs=seqs)
+    for _ in range(passes):
+        ov.verify_chain(arrs["target"], arrs["draft"], arrs["tokens"], arrs["tt"], arrs["td"],
+                        None, None, seed=spec["seed"], seqs=seqs, **spec["filters"])
     dt = time.perf_counter() - t0
     del arrs
     for shm in shms:
@@ -227,10 +235,11 @@ def _oracle_worker(spec, seqs):
     return dt
 
 
-def oracle_all_cores(w, n_seqs):
+def oracle_all_cores(w, n_seqs, min_s=0.0):
     """The CPU oracle on the first n_seqs sequences, split over every host core
-    (spawned processes reading the workload from shared memory): (rows per
-    second, wall seconds, processes)."""
+    (spawned processes reading the workload from shared memory), repeated so
+    that the timed run takes about min_s seconds: (rows per second, wall
+    seconds, processes, passes)."""
     import concurrent.futures as cf
     import multiprocessing as mp
     from multiprocessing import shared_memory
@@ -238,7 +247,7 @@ def oracle_all_cores(w, n_seqs):
     arrays = {"target": w["target"], "draft": w["draft"], "tokens": w["tokens"],
               "tt": np.asarray(w["target_temperature"], np.float32),
               "td": np.asarray(w["draft_temperature"], np.float32)}
-    shms, spec = [], {"arrays": {}, "seed": w["seed"]}
+    shms, spec = [], {"arrays": {}, "seed": w["seed"], "filters": w.get("filters", {})}
     try:
         for key, a in arrays.items():
             a = np.ascontiguousarray(a)
@@ -249,20 +258,26 @@ def oracle_all_cores(w, n_seqs):
         parts = [list(range(i, n_seqs, cores)) for i in range(cores)]
         parts = [p for p in parts if p]
         with cf.ProcessPoolExecutor(len(parts), mp_context=mp.get_context("spawn")) as ex:
-            list(ex.map(_oracle_worker, [spec], [[0]]))  # start-up outside the timing
+            # start-up outside the timing; one pass sizes the repeat count
+            list(ex.map(_oracle_worker, [spec] * len(parts), [[p[0]] for p in parts]))
             t0 = time.perf_counter()
             list(ex.map(_oracle_worker, [spec] * len(parts), parts))
+            one = time.perf_counter() - t0
+            passes = max(1, min(50, int(min_s / max(one, 1e-6))))
+            t0 = time.perf_counter()
+            list(ex.map(_oracle_worker, [spec] * len(parts), parts, [passes] * len(parts)))
             dt = time.perf_counter() - t0
     finally:
         for shm in shms:
             shm.close()
             shm.unlink()
-    return n_seqs * (w["gamma"] + 1) / dt, dt, len(parts)
+    return passes * n_seqs * (w["gamma"] + 1) / dt, dt, len(parts), passes
 
 
 def config_entry(w):
+    filt = ", top-p 0.9 and min-p 0.05 on both sides" if w.get("filters") else ""
     return {"workload": f"chain verify B={w['B']} gamma={w['gamma']} V={w['V']} {w['dtype']} "
-                        "(temperature 1, Zipf logits, draft sigma 0.4)",
+                        f"(temperature 1, Zipf logits, draft sigma 0.4{filt})",
             "B": w["B"], "gamma": w["gamma"], "V": w["V"],
             "logit_bytes_per_step": logit_bytes(w),
             "l2": l2_note(logit_bytes(w), "logits")}
@@ -280,14 +295,21 @@ def logit_bytes(w):
 
 def bench_workload(args):
     """The timed workload: B = 256, gamma = 7, V = 128256 bf16, or the same
-    recipe with --batch sequences (smaller cases for profiling)."""
+    recipe with --batch sequences (smaller cases for profiling).  --op filters
+    adds top-p 0.9 and min-p 0.05 on both sides of every sequence."""
     from speculative_decoding_verification_temp_gb300 import workloads
     if not args.batch:
-        return workloads.config(WORKLOAD)
-    c = dict(workloads.CONFIGS[WORKLOAD])
-    c.pop("kind")
-    c["B"] = args.batch
-    return workloads.make_chain(seed=1000 + WORKLOAD, **c)
+        w = workloads.config(WORKLOAD)
+    else:
+        c = dict(workloads.CONFIGS[WORKLOAD])
+        c.pop("kind")
+        c["B"] = args.batch
+        w = workloads.make_chain(seed=1000 + WORKLOAD, **c)
+    if getattr(args, "op", "verify") == "filters":
+        P = np.full(w["B"], FILTER_TOP_P, np.float32)
+        M = np.full(w["B"], FILTER_MIN_P, np.float32)
+        w["filters"] = dict(target_top_p=P, draft_top_p=P, target_min_p=M, draft_min_p=M)
+    return w
 
 
 def run_reference(args):
@@ -350,9 +372,10 @@ def run_ours(args):
     tp = torch.from_numpy(w["target_temperature"]).to(dev)
     tq = torch.from_numpy(w["draft_temperature"]).to(dev)
     stream = torch.cuda.current_stream(dev)
+    filters = {k: torch.from_numpy(v).to(dev) for k, v in w.get("filters", {}).items()}
 
     def step():
-        return sv.verify_chain(target, draft, tokens, tp, tq, seed=seed)
+        return sv.verify_chain(target, draft, tokens, tp, tq, seed=seed, **filters)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -392,14 +415,20 @@ def run_ours(args):
     # above: events between the kernels hold back the next kernel's early
     # launch, which the headline number should not pay for)
     k_steps = min(args.steps, 500)
-    k_starts, k_ends = events(k_steps), events(k_steps)
-    torch.cuda.synchronize()
-    for i in range(k_steps):
-        lib.spec_set_profile_events(k_starts[i].cuda_event, k_ends[i].cuda_event)
-        step()
-    torch.cuda.synchronize()
-    lib.spec_set_profile_events(None, None)
-    kernel_ms = [s_.elapsed_time(e_) for s_, e_ in zip(k_starts, k_ends)]
+    if filters:
+        # filtered rows take the resident kernel, which the events do not
+        # bracket: the whole call is the kernel's bound
+        k_steps = 0
+        kernel_ms = None
+    else:
+        k_starts, k_ends = events(k_steps), events(k_steps)
+        torch.cuda.synchronize()
+        for i in range(k_steps):
+            lib.spec_set_profile_events(k_starts[i].cuda_event, k_ends[i].cuda_event)
+            step()
+        torch.cuda.synchronize()
+        lib.spec_set_profile_events(None, None)
+        kernel_ms = [s_.elapsed_time(e_) for s_, e_ in zip(k_starts, k_ends)]
     ms_per_step = elapsed_ms / args.steps
     value = job_rate(world, rows, args.steps, elapsed_ms / 1e3)
     clocks = clk.summary()
@@ -418,11 +447,12 @@ def run_ours(args):
     # what the pages ask a verifier to report beside its speed: the accepted
     # length per target invocation and the per-position acceptance rate beta
     n_acc = r.num_accepted.to("cpu").numpy()
-    beta = sv.overlap(target, draft, tp, tq).beta.to("cpu").numpy()
     acceptance = {"mean_emitted_tokens": float(np.mean(n_acc + 1)),
-                  "mean_accepted_drafts": float(np.mean(n_acc)),
-                  "mean_beta_per_position": [round(float(x), 4) for x in beta.mean(axis=0)],
-                  "mean_beta": float(beta.mean())}
+                  "mean_accepted_drafts": float(np.mean(n_acc))}
+    if not filters:  # beta of the unfiltered distributions
+        beta = sv.overlap(target, draft, tp, tq).beta.to("cpu").numpy()
+        acceptance["mean_beta_per_position"] = [round(float(x), 4) for x in beta.mean(axis=0)]
+        acceptance["mean_beta"] = float(beta.mean())
 
     # end to end through the binding: pinned host inputs in, results back out
     e2e_steps = max(1, args.e2e_steps)
@@ -432,7 +462,7 @@ def run_ours(args):
         t_d = target_h.to(dev, non_blocking=True)
         d_d = draft_h.to(dev, non_blocking=True)
         k_d = tokens_h.to(dev, non_blocking=True)
-        r2 = sv.verify_chain(t_d, d_d, k_d, tp, tq, seed=seed)
+        r2 = sv.verify_chain(t_d, d_d, k_d, tp, tq, seed=seed, **filters)
         n_out = r2.num_accepted.to("cpu")
         t_out = r2.tokens.to("cpu")
     torch.cuda.synchronize()
@@ -458,15 +488,30 @@ def run_ours(args):
     n_check = min(B, 8)
     from oracle import verify as ov
     want = ov.verify_chain(w["target"], w["draft"], w["tokens"], w["target_temperature"],
-                           w["draft_temperature"], seed=seed, seqs=range(n_check))
+                           w["draft_temperature"], seed=seed, seqs=range(n_check),
+                           **w.get("filters", {}))
     got_n, got_t = r.num_accepted.to("cpu").numpy(), r.tokens.to("cpu").numpy()
     mismatched = sum(1 for b, o in enumerate(want)
                      if got_n[b] != o["num_accepted"] or list(got_t[b]) != o["tokens"])
 
-    avg_kernel_ms = statistics.mean(kernel_ms)
     avg_call_ms = statistics.mean(call_ms)
+    avg_kernel_ms = statistics.mean(kernel_ms) if kernel_ms else avg_call_ms
     peak, peak_kind = measured_peak()
     achieved = nbytes / (avg_kernel_ms / 1e3) / 1e9
+    if filters:
+        kernel = ("unit_kernel + refine_kernel (filtered rows take the resident kernel; "
+                  "timed as whole calls by the per-call events of the headline loop)")
+        traffic = None
+        launches = FILTER_LAUNCHES_PER_STEP
+        kmed = statistics.median(call_ms)
+    else:
+        kernel = ("chain_rows_kernel (every logit row read once; timed by CUDA "
+                  "events the library records around it on the call's stream, "
+                  f"{k_steps} calls after the headline loop)")
+        # the record is for the full-size workload only
+        traffic = None if args.batch else recorded_traffic()
+        launches = LAUNCHES_PER_STEP
+        kmed = statistics.median(kernel_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -477,17 +522,13 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h,
                 "h2d_copy_alone_gbs": h2d / copy_s / 1e9,
                 "h2d_copy_alone_ms": 1e3 * copy_s},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     # the record is for the full-size workload only
-                     "traffic": None if args.batch else recorded_traffic(),
+                     "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "chain_rows_kernel (every logit row read once; timed by CUDA "
-                               "events the library records around it on the call's stream, "
-                               f"{k_steps} calls after the headline loop)",
+                     "kernel": kernel,
                      "launch_ms_avg": avg_kernel_ms,
-                     "launch_ms_median": statistics.median(kernel_ms)},
+                     "launch_ms_median": kmed},
         "whole_call": {"ms_avg": avg_call_ms, "achieved_gbs": nbytes / (avg_call_ms / 1e3) / 1e9,
                        "frac_of_peak": nbytes / (avg_call_ms / 1e3) / 1e9 / peak,
                        "frac_of_8tbs_nominal": nbytes / (avg_call_ms / 1e3) / 1e9 / 8000.0},
@@ -498,12 +539,12 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         rate, dt, passes = oracle_sample_rate(w, args.cpu_seqs, min_s=10.0, max_passes=8)
         n_all = min(B, max(args.cpu_seqs, 64))
-        rate_all, dt_all, procs = oracle_all_cores(w, n_all)
+        rate_all, dt_all, procs, passes_all = oracle_all_cores(w, n_all, min_s=8.0)
         line["cpu_baseline"] = {"value": rate_all, "unit": "rows/s", "cores": procs,
                                 "kind": "oracle",
-                                "sample": f"the first {n_all} of {B} sequences split over "
-                                          f"{procs} processes ({os.cpu_count()} host cores), "
-                                          f"{dt_all:.1f} s",
+                                "sample": f"{passes_all} passes over the first {n_all} of {B} "
+                                          f"sequences split over {procs} processes "
+                                          f"({os.cpu_count()} host cores), {dt_all:.1f} s",
                                 "one_core": {"value": rate, "cores": 1,
                                              "sample": f"{passes} passes over the first "
                                                        f"{args.cpu_seqs} of {B} sequences, "
@@ -931,8 +972,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per batch (default: the B = 256 workload); for profiling")
     ap.add_argument("--op", default="verify",
-                    choices=["verify", "overlap", "typical", "rerank", "workloads"],
-                    help="verify: the chain verifier (default); overlap: beta_i per position; "
+                    choices=["verify", "filters", "overlap", "typical", "rerank", "workloads"],
+                    help="verify: the chain verifier (default); filters: the same with top-p "
+                         "0.9 and min-p 0.05; overlap: beta_i per position; "
                          "typical: typical acceptance; rerank: EAGLE-2 tree rerank; "
                          "workloads: per-call times of workloads 0-4 and the tree mask")
     ap.add_argument("--only", default="",

@@ -128,7 +128,10 @@ typedef struct {
 #define SPEC_FLAG_DEGENERATE_RESIDUAL 8u /* sum [p - q]+ <= 0 at a rejection: the chain
                                             draws from p; the tree keeps its current p */
 #define SPEC_FLAG_DEPTH 16u              /* a tree node deeper than max_depth */
-#define SPEC_FLAG_TIMEOUT 32u            /* a bounded on-device wait gave up */
+#define SPEC_FLAG_TIMEOUT 32u            /* a bounded on-device wait gave up; on the
+                                            streaming chain path the sequence then
+                                            gets the fallback outputs: 0 accepted
+                                            drafts, every token -1 */
 #define SPEC_FLAG_BAD_TREE 64u           /* parent[0] != -1 or parent[n] not in [0, n) */
 
 /* Bytes of workspace spec_verify_chain needs for B sequences of gamma drafts
@@ -304,6 +307,18 @@ const char *spec_status_string(spec_status status);
  * two is NULL (the previous setting is kept), SPEC_OK otherwise.
  */
 spec_status spec_set_profile_events(void *start_event, void *stop_event);
+
+/* Bound on one on-device wait (diagnostics and tests; the pages have no
+ * counterpart).  Every wait inside the kernels gives up after a bound (about two
+ * seconds by default) and sets SPEC_FLAG_TIMEOUT instead of hanging.  This
+ * shortens the first wait the streaming chain path's rows kernel makes for each
+ * chunk to `cycles` SM clock cycles (0: a single non-blocking test); negative
+ * restores the default.  When that wait gives up the kernel flags the call and
+ * then waits again with the full bound, so no copy is left in flight and the
+ * call completes; every sequence of the call gets SPEC_FLAG_TIMEOUT and the
+ * fallback outputs.  Process-wide, read at each call's launch.  Returns SPEC_OK.
+ */
+spec_status spec_set_wait_limit(int64_t cycles);
 
 /* Bytes of workspace spec_typical_accept needs: 8 per target row,
  * B * (gamma + 1) rows (0 for a negative size). */

@@ -24,7 +24,7 @@ def __getattr__(name):
     if name in ("verify_chain", "verify_chain_static", "verify_tree", "tree_mask", "overlap",
                 "typical_accept", "tree_rerank", "SpecVerifyError", "workspace",
                 "ChainResult", "TreeResult", "MaskResult", "OverlapResult", "TypicalResult",
-                "RerankResult", "api"):
+                "RerankResult", "set_wait_limit", "api"):
         import importlib
         api = importlib.import_module(__name__ + ".api")
         return api if name == "api" else getattr(api, name)

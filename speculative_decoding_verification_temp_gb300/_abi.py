@@ -40,6 +40,7 @@ EXPORTS = (
     "spec_tree_rerank",
     "spec_status_string",
     "spec_set_profile_events",
+    "spec_set_wait_limit",
 )
 
 
@@ -104,6 +105,8 @@ def load():
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_set_profile_events.argtypes = [_p, _p]
     lib.spec_set_profile_events.restype = _i
+    lib.spec_set_wait_limit.argtypes = [_i64]
+    lib.spec_set_wait_limit.restype = _i
     _lib = lib
     return lib
 

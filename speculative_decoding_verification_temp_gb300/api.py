@@ -36,6 +36,14 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def set_wait_limit(cycles=None):
+    """spec_set_wait_limit: bound the streaming chain path's first wait on each
+    chunk to `cycles` SM clock cycles (0: one non-blocking test); None restores
+    the default bound.  A wait that gives up turns the call's outputs into the
+    documented fallback with FLAG_TIMEOUT (diagnostics and tests)."""
+    _check(_abi.load().spec_set_wait_limit(-1 if cycles is None else int(cycles)))
+
+
 _WORKSPACES = {}
 
 

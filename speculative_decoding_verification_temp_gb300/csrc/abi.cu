@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "ops.cuh"
 #include "precise.cuh"
 #include "specverify.h"
 #include "verify_units.cuh"
@@ -259,10 +260,15 @@ const sv::Exp2Table &exp2_table() {
 
 spec_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
+// Cycles the chain rows kernel's first wait on a chunk may take (see
+// spec_set_wait_limit); the full bound unless a caller shortened it.
+std::atomic<long long> g_first_wait{sv::kWaitLimitCycles};
+
 int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0); }
 
 // Shared launch path of the chain and tree verifiers.  16-byte aligned rows
-// without top-k filtering take the chain pass kernel (chains of gamma <= 31)
+// without top-k, top-p or min-p filtering take the streaming chain path
+// (chains of gamma <= 31: rows, decide, weights, search and precise kernels)
 // or the streaming kernel (trees, longer chains); everything else the
 // resident kernel.
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
@@ -325,6 +331,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.ppart = reinterpret_cast<double *>(ws + L.ppart);
     P.near_list = reinterpret_cast<int32_t *>(ws + L.near_list);
     P.pctr = reinterpret_cast<uint32_t *>(ws + L.pctr);
+    P.first_wait = g_first_wait.load(std::memory_order_relaxed);
     // rows kernel: its control block, then the ring of chunk slots
     const size_t rows_off = align_up(sv::chain_rows_ctl_bytes(), 128);
     P.data_off = static_cast<int>(rows_off);
@@ -371,7 +378,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
   }
   if (e != cudaSuccess) return map_cuda(e);
-  if (!pass) {  // the pass kernel redraws near-boundary draws itself
+  if (!pass) {  // the streaming chain path has its own precise redraw
     e = sv::launch_refine(P, esize, exp2_table(), stream);
     if (e != cudaSuccess) return map_cuda(e);
   }
@@ -407,6 +414,12 @@ spec_status check_chain_args(const void *target_logits, int64_t ld_target,
 }  // namespace sv
 
 extern "C" {
+
+spec_status spec_set_wait_limit(int64_t cycles) {
+  g_first_wait.store(cycles < 0 ? sv::kWaitLimitCycles : static_cast<long long>(cycles),
+                     std::memory_order_relaxed);
+  return SPEC_OK;
+}
 
 spec_status spec_set_profile_events(void *start_event, void *stop_event) {
   return sv::set_profile_events(start_event, stop_event) ? SPEC_OK : SPEC_ERR_INVALID_ARG;

@@ -324,9 +324,11 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
   for (long long k = blockIdx.x; k < total; k += gridDim.x, ++i) {
     const int slot = i % NS;
     const uint32_t phase = static_cast<uint32_t>(i / NS) & 1u;
-    if (!mbar_wait_bounded(&ctl.full[slot], phase)) {
+    if (!mbar_wait_limit(&ctl.full[slot], phase, P.first_wait)) {
+      // gave up: flag it, then wait again with the full bound, so that no copy
+      // is left in flight and the chunk is read only once it has landed
       if (lane == 0) atomicOr(P.err, 1u);
-      mbar_wait_bounded(&ctl.full[slot], phase);  // do not leave a copy in flight
+      mbar_wait_bounded(&ctl.full[slot], phase);
     }
     const SlotInfo si = ctl.info[slot];
     const TE *sm = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * P.slot_bytes);

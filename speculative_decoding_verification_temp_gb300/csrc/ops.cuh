@@ -81,6 +81,30 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t 
   return ok != 0;
 }
 
+// One non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(unsigned long long *bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+// A wait that gives up after `limit` cycles (limit <= 0: one non-blocking
+// test).  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_limit(unsigned long long *bar, uint32_t phase,
+                                                long long limit) {
+  if (limit <= 0) return mbar_test_wait(bar, phase);
+  if (mbar_try_wait(bar, phase)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, phase))
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
 // Returns false when the wait gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint32_t phase) {
   if (mbar_try_wait(bar, phase)) return true;

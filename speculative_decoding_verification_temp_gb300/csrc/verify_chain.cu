@@ -398,8 +398,20 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
   fo |= __shfl_sync(0xFFFFFFFFu, i < gamma ? f : dp.flags, j);  // position j's flags
   const RowDesc djp = shfl_desc(dp, j);
   const RowDesc djq = shfl_desc(dq, j);
+  if (lane == 0 && __ldcg(P.err)) {
+    // a bounded wait of the rows kernel gave up: the documented fallback, no
+    // accepted drafts and no tokens
+    const long long obase = static_cast<long long>(seq) * (gamma + 1);
+    for (int x = 0; x <= gamma; ++x) P.out_tokens[obase + x] = -1;
+    P.out_num[seq] = 0;
+    if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
+    P.final_unit[seq] = -1;
+    PassSeq ps = {};
+    ps.draw = 0;
+    reinterpret_cast<PassSeq *>(P.pseqw)[seq] = ps;
+    return;
+  }
   if (lane == 0) {
-    if (__ldcg(P.err)) fo |= SPEC_FLAG_TIMEOUT;  // a bounded wait of the rows kernel gave up
     PassSeq ps;
     ps.dp = djp;
     ps.residual = j < gamma ? 1 : 0;
@@ -884,6 +896,18 @@ __global__ void __launch_bounds__(kDThreads) chain_search_kernel(const Params P)
   const int seq = blockIdx.x;
   PassSeq ps = reinterpret_cast<const PassSeq *>(P.pseqw)[seq];
   if (!ps.draw) return;  // the decide kernel wrote the outputs
+  if (__ldcg(P.err)) {
+    // a bounded wait of the weights kernel gave up: the step totals may be
+    // incomplete, so the draw gets the fallback outputs
+    if (threadIdx.x == 0) {
+      const long long obase = static_cast<long long>(seq) * (P.gamma + 1);
+      for (int x = 0; x <= P.gamma; ++x) P.out_tokens[obase + x] = -1;
+      P.out_num[seq] = 0;
+      if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
+      P.final_unit[seq] = -1;
+    }
+    return;
+  }
   const int V = P.V, nsteps = P.steps;
   float *fst = reinterpret_cast<float *>(P.fstep) + static_cast<long long>(seq) * nsteps;
   const TE *gp, *gq;
@@ -1282,7 +1306,6 @@ void set_chain_split(Params &P) {
   const int steps = P.steps;
   P.wj_steps = steps < 16 ? steps : 16;
   P.wj = (steps + P.wj_steps - 1) / P.wj_steps;
-  P.wj_stride = 0;
   const int kp = steps < 64 ? steps : 64;
   P.pj_steps = (steps + kp - 1) / kp;
   P.pj = (steps + P.pj_steps - 1) / P.pj_steps;

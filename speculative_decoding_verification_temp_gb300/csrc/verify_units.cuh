@@ -89,8 +89,8 @@ constexpr int kChainRecordsPerChunk = 8;
 
 // One work unit of the precise redraw (a slice of one queued draw's
 // vocabulary): its partial sums, published for the other units of the draw.
-// A chain's final draw, published by the sequence's deciding group for the
-// groups that run its weight jobs (chain pass kernel).
+// A chain's final draw, written by the chain decide kernel for the weights,
+// search and precise kernels of the streaming chain path.
 struct __align__(16) PassSeq {
   RowDesc dp, dq;  // the draw distribution: [p - q]_+ (residual) or p
   float u;         // draw uniform
@@ -148,6 +148,7 @@ struct Params {
   int data_off;   // byte offset of the data slices in dynamic shared memory
   int hist_off;   // byte offset of the top-k histograms (0: no top-k in this launch)
   int mass_off;   // byte offset of the top-p mass histograms (0: no top-p in this launch)
+  long long first_wait;  // cycles the chain rows kernel's first wait on a chunk may take
   // streaming (persistent) kernel only
   const int32_t *first_child;  // [T*N] first child of each tree node, -1 for leaves
   int n_units;
@@ -171,25 +172,20 @@ struct Params {
   RefinePart *rpart;              // [max(kRefineMaxGrid, nseq)] work-unit partials
   double *rc;                     // [nseq] residual multiplier of each queued draw
   uint32_t *rbar;                 // grid-barrier arrivals of the redraw kernel
-  // chain pass kernel
-  unsigned long long *srec;       // [rows][chunks][8] per-warp records, 0 = not yet written
-  uint32_t *seq_cnt;              // [nseq] chunks of the sequence with stored records (a hint)
+  // streaming chain path (rows, decide, weights, search, precise kernels)
+  unsigned long long *srec;       // [rows][chunks][8] per-warp records of the rows kernel
   uint32_t *err;                  // bit 0: a bounded wait gave up
   int chunk_elems;                // entries per chunk
   int cpr;                        // chunks per row
   int steps;                      // draw search steps per row (256 entries each)
-  // chain pass kernel: draws split into jobs
-  unsigned long long *pseqw;      // [nseq][sizeof(PassSeq) / 4] draw descriptors, one 32-bit
-                                  //   word per 64-bit entry with a nonzero tag (0: unset)
-  uint32_t *sctr;                 // [nseq][4] [1] weight jobs done, [2] precise jobs done,
-                                  //   [3] precise jobs that met an uncertain step
-  unsigned long long *fstep;      // [nseq][steps] single-precision step totals, tagged (0: unset)
+  unsigned long long *pseqw;      // [nseq] PassSeq draw descriptors (decide kernel)
+  uint32_t *sctr;                 // [nseq][4] [3] precise jobs that met an uncertain step
+  unsigned long long *fstep;      // [nseq][steps] single-precision step totals
   double *pstep;                  // [nseq][2][steps] precise step sums A (e_p) and B (e_q)
   double *ppart;                  // [nseq][pj][2] shares of S_p, S_q
-  int *near_list;                 // [nseq] sequence + 1 of each precise redraw (0: unset)
-  uint32_t *pctr;                 // [0] precise redraws queued, [1] precise jobs claimed,
-                                  // [2] sequences final
-  int wj, wj_steps, wj_stride;    // weight jobs per draw, steps per job, group stride
+  int *near_list;                 // [nseq] sequence + 1 of each queued precise redraw
+  uint32_t *pctr;                 // [0] precise redraws queued
+  int wj, wj_steps;               // slices per draw of the weights kernel, steps per slice
   int pj, pj_steps;               // precise jobs per phase, steps per job
 };
 

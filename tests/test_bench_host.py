@@ -61,6 +61,14 @@ def test_all_core_oracle_baseline_matches_the_oracle_rows():
     # oracle's rows per second on a small chain workload
     from speculative_decoding_verification_temp_gb300 import workloads
     w = workloads.make_chain(3, 2, 300, dtype="f32", seed=5)
-    rate, dt, procs = bench.oracle_all_cores(w, 3)
+    rate, dt, procs, passes = bench.oracle_all_cores(w, 3)
     assert procs == min(3, os.cpu_count() or 1)
-    assert rate > 0 and dt > 0
+    assert rate > 0 and dt > 0 and passes == 1
+    # the filtered workload of --op filters reaches the oracle's policy
+    import numpy as np
+    P = np.full(3, 0.5, np.float32)
+    w["filters"] = dict(target_top_p=P, draft_top_p=P, target_min_p=P * 0.1, draft_min_p=P * 0.1)
+    rate, dt, procs, passes = bench.oracle_all_cores(w, 3, min_s=0.05)
+    assert rate > 0 and passes >= 1
+    r1, _, _ = bench.oracle_sample_rate(w, 2)
+    assert r1 > 0

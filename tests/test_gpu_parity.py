@@ -78,6 +78,17 @@ def test_chain_residual_output(cfg, exception_log):
                   check_residual=True)
 
 
+@pytest.mark.parametrize("cfg,path", [(2, "stream"), (2, "resident"), (3, "resident")])
+def test_chain_residual_output_full_size(cfg, path, exception_log):
+    # every sequence of the full batch, in the bench's launch configuration:
+    # the B = 256, V = 128256 workload on both kernels (residual within 2e-3
+    # in bf16), and the V = 152064 workload with top-k 50 and 64 greedy rows
+    w = workloads.config(cfg)
+    res = run_chain(w, return_residual=True, force_resident=path == "resident")
+    compare_chain(res, oracle_chain(w), exception_log, f"resid{cfg}-{path}", w["dtype"],
+                  check_residual=True)
+
+
 def test_tree_residual_output(exception_log):
     w = workloads.make_tree(16, 40, 8192, dtype="bf16", seed=5, branching=(4, 3, 2, 2, 1))
     res = run_tree(w, return_residual=True)

@@ -42,7 +42,7 @@ def _same(a, b, dtype):
 
 
 @pytest.mark.parametrize("case", [
-    # chain pass kernel: bf16, aligned rows, no top-k; 1024 units (the largest
+    # streaming chain path: bf16, aligned rows, no filters; 1024 units (the largest
     # B = 128, gamma = 7 batch that fits the scratch)
     dict(B=128, gamma=7, V=32000, dtype="bf16", greedy_seqs=8, top_k=0),
     # resident kernel: fp32 with top-k filtering
