@@ -50,7 +50,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_rows_kernel_b256_g7_v128256
 TRAFFIC_UNIT = "chain_rows.cu"
 # kernels the library launches per chain call on this workload: rows, decide,
 # weights, search, precise jobs, precise search
-LAUNCHES_PER_STEP = 6
+LAUNCHES_PER_STEP = 3  # rows kernel, draw kernel, precise kernel
 # --op filters: top-p and min-p of every sequence (both sides); the resident
 # kernel and the precise redraw kernel run
 FILTER_TOP_P, FILTER_MIN_P = 0.9, 0.05

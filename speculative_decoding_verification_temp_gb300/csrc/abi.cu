@@ -116,10 +116,11 @@ bool make_stream_plan(long long V, int esize, StreamPlan &sp) {
 // (arrival counters, the weight-task queue and its counters) come first and
 // are cleared by every call; everything after them is written before it is
 // read within a call.
-// Chain path (rows -> decide -> weights -> search -> precise kernels): 32 KB
-// chunks through a ring of two slots (three rows-kernel CTAs per SM); every
-// row's chunks leave one record per consumer warp; the draw search works in
-// 256-entry steps.
+// Chain path (rows kernel -> draw kernel -> precise kernel): 32 KB chunks
+// through a ring of two slots (three rows-kernel CTAs per SM); every row's
+// chunks leave one record per consumer warp; the draw works in 256-entry
+// steps, whose sums the draw and precise kernels keep in shared memory (4 and
+// 16 bytes a step: at most kPassMaxSteps).
 struct PassPlan {
   int chunk_elems;
   int cpr;
@@ -129,41 +130,30 @@ struct PassPlan {
 };
 
 constexpr int kPassMaxGamma = 31;
+constexpr long long kPassMaxSteps = 8192;  // V <= 2,097,152
 
 bool make_pass_plan(long long V, int esize, int gamma, PassPlan &pp) {
   if (gamma > kPassMaxGamma || esize <= 0) return false;
+  const long long steps = (V + 255) / 256;
+  if (steps > kPassMaxSteps) return false;
   pp.slot_bytes = 32 * 1024;
   pp.ring = 2;  // three CTAs of the rows kernel per SM
   pp.chunk_elems = pp.slot_bytes / esize;
   pp.cpr = static_cast<int>((V + pp.chunk_elems - 1) / pp.chunk_elems);
-  pp.steps = static_cast<int>((V + 255) / 256);
+  pp.steps = static_cast<int>(steps);
   return true;
 }
 
-// Draw-search steps per row of the chain path (0: it cannot run the shape).
-long long pass_steps(long long V, int esize, int gamma) {
-  PassPlan pp{};
-  return make_pass_plan(V, esize, gamma, pp) ? pp.steps : 0;
-}
-
 // 64-bit records the chain rows kernel writes for B sequences of gamma drafts
-// (one per consumer warp per chunk).
+// (one per consumer warp per chunk; 0 when the chain path cannot run the shape).
 long long pass_records(long long B, int gamma, long long V, int esize) {
   PassPlan pp{};
   if (!make_pass_plan(V, esize, gamma, pp)) return 0;
   return B * (2 * gamma + 1) * static_cast<long long>(pp.cpr) * sv::chain_records_per_chunk();
 }
 
-// Rows of the chain path (2 gamma + 1 per sequence; 0 when it cannot run).
-long long chain_rows(long long B, int gamma, long long V, int esize) {
-  PassPlan pp{};
-  if (!make_pass_plan(V, esize, gamma, pp)) return 0;
-  return B * (2 * gamma + 1);
-}
-
 struct Layout {
-  size_t wq_ctr, counters, unit_done, w_done, wq, srec, err, sctr, near_list, pctr, zero_bytes;
-  size_t pseq, fstep, pstep, ppart;
+  size_t wq_ctr, counters, unit_done, w_done, wq, srec, err, pctr, pseq, near_list, zero_bytes;
   size_t outs, stats, final_unit, first_child, refine, rpart, rc, partials, dstate, wpart, wblk, total;
   long long wq_cap;
 };
@@ -171,12 +161,9 @@ struct Layout {
 constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
 // slices: slices per unit of the streaming kernel, 0 when only the resident
-// kernel can run the shape; recs, rows: records and rows of the chain path;
-// psteps: its draw-search steps per row (0 when the chain path cannot run the
-// shape).
-Layout layout(long long nseq, long long units, long long slices, long long recs, long long rows,
-              long long psteps) {
-  const long long pseqs = psteps ? nseq : 0;
+// kernel can run the shape; recs: records of the chain path (0 when it cannot
+// run the shape).
+Layout layout(long long nseq, long long units, long long slices, long long recs) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -191,7 +178,7 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
   L.wq_ctr = take(8 * sizeof(uint32_t));
   L.counters = take(static_cast<size_t>(nseq) * sizeof(uint32_t));
   L.err = take(sizeof(uint32_t));
-  const size_t zero_base = off;
+  L.pctr = take(4 * sizeof(uint32_t));  // chain path: precise redraws queued
   // zero prefix, streaming kernel
   L.unit_done = take(static_cast<size_t>(slices ? units : 0) * sizeof(uint32_t));
   L.w_done = take(static_cast<size_t>(slices ? units : 0) * sizeof(uint32_t));
@@ -200,12 +187,6 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
   // final draw at each node), one entry per slice
   L.wq_cap = 3 * units * slices;
   L.wq = take(static_cast<size_t>(L.wq_cap) * sizeof(int4));
-  const size_t zero_stream = off;
-  // zero prefix, chain path: the arrival counters
-  off = zero_base;
-  L.sctr = take(static_cast<size_t>(pseqs) * 4 * sizeof(uint32_t));
-  L.pctr = take(4 * sizeof(uint32_t));
-  off = std::max(off, zero_stream);
   L.zero_bytes = off;
   // common
   L.outs = take(static_cast<size_t>(units) * sizeof(sv::UnitOut));
@@ -223,15 +204,14 @@ Layout layout(long long nseq, long long units, long long slices, long long recs,
   L.wpart = take(static_cast<size_t>(units * slices) * sizeof(float));
   L.wblk = take(static_cast<size_t>(units * slices * kMaxSliceBlocks) * sizeof(float));
   const size_t end_stream = off;
-  // chain path: written before they are read within a call (the records by
-  // the rows kernel, read by the decide kernel after it)
+  // chain path: the records, written by the rows kernel before the draw
+  // kernel reads them; the queue of precise redraws, written by the draw
+  // kernel before the precise kernel reads it
   off = base;
+  const long long qseqs = recs ? nseq : 0;
   L.srec = take(static_cast<size_t>(recs) * sizeof(unsigned long long));
-  L.pseq = take(static_cast<size_t>(pseqs) * sizeof(sv::PassSeq));
-  L.near_list = take(static_cast<size_t>(pseqs) * sizeof(int32_t));
-  L.fstep = take(static_cast<size_t>(pseqs * psteps) * sizeof(float));
-  L.pstep = take(static_cast<size_t>(pseqs * psteps) * 2 * sizeof(float2));
-  L.ppart = take(static_cast<size_t>(pseqs) * sv::kPassPreciseJobs * 2 * sizeof(float2));
+  L.pseq = take(static_cast<size_t>(qseqs) * sizeof(sv::PassSeq));
+  L.near_list = take(static_cast<size_t>(qseqs) * sizeof(int32_t));
   L.total = std::max(off, end_stream);
   return L;
 }
@@ -268,8 +248,8 @@ int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0)
 
 // Shared launch path of the chain and tree verifiers.  16-byte aligned rows
 // without top-k, top-p or min-p filtering take the streaming chain path
-// (chains of gamma <= 31: rows, decide, weights, search and precise kernels)
-// or the streaming kernel (trees, longer chains); everything else the
+// (chains of gamma <= 31 and V <= 2,097,152: the rows, draw and precise
+// kernels) or the streaming kernel (trees, longer chains); everything else the
 // resident kernel.
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                       float *out_residual, void *workspace, size_t workspace_bytes,
@@ -293,15 +273,12 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   const bool chain = P.mode == sv::kModeChain;
   const size_t promised =
       layout(P.nseq, n_units, stream_slices(P.V, esize),
-             chain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0,
-             chain ? chain_rows(P.nseq, P.gamma, P.V, esize) : 0,
-             chain ? pass_steps(P.V, esize, P.gamma) : 0)
+             chain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0)
           .total;
   if (workspace_bytes < promised) return SPEC_ERR_INVALID_ARG;
   const long long rows = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) : 0;
   const long long recs = rows * pp.cpr * sv::chain_records_per_chunk();
-  const Layout L =
-      layout(P.nseq, n_units, streaming ? sp.slices : 0, recs, rows, pass ? pp.steps : 0);
+  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
   cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, stream);
@@ -325,10 +302,6 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.steps = pp.steps;
     P.srec = reinterpret_cast<unsigned long long *>(ws + L.srec);
     P.pseqw = reinterpret_cast<unsigned long long *>(ws + L.pseq);
-    P.sctr = reinterpret_cast<uint32_t *>(ws + L.sctr);
-    P.fstep = reinterpret_cast<unsigned long long *>(ws + L.fstep);
-    P.pstep = reinterpret_cast<double *>(ws + L.pstep);
-    P.ppart = reinterpret_cast<double *>(ws + L.ppart);
     P.near_list = reinterpret_cast<int32_t *>(ws + L.near_list);
     P.pctr = reinterpret_cast<uint32_t *>(ws + L.pctr);
     P.first_wait = g_first_wait.load(std::memory_order_relaxed);
@@ -439,15 +412,14 @@ size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtyp
   const int esize = esize_of(dtype);
   if (B < 0 || gamma < 0 || V < 1 || esize == 0) return 0;
   return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize),
-                pass_records(B, gamma, V, esize), chain_rows(B, gamma, V, esize),
-                pass_steps(V, esize, gamma))
+                pass_records(B, gamma, V, esize))
       .total;
 }
 
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
-  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0, 0, 0).total;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0).total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

@@ -83,10 +83,14 @@ constexpr float kLn2Lo = static_cast<float>(kLn2d - static_cast<double>(kLn2Hi))
 //   2^t = 2^(n div 64) * 2^((n mod 64)/64) * e^(r ln 2), the middle factor
 //   from the table and e^y = 1 + y + y^2/2 + ... + y^5/120 for |y| < 0.006
 //   (truncation below 1e-15), the terms after y carried in single precision.
-// Results below 2^-126 flush to zero.
+// Results below 2^-126 flush to zero.  Branch-free (the out-of-range case is
+// computed on a stand-in argument and selected away), so that the compiler can
+// interleave the independent evaluations of an unrolled loop.
 __device__ __forceinline__ Df df_exp2(Df t, const float *tab_hi, const float *tab_lo) {
-  const float nf = rintf(__fmul_rn(t.hi, 64.f));
-  if (!(nf >= -64.f * 126.f)) return Df{0.f, 0.f};  // also -inf and NaN
+  const float nf0 = rintf(__fmul_rn(t.hi, 64.f));
+  const bool under = !(nf0 >= -64.f * 126.f);  // also -inf and NaN
+  if (under) t = Df{0.f, 0.f};
+  const float nf = under ? 0.f : nf0;
   const float rh = fmaf(nf, -0.015625f, t.hi);  // exact: t.hi - nf / 64
   float r_hi, r_lo;
   two_sum(rh, t.lo, r_hi, r_lo);
@@ -111,8 +115,8 @@ __device__ __forceinline__ Df df_exp2(Df t, const float *tab_hi, const float *ta
   const float tail = __fadd_rn(__fadd_rn(se, pe), fmaf(Th, lo, fmaf(Tl, yh, Tl)));
   Df r = df_norm(s, tail);
   const float scale = __int_as_float((e + 127) << 23);  // 2^e, -126 <= e <= 0
-  r.hi = __fmul_rn(r.hi, scale);
-  r.lo = __fmul_rn(r.lo, scale);
+  r.hi = under ? 0.f : __fmul_rn(r.hi, scale);
+  r.lo = under ? 0.f : __fmul_rn(r.lo, scale);
   return r;
 }
 

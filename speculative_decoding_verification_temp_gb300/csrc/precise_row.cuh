@@ -31,14 +31,18 @@ __device__ __forceinline__ HpRow hp_row(const RowDesc &d, float T) {
 }
 
 // exp((z - max) / T) as a double-float; 0 below the top-k threshold.
+// Branch-free like df_exp2 (an excluded entry is computed as z = max and
+// selected away).
 __device__ __forceinline__ Df hp_exp(const HpRow &r, float z, const float *th, const float *tl) {
-  if (!(z > -INFINITY) || z < r.thr) return Df{0.f, 0.f};
+  const bool zero = !(z > -INFINITY) || z < r.thr;
+  const float zz = zero ? r.m : z;
   float dh, dl;
-  two_sum(z, -r.m, dh, dl);  // z - max exactly
+  two_sum(zz, -r.m, dh, dl);  // z - max exactly
   const float t_hi = __fmul_rn(dh, r.khi);
   const float t_lo =
       __fadd_rn(fmaf(dh, r.khi, -t_hi), fmaf(dh, r.klo, __fmul_rn(dl, r.khi)));
-  return df_exp2(df_norm(t_hi, t_lo), th, tl);
+  const Df v = df_exp2(df_norm(t_hi, t_lo), th, tl);
+  return zero ? Df{0.f, 0.f} : v;
 }
 
 // Logits of the 8 entries from `base` (a multiple of 8); -inf at or past `end`.

@@ -1,42 +1,34 @@
-// Chain verification as four stream-ordered kernels (rows 16-byte aligned,
-// no top-k, gamma <= 31).
+// Chain verification (rows 16-byte aligned, no row filters, gamma <= 31) as
+// two stream-ordered kernels.  No CTA waits on another CTA's progress except
+// at the cluster barriers of one sequence's cluster.
 //
-// No kernel here waits on another CTA's progress.  Hand-offs between CTAs are
-// kernel boundaries, plus one per-sequence arrival counter in the weights
-// kernel: each slice stores its totals, fences (release), and adds one to the
-// counter; the slice whose add completes the count fences again (acquire) and
-// searches.
-//
-//  1. rows kernel (the HBM stream).  Every logit row of the batch - the
-//     gamma + 1 target rows and the gamma draft rows of each sequence - is cut
-//     into 32 KB chunks, numbered sequence-major and handed out round-robin
-//     over a persistent grid.  In each CTA one producer warp streams its chunks
-//     into a ring of shared-memory slots with bulk asynchronous copies
-//     (cp.async.bulk, one "full" and one "empty" mbarrier per slot); eight
-//     consumer warps reduce each chunk to one 64-bit record per warp: the
-//     (max, sum of 2^((z - max) k)) of a sampling row, k = log2(e) / T, or the
-//     (finite max, lowest index + 1) of a greedy row.  Every logit is read from
-//     HBM once and costs one exponential; nothing else happens on this path.
-//  2. decide kernel, one CTA per sequence: a warp per row merges the row's
-//     records into its softmax normaliser (or argmax); one warp then runs the
-//     acceptance tests of all gamma positions at once (u < min(1, p/q), one
-//     lane each, Philox uniforms), finds the first rejection j with a ballot,
-//     and either writes the outputs (a one-hot draw needs no weights) or leaves
-//     the draw's description.
-//  3. weights kernel, persistent: work items are (sequence, slice); a producer
-//     warp copies the slice of the draw row(s) into a ring of shared-memory
-//     slots, eight warps sum the draw weights per 256-entry step ([p_j - q_j]_+
-//     for a correction, p_gamma for the bonus).  The last slice of a sequence
-//     to finish finds the step holding u * W by a prefix over the step totals,
-//     scans it, and writes the outputs.  A draw that lands within the
-//     single-precision error bound of a CDF boundary is queued.
-//  4. precise kernel.  Each queued draw is recomputed with double-float
-//     weights, split into pj jobs over its steps; the last job of a draw
-//     searches and overwrites the token.
+//  1. rows kernel (chain_rows.cu), the HBM stream.  Every logit row of the
+//     batch - the gamma + 1 target rows and the gamma draft rows of each
+//     sequence - is cut into 32 KB chunks, streamed once through shared memory
+//     by bulk asynchronous copies, and reduced to one 64-bit record per warp
+//     per chunk: (max, sum of 2^((z - max) k)) of a sampling row,
+//     k = log2(e) / T, or (finite max, lowest index + 1) of a greedy row.
+//  2. draw kernel (this file), one cluster of C CTAs per sequence.  Every CTA
+//     of the cluster merges the sequence's records into softmax normalisers
+//     (or argmaxes), runs the acceptance tests of all gamma positions at once
+//     (u < min(1, p/q), one lane each, Philox uniforms) and finds the first
+//     rejection j with a ballot: the same deterministic arithmetic in every
+//     CTA, so they agree without exchanging anything.  A one-hot draw needs
+//     no weights and CTA 0 writes the outputs.  Otherwise CTA r sums the draw
+//     weights ([p_j - q_j]_+ for a correction, p_gamma for the bonus) over
+//     its 1/C share of the 256-entry steps, the step totals are gathered into
+//     every CTA through distributed shared memory, and each CTA finds the step
+//     holding u * W by a double-float prefix and scans it; CTA 0 writes the
+//     outputs.  A draw within 1e-6 W of a CDF boundary, closer than the
+//     single-precision error of the sums, is redrawn by the same cluster in
+//     double-float arithmetic: per-CTA double-float step sums, the exact
+//     normaliser ratio from the gathered shares, a double-float search in
+//     CTA 0.
 //
 // Exponent arithmetic: 2^((z - m) k) with z - m computed exactly (one rounding
 // in the product), in the records, the merge, the acceptance test and the draw
 // alike, so the normalisers and the draw weights share their scale.
+#include <algorithm>
 #include <mutex>
 
 #include "ops.cuh"
@@ -48,24 +40,19 @@ cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStrea
 
 namespace {
 
-constexpr int kKWarps = 16;                            // decide kernel
-constexpr int kKThreads = kKWarps * 32;
-constexpr int kWWarps = 8;                             // weights kernel: compute warps
-constexpr int kWThreads = (kWWarps + 1) * 32;          // + the producer warp
-constexpr int kWRing = 4;
-constexpr int kDWarps = kWWarps;
-constexpr int kDThreads = kWWarps * 32;                // threads of a search
-constexpr int kQThreads = 128;                         // precise kernel
-constexpr int kQWarps = kQThreads / 32;
+constexpr int kDWarps = 4;                   // draw kernel
+constexpr int kDThreads = kDWarps * 32;
+constexpr int kDrawCluster = 4;              // CTAs per sequence (fewer when the row is short)
+constexpr int kDrawRecords = 2048;           // records a draw CTA stages in shared memory
+constexpr int kPWarps = 16;                  // precise kernel
+constexpr int kPThreads = kPWarps * 32;
+constexpr int kPreciseCluster = 8;           // CTAs per queued draw (fewer when it cannot run)
+constexpr int kPreciseGrid = 32;             // clusters of the precise kernel (queued draws stride)
 constexpr int kStep = 256;  // entries per draw-search step
 constexpr int kCMaxGamma = 31;
 constexpr int kCMaxRows = 2 * kCMaxGamma + 1;
 constexpr uint32_t kNoIndex = 0x3FFFFFFFu;  // record index: no finite entry
 constexpr uint32_t kBadBit = 0x80000000u;   // record index bit: NaN or +inf seen
-
-__device__ __forceinline__ void mbar_arrive1_c(unsigned long long *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // Double-float helpers (FP32 operations only: GB300's FP64 rate is far below
 // its FP32 rate).
@@ -85,15 +72,6 @@ __device__ __forceinline__ Df df_warp_sum(Df a) {
 }
 // a > b for normalised double-floats
 __device__ __forceinline__ bool df_gt(Df a, Df b) { return df_sub(a, b).hi > 0.f; }
-__device__ __forceinline__ Df ld_df(const float2 *p) {
-  const float2 v = __ldcg(p);
-  return Df{v.x, v.y};
-}
-// from shared memory when staged, else from global memory
-__device__ __forceinline__ Df ld_dfs(const float2 *p, bool staged) {
-  if (staged) return Df{p->x, p->y};
-  return ld_df(p);
-}
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel in the stream finishes;
@@ -107,8 +85,8 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Barrier over the compute warps of the weights kernel (named barrier 1).
-__device__ __forceinline__ void wsync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier over the draw kernel's CTA (named barrier 1, all kDThreads threads).
+__device__ __forceinline__ void wsync() { asm volatile("bar.sync 1, %0;" ::"n"(kDThreads) : "memory"); }
 
 // ---------------------------------------------------------------------------
 // 1. rows kernel: chain_rows.cu
@@ -138,7 +116,7 @@ __device__ __forceinline__ void load_vec<float>(const float *s, float z[8]) {
 }
 
 // ---------------------------------------------------------------------------
-// 2. decide kernel
+// 2. draw kernel: the decision
 // ---------------------------------------------------------------------------
 
 // 2^((z - m) k): the exponent form every step of the chain path uses.
@@ -272,24 +250,24 @@ __device__ void write_outputs(const Params &P, int s, const PassSeq &ps, int tok
 }
 
 // The merged record of row r of sequence seq (one warp; the value in every
-// lane): the rows kernel stored all of the row's records before this kernel.
-__device__ unsigned long long merge_row(const Params &P, int seq, int r) {
+// lane) from the row's R records at `rec` (global memory, or a shared-memory
+// copy): the rows kernel stored all of them before this kernel.
+__device__ unsigned long long merge_row(const Params &P, int seq, int r,
+                                        const unsigned long long *rec, bool shared) {
   const int lane = threadIdx.x & 31;
-  const int rps = 2 * P.gamma + 1;
   const bool draft = r > P.gamma;
   const float T = __ldg((draft ? P.Tq : P.Tp) + seq);
   const bool arg = row_is_arg(T);
   const float k = arg ? 0.f : kLog2e / T;
   const int R = P.cpr * kChainRecordsPerChunk;
-  const unsigned long long *rec =
-      P.srec + (static_cast<long long>(seq) * rps + r) * static_cast<long long>(R);
   float m = -INFINITY, S = 0.f, bv = -INFINITY;
   uint32_t bi = kNoIndex;
   int bad = 0;
   for (int x0 = lane; x0 < R; x0 += 4 * 32) {
     unsigned long long b[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) b[i] = x0 + i * 32 < R ? __ldcg(rec + x0 + i * 32) : 0ull;
+    for (int i = 0; i < 4; ++i)
+      b[i] = x0 + i * 32 < R ? (shared ? rec[x0 + i * 32] : __ldcg(rec + x0 + i * 32)) : 0ull;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if (x0 + i * 32 >= R) continue;
@@ -334,14 +312,40 @@ __device__ unsigned long long merge_row(const Params &P, int seq, int r) {
   return static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
 }
 
-// Decide sequence seq from its rows' records (one warp): the acceptance
-// tests, the first rejection j, and either the outputs (a one-hot draw needs
-// no weights) or the draw's description for the weights kernel.
+// What the decision of sequence seq reads from the inputs alone (one warp,
+// lane i: draft position i), loaded before the rows kernel has finished.
+struct DecideIn {
+  float Tp, Tq;
+  int x;         // draft token of position i
+  float zp, zq;  // logits of x in target row i and draft row i (0 when x is not valid)
+  float ua, ud;  // acceptance and draw uniforms of position i
+};
+
 template <typename TE>
-__device__ void decide_seq(const Params &P, int seq, const unsigned long long *rr) {
+__device__ DecideIn decide_inputs(const Params &P, int seq) {
+  const int i = threadIdx.x & 31;
+  const int gamma = P.gamma, V = P.V;
+  DecideIn in;
+  in.Tp = __ldg(P.Tp + seq);
+  in.Tq = __ldg(P.Tq + seq);
+  in.x = i < gamma ? __ldg(P.tokens + static_cast<long long>(seq) * gamma + i) : -1;
+  const bool valid = i < gamma && in.x >= 0 && in.x < V;
+  in.zp = valid ? to_f32(chain_row<TE>(P, seq, i)[in.x]) : 0.f;
+  in.zq = valid ? to_f32(chain_row<TE>(P, seq, gamma + 1 + i)[in.x]) : 0.f;
+  in.ua = i < gamma ? unit_uniform(P, seq, i, 0) : 0.f;
+  in.ud = i <= gamma ? unit_uniform(P, seq, i, 1) : 0.f;
+  return in;
+}
+
+// Decide sequence seq from its rows' records (one warp): the acceptance
+// tests, the first rejection j, and the draw's description in `out` (lane 0).
+// A one-hot draw needs no weights: the writer CTA writes its outputs.
+template <typename TE>
+__device__ void decide_seq(const Params &P, int seq, const unsigned long long *rr,
+                           const DecideIn &in, bool writer, PassSeq &out) {
   const int lane = threadIdx.x & 31;
   const int gamma = P.gamma, V = P.V;
-  const float Tp = __ldg(P.Tp + seq), Tq = __ldg(P.Tq + seq);
+  const float Tp = in.Tp, Tq = in.Tq;
   const bool p_arg = row_is_arg(Tp), q_arg = row_is_arg(Tq);
   const bool tp_bad = !(Tp >= 0.f) || Tp == INFINITY, tq_bad = !(Tq >= 0.f) || Tq == INFINITY;
   const float kp = p_arg ? 0.f : kLog2e / Tp, kq = q_arg ? 0.f : kLog2e / Tq;
@@ -368,7 +372,7 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
   uint32_t f = 0u;
   bool reject = true;
   if (i < gamma) {
-    const int x = __ldg(P.tokens + static_cast<long long>(seq) * gamma + i);
+    const int x = in.x;
     f = dp.flags;
     const bool valid = x >= 0 && x < V;
     if (!valid) f |= SPEC_FLAG_BAD_TOKEN;
@@ -377,23 +381,19 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
     } else {
       f |= dq.flags;
       if (valid) {
-        const TE *gp = chain_row<TE>(P, seq, i);
-        const TE *gq = chain_row<TE>(P, seq, gamma + 1 + i);
-        const float px = pprob(dp, to_f32(gp[x]), x);
-        const float qx = pprob(dq, dq.onehot ? 0.f : to_f32(gq[x]), x);
+        const float px = pprob(dp, in.zp, x);
+        const float qx = pprob(dq, dq.onehot ? 0.f : in.zq, x);
         if (!(qx > 0.f)) {
           f |= SPEC_FLAG_ZERO_Q;
         } else {
-          const float uu = unit_uniform(P, seq, i, 0);
-          reject = !(uu < fminf(1.f, px / qx));
+          reject = !(in.ua < fminf(1.f, px / qx));
         }
       }
     }
   }
   const unsigned rej = __ballot_sync(0xFFFFFFFFu, reject && i < gamma);
   const int j = rej ? __ffs(rej) - 1 : gamma;
-  const float ud = i <= gamma ? unit_uniform(P, seq, i, 1) : 0.f;
-  const float u_draw = __shfl_sync(0xFFFFFFFFu, ud, j);
+  const float u_draw = __shfl_sync(0xFFFFFFFFu, in.ud, j);
   uint32_t fo = warp_or(i < j ? f : 0u);
   fo |= __shfl_sync(0xFFFFFFFFu, i < gamma ? f : dp.flags, j);  // position j's flags
   const RowDesc djp = shfl_desc(dp, j);
@@ -401,14 +401,16 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
   if (lane == 0 && __ldcg(P.err)) {
     // a bounded wait of the rows kernel gave up: the documented fallback, no
     // accepted drafts and no tokens
-    const long long obase = static_cast<long long>(seq) * (gamma + 1);
-    for (int x = 0; x <= gamma; ++x) P.out_tokens[obase + x] = -1;
-    P.out_num[seq] = 0;
-    if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
-    P.final_unit[seq] = -1;
+    if (writer) {
+      const long long obase = static_cast<long long>(seq) * (gamma + 1);
+      for (int x = 0; x <= gamma; ++x) P.out_tokens[obase + x] = -1;
+      P.out_num[seq] = 0;
+      if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
+      P.final_unit[seq] = -1;
+    }
     PassSeq ps = {};
     ps.draw = 0;
-    reinterpret_cast<PassSeq *>(P.pseqw)[seq] = ps;
+    out = ps;
     return;
   }
   if (lane == 0) {
@@ -433,31 +435,14 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
       ps.residual = 0;
       ps.draw = 0;
       ps.u = 0.f;
-      write_outputs(P, seq, ps, ps.dp.a, 0.0, 0);
+      if (writer) write_outputs(P, seq, ps, ps.dp.a, 0.0, 0);
     }
-    reinterpret_cast<PassSeq *>(P.pseqw)[seq] = ps;  // read by the weights kernel
+    out = ps;
   }
-}
-
-// One CTA per sequence: a warp per row merges, warp 0 decides.
-template <typename TE>
-__global__ void __launch_bounds__(kKThreads) chain_decide_kernel(const Params P) {
-  __shared__ unsigned long long rr[kCMaxRows];
-  launch_dependents();
-  grid_dependency_wait();
-  const int seq = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rps = 2 * P.gamma + 1;
-  for (int r = warp; r < rps; r += kKWarps) {
-    const unsigned long long rec = merge_row(P, seq, r);
-    if (lane == 0) rr[r] = rec;
-  }
-  __syncthreads();
-  if (warp == 0) decide_seq<TE>(P, seq, rr);
 }
 
 // ---------------------------------------------------------------------------
-// 3. weights kernel
+// 3. draw kernel: the draw weights
 // ---------------------------------------------------------------------------
 
 // Eight consecutive logits held as loaded (16 or 32 bytes), converted on use.
@@ -557,183 +542,44 @@ __device__ __forceinline__ void step_weights(const TE *gp, const TE *gq, const R
 }
 
 // Totals of the draw weights of steps [b0, b1) (256 entries each) into
-// fst[step] (the whole CTA, one warp per step; full steps four per warp at a
-// time with their loads issued before any is used).
-template <typename TE>
+// fst[step] (the NW warps of the CTA, one warp per step; full steps four (bf16)
+// or two (fp32) per warp at a time with their loads issued before any is used).
+template <typename TE, int NW>
 __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const RowDesc &dq,
                             int residual, int V, int b0, int b1, float *fst) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  constexpr int kU = 4;
+  constexpr int kU = sizeof(TE) == 2 ? 4 : 2;  // 16 or 32 raw bytes a lane per step and row
   const int nfull = min(b1, V / kStep);
   int st0 = b0 + w;
   if (!dp.onehot && (!residual || !dq.onehot)) {
-    for (; st0 + (kU - 1) * kDWarps < nfull; st0 += kDWarps * kU) {
+    for (; st0 + (kU - 1) * NW < nfull; st0 += NW * kU) {
       Raw8<TE> rp[kU], rq[kU];
 #pragma unroll
       for (int q = 0; q < kU; ++q) {
-        const int base = (st0 + q * kDWarps) * kStep + lane * 8;
+        const int base = (st0 + q * NW) * kStep + lane * 8;
         rp[q].load(gp + base);
         if (residual) rq[q].load(gq + base);
       }
 #pragma unroll
       for (int q = 0; q < kU; ++q) {
-        const int base = (st0 + q * kDWarps) * kStep + lane * 8;
+        const int base = (st0 + q * NW) * kStep + lane * 8;
         float zp[8], zq[8], x[8];
         rp[q].get(zp);
         rq[q].get(zq);
         weights8(dp, dq, residual, base, zp, zq, x);
         float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
         sm = warp_sum(sm);
-        if (lane == 0) fst[st0 + q * kDWarps] = sm;
+        if (lane == 0) fst[st0 + q * NW] = sm;
       }
     }
   }
-  for (int st = st0; st < b1; st += kDWarps) {
+  for (int st = st0; st < b1; st += NW) {
     float x[8];
     step_weights<TE>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x);
     float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
     sm = warp_sum(sm);
     if (lane == 0) fst[st] = sm;
   }
-}
-
-// Step totals the draw search stages in shared memory (rows of up to
-// kSmemSteps * 256 entries; longer rows are searched from global memory).
-constexpr int kSmemSteps = 2048;
-
-struct DrawCtl {
-  double W;
-  int token;
-  float margin;
-  int is_last;
-  float tot[kSmemSteps];
-};
-
-// Inverse-CDF search over the step totals fst[0, nsteps) (the compute warps;
-// warp 0 works): a double-float prefix over the lanes' runs of steps finds the
-// step holding u * W, one warp scan of its weights the token.  The token goes
-// to ctl.token (-1: no positive weight), the total to ctl.W and the distance
-// of the draw from the nearer boundary of its token to ctl.margin.
-template <typename TE>
-__device__ void step_search(DrawCtl &ctl, const float *gst, int nsteps, const TE *gp,
-                            const TE *gq, const RowDesc &dp, const RowDesc &dq, int residual,
-                            int V, float u) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  // the totals in one coalesced pass
-  const bool staged = nsteps <= kSmemSteps;
-  if (staged)
-    for (int st0 = threadIdx.x; st0 < nsteps; st0 += 4 * kDThreads) {  // four loads in flight
-      float x[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) x[q] = st0 + q * kDThreads < nsteps ? __ldcg(gst + st0 + q * kDThreads) : 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (st0 + q * kDThreads < nsteps) ctl.tot[st0 + q * kDThreads] = x[q];
-    }
-  wsync();
-  const float *fst = staged ? ctl.tot : gst;
-  if (w == 0) {
-    const int per = (nsteps + 31) / 32;
-    const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
-    Df seg{0.f, 0.f};
-    int lastpos = -1;
-    for (int st = s0; st < s1; ++st) {
-      const float x = staged ? fst[st] : __ldcg(fst + st);
-      seg = df_add(seg, Df{x, 0.f});
-      if (x > 0.f) lastpos = st;
-    }
-    Df incl = seg;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const Df y = df_shfl_up(incl, off);
-      if (lane >= off) incl = df_add(incl, y);
-    }
-    const Df W = df_shfl(incl, 31);
-    const Df tt = df_mul(Df{u, 0.f}, W);
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, df_gt(incl, tt) && seg.hi > 0.f);
-    int step = -1;
-    float trel = 0.f;
-    bool exact = true;
-    if (hit) {
-      const int first = __ffs(hit) - 1;
-      if (lane == first) {
-        Df acc = df_sub(incl, seg);
-        for (int st = s0; st < s1; ++st) {
-          const float x = staged ? fst[st] : __ldcg(fst + st);
-          const Df nx = df_add(acc, Df{x, 0.f});
-          if (df_gt(nx, tt) && x > 0.f) {
-            step = st;
-            const Df r = df_sub(tt, acc);
-            trel = r.hi + r.lo;
-            break;
-          }
-          acc = nx;
-        }
-        if (step < 0) {
-          step = lastpos;
-          exact = false;
-        }
-      }
-      step = __shfl_sync(0xFFFFFFFFu, step, first);
-      trel = __shfl_sync(0xFFFFFFFFu, trel, first);
-      exact = __shfl_sync(0xFFFFFFFFu, exact ? 1 : 0, first) != 0;
-    } else {
-      step = warp_max_i(lastpos);
-      exact = false;
-    }
-    int token = -1;
-    float margin = 0.f;
-    if (step >= 0) {
-      const float tr = trel;
-      const int base = step * kStep + lane * 8;
-      float x[8];
-      step_weights<TE>(gp, gq, dp, dq, residual, base, V, x);
-      float sm = 0.f;
-      int lp = -1;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sm += x[e];
-        if (x[e] > 0.f) lp = base + e;
-      }
-      float fin = sm;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xFFFFFFFFu, fin, off);
-        if (lane >= off) fin += y;
-      }
-      const float excl = fin - sm;
-      const unsigned h2 = exact ? __ballot_sync(0xFFFFFFFFu, fin > tr && sm > 0.f) : 0u;
-      if (h2) {
-        const int first = __ffs(h2) - 1;
-        int found = -1;
-        float mg = 0.f;
-        if (lane == first) {
-          float run = excl;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float prev = run;
-            run += x[e];
-            if (found < 0 && x[e] > 0.f && run > tr) {
-              found = base + e;
-              mg = fminf(tr - prev, run - tr);
-            }
-          }
-          if (found < 0) found = lp;
-        }
-        token = __shfl_sync(0xFFFFFFFFu, found, first);
-        margin = __shfl_sync(0xFFFFFFFFu, mg, first);
-      } else {
-        token = warp_max_i(lp);
-        margin = 0.f;
-      }
-    }
-    if (lane == 0) {
-      ctl.W = static_cast<double>(W.hi) + static_cast<double>(W.lo);
-      ctl.token = token;
-      ctl.margin = margin;
-    }
-  }
-  wsync();
 }
 
 // Rows of a sequence's draw position j.
@@ -746,195 +592,299 @@ __device__ __forceinline__ void draw_rows(const Params &P, int s, int j, const T
       P.draft, static_cast<long long>(s) * P.gamma + (j < P.gamma ? j : 0), P.ld_d, sizeof(TE)));
 }
 
-// One work item of the weights kernel in a ring slot: a slice of a draw's
-// row(s), with the draw's description.
-struct WItem {
-  PassSeq ps;
-  int seq;
-  int b0, b1;  // steps of the slice
-  int nb;      // entries of the slice copied to shared memory (the rest: global)
-  int pad[3];
-};
-
-struct WCtl {
-  unsigned long long full[kWRing];
-  unsigned long long empty[kWRing];
-  WItem item[kWRing];
-};
-
-// Totals of the draw weights of the slice's steps from the slot (entries past
-// nb, fewer than 8 at the row's end, from global memory) into fst[step].
+// Double-float weights of the 8 entries from `base` (precise redraw).  Runs
+// once per call site and step, so the entry loop stays rolled: unrolled, its
+// code would come from the instruction cache's misses.
 template <typename TE>
-__device__ void slot_step_totals(const TE *sp, const TE *sq, const TE *gp, const TE *gq,
-                                 const WItem &it, int V, float *fst) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const PassSeq &ps = it.ps;
-  const int v0 = it.b0 * kStep;
-  for (int st = it.b0 + w; st < it.b1; st += kWWarps) {
-    const int base = st * kStep + lane * 8;  // vocabulary index
-    const int e = base - v0;                 // slot index
-    float x[8];
-    if (e + 8 <= it.nb && !ps.dp.onehot && (!ps.residual || !ps.dq.onehot)) {
-      float zp[8], zq[8];
-      load_vec<TE>(sp + e, zp);
-      if (ps.residual) load_vec<TE>(sq + e, zq);
-      else
-#pragma unroll
-        for (int q = 0; q < 8; ++q) zq[q] = 0.f;
-      weights8(ps.dp, ps.dq, ps.residual, base, zp, zq, x);
-    } else {
-      step_weights<TE>(gp, gq, ps.dp, ps.dq, ps.residual, base, V, x);
+__device__ __forceinline__ void pweights8(const TE *gp, const TE *gq, const HpRow &rp,
+                                          const HpRow &rq, int residual, Df rho, int base, int V,
+                                          bool vec, const float *th, const float *tl,
+                                          Df w[8]) {
+  float zp[8], zq[8];
+  hp_load8<TE>(gp, base, V, vec, zp);
+  if (residual) hp_load8<TE>(gq, base, V, vec, zq);
+#pragma unroll 1
+  for (int e = 0; e < 8; ++e) {
+    const Df ep = hp_exp(rp, zp[e], th, tl);
+    if (!residual || ep.hi == 0.f) {
+      w[e] = ep;
+      continue;
     }
-    float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-    sm = warp_sum(sm);
-    if (lane == 0) fst[st] = sm;
+    const Df eq = hp_exp(rq, zq[e], th, tl);
+    const Df d = df_sub(ep, df_mul(rho, eq));
+    w[e] = d.hi > 0.f ? d : Df{0.f, 0.f};
   }
 }
 
-// Persistent: item k (sequence k / wj, slice k % wj) goes to CTA k mod grid.
+// ---------------------------------------------------------------------------
+// 3. draw kernel: the search
+// ---------------------------------------------------------------------------
+
+// Shared state of a draw-kernel CTA (the step totals are dynamic shared
+// memory: see chain_draw_kernel).
+struct DrawShared {
+  unsigned long long rr[kCMaxRows];  // merged row records
+  PassSeq ps;                        // the draw's description
+  DecideIn in[32];                   // the decision's inputs, one per lane of warp 0
+  Df wsum[kDWarps];                  // search: per-warp sums of the step totals
+  int wlast[kDWarps];                // search: per-warp last step with positive total
+  int wfirst[kDWarps];               // search: per-warp first thread whose run crosses u W
+  int step;
+  float trel;
+  int exact;
+  double W;
+  int token;
+  float margin;
+};
+
+// Inverse-CDF search over the step totals tot[0, nsteps) (the whole CTA): a
+// double-float prefix over the threads' runs of steps finds the step holding
+// u * W, one warp scan of its weights the token.  The token goes to sh.token
+// (-1: no positive weight), the total to sh.W and the distance of the draw
+// from the nearer boundary of its token to sh.margin.
 template <typename TE>
-__global__ void __launch_bounds__(kWThreads) chain_weights_kernel(const Params P) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  WCtl &ctl = *reinterpret_cast<WCtl *>(smem_raw);
-  unsigned char *ring = smem_raw + P.data_off;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int V = P.V, nsteps = P.steps, S = P.wj;
-  const long long total = static_cast<long long>(P.nseq) * S;
-  const int slot_bytes = P.slot_bytes;  // one slice of one row
-  launch_dependents();
-  grid_dependency_wait();
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kWRing; ++s) {
-      mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], kWWarps);
+__device__ void step_search(DrawShared &sh, const float *tot, int nsteps, const TE *gp,
+                            const TE *gq, const RowDesc &dp, const RowDesc &dq, int residual,
+                            int V, float u) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int per = (nsteps + kDThreads - 1) / kDThreads;
+  const int s0 = min(nsteps, t * per), s1 = min(nsteps, s0 + per);
+  Df seg{0.f, 0.f};
+  int lastpos = -1;
+  for (int st = s0; st < s1; ++st) {
+    const float x = tot[st];
+    seg = df_add(seg, Df{x, 0.f});
+    if (x > 0.f) lastpos = st;
+  }
+  Df incl = seg;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const Df y = df_shfl_up(incl, off);
+    if (lane >= off) incl = df_add(incl, y);
+  }
+  const int wl = warp_max_i(lastpos);
+  if (lane == 31) sh.wsum[w] = incl;
+  if (lane == 0) sh.wlast[w] = wl;
+  wsync();
+  // the warps' sums in a fixed order: every thread gets the same total
+  Df base{0.f, 0.f}, W{0.f, 0.f};
+  int last = -1;
+#pragma unroll
+  for (int x = 0; x < kDWarps; ++x) {
+    if (x == w) base = W;
+    W = df_add(W, sh.wsum[x]);
+    last = max(last, sh.wlast[x]);
+  }
+  incl = df_add(base, incl);
+  const Df tt = df_mul(Df{u, 0.f}, W);
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, df_gt(incl, tt) && seg.hi > 0.f);
+  if (lane == 0) sh.wfirst[w] = hit ? __ffs(hit) - 1 : 32;
+  wsync();
+  int first = -1;
+#pragma unroll
+  for (int x = kDWarps - 1; x >= 0; --x)
+    if (sh.wfirst[x] < 32) first = x * 32 + sh.wfirst[x];
+  if (first < 0) {
+    if (t == 0) {
+      sh.step = last;
+      sh.trel = 0.f;
+      sh.exact = 0;
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else if (t == first) {
+    Df acc = df_sub(incl, seg);
+    int step = -1;
+    float trel = 0.f;
+    for (int st = s0; st < s1; ++st) {
+      const float x = tot[st];
+      const Df nx = df_add(acc, Df{x, 0.f});
+      if (df_gt(nx, tt) && x > 0.f) {
+        step = st;
+        const Df r = df_sub(tt, acc);
+        trel = r.hi + r.lo;
+        break;
+      }
+      acc = nx;
+    }
+    sh.step = step < 0 ? lastpos : step;
+    sh.trel = trel;
+    sh.exact = step < 0 ? 0 : 1;
+  }
+  wsync();
+  if (w == 0) {
+    const int step = sh.step;
+    const bool exact = sh.exact != 0;
+    int token = -1;
+    float margin = 0.f;
+    if (step >= 0) {
+      const float tr = sh.trel;
+      const int base8 = step * kStep + lane * 8;
+      float x[8];
+      step_weights<TE>(gp, gq, dp, dq, residual, base8, V, x);
+      float sm = 0.f;
+      int lp = -1;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sm += x[e];
+        if (x[e] > 0.f) lp = base8 + e;
+      }
+      float fin = sm;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, fin, off);
+        if (lane >= off) fin += y;
+      }
+      const float excl = fin - sm;
+      const unsigned h2 = exact ? __ballot_sync(0xFFFFFFFFu, fin > tr && sm > 0.f) : 0u;
+      if (h2) {
+        const int f2 = __ffs(h2) - 1;
+        int found = -1;
+        float mg = 0.f;
+        if (lane == f2) {
+          float run = excl;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float prev = run;
+            run += x[e];
+            if (found < 0 && x[e] > 0.f && run > tr) {
+              found = base8 + e;
+              mg = fminf(tr - prev, run - tr);
+            }
+          }
+          if (found < 0) found = lp;
+        }
+        token = __shfl_sync(0xFFFFFFFFu, found, f2);
+        margin = __shfl_sync(0xFFFFFFFFu, mg, f2);
+      } else {
+        token = warp_max_i(lp);
+        margin = 0.f;
+      }
+    }
+    if (lane == 0) {
+      sh.W = static_cast<double>(W.hi) + static_cast<double>(W.lo);
+      sh.token = token;
+      sh.margin = margin;
+    }
+  }
+  wsync();
+}
+
+// One cluster of C CTAs per sequence (grid: nseq * C CTAs), every CTA of the
+// cluster resident at once for the batches the path is built for.  Dynamic
+// shared memory: the step totals tot[steps] (CTA 0 gathers all of them) and
+// room for kDrawRecords row records.
+template <typename TE>
+__global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char draw_smem[];
+  __shared__ DrawShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int seq = static_cast<int>(blockIdx.x) / C;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nsteps = P.steps;
+  float *tot = reinterpret_cast<float *>(draw_smem);
+  unsigned long long *srec = reinterpret_cast<unsigned long long *>(
+      draw_smem + (static_cast<size_t>(nsteps) * sizeof(float) + 15) / 16 * 16);
+  // every CTA of the cluster has started before the first remote access: the
+  // arrive here pairs with the first wait below
+  cluster_arrive();
+  launch_dependents();
+  // the decision's inputs (tokens, their logits, the uniforms) do not depend
+  // on the rows kernel: CTA 0 loads them while it drains
+  if (rank == 0 && warp == 0) sh.in[lane] = decide_inputs<TE>(P, seq);
+  grid_dependency_wait();  // the rows kernel's records are visible
+  // 1. the decision.  CTA r merges rows r, r + C, ... (records staged in
+  // shared memory with all loads in flight at once when they fit) and puts
+  // the merged records into CTA 0, which decides and hands the draw's
+  // description to every CTA.
+  const int rps = 2 * P.gamma + 1;
+  const int R = P.cpr * kChainRecordsPerChunk;
+  const int nmine = rank < rps ? (rps - 1 - rank) / C + 1 : 0;  // rows rank, rank + C, ...
+  const int nrec = nmine * R;
+  const bool staged = nrec <= kDrawRecords;
+  if (staged) {
+    for (int x0 = threadIdx.x; x0 < nrec; x0 += 4 * kDThreads) {
+      unsigned long long b[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int x = x0 + q * kDThreads;
+        const int r = rank + (x / R) * C;
+        b[q] = x < nrec ? __ldcg(P.srec + (static_cast<long long>(seq) * rps + r) * R + x % R)
+                        : 0ull;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (x0 + q * kDThreads < nrec) srec[x0 + q * kDThreads] = b[q];
+    }
+    __syncthreads();
+  }
+  unsigned long long *rr0 = cluster.map_shared_rank(sh.rr, 0);
+  for (int k = warp; k < nmine; k += kDWarps) {
+    const int r = rank + k * C;
+    const unsigned long long *src =
+        staged ? srec + static_cast<long long>(k) * R
+               : P.srec + (static_cast<long long>(seq) * rps + r) * R;
+    const unsigned long long rec = merge_row(P, seq, r, src, staged);
+    if (lane == 0) sh.rr[r] = rec;  // staged locally, pushed after the first wait
   }
   __syncthreads();
-  if (warp == kWWarps) {
-    // producer: the item's description, then bulk copies of its slice; the
-    // next item's description is loaded while this one's slot is awaited
-    if (lane != 0) return;
-    int i = 0;
-    long long k = blockIdx.x;
-    PassSeq nxt;
-    if (k < total) nxt = reinterpret_cast<const PassSeq *>(P.pseqw)[k / S];
-    for (; k < total; k += gridDim.x, ++i) {
-      const PassSeq cur = nxt;
-      if (k + gridDim.x < total) nxt = reinterpret_cast<const PassSeq *>(P.pseqw)[(k + gridDim.x) / S];
-      const int slot = i % kWRing;
-      if (i >= kWRing) {
-        const uint32_t ph = static_cast<uint32_t>((i - kWRing) / kWRing) & 1u;
-        if (!mbar_wait_bounded(&ctl.empty[slot], ph)) atomicOr(P.err, 1u);
-      }
-      WItem &it = ctl.item[slot];
-      it.seq = static_cast<int>(k / S);
-      const int s = static_cast<int>(k - static_cast<long long>(it.seq) * S);
-      it.ps = cur;
-      it.b0 = s * P.wj_steps;
-      it.b1 = min(nsteps, it.b0 + P.wj_steps);
-      uint32_t bytes = 0u;
-      it.nb = 0;
-      if (cur.draw && it.b0 < it.b1) {
-        const TE *gp, *gq;
-        draw_rows<TE>(P, it.seq, cur.j, gp, gq);
-        const int v0 = it.b0 * kStep, v1 = min(V, it.b1 * kStep);
-        const uint32_t rb = static_cast<uint32_t>((v1 - v0) * sizeof(TE)) / 16u * 16u;
-        it.nb = static_cast<int>(rb / sizeof(TE));
-        unsigned char *dst = ring + static_cast<size_t>(slot) * 2 * slot_bytes;
-        bytes = cur.residual ? 2u * rb : rb;
-        mbar_arrive_expect_tx(&ctl.full[slot], bytes);
-        if (rb) {
-          bulk_g2s_plain(dst, gp + v0, rb, &ctl.full[slot]);
-          if (cur.residual) bulk_g2s_plain(dst + slot_bytes, gq + v0, rb, &ctl.full[slot]);
-        }
-      } else {
-        mbar_arrive_expect_tx(&ctl.full[slot], 0u);
-      }
+  cluster_wait();  // every CTA has started
+  if (rank != 0)
+    for (int k = threadIdx.x; k < nmine; k += kDThreads) rr0[rank + k * C] = sh.rr[rank + k * C];
+  cluster_sync_all();  // CTA 0 holds every merged record
+  if (rank == 0) {
+    if (warp == 0) decide_seq<TE>(P, seq, sh.rr, sh.in[lane], true, sh.ps);
+    __syncthreads();
+    // the description to every other CTA (as 32-bit words)
+    constexpr int kWords = static_cast<int>(sizeof(PassSeq) / 4);
+    static_assert(sizeof(PassSeq) % 4 == 0, "PassSeq is copied as 32-bit words");
+    for (int x = threadIdx.x; x < (C - 1) * kWords; x += kDThreads) {
+      const int r = 1 + x / kWords, k = x % kWords;
+      cluster.map_shared_rank(reinterpret_cast<uint32_t *>(&sh.ps), r)[k] =
+          reinterpret_cast<const uint32_t *>(&sh.ps)[k];
     }
-    const int issued = i;
-    for (int d = max(0, issued - kWRing); d < issued; ++d) {
-      const uint32_t ph = static_cast<uint32_t>(d / kWRing) & 1u;
-      if (!mbar_wait_bounded(&ctl.empty[d % kWRing], ph)) atomicOr(P.err, 1u);
-    }
-    return;
   }
-  int i = 0;
-  for (long long k = blockIdx.x; k < total; k += gridDim.x, ++i) {
-    const int slot = i % kWRing;
-    const uint32_t phase = static_cast<uint32_t>(i / kWRing) & 1u;
-    if (!mbar_wait_bounded(&ctl.full[slot], phase)) {
-      if (lane == 0) atomicOr(P.err, 1u);
-      mbar_wait_bounded(&ctl.full[slot], phase);  // do not leave a copy in flight
-    }
-    const WItem it = ctl.item[slot];
-    const int seq = it.seq;
-    const bool work = it.ps.draw && it.b0 < it.b1;
-    float *fst = reinterpret_cast<float *>(P.fstep) + static_cast<long long>(seq) * nsteps;
-    const TE *gp, *gq;
-    draw_rows<TE>(P, seq, it.ps.j, gp, gq);
-    if (work) {
-      const TE *sp = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * 2 * slot_bytes);
-      const TE *sq = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * 2 * slot_bytes +
-                                                  slot_bytes);
-      slot_step_totals<TE>(sp, sq, gp, gq, it, V, fst);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);  // the slot's data is no longer read
-  }
-}
-
-// One CTA per sequence, after the weights kernel: the inverse-CDF search over
-// the draw's step totals, the outputs, and the queue of draws for the precise
-// redraw.
-template <typename TE>
-__global__ void __launch_bounds__(kDThreads) chain_search_kernel(const Params P) {
-  __shared__ DrawCtl ctl;
-  launch_dependents();
-  grid_dependency_wait();
-  const int seq = blockIdx.x;
-  PassSeq ps = reinterpret_cast<const PassSeq *>(P.pseqw)[seq];
-  if (!ps.draw) return;  // the decide kernel wrote the outputs
-  if (__ldcg(P.err)) {
-    // a bounded wait of the weights kernel gave up: the step totals may be
-    // incomplete, so the draw gets the fallback outputs
-    if (threadIdx.x == 0) {
-      const long long obase = static_cast<long long>(seq) * (P.gamma + 1);
-      for (int x = 0; x <= P.gamma; ++x) P.out_tokens[obase + x] = -1;
-      P.out_num[seq] = 0;
-      if (P.out_flags) P.out_flags[seq] = SPEC_FLAG_TIMEOUT;
-      P.final_unit[seq] = -1;
-    }
-    return;
-  }
-  const int V = P.V, nsteps = P.steps;
-  float *fst = reinterpret_cast<float *>(P.fstep) + static_cast<long long>(seq) * nsteps;
+  cluster_sync_all();  // every CTA holds the description
+  PassSeq ps = sh.ps;
+  if (!ps.draw) return;  // CTA 0 wrote the outputs (every CTA returns here)
+  // 2. step totals of this CTA's steps, pushed into CTA 0's array
+  const int per = (nsteps + C - 1) / C;
+  const int b0 = min(nsteps, rank * per), b1 = min(nsteps, b0 + per);
   const TE *gp, *gq;
   draw_rows<TE>(P, seq, ps.j, gp, gq);
-  step_search<TE>(ctl, fst, nsteps, gp, gq, ps.dp, ps.dq, ps.residual, V, ps.u);
-  int token = ctl.token;
-  double W = ctl.W;
-  float margin = ctl.margin;
+  step_totals<TE, kDWarps>(gp, gq, ps.dp, ps.dq, ps.residual, P.V, b0, b1, tot);
+  __syncthreads();
+  if (rank != 0) {
+    float *dst = cluster.map_shared_rank(tot, 0);
+    for (int st = b0 + threadIdx.x; st < b1; st += kDThreads) dst[st] = tot[st];
+    cluster_arrive();  // release: CTA 0 reads the totals after its wait
+    return;
+  }
+  cluster_arrive();
+  cluster_wait();
+  // 3. the search (CTA 0)
+  step_search<TE>(sh, tot, nsteps, gp, gq, ps.dp, ps.dq, ps.residual, P.V, ps.u);
+  int token = sh.token;
+  double W = sh.W;
+  float margin = sh.margin;
   if (ps.residual && !(W > 0.0)) {
-    // degenerate residual: draw from p itself
+    // degenerate residual: draw from p itself (this CTA sums the whole row)
     ps.flags |= SPEC_FLAG_DEGENERATE_RESIDUAL;
     ps.residual = 0;
     ps.dq = ps.dp;
     ps.dq.onehot = 1;
     ps.dq.a = 0;
-    wsync();
-    step_totals<TE>(gp, gq, ps.dp, ps.dq, 0, V, 0, nsteps, fst);
-    wsync();
-    step_search<TE>(ctl, fst, nsteps, gp, gq, ps.dp, ps.dq, 0, V, ps.u);
-    token = ctl.token;
-    W = ctl.W;
-    margin = ctl.margin;
+    step_totals<TE, kDWarps>(gp, gq, ps.dp, ps.dq, 0, P.V, 0, nsteps, tot);
+    __syncthreads();
+    step_search<TE>(sh, tot, nsteps, gp, gq, ps.dp, ps.dq, 0, P.V, ps.u);
+    token = sh.token;
+    W = sh.W;
+    margin = sh.margin;
   }
   if (token < 0) token = ps.dp.a;  // no positive weight at all (not reachable with finite rows)
-  // redraw precisely when the draw came within 1e-6 of the draw mass of a
-  // boundary (the single-precision boundary error measured on 128K-entry rows
-  // stays below 3e-7 of it)
+  // a draw within 1e-6 of the draw mass of a boundary is queued for the
+  // precise kernel (the single-precision boundary error measured on
+  // 128K-entry rows stays below 3e-7 of it)
   const int near = margin < 1e-6f * static_cast<float>(W) ? 1 : 0;
   if (threadIdx.x == 0) {
     ps.W = static_cast<float>(W);
@@ -948,269 +898,70 @@ __global__ void __launch_bounds__(kDThreads) chain_search_kernel(const Params P)
 }
 
 // ---------------------------------------------------------------------------
-// 3. precise kernel
+// 4. precise kernel: one cluster per queued draw
 // ---------------------------------------------------------------------------
 
-// Step sums the precise search stages in shared memory (rows of up to
-// kQSmemSteps * 256 entries; longer rows are searched from global memory).
-constexpr int kQSmemSteps = 2048;
-
-struct QCtl {
+struct PreciseShared {
+  Df part[kPreciseCluster][2];  // every CTA's shares of S_p, S_q
+  Df pred[2][kPWarps];
   float tab_hi[64], tab_lo[64];
-  Df pred[2][kQWarps];
-  int red_i[kQWarps];
-  int redo;
-  float2 sa[kQSmemSteps], sb[kQSmemSteps];
 };
 
-// Double-float weights of the 8 entries from `base` (precise redraw).
-template <typename TE>
-__device__ __forceinline__ void pweights8(const TE *gp, const TE *gq, const HpRow &rp,
-                                          const HpRow &rq, int residual, Df rho, int base, int V,
-                                          bool vec, const QCtl &ctl, Df w[8]) {
-  float zp[8], zq[8];
-  hp_load8<TE>(gp, base, V, vec, zp);
-  if (residual) hp_load8<TE>(gq, base, V, vec, zq);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const Df ep = hp_exp(rp, zp[e], ctl.tab_hi, ctl.tab_lo);
-    if (!residual || ep.hi == 0.f) {
-      w[e] = ep;
-      continue;
-    }
-    const Df eq = hp_exp(rq, zq[e], ctl.tab_hi, ctl.tab_lo);
-    const Df d = df_sub(ep, df_mul(rho, eq));
-    w[e] = d.hi > 0.f ? d : Df{0.f, 0.f};
-  }
-}
-
-// Sum over the pj normaliser shares of sequence s (the same value in every
-// lane: lane-strided sums, a butterfly).
-__device__ __forceinline__ Df pshare_sum(const Params &P, int s, int which) {
-  const int lane = threadIdx.x & 31;
-  const float2 *x = reinterpret_cast<const float2 *>(P.ppart) + static_cast<long long>(s) * P.pj * 2 + which;
-  Df v{0.f, 0.f};
-  for (int k0 = 0; k0 < P.pj; k0 += 64) {  // two loads in flight per lane
-    const int ka = k0 + lane, kb = k0 + 32 + lane;
-    const Df a = ka < P.pj ? ld_df(x + 2 * ka) : Df{0.f, 0.f};
-    const Df b = kb < P.pj ? ld_df(x + 2 * kb) : Df{0.f, 0.f};
-    v = df_add(v, df_add(a, b));
-  }
-  return df_warp_sum(v);
-}
-
-// Search of a precise redraw (the CTA that completed the draw's jobs).  The
-// step totals are A - rho B with rho = S_p / S_q from the normaliser shares (A
-// alone for a draw from p); steps a job marked uncertain are first recomputed
-// entry by entry.  One warp then finds the step by a prefix over its lanes'
-// runs of steps and scans it with double-float weights; the token is
-// overwritten.  All sums are double-float (about 48 significant bits).
-template <typename TE>
-__device__ void psearch(const Params &P, QCtl &ctl, int s, const PassSeq &ps, const TE *gp,
-                        const TE *gq, const HpRow &rp, const HpRow &rq, bool vec) {
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int nsteps = P.steps;
-  float2 *pa = reinterpret_cast<float2 *>(P.pstep) + static_cast<long long>(s) * 2 * nsteps;
-  float2 *pb = pa + nsteps;
-  Df rho{0.f, 0.f};
-  if (ps.residual) {
-    const Df Sp = pshare_sum(P, s, 0), Sq = pshare_sum(P, s, 1);
-    // rho = Sp / Sq as a double-float: q1 = Sp.hi / Sq.hi, then one correction
-    // step q2 = (Sp - q1 Sq) / Sq.hi
-    const float q1 = __fdiv_rn(Sp.hi, Sq.hi);
-    const Df r = df_sub(Sp, df_mul(Df{q1, 0.f}, Sq));
-    const float q2 = __fdiv_rn(r.hi, Sq.hi);
-    rho = df_norm(q1, q2);
-  }
-  if (t == 0) ctl.redo = static_cast<int>(__ldcg(P.sctr + 4ll * s + 3));
-  __syncthreads();
-  if (ctl.redo) {
-    // uncertain steps (B < 0): their exact totals, one warp per step
-    for (int base = w * 32; base < nsteps; base += kQWarps * 32) {
-      const int st = base + lane;
-      unsigned todo = __ballot_sync(0xFFFFFFFFu, st < nsteps && __ldcg(&pb[st].x) < 0.f);
-      while (todo) {
-        const int x = base + __ffs(todo) - 1;
-        todo &= todo - 1;
-        Df wd[8];
-        pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, x * kStep + lane * 8, P.V, vec, ctl, wd);
-        Df acc{0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc = df_add(acc, wd[e]);
-        acc = df_warp_sum(acc);
-        if (lane == 0) {
-          pa[x] = make_float2(acc.hi, acc.lo);
-          pb[x] = make_float2(0.f, 0.f);
-        }
-      }
-    }
-    __threadfence_block();
-    __syncthreads();
-  }
-  // the step sums in one coalesced pass (other CTAs wrote most of them)
-  const bool staged = nsteps <= kQSmemSteps;
-  if (staged)
-    for (int st0 = t; st0 < nsteps; st0 += 4 * kQThreads) {  // eight loads in flight
-      float2 xa[4], xb[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int st = st0 + q * kQThreads;
-        xa[q] = st < nsteps ? __ldcg(pa + st) : make_float2(0.f, 0.f);
-        xb[q] = st < nsteps ? __ldcg(pb + st) : make_float2(0.f, 0.f);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int st = st0 + q * kQThreads;
-        if (st < nsteps) {
-          ctl.sa[st] = xa[q];
-          ctl.sb[st] = xb[q];
-        }
-      }
-    }
-  __syncthreads();
-  const float2 *qa = staged ? ctl.sa : pa, *qb = staged ? ctl.sb : pb;
-  if (w == 0) {
-    const int per = (nsteps + 31) / 32;
-    const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
-    const Df nrho{-rho.hi, -rho.lo};
-    Df seg{0.f, 0.f};
-    int lastpos = -1;
-    for (int st = s0; st < s1; ++st) {
-      const Df x = df_add(ld_dfs(qa + st, staged), df_mul(nrho, ld_dfs(qb + st, staged)));
-      seg = df_add(seg, x);
-      if (x.hi > 0.f) lastpos = st;
-    }
-    Df incl = seg;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const Df y = df_shfl_up(incl, off);
-      if (lane >= off) incl = df_add(incl, y);
-    }
-    const Df Z = df_shfl(incl, 31);
-    const Df tt = df_mul(Df{ps.u, 0.f}, Z);
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, df_gt(incl, tt) && seg.hi > 0.f);
-    int step = -1;
-    Df trel{0.f, 0.f};
-    bool exact = true;
-    if (hit) {
-      const int first = __ffs(hit) - 1;
-      if (lane == first) {
-        Df acc = df_sub(incl, seg);
-        for (int st = s0; st < s1 && step < 0; ++st) {
-          const Df x = df_add(ld_dfs(qa + st, staged), df_mul(nrho, ld_dfs(qb + st, staged)));
-          if (df_gt(df_add(acc, x), tt) && x.hi > 0.f) {
-            step = st;
-            trel = df_sub(tt, acc);
-          }
-          acc = df_add(acc, x);
-        }
-        if (step < 0) {
-          step = lastpos;
-          exact = false;
-        }
-      }
-      step = __shfl_sync(0xFFFFFFFFu, step, first);
-      trel = df_shfl(trel, first);
-      exact = __shfl_sync(0xFFFFFFFFu, exact ? 1 : 0, first) != 0;
-    } else {
-      step = warp_max_i(lastpos);
-      exact = false;
-    }
-    int token = -1;
-    if (step >= 0) {
-      const int base = step * kStep + lane * 8;
-      Df wd[8];
-      pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, base, P.V, vec, ctl, wd);
-      Df sm{0.f, 0.f};
-      int lp = -1;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sm = df_add(sm, wd[e]);
-        if (wd[e].hi > 0.f) lp = base + e;
-      }
-      Df fin = sm;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const Df y = df_shfl_up(fin, off);
-        if (lane >= off) fin = df_add(fin, y);
-      }
-      const unsigned h2 = exact ? __ballot_sync(0xFFFFFFFFu, df_gt(fin, trel) && sm.hi > 0.f) : 0u;
-      if (h2) {
-        const int first = __ffs(h2) - 1;
-        int found = -1;
-        if (lane == first) {
-          Df run = df_sub(fin, sm);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            run = df_add(run, wd[e]);
-            if (found < 0 && wd[e].hi > 0.f && df_gt(run, trel)) found = base + e;
-          }
-          if (found < 0) found = lp;
-        }
-        token = __shfl_sync(0xFFFFFFFFu, found, first);
-      } else {
-        token = warp_max_i(lp);
-      }
-    }
-    if (lane == 0 && token >= 0) {
-      const long long obase = static_cast<long long>(s) * (P.gamma + 1);
-      P.out_tokens[obase + ps.j] = token;
-      P.outs[obase + ps.j].token = token;
-    }
-  }
-  __syncthreads();
-}
-
-// Precise job (item, k): redraw item `item` of the queue, slice k of its
-// steps.  For each 256-entry step of the slice it stores the double-float sums
-// A of e_p and B of e_q over the entries whose weight e_p - rho e_q is
-// certainly positive, classified with the single-precision rho of the row
-// statistics (within 1e-6 of the exact one; an entry is certain when
+// Per 256-entry step of this CTA's steps [b0, b1): the double-float sums A of
+// e_p and B of e_q over the entries whose weight e_p - rho e_q is certainly
+// positive, classified with the single-precision rho of the row statistics
+// (within 1e-6 of the exact one; an entry is certain when
 // |e_p - rho e_q| > 1e-5 e_p), or B = -1 when an entry of the step is
-// uncertain; and the slice's shares of S_p and S_q.  A draw from p stores
-// A = the sum of e_p, B = 0.
+// uncertain; and the CTA's shares of S_p and S_q into sh.pred.  A draw from p
+// stores A = the sum of e_p, B = 0.  The step loop stays rolled (its body is
+// long: unrolled, the code would miss the instruction cache once per step)
+// and loads the warp's next step while it computes this one.
 template <typename TE>
-__device__ void pjob(const Params &P, QCtl &ctl, int item, int k) {
+__device__ void precise_steps(PreciseShared &sh, const PassSeq &ps, const TE *gp, const TE *gq,
+                              const HpRow &rp, const HpRow &rq, bool vec, int V, int b0, int b1,
+                              float2 *sa, float2 *sb) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int kp = P.pj;
-  const int s = __ldcg(P.near_list + item) - 1;  // written by the draw kernel
-  if (s < 0 || s >= P.nseq) return;
-  const PassSeq ps = reinterpret_cast<const PassSeq *>(P.pseqw)[s];
-  if (ps.j < 0 || ps.j > P.gamma) return;  // not a drawn position: never use it as a row
-  const TE *gp, *gq;
-  draw_rows<TE>(P, s, ps.j, gp, gq);
-  const bool vec = ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(gq)) & 15u) == 0;
-  const HpRow rp = hp_row(ps.dp, __ldg(P.Tp + s));
-  const HpRow rq = ps.residual ? hp_row(ps.dq, __ldg(P.Tq + s)) : rp;
   const int residual = ps.residual;
   const float rho_a = residual ? ps.dq.invS / ps.dp.invS : 0.f;  // S_p / S_q, single precision
-  const int V = P.V;
-  const int b0 = k * P.pj_steps, b1 = min(P.steps, b0 + P.pj_steps);
-  float2 *pa = reinterpret_cast<float2 *>(P.pstep) + static_cast<long long>(s) * 2 * P.steps;
-  float2 *pb = pa + P.steps;
-  uint32_t *cnt = P.sctr + 4ll * s;
   Df sp_tot{0.f, 0.f}, sq_tot{0.f, 0.f};
-  bool unc_any = false;
-  for (int st = b0 + w; st < b1; st += kQWarps) {
-    const int base = st * kStep + lane * 8;
+  float np[8], nq[8];
+  int st = b0 + w;
+  if (st < b1) {
+    hp_load8<TE>(gp, st * kStep + lane * 8, V, vec, np);
+    if (residual) hp_load8<TE>(gq, st * kStep + lane * 8, V, vec, nq);
+  }
+#pragma unroll 1
+  for (; st < b1; st += kPWarps) {
     float zp[8], zq[8];
-    hp_load8<TE>(gp, base, V, vec, zp);
-    if (residual) hp_load8<TE>(gq, base, V, vec, zq);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      zp[e] = np[e];
+      zq[e] = residual ? nq[e] : 0.f;
+    }
+    const int nx = st + kPWarps;
+    if (nx < b1) {
+      hp_load8<TE>(gp, nx * kStep + lane * 8, V, vec, np);
+      if (residual) hp_load8<TE>(gq, nx * kStep + lane * 8, V, vec, nq);
+    }
+    Df ep[8], eq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ep[e] = hp_exp(rp, zp[e], sh.tab_hi, sh.tab_lo);
+      eq[e] = residual ? hp_exp(rq, zq[e], sh.tab_hi, sh.tab_lo) : Df{0.f, 0.f};
+    }
     Df sp{0.f, 0.f}, sq{0.f, 0.f}, a{0.f, 0.f}, b{0.f, 0.f};
     bool unc = false;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const Df ep = hp_exp(rp, zp[e], ctl.tab_hi, ctl.tab_lo);
-      sp = df_add(sp, ep);
+      sp = df_add(sp, ep[e]);
       if (!residual) continue;
-      const Df eq = hp_exp(rq, zq[e], ctl.tab_hi, ctl.tab_lo);
-      sq = df_add(sq, eq);
-      if (ep.hi > 0.f) {
-        const float d = fmaf(-rho_a, eq.hi, ep.hi);
-        if (d > 1e-5f * ep.hi) {
-          a = df_add(a, ep);
-          b = df_add(b, eq);
-        } else if (d >= -1e-5f * ep.hi) {
+      sq = df_add(sq, eq[e]);
+      if (ep[e].hi > 0.f) {
+        const float d = fmaf(-rho_a, eq[e].hi, ep[e].hi);
+        if (d > 1e-5f * ep[e].hi) {
+          a = df_add(a, ep[e]);
+          b = df_add(b, eq[e]);
+        } else if (d >= -1e-5f * ep[e].hi) {
           unc = true;
         }
       }
@@ -1219,145 +970,301 @@ __device__ void pjob(const Params &P, QCtl &ctl, int item, int k) {
     const Df Bq = df_warp_sum(b);
     unc = __any_sync(0xFFFFFFFFu, unc);
     if (lane == 0) {
-      pa[st] = make_float2(A.hi, A.lo);
-      pb[st] = unc ? make_float2(-1.f, 0.f) : make_float2(Bq.hi, Bq.lo);
+      sa[st] = make_float2(A.hi, A.lo);
+      sb[st] = unc ? make_float2(-1.f, 0.f) : make_float2(Bq.hi, Bq.lo);
     }
-    unc_any |= unc;
     sp_tot = df_add(sp_tot, sp);
     sq_tot = df_add(sq_tot, sq);
   }
   sp_tot = df_warp_sum(sp_tot);
   sq_tot = df_warp_sum(sq_tot);
   if (lane == 0) {
-    ctl.pred[0][w] = sp_tot;
-    ctl.pred[1][w] = sq_tot;
-    ctl.red_i[w] = unc_any ? 1 : 0;
+    sh.pred[0][w] = sp_tot;
+    sh.pred[1][w] = sq_tot;
   }
   __syncthreads();
-  if (t == 0) {
-    Df A{0.f, 0.f}, B{0.f, 0.f};
-    int u = 0;
-    for (int x = 0; x < kQWarps; ++x) {
-      A = df_add(A, ctl.pred[0][x]);
-      B = df_add(B, ctl.pred[1][x]);
-      u |= ctl.red_i[x];
+}
+
+// CTA 0, warp 0, after every CTA's step sums are in sa / sb: a double-float
+// prefix of A - rho B over the lanes' runs of steps finds the step, a
+// double-float scan of its weights the token (the same value in every lane;
+// -1: no positive weight).  All sums are double-float (about 48 significant
+// bits).
+template <typename TE>
+__device__ int precise_search(const PreciseShared &sh, const float2 *sa, const float2 *sb,
+                              int nsteps, const PassSeq &ps, Df rho, const TE *gp, const TE *gq,
+                              const HpRow &rp, const HpRow &rq, bool vec, int V) {
+  const int lane = threadIdx.x & 31;
+  const int per = (nsteps + 31) / 32;
+  const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
+  const Df nrho{-rho.hi, -rho.lo};
+  Df seg{0.f, 0.f};
+  int lastpos = -1;
+  for (int st = s0; st < s1; ++st) {
+    const Df x = df_add(Df{sa[st].x, sa[st].y}, df_mul(nrho, Df{sb[st].x, sb[st].y}));
+    seg = df_add(seg, x);
+    if (x.hi > 0.f) lastpos = st;
+  }
+  Df incl = seg;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const Df y = df_shfl_up(incl, off);
+    if (lane >= off) incl = df_add(incl, y);
+  }
+  const Df Z = df_shfl(incl, 31);
+  const Df tt = df_mul(Df{ps.u, 0.f}, Z);
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, df_gt(incl, tt) && seg.hi > 0.f);
+  int step = -1;
+  Df trel{0.f, 0.f};
+  bool exact = true;
+  if (hit) {
+    const int first = __ffs(hit) - 1;
+    if (lane == first) {
+      Df acc = df_sub(incl, seg);
+      for (int st = s0; st < s1 && step < 0; ++st) {
+        const Df x = df_add(Df{sa[st].x, sa[st].y}, df_mul(nrho, Df{sb[st].x, sb[st].y}));
+        if (df_gt(df_add(acc, x), tt) && x.hi > 0.f) {
+          step = st;
+          trel = df_sub(tt, acc);
+        }
+        acc = df_add(acc, x);
+      }
+      if (step < 0) {
+        step = lastpos;
+        exact = false;
+      }
     }
-    float2 *dst = reinterpret_cast<float2 *>(P.ppart) + (static_cast<long long>(s) * kp + k) * 2;
-    dst[0] = make_float2(A.hi, A.lo);
-    dst[1] = make_float2(B.hi, B.lo);
-    if (u) atomicAdd(cnt + 3, 1u);  // read by the search kernel, after this one
+    step = __shfl_sync(0xFFFFFFFFu, step, first);
+    trel = df_shfl(trel, first);
+    exact = __shfl_sync(0xFFFFFFFFu, exact ? 1 : 0, first) != 0;
+  } else {
+    step = warp_max_i(lastpos);
+    exact = false;
   }
-  __syncthreads();  // ctl.pred is reused by the CTA's next item
+  if (step < 0) return -1;
+  const int base = step * kStep + lane * 8;
+  Df wd[8];
+  pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, base, V, vec, sh.tab_hi, sh.tab_lo, wd);
+  Df sm{0.f, 0.f};
+  int lp = -1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sm = df_add(sm, wd[e]);
+    if (wd[e].hi > 0.f) lp = base + e;
+  }
+  Df fin = sm;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const Df y = df_shfl_up(fin, off);
+    if (lane >= off) fin = df_add(fin, y);
+  }
+  const unsigned h2 = exact ? __ballot_sync(0xFFFFFFFFu, df_gt(fin, trel) && sm.hi > 0.f) : 0u;
+  if (!h2) return warp_max_i(lp);
+  const int first = __ffs(h2) - 1;
+  int found = -1;
+  if (lane == first) {
+    Df run = df_sub(fin, sm);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      run = df_add(run, wd[e]);
+      if (found < 0 && wd[e].hi > 0.f && df_gt(run, trel)) found = base + e;
+    }
+    if (found < 0) found = lp;
+  }
+  return __shfl_sync(0xFFFFFFFFu, found, first);
 }
 
-// Grid (job, item stride): CTA (k, y) runs job k of queued draws
-// y, y + gridDim.y, ...
+// Clusters of Cp CTAs (grid: kPreciseGrid * Cp CTAs); cluster y redraws the
+// queued draws y, y + kPreciseGrid, ... : double-float step sums of each
+// CTA's steps; the exact rho = S_p / S_q from every CTA's shares; exact totals
+// of the steps an entry of which was uncertain; then CTA 0 searches and
+// overwrites the token.  Dynamic shared memory: sa[steps], sb[steps].
 template <typename TE>
-__global__ void __launch_bounds__(kQThreads) chain_precise_kernel(const Params P,
-                                                                  const Exp2Table tab) {
-  __shared__ QCtl ctl;
+__global__ void __launch_bounds__(kPThreads, 1) chain_precise_kernel(const Params P,
+                                                                     const Exp2Table tab) {
+  extern __shared__ __align__(16) unsigned char precise_smem[];
+  __shared__ PreciseShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int y = static_cast<int>(blockIdx.x) / C, ny = static_cast<int>(gridDim.x) / C;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int V = P.V, nsteps = P.steps;
+  float2 *sa = reinterpret_cast<float2 *>(precise_smem);
+  float2 *sb = sa + nsteps;
+  cluster_arrive();
   launch_dependents();
-  grid_dependency_wait();
-  const uint32_t count = min(__ldcg(P.pctr), static_cast<uint32_t>(P.nseq));
-  if (blockIdx.y >= count) return;
-  for (int i = threadIdx.x; i < 64; i += kQThreads) {
-    ctl.tab_hi[i] = tab.hi[i];
-    ctl.tab_lo[i] = tab.lo[i];
+  if (t < 64) {
+    sh.tab_hi[t] = tab.hi[t];
+    sh.tab_lo[t] = tab.lo[t];
   }
+  grid_dependency_wait();  // the draw kernel's queue is complete
+  const int count = static_cast<int>(min(__ldcg(P.pctr), static_cast<uint32_t>(P.nseq)));
+  if (y >= count) return;  // every CTA of this cluster returns
+  cluster_wait();
   __syncthreads();
-  for (uint32_t item = blockIdx.y; item < count; item += gridDim.y)
-    pjob<TE>(P, ctl, static_cast<int>(item), blockIdx.x);
-}
-
-// One CTA per queued draw (stride gridDim.x), after the precise jobs: the
-// double-float search and the token.
-template <typename TE>
-__global__ void __launch_bounds__(kQThreads) chain_psearch_kernel(const Params P,
-                                                                  const Exp2Table tab) {
-  __shared__ QCtl ctl;
-  launch_dependents();
-  grid_dependency_wait();
-  const uint32_t count = min(__ldcg(P.pctr), static_cast<uint32_t>(P.nseq));
-  if (blockIdx.x >= count) return;
-  for (int i = threadIdx.x; i < 64; i += kQThreads) {
-    ctl.tab_hi[i] = tab.hi[i];
-    ctl.tab_lo[i] = tab.lo[i];
-  }
-  __syncthreads();
-  for (uint32_t item = blockIdx.x; item < count; item += gridDim.x) {
-    const int s = __ldcg(P.near_list + item) - 1;
-    if (s < 0 || s >= P.nseq) continue;
-    const PassSeq ps = reinterpret_cast<const PassSeq *>(P.pseqw)[s];
-    if (ps.j < 0 || ps.j > P.gamma) continue;  // not a drawn position: never use it as a row
-    const TE *gp, *gq;
-    draw_rows<TE>(P, s, ps.j, gp, gq);
+  const int per = (nsteps + C - 1) / C;
+  const int b0 = min(nsteps, rank * per), b1 = min(nsteps, b0 + per);
+  for (int item = y; item < count; item += ny) {
+    const int s = __ldcg(P.near_list + item) - 1;  // written by the draw kernel
+    const bool ok = s >= 0 && s < P.nseq;
+    const PassSeq ps = ok ? reinterpret_cast<const PassSeq *>(P.pseqw)[s] : PassSeq{};
+    // an entry outside the batch or a position that is not a draw is skipped
+    // (the same decision in every CTA, so the barriers below still pair up)
+    const bool run = ok && ps.j >= 0 && ps.j <= P.gamma;
+    const TE *gp = nullptr, *gq = nullptr;
+    if (run) draw_rows<TE>(P, s, ps.j, gp, gq);
     const bool vec =
         ((reinterpret_cast<uintptr_t>(gp) | reinterpret_cast<uintptr_t>(gq)) & 15u) == 0;
-    const HpRow rp = hp_row(ps.dp, __ldg(P.Tp + s));
-    const HpRow rq = ps.residual ? hp_row(ps.dq, __ldg(P.Tq + s)) : rp;
-    psearch<TE>(P, ctl, s, ps, gp, gq, rp, rq, vec);
+    const HpRow rp = hp_row(ps.dp, run ? __ldg(P.Tp + s) : 1.f);
+    const HpRow rq = ps.residual ? hp_row(ps.dq, run ? __ldg(P.Tq + s) : 1.f) : rp;
+    if (run) {
+      precise_steps<TE>(sh, ps, gp, gq, rp, rq, vec, V, b0, b1, sa, sb);
+      // this CTA's shares to every CTA; its step sums to CTA 0
+      if (t < C) {
+        Df A{0.f, 0.f}, B{0.f, 0.f};
+        for (int x = 0; x < kPWarps; ++x) {
+          A = df_add(A, sh.pred[0][x]);
+          B = df_add(B, sh.pred[1][x]);
+        }
+        Df *dst = cluster.map_shared_rank(&sh.part[0][0], t);
+        dst[2 * rank] = A;
+        dst[2 * rank + 1] = B;
+      }
+      if (rank != 0) {
+        float2 *ra = cluster.map_shared_rank(sa, 0), *rb = cluster.map_shared_rank(sb, 0);
+        for (int st = b0 + t; st < b1; st += kPThreads) {
+          ra[st] = sa[st];
+          rb[st] = sb[st];
+        }
+      }
+    }
+    cluster_sync_all();
+    Df rho{0.f, 0.f};
+    if (run && ps.residual) {
+      // the exact normaliser ratio, summed in the same order in every CTA
+      Df Sp{0.f, 0.f}, Sq{0.f, 0.f};
+      for (int r = 0; r < C; ++r) {
+        Sp = df_add(Sp, sh.part[r][0]);
+        Sq = df_add(Sq, sh.part[r][1]);
+      }
+      // rho = Sp / Sq as a double-float: q1 = Sp.hi / Sq.hi, then one
+      // correction step q2 = (Sp - q1 Sq) / Sq.hi
+      const float q1 = __fdiv_rn(Sp.hi, Sq.hi);
+      const Df r = df_sub(Sp, df_mul(Df{q1, 0.f}, Sq));
+      const float q2 = __fdiv_rn(r.hi, Sq.hi);
+      rho = df_norm(q1, q2);
+      // uncertain steps of this CTA (B < 0): their exact totals, one warp per step
+      float2 *ra = cluster.map_shared_rank(sa, 0), *rb = cluster.map_shared_rank(sb, 0);
+      for (int base = b0 + w * 32; base < b1; base += kPWarps * 32) {
+        const int st = base + lane;
+        unsigned todo = __ballot_sync(0xFFFFFFFFu, st < b1 && sb[st].x < 0.f);
+        while (todo) {
+          const int x = base + __ffs(todo) - 1;
+          todo &= todo - 1;
+          Df wd[8];
+          pweights8<TE>(gp, gq, rp, rq, 1, rho, x * kStep + lane * 8, V, vec, sh.tab_hi,
+                        sh.tab_lo, wd);
+          Df acc{0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = df_add(acc, wd[e]);
+          acc = df_warp_sum(acc);
+          if (lane == 0) {
+            ra[x] = make_float2(acc.hi, acc.lo);
+            rb[x] = make_float2(0.f, 0.f);
+          }
+        }
+      }
+    }
+    cluster_sync_all();
+    if (run && rank == 0 && w == 0) {
+      const int token = precise_search<TE>(sh, sa, sb, nsteps, ps, rho, gp, gq, rp, rq, vec, V);
+      if (lane == 0 && token >= 0) {
+        const long long obase = static_cast<long long>(s) * (P.gamma + 1);
+        P.out_tokens[obase + ps.j] = token;
+        P.outs[obase + ps.j].token = token;
+      }
+    }
+    cluster_sync_all();  // CTA 0 has read sa / sb before the next item writes them
   }
 }
 
-// Slices of the draw and jobs of the precise redraw: slices of 16 steps
-// (4096 entries) and about 64 precise jobs per draw, whole 256-entry steps
-// each.
-void set_chain_split(Params &P) {
-  const int steps = P.steps;
-  P.wj_steps = steps < 16 ? steps : 16;
-  P.wj = (steps + P.wj_steps - 1) / P.wj_steps;
-  const int kp = steps < 64 ? steps : 64;
-  P.pj_steps = (steps + kp - 1) / kp;
-  P.pj = (steps + P.pj_steps - 1) / P.pj_steps;
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+// Launch with clusters of C CTAs and programmatic stream serialisation (the
+// kernel may begin while the previous one drains; it waits in
+// grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster_pdl(void (*kern)(KArgs...), int blocks, int threads, int C,
+                               size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Resident CTAs per SM of a kernel (cached per device and shared-memory size
-// under a lock shared by every host thread).
-struct OccCache {
+// The largest cluster size (`want`, halved while it cannot be scheduled) of
+// a kernel with `smem` bytes of dynamic shared memory, cached per device and
+// size under a lock shared by every host thread.
+struct ClusterCache {
   std::mutex mu;
-  int dev = -1, smem = -1, blocks = 0;
+  int dev = -1;
+  size_t smem = 0;
+  int C = 0;
 };
 
-template <typename K>
-cudaError_t occupancy(OccCache &c, K kern, int threads, size_t smem, int &blocks) {
+template <typename... KArgs>
+cudaError_t cluster_size(ClusterCache &c, void (*kern)(KArgs...), int threads, int want,
+                         size_t smem, int &C) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(c.mu);
-  if (dev != c.dev || static_cast<int>(smem) != c.smem) {
+  if (dev != c.dev || smem != c.smem) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    c.blocks = per_sm * sms;
+    if (want > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    int size = want;
+    for (; size > 1; size /= 2) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(size), 1, 1);
+      cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n > 0) break;
+    }
+    c.C = size;
     c.dev = dev;
-    c.smem = static_cast<int>(smem);
+    c.smem = smem;
   }
-  blocks = c.blocks;
+  C = c.C;
   return cudaSuccess;
-}
-
-// Launch with programmatic stream serialisation: the kernel may begin while
-// the previous one in the stream drains (it waits in grid_dependency_wait).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // Events a benchmark asked to be recorded around the rows kernel (both set
@@ -1366,17 +1273,26 @@ std::mutex g_prof_mu;
 cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 
 template <typename TE>
-cudaError_t launch_chain_t(Params P, const Exp2Table &tab, size_t smem, cudaStream_t stream) {
+cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
+                           cudaStream_t stream) {
   cudaEvent_t prof_start, prof_stop;
   {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     prof_start = g_prof_start;
     prof_stop = g_prof_stop;
   }
-  static OccCache w_occ;
-  int w_blocks = 0;
-  cudaError_t e;
-  set_chain_split(P);
+  static ClusterCache draw_cache, precise_cache;
+  const size_t dsmem = (static_cast<size_t>(P.steps) * sizeof(float) + 15) / 16 * 16 +
+                       kDrawRecords * sizeof(unsigned long long);
+  const size_t psmem = static_cast<size_t>(P.steps) * 2 * sizeof(float2);
+  int Cd = 1, Cp = 1;
+  cudaError_t e =
+      cluster_size(draw_cache, chain_draw_kernel<TE>, kDThreads, kDrawCluster, dsmem, Cd);
+  if (e != cudaSuccess) return e;
+  e = cluster_size(precise_cache, chain_precise_kernel<TE>, kPThreads, kPreciseCluster, psmem, Cp);
+  if (e != cudaSuccess) return e;
+  Cd = std::max(1, std::min(Cd, P.steps));
+  Cp = std::max(1, std::min(Cp, P.steps));
   if (prof_start) {
     e = cudaEventRecord(prof_start, stream);
     if (e != cudaSuccess) return e;
@@ -1387,26 +1303,11 @@ cudaError_t launch_chain_t(Params P, const Exp2Table &tab, size_t smem, cudaStre
     e = cudaEventRecord(prof_stop, stream);
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(chain_decide_kernel<TE>, dim3(P.nseq), dim3(kKThreads), 0, stream, P);
+  e = launch_cluster_pdl(chain_draw_kernel<TE>, P.nseq * Cd, kDThreads, Cd, dsmem, stream, P);
   if (e != cudaSuccess) return e;
-  // weights kernel: a ring of kWRing slots, each one slice of the p row and one
-  // of the q row
-  Params W = P;
-  W.slot_bytes = static_cast<int>(static_cast<size_t>(P.wj_steps) * kStep * sizeof(TE));
-  W.data_off = static_cast<int>((sizeof(WCtl) + 127) / 128 * 128);
-  const size_t wsmem = W.data_off + static_cast<size_t>(kWRing) * 2 * W.slot_bytes;
-  e = occupancy(w_occ, chain_weights_kernel<TE>, kWThreads, wsmem, w_blocks);
-  if (e != cudaSuccess) return e;
-  const long long witems = static_cast<long long>(P.nseq) * P.wj;
-  e = launch_pdl(chain_weights_kernel<TE>, dim3(static_cast<int>(witems < w_blocks ? witems : w_blocks)),
-                 dim3(kWThreads), wsmem, stream, W);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(chain_search_kernel<TE>, dim3(P.nseq), dim3(kDThreads), 0, stream, P);
-  if (e != cudaSuccess) return e;
-  const int gy = P.nseq < 32 ? P.nseq : 32;
-  e = launch_pdl(chain_precise_kernel<TE>, dim3(P.pj, gy), dim3(kQThreads), 0, stream, P, tab);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(chain_psearch_kernel<TE>, dim3(gy), dim3(kQThreads), 0, stream, P, tab);
+  const int gy = std::min(P.nseq, kPreciseGrid);
+  return launch_cluster_pdl(chain_precise_kernel<TE>, gy * Cp, kPThreads, Cp, psmem, stream, P,
+                            tab);
 }
 
 }  // namespace

@@ -80,17 +80,14 @@ constexpr float kRefineGuard = 4e-6f;
 // The precise redraw runs on at most this many CTAs.
 constexpr int kRefineMaxGrid = 1024;
 
-// Precise-redraw jobs of one chain draw (at most).
-constexpr int kPassPreciseJobs = 64;
-
 // 64-bit records the chain rows kernel leaves per 32 KB chunk (one per
 // consumer warp).
 constexpr int kChainRecordsPerChunk = 8;
 
 // One work unit of the precise redraw (a slice of one queued draw's
 // vocabulary): its partial sums, published for the other units of the draw.
-// A chain's final draw, written by the chain decide kernel for the weights,
-// search and precise kernels of the streaming chain path.
+// A chain's final draw: the decision the chain draw kernel's CTAs share, and
+// the description a queued precise redraw reads.
 struct __align__(16) PassSeq {
   RowDesc dp, dq;  // the draw distribution: [p - q]_+ (residual) or p
   float u;         // draw uniform
@@ -172,21 +169,15 @@ struct Params {
   RefinePart *rpart;              // [max(kRefineMaxGrid, nseq)] work-unit partials
   double *rc;                     // [nseq] residual multiplier of each queued draw
   uint32_t *rbar;                 // grid-barrier arrivals of the redraw kernel
-  // streaming chain path (rows, decide, weights, search, precise kernels)
+  // streaming chain path (rows kernel, draw kernel, precise kernel)
   unsigned long long *srec;       // [rows][chunks][8] per-warp records of the rows kernel
   uint32_t *err;                  // bit 0: a bounded wait gave up
   int chunk_elems;                // entries per chunk
   int cpr;                        // chunks per row
   int steps;                      // draw search steps per row (256 entries each)
-  unsigned long long *pseqw;      // [nseq] PassSeq draw descriptors (decide kernel)
-  uint32_t *sctr;                 // [nseq][4] [3] precise jobs that met an uncertain step
-  unsigned long long *fstep;      // [nseq][steps] single-precision step totals
-  double *pstep;                  // [nseq][2][steps] precise step sums A (e_p) and B (e_q)
-  double *ppart;                  // [nseq][pj][2] shares of S_p, S_q
+  unsigned long long *pseqw;      // [nseq] PassSeq of each queued precise redraw
   int *near_list;                 // [nseq] sequence + 1 of each queued precise redraw
-  uint32_t *pctr;                 // [0] precise redraws queued
-  int wj, wj_steps;               // slices per draw of the weights kernel, steps per slice
-  int pj, pj_steps;               // precise jobs per phase, steps per job
+  uint32_t *pctr;                 // [0] precise redraws queued (cleared by every call)
 };
 
 

@@ -100,10 +100,14 @@ def test_chain_unsupported_vocabulary(lib):
     # one cluster's shared memory: refused before any launch
     topk = _abi.spec_policy(FAKE.value, FAKE.value)
     assert chain(lib, V=100_000_000, pol=topk) == _abi.SPEC_ERR_UNSUPPORTED
-    # without top-k the streaming chain path takes any vocabulary; this call's
-    # workspace (0 bytes) is too small for it
-    assert lib.spec_verify_chain_workspace_size(2, 3, 100_000_000, 0) > 0
-    assert chain(lib, V=100_000_000) == _abi.SPEC_ERR_INVALID_ARG
+    # without top-k the streaming chain path takes vocabularies up to
+    # 2,097,152 entries (the draw kernel keeps 20 bytes per 256-entry step in
+    # shared memory); this call's workspace (0 bytes) is too small for it
+    assert lib.spec_verify_chain_workspace_size(2, 3, 2_097_152, 0) > 0
+    assert chain(lib, V=2_097_152) == _abi.SPEC_ERR_INVALID_ARG
+    # beyond that no kernel takes a float32 row: refused before any launch
+    assert chain(lib, V=2_097_153) == _abi.SPEC_ERR_UNSUPPORTED
+    assert chain(lib, V=100_000_000) == _abi.SPEC_ERR_UNSUPPORTED
 
 
 def test_static_chain_refuses_before_any_cuda_call(lib):
