@@ -888,10 +888,14 @@ def run_rerank(args):
 
 
 def run_workloads(args):
-    """Per-call times of the five verification workloads and the tree mask:
-    CUDA events around each call through the Python API, inputs resident in
-    HBM, the L2 flushed (a 256 MB write) before every call; the median of
-    --steps calls after --warmup calls.  One JSON line with every workload."""
+    """Per-call device times of the five verification workloads (plus workload
+    2 with top-p 0.9 and min-p 0.05) and the tree mask: CUDA events around each
+    call through the Python API, every input (logits, tokens, temperatures,
+    filter arrays) resident on the device before the timing, the L2 flushed (a
+    256 MB write) and the GPU held busy for about 100 us before every call so
+    that the binding's host work is done before the first kernel starts; the
+    median of --steps calls after --warmup calls.  One JSON line with every
+    workload."""
     import torch
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -910,6 +914,7 @@ def run_workloads(args):
         ts = []
         for _ in range(args.steps):
             flush.zero_()
+            torch.cuda._sleep(200_000)  # the host queues the call meanwhile
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -924,9 +929,12 @@ def run_workloads(args):
         return t.to(torch.bfloat16) if dtype == "bf16" else t
 
     def top_k(x):
-        # only a real filter is passed: any top-k array routes the call to the
-        # kernels that apply top-k
-        return x if x is not None and (x > 0).any() else None
+        # only a real filter is passed (any top-k array routes the call to the
+        # kernels that apply top-k), as a device array
+        return torch.from_numpy(x).to(dev) if x is not None and (x > 0).any() else None
+
+    def on_dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
 
     per = {}
     ids = [int(x) for x in args.only.split(",")] if args.only else range(5)
@@ -935,19 +943,26 @@ def run_workloads(args):
         t = dev_logits(w["target"], w["dtype"])
         d = dev_logits(w["draft"], w["dtype"])
         esize = 2 if w["dtype"] == "bf16" else 4
+        tp, tq = on_dev(w["target_temperature"]), on_dev(w["draft_temperature"])
+        kp, kq = top_k(w.get("target_top_k")), top_k(w.get("draft_top_k"))
+        tok = torch.from_numpy(w["tokens"]).to(dev)
         if "B" in w:
-            tok = torch.from_numpy(w["tokens"]).to(dev)
-            us = median_call_us(lambda: sv.verify_chain(
-                t, d, tok, w["target_temperature"], w["draft_temperature"],
-                top_k(w.get("target_top_k")), top_k(w.get("draft_top_k")), seed=w["seed"]))
+            us = median_call_us(lambda: sv.verify_chain(t, d, tok, tp, tq, kp, kq, seed=w["seed"]))
             rows = w["B"] * (w["gamma"] + 1)
+            if i == 2:
+                fp = torch.full((w["B"],), FILTER_TOP_P, dtype=torch.float32, device=dev)
+                fm = torch.full((w["B"],), FILTER_MIN_P, dtype=torch.float32, device=dev)
+                fus = median_call_us(lambda: sv.verify_chain(
+                    t, d, tok, tp, tq, seed=w["seed"], target_top_p=fp, draft_top_p=fp,
+                    target_min_p=fm, draft_min_p=fm))
+                per["workload_2_filters"] = {
+                    "us_per_call": fus, "rows_per_s": rows / (fus / 1e6), "dtype": w["dtype"],
+                    "V": w["V"], "esize": esize,
+                    "filters": f"top-p {FILTER_TOP_P} and min-p {FILTER_MIN_P}, both sides"}
         else:
-            tok = torch.from_numpy(w["tokens"]).to(dev)
             par = torch.from_numpy(w["parent"]).to(dev)
             us = median_call_us(lambda: sv.verify_tree(
-                t, d, tok, par, w["max_depth"], w["target_temperature"],
-                w["draft_temperature"], top_k(w.get("target_top_k")),
-                top_k(w.get("draft_top_k")), seed=w["seed"]))
+                t, d, tok, par, w["max_depth"], tp, tq, kp, kq, seed=w["seed"]))
             rows = w["T"] * w["N"]
             per["tree_mask"] = {"us_per_call": median_call_us(
                 lambda: sv.tree_mask(par, w["max_depth"])), "trees": w["T"], "nodes": w["N"]}
@@ -956,6 +971,8 @@ def run_workloads(args):
     print(json.dumps({"metric": "per-call time of each workload", "unit": "us",
                       "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
                       "l2": "flushed (a 256 MB write) before every call",
+                      "timing": "device time: inputs on the device, the GPU busy while the "
+                                "host queues each call",
                       "workloads": per}), flush=True)
 
 

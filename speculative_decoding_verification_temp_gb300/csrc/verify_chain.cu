@@ -44,9 +44,9 @@ constexpr int kDWarps = 4;                   // draw kernel
 constexpr int kDThreads = kDWarps * 32;
 constexpr int kDrawCluster = 4;              // CTAs per sequence (fewer when the row is short)
 constexpr int kDrawRecords = 2048;           // records a draw CTA stages in shared memory
-constexpr int kPWarps = 16;                  // precise kernel
+constexpr int kPWarps = 8;                   // precise kernel
 constexpr int kPThreads = kPWarps * 32;
-constexpr int kPreciseCluster = 8;           // CTAs per queued draw (fewer when it cannot run)
+constexpr int kPreciseCluster = 16;          // CTAs per queued draw (fewer when it cannot run)
 constexpr int kPreciseGrid = 32;             // clusters of the precise kernel (queued draws stride)
 constexpr int kStep = 256;  // entries per draw-search step
 constexpr int kCMaxGamma = 31;
@@ -904,8 +904,56 @@ __global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P
 struct PreciseShared {
   Df part[kPreciseCluster][2];  // every CTA's shares of S_p, S_q
   Df pred[2][kPWarps];
+  Df wsum[kPWarps];             // search: per-warp sums
+  int wfirst[kPWarps];          // search: per-warp first thread past the target
+  int wlast[kPWarps];           // search: per-warp last positive index
+  int step, exact;
+  Df trel;
   float tab_hi[64], tab_lo[64];
 };
+
+// Inclusive double-float prefix of v over the CTA's threads (kPThreads), and
+// the CTA total in `tot` (the same value in every thread: the warps' sums are
+// added in a fixed order).
+__device__ __forceinline__ Df block_df_scan(PreciseShared &sh, Df v, Df &tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  Df incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const Df y = df_shfl_up(incl, off);
+    if (lane >= off) incl = df_add(incl, y);
+  }
+  if (lane == 31) sh.wsum[w] = incl;
+  __syncthreads();
+  Df base{0.f, 0.f}, T{0.f, 0.f};
+  for (int x = 0; x < kPWarps; ++x) {
+    if (x == w) base = T;
+    T = df_add(T, sh.wsum[x]);
+  }
+  tot = T;
+  return df_add(base, incl);
+}
+
+// The first thread of the CTA for which `hit` holds (-1: none), and the
+// largest `idx` of the CTA (-1 when every idx is -1).
+__device__ __forceinline__ int block_first(PreciseShared &sh, bool hit, int idx, int &last) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned b = __ballot_sync(0xFFFFFFFFu, hit);
+  const int wl = warp_max_i(idx);
+  if (lane == 0) {
+    sh.wfirst[w] = b ? __ffs(b) - 1 : 32;
+    sh.wlast[w] = wl;
+  }
+  __syncthreads();
+  int first = -1;
+  last = -1;
+  for (int x = kPWarps - 1; x >= 0; --x) {
+    if (sh.wfirst[x] < 32) first = x * 32 + sh.wfirst[x];
+    last = max(last, sh.wlast[x]);
+  }
+  __syncthreads();  // sh.wfirst / wlast are reused by the next call
+  return first;
+}
 
 // Per 256-entry step of this CTA's steps [b0, b1): the double-float sums A of
 // e_p and B of e_q over the entries whose weight e_p - rho e_q is certainly
@@ -985,18 +1033,18 @@ __device__ void precise_steps(PreciseShared &sh, const PassSeq &ps, const TE *gp
   __syncthreads();
 }
 
-// CTA 0, warp 0, after every CTA's step sums are in sa / sb: a double-float
-// prefix of A - rho B over the lanes' runs of steps finds the step, a
-// double-float scan of its weights the token (the same value in every lane;
-// -1: no positive weight).  All sums are double-float (about 48 significant
-// bits).
+// CTA 0 (every thread), after every CTA's step sums are in sa / sb: a
+// double-float prefix of A - rho B over the threads' runs of steps finds the
+// step holding u Z, then a double-float prefix of the step's 256 weights (one
+// entry a thread) the token (-1: no positive weight).  All sums are
+// double-float (about 48 significant bits).
 template <typename TE>
-__device__ int precise_search(const PreciseShared &sh, const float2 *sa, const float2 *sb,
-                              int nsteps, const PassSeq &ps, Df rho, const TE *gp, const TE *gq,
-                              const HpRow &rp, const HpRow &rq, bool vec, int V) {
-  const int lane = threadIdx.x & 31;
-  const int per = (nsteps + 31) / 32;
-  const int s0 = min(nsteps, lane * per), s1 = min(nsteps, s0 + per);
+__device__ int precise_search(PreciseShared &sh, const float2 *sa, const float2 *sb, int nsteps,
+                              const PassSeq &ps, Df rho, const TE *gp, const TE *gq,
+                              const HpRow &rp, const HpRow &rq, int V) {
+  const int t = threadIdx.x;
+  const int per = (nsteps + kPThreads - 1) / kPThreads;
+  const int s0 = min(nsteps, t * per), s1 = min(nsteps, s0 + per);
   const Df nrho{-rho.hi, -rho.lo};
   Df seg{0.f, 0.f};
   int lastpos = -1;
@@ -1005,73 +1053,54 @@ __device__ int precise_search(const PreciseShared &sh, const float2 *sa, const f
     seg = df_add(seg, x);
     if (x.hi > 0.f) lastpos = st;
   }
-  Df incl = seg;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const Df y = df_shfl_up(incl, off);
-    if (lane >= off) incl = df_add(incl, y);
-  }
-  const Df Z = df_shfl(incl, 31);
+  Df Z;
+  const Df incl = block_df_scan(sh, seg, Z);
   const Df tt = df_mul(Df{ps.u, 0.f}, Z);
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, df_gt(incl, tt) && seg.hi > 0.f);
-  int step = -1;
-  Df trel{0.f, 0.f};
-  bool exact = true;
-  if (hit) {
-    const int first = __ffs(hit) - 1;
-    if (lane == first) {
-      Df acc = df_sub(incl, seg);
-      for (int st = s0; st < s1 && step < 0; ++st) {
-        const Df x = df_add(Df{sa[st].x, sa[st].y}, df_mul(nrho, Df{sb[st].x, sb[st].y}));
-        if (df_gt(df_add(acc, x), tt) && x.hi > 0.f) {
-          step = st;
-          trel = df_sub(tt, acc);
-        }
-        acc = df_add(acc, x);
-      }
-      if (step < 0) {
-        step = lastpos;
-        exact = false;
-      }
+  int last;
+  const int first = block_first(sh, df_gt(incl, tt) && seg.hi > 0.f, lastpos, last);
+  if (first < 0) {
+    if (t == 0) {
+      sh.step = last;
+      sh.exact = 0;
     }
-    step = __shfl_sync(0xFFFFFFFFu, step, first);
-    trel = df_shfl(trel, first);
-    exact = __shfl_sync(0xFFFFFFFFu, exact ? 1 : 0, first) != 0;
-  } else {
-    step = warp_max_i(lastpos);
-    exact = false;
+  } else if (t == first) {
+    Df acc = df_sub(incl, seg);
+    int step = -1;
+    for (int st = s0; st < s1 && step < 0; ++st) {
+      const Df x = df_add(Df{sa[st].x, sa[st].y}, df_mul(nrho, Df{sb[st].x, sb[st].y}));
+      if (df_gt(df_add(acc, x), tt) && x.hi > 0.f) {
+        step = st;
+        sh.trel = df_sub(tt, acc);
+      }
+      acc = df_add(acc, x);
+    }
+    sh.step = step < 0 ? lastpos : step;
+    sh.exact = step < 0 ? 0 : 1;
   }
+  __syncthreads();
+  const int step = sh.step;
   if (step < 0) return -1;
-  const int base = step * kStep + lane * 8;
-  Df wd[8];
-  pweights8<TE>(gp, gq, rp, rq, ps.residual, rho, base, V, vec, sh.tab_hi, sh.tab_lo, wd);
-  Df sm{0.f, 0.f};
-  int lp = -1;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    sm = df_add(sm, wd[e]);
-    if (wd[e].hi > 0.f) lp = base + e;
-  }
-  Df fin = sm;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const Df y = df_shfl_up(fin, off);
-    if (lane >= off) fin = df_add(fin, y);
-  }
-  const unsigned h2 = exact ? __ballot_sync(0xFFFFFFFFu, df_gt(fin, trel) && sm.hi > 0.f) : 0u;
-  if (!h2) return warp_max_i(lp);
-  const int first = __ffs(h2) - 1;
-  int found = -1;
-  if (lane == first) {
-    Df run = df_sub(fin, sm);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      run = df_add(run, wd[e]);
-      if (found < 0 && wd[e].hi > 0.f && df_gt(run, trel)) found = base + e;
+  const bool exact = sh.exact != 0;
+  const Df trel = sh.trel;
+  // the step's weights, one entry a thread
+  const int v = step * kStep + t;
+  Df wv{0.f, 0.f};
+  if (t < kStep && v < V) {
+    const Df ep = hp_exp(rp, to_f32(gp[v]), sh.tab_hi, sh.tab_lo);
+    if (!ps.residual || ep.hi == 0.f) {
+      wv = ep;
+    } else {
+      const Df eq = hp_exp(rq, to_f32(gq[v]), sh.tab_hi, sh.tab_lo);
+      const Df d = df_sub(ep, df_mul(rho, eq));
+      wv = d.hi > 0.f ? d : Df{0.f, 0.f};
     }
-    if (found < 0) found = lp;
   }
-  return __shfl_sync(0xFFFFFFFFu, found, first);
+  Df Ts;
+  const Df cum = block_df_scan(sh, wv, Ts);
+  const bool pos = wv.hi > 0.f;
+  int lp;
+  const int f = block_first(sh, exact && pos && df_gt(cum, trel), pos ? v : -1, lp);
+  return f >= 0 ? step * kStep + f : lp;
 }
 
 // Clusters of Cp CTAs (grid: kPreciseGrid * Cp CTAs); cluster y redraws the
@@ -1080,7 +1109,7 @@ __device__ int precise_search(const PreciseShared &sh, const float2 *sa, const f
 // of the steps an entry of which was uncertain; then CTA 0 searches and
 // overwrites the token.  Dynamic shared memory: sa[steps], sb[steps].
 template <typename TE>
-__global__ void __launch_bounds__(kPThreads, 1) chain_precise_kernel(const Params P,
+__global__ void __launch_bounds__(kPThreads, 2) chain_precise_kernel(const Params P,
                                                                      const Exp2Table tab) {
   extern __shared__ __align__(16) unsigned char precise_smem[];
   __shared__ PreciseShared sh;
@@ -1177,9 +1206,9 @@ __global__ void __launch_bounds__(kPThreads, 1) chain_precise_kernel(const Param
       }
     }
     cluster_sync_all();
-    if (run && rank == 0 && w == 0) {
-      const int token = precise_search<TE>(sh, sa, sb, nsteps, ps, rho, gp, gq, rp, rq, vec, V);
-      if (lane == 0 && token >= 0) {
+    if (run && rank == 0) {
+      const int token = precise_search<TE>(sh, sa, sb, nsteps, ps, rho, gp, gq, rp, rq, V);
+      if (t == 0 && token >= 0) {
         const long long obase = static_cast<long long>(s) * (P.gamma + 1);
         P.out_tokens[obase + ps.j] = token;
         P.outs[obase + ps.j].token = token;
