@@ -437,6 +437,30 @@ static __device__ float block_sum(float v, RedScratch &ctl) {
 // cluster-wide top-k threshold: radix select on order keys, 8 bits per round
 // ---------------------------------------------------------------------------
 
+// Mass-histogram adds of one warp (every lane calls; bin < 0: nothing to
+// add): the lanes that share a bin are summed first, so each distinct bin of
+// the warp takes one 64-bit shared-memory atomic.  The radix rounds' keys
+// concentrate in a few bins (the high byte of an order key is mostly the
+// exponent), where per-lane 64-bit atomics on one address serialise.  Integer
+// sums: the result does not depend on the grouping.
+__device__ __forceinline__ void warp_hist_mass(unsigned long long *hist, int bin,
+                                               unsigned long long x) {
+  const int lane = threadIdx.x & 31;
+  unsigned pend = __ballot_sync(0xFFFFFFFFu, bin >= 0);
+  while (pend) {
+    const int leader = __ffs(pend) - 1;
+    const int b = __shfl_sync(0xFFFFFFFFu, bin, leader);
+    const unsigned grp = __ballot_sync(0xFFFFFFFFu, bin == b);
+    unsigned long long v = bin == b ? x : 0ull;
+    if (__popc(grp) > 1) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    }
+    if (lane == leader) atomicAdd(&hist[b], v);
+    pend &= ~grp;
+  }
+}
+
 template <typename TE>
 __device__ void topk_thresholds(const TE *sp, const TE *sq, int len, bool do_p, bool do_q,
                                 int kp, int kq, Ctl &ctl, TopkScratch &tk,
@@ -538,16 +562,25 @@ __device__ __forceinline__ unsigned long long mass_fixed(float z, float m, float
 // boundary is kept.  One radix round per 8 bits of the order key; per round a
 // mass histogram of the entries under the current prefix, summed over the
 // cluster, and a scan from the top digit by one warp per row.
+//
+// hcut[row] >= cut[row] restricts the histograms to the entries at or above
+// it (the min-p boundary, when min-p applies too): the final kept set is
+// {z >= max(top-p boundary, hcut)}, so a top-p boundary below hcut need not be
+// found - when the entries at or above hcut hold less than top_p of the mass
+// the result is -inf.  The total mass (all entries at or above cut) is summed
+// separately in round 0.
 template <typename TE>
 __device__ void topp_thresholds(const TE *sp, const TE *sq, int len, bool do_p, bool do_q,
-                                const float cut[2], const float m[2], const float k[2],
-                                const float top_p[2], Ctl &ctl, MassScratch &ms,
-                                cg::cluster_group &cluster, int C, float thr[2]) {
+                                const float cut[2], const float hcut[2], const float m[2],
+                                const float k[2], const float top_p[2], Ctl &ctl,
+                                MassScratch &ms, cg::cluster_group &cluster, int C,
+                                float thr[2]) {
   constexpr int R = Elem<TE>::kKeyRounds;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < 2) {
     ctl.prefix[tid] = 0u;
     ms.remaining[tid] = 0ull;  // set from the total in round 0
+    ms.below[tid] = 0;
   }
   for (int round = 0; round < R; ++round) {
     const int buf = round & 1;
@@ -561,13 +594,33 @@ __device__ void topp_thresholds(const TE *sp, const TE *sq, int len, bool do_p, 
       const TE *s = row == 0 ? sp : sq;
       const uint32_t want =
           static_cast<uint32_t>(static_cast<unsigned long long>(ctl.prefix[row]) << (shift + 8));
-      for (int v = tid; v < len; v += kThreads) {
-        const float z = to_f32(s[v]);
-        if (!(z >= cut[row])) continue;
-        const uint32_t key = order_key(s[v]);
-        if ((key & hmask) == want)
-          atomicAdd(&ms.hist[buf][row][(key >> shift) & 255u], mass_fixed(z, m[row], k[row]));
+      unsigned long long tot = 0ull;  // round 0: the mass of every entry at or above cut
+      for (int v0 = tid - lane; v0 < len; v0 += kThreads) {  // warp-uniform trip count
+        const int v = v0 + lane;
+        int bin = -1;
+        unsigned long long x = 0ull;
+        if (v < len) {
+          const float z = to_f32(s[v]);
+          const uint32_t key = order_key(s[v]);
+          if (round == 0 ? z >= cut[row] : z >= hcut[row] && (key & hmask) == want) {
+            x = mass_fixed(z, m[row], k[row]);
+            tot += x;
+            if (z >= hcut[row]) bin = static_cast<int>((key >> shift) & 255u);
+          }
+        }
+        warp_hist_mass(ms.hist[buf][row], bin, bin >= 0 ? x : 0ull);
       }
+      if (round == 0) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, off);
+        if (lane == 0) ms.wtot[warp][row] = tot;
+      }
+    }
+    csync();
+    if (round == 0 && tid < 2) {
+      unsigned long long t = 0ull;
+      for (int x = 0; x < kWarps; ++x) t += ms.wtot[x][tid];
+      ms.ctot[tid] = t;
     }
     csync();
     cluster_sync_all();
@@ -575,6 +628,11 @@ __device__ void topp_thresholds(const TE *sp, const TE *sq, int len, bool do_p, 
       unsigned long long g = 0ull;
       for (int r = 0; r < C; ++r) g += cluster.map_shared_rank(&ms.hist[buf][0][0], r)[i];
       (&ms.ghist[0][0])[i] = g;
+    }
+    if (round == 0 && tid < 2) {
+      unsigned long long g = 0ull;
+      for (int r = 0; r < C; ++r) g += cluster.map_shared_rank(&ms.ctot[0], r)[tid];
+      ms.gtot[tid] = g;
     }
     csync();
     if (warp < 2 && (warp == 0 ? do_p : do_q)) {
@@ -595,18 +653,25 @@ __device__ void topp_thresholds(const TE *sp, const TE *sq, int len, bool do_p, 
       }
       if (round == 0) {
         // the target: top_p of the kept mass (at least one unit, so that
-        // top_p = 0 keeps the largest value)
-        const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        // top_p = 0 keeps the largest value); below hcut when the entries at
+        // or above it do not reach it
+        const unsigned long long total = ms.gtot[row];
+        const unsigned long long hsum = __shfl_sync(0xFFFFFFFFu, incl, 31);
         double t = static_cast<double>(top_p[row]) * static_cast<double>(total);
         unsigned long long tg = static_cast<unsigned long long>(t);
         if (static_cast<double>(tg) < t) ++tg;  // ceil: the mass must reach top_p
-        if (lane == 0) ms.remaining[row] = tg > 0ull ? tg : 1ull;
+        if (tg == 0ull) tg = 1ull;
+        if (lane == 0) {
+          ms.remaining[row] = tg;
+          if (hsum < tg) ms.below[row] = 1;
+        }
         __syncwarp();
       }
       const unsigned long long need = ms.remaining[row];
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, incl >= need);
+      const bool below = ms.below[row] != 0;
+      const unsigned bal = below ? 0u : __ballot_sync(0xFFFFFFFFu, incl >= need);
       const int first = bal ? __ffs(bal) - 1 : 31;
-      if (lane == first) {
+      if (!below && lane == first) {
         unsigned long long acc = incl - s;
         int d = 255 - 8 * lane - 7;
         unsigned long long left = need - (acc < need ? acc : need);
@@ -627,7 +692,9 @@ __device__ void topp_thresholds(const TE *sp, const TE *sq, int len, bool do_p, 
   }
 #pragma unroll
   for (int row = 0; row < 2; ++row)
-    thr[row] = sizeof(TE) == 2 ? key_value_bf16(ctl.prefix[row]) : key_value_f32(ctl.prefix[row]);
+    thr[row] = ms.below[row] ? -INFINITY
+               : sizeof(TE) == 2 ? key_value_bf16(ctl.prefix[row])
+                                 : key_value_f32(ctl.prefix[row]);
   csync();
 }
 

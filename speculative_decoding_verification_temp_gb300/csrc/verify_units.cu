@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(kThreads) unit_kernel(const Params P) {
         MassScratch &ms = *reinterpret_cast<MassScratch *>(smem_raw + P.mass_off);
         float tt[2];
         const float tpv[2] = {fmaxf(topp_v[0], 0.f), fmaxf(topp_v[1], 0.f)};
-        topp_thresholds<TE>(sp, sq, len, do_topp[0], do_topp[1], cut, mm, kk2, tpv, ctl, ms,
-                            cluster, C, tt);
+        // the histograms only over the entries min-p keeps (nthr)
+        topp_thresholds<TE>(sp, sq, len, do_topp[0], do_topp[1], cut, nthr, mm, kk2, tpv, ctl,
+                            ms, cluster, C, tt);
 #pragma unroll
         for (int row = 0; row < 2; ++row)
           if (do_topp[row]) nthr[row] = fmaxf(nthr[row], tt[row]);

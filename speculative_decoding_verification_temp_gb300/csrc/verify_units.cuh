@@ -207,6 +207,10 @@ struct MassScratch {
   unsigned long long hist[2][2][256];
   unsigned long long ghist[2][256];
   unsigned long long remaining[2];
+  unsigned long long wtot[kWarps][2];  // round 0: per-warp total masses
+  unsigned long long ctot[2];          // this CTA's total masses
+  unsigned long long gtot[2];          // the cluster's total masses
+  int below[2];                        // the top-p boundary lies below hcut
 };
 
 struct __align__(16) Ctl {
