@@ -51,8 +51,8 @@
  *     stride shorter than the row, a size above the limits below, a workspace
  *     that is too small) return SPEC_ERR_INVALID_ARG before anything is
  *     launched.  SPEC_ERR_UNSUPPORTED means the call cannot be run by this
- *     build: a vocabulary too large for one thread-block cluster (the
- *     verifiers), or a top-k policy passed to spec_overlap or
+ *     build: a vocabulary beyond the limits below (the verifiers), or a
+ *     top-k, top-p or min-p policy passed to spec_overlap or
  *     spec_typical_accept.
  *     SPEC_ERR_CUDA reports a failed launch (cudaGetLastError).
  *   - Data-dependent problems never trap the GPU: they set per-sequence flag
@@ -64,10 +64,16 @@
  *     (arrival counters and the weight-task queue).  Calls that share one
  *     workspace must not overlap on the GPU.
  *
- * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; for the verifiers V >= 1 and
- * small enough that a target+draft row pair fits in 16 thread blocks' shared
- * memory (about 800k bf16 or 400k fp32 entries); spec_overlap and
- * spec_typical_accept read rows from global memory and take any V >= 1.
+ * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; V >= 1, and for the verifiers
+ * a V that the call's kernel path takes (SPEC_ERR_UNSUPPORTED otherwise):
+ *   - chains of gamma <= 31 with 16-byte-aligned rows and no row filter
+ *     (top-k, top-p, min-p) stream their rows: V <= 2,097,152;
+ *   - trees and longer chains with aligned rows and no row filter stream
+ *     slices of at most 32 KB, 64 per row: V <= 1,048,576 bf16 / 524,288 fp32;
+ *   - rows with a filter, or unaligned rows, hold a target+draft row pair in
+ *     16 thread blocks' shared memory: about 800k bf16 or 400k fp32 entries.
+ * spec_overlap and spec_typical_accept read rows from global memory and take
+ * any V >= 1.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -189,7 +195,7 @@ spec_status spec_verify_chain(
  * Size limit: shapes with spec_verify_chain_workspace_size(B, gamma, V, dtype)
  *   > SPEC_STATIC_SCRATCH_BYTES return SPEC_ERR_UNSUPPORTED before any CUDA
  *   call; use spec_verify_chain there.  For V = 128256 bf16 and gamma = 7,
- *   B = 512 fits (8.6 MiB) and B = 1024 does not (17.1 MiB).
+ *   B = 512 fits (8.7 MiB) and B = 1024 does not (17.3 MiB).
  * Address: every call looks the array's address up with cudaGetSymbolAddress
  *   in the device context current on the calling thread, so a call made after
  *   a device reset works in the new context.  The first call on each device
