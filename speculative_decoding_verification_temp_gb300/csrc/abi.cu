@@ -152,8 +152,23 @@ long long pass_records(long long B, int gamma, long long V, int esize) {
   return B * (2 * gamma + 1) * static_cast<long long>(pp.cpr) * sv::chain_records_per_chunk();
 }
 
+// 512-entry blocks of a row (the filter kernel's candidates).
+long long pass_blocks(long long V) { return (V + 511) / 512; }
+
+// Bytes of the chain path's filter data for B sequences: the rows' block
+// maxima (element type) and one (threshold, S) pair per row; 0 when the chain
+// path cannot run the shape.
+size_t pass_filter_bytes(long long B, int gamma, long long V, int esize) {
+  PassPlan pp{};
+  if (!make_pass_plan(V, esize, gamma, pp)) return 0;
+  const long long rows = B * (2 * gamma + 1);
+  return static_cast<size_t>(rows * pass_blocks(V) * esize) + 256 +
+         static_cast<size_t>(rows) * sizeof(float2);
+}
+
 struct Layout {
-  size_t wq_ctr, counters, unit_done, w_done, wq, srec, err, pctr, pseq, near_list, zero_bytes;
+  size_t wq_ctr, counters, unit_done, w_done, wq, srec, err, pctr, pseq, near_list, bmax, frec,
+      zero_bytes;
   size_t outs, stats, final_unit, first_child, refine, rpart, rc, partials, dstate, wpart, wblk, total;
   long long wq_cap;
 };
@@ -162,8 +177,9 @@ constexpr long long kMaxSliceBlocks = 2 * 16 + 1;
 
 // slices: slices per unit of the streaming kernel, 0 when only the resident
 // kernel can run the shape; recs: records of the chain path (0 when it cannot
-// run the shape).
-Layout layout(long long nseq, long long units, long long slices, long long recs) {
+// run the shape); fbytes: its filter data (pass_filter_bytes).
+Layout layout(long long nseq, long long units, long long slices, long long recs,
+              size_t fbytes) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -212,6 +228,8 @@ Layout layout(long long nseq, long long units, long long slices, long long recs)
   L.srec = take(static_cast<size_t>(recs) * sizeof(unsigned long long));
   L.pseq = take(static_cast<size_t>(qseqs) * sizeof(sv::PassSeq));
   L.near_list = take(static_cast<size_t>(qseqs) * sizeof(int32_t));
+  L.bmax = take(fbytes);  // block maxima, then the per-row filter records
+  L.frec = L.bmax;
   L.total = std::max(off, end_stream);
   return L;
 }
@@ -247,14 +265,14 @@ std::atomic<long long> g_first_wait{sv::kWaitLimitCycles};
 int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0); }
 
 // Shared launch path of the chain and tree verifiers.  16-byte aligned rows
-// without top-k, top-p or min-p filtering take the streaming chain path
-// (chains of gamma <= 31 and V <= 2,097,152: the rows, draw and precise
-// kernels) or the streaming kernel (trees, longer chains); everything else the
-// resident kernel.
+// take the streaming chain path (chains of gamma <= 31 and V <= 2,097,152:
+// the rows, filter (with a top-k, top-p or min-p array), draw and precise
+// kernels); aligned rows without filters of trees and longer chains the
+// streaming kernel; everything else the resident kernel.
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                       float *out_residual, void *workspace, size_t workspace_bytes,
                       cudaStream_t stream, bool need_draft_rows) {
-  // top-k, top-p and min-p filters all run on the resident kernel
+  // off the chain path, top-k, top-p and min-p filters run on the resident kernel
   const bool topp = P.pp != nullptr || P.pq != nullptr;
   const bool topk = P.kp != nullptr || P.kq != nullptr || topp || P.mp != nullptr ||
                     P.mq != nullptr;
@@ -263,7 +281,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   StreamPlan sp;
   PassPlan pp{};
   Plan pl;
-  const bool pass = vec && !topk && P.mode == sv::kModeChain &&
+  const bool pass = vec && P.mode == sv::kModeChain &&
                     make_pass_plan(P.V, esize, P.gamma, pp) &&
                     static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr < 0x7FFFFFFFll;
   const bool streaming = !pass && vec && !topk && make_stream_plan(P.V, esize, sp);
@@ -273,12 +291,14 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   const bool chain = P.mode == sv::kModeChain;
   const size_t promised =
       layout(P.nseq, n_units, stream_slices(P.V, esize),
-             chain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0)
+             chain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0,
+             chain ? pass_filter_bytes(P.nseq, P.gamma, P.V, esize) : 0)
           .total;
   if (workspace_bytes < promised) return SPEC_ERR_INVALID_ARG;
   const long long rows = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) : 0;
   const long long recs = rows * pp.cpr * sv::chain_records_per_chunk();
-  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs);
+  const size_t fbytes = pass && topk ? pass_filter_bytes(P.nseq, P.gamma, P.V, esize) : 0;
+  const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs, fbytes);
   if (workspace_bytes < L.total) return SPEC_ERR_INVALID_ARG;
   char *ws = static_cast<char *>(workspace);
   cudaError_t e = cudaMemsetAsync(ws, 0, L.zero_bytes, stream);
@@ -304,6 +324,15 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.pseqw = reinterpret_cast<unsigned long long *>(ws + L.pseq);
     P.near_list = reinterpret_cast<int32_t *>(ws + L.near_list);
     P.pctr = reinterpret_cast<uint32_t *>(ws + L.pctr);
+    P.nblk = static_cast<int>(pass_blocks(P.V));
+    if (topk) {  // block maxima, then 256-byte aligned per-row filter records
+      P.bmax = ws + L.bmax;
+      P.frec = reinterpret_cast<float2 *>(
+          ws + L.bmax + align_up(static_cast<size_t>(rows * P.nblk * esize), 256));
+    } else {
+      P.bmax = nullptr;
+      P.frec = nullptr;
+    }
     P.first_wait = g_first_wait.load(std::memory_order_relaxed);
     // rows kernel: its control block, then the ring of chunk slots
     const size_t rows_off = align_up(sv::chain_rows_ctl_bytes(), 128);
@@ -412,14 +441,14 @@ size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtyp
   const int esize = esize_of(dtype);
   if (B < 0 || gamma < 0 || V < 1 || esize == 0) return 0;
   return layout(B, static_cast<long long>(B) * (gamma + 1), stream_slices(V, esize),
-                pass_records(B, gamma, V, esize))
+                pass_records(B, gamma, V, esize), pass_filter_bytes(B, gamma, V, esize))
       .total;
 }
 
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
-  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0).total;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0, 0).total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

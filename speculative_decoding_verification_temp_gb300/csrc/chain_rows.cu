@@ -40,7 +40,7 @@ struct SlotInfo {
   float k;         // log2(e) / T, 0 for a greedy row
   int arg;         // greedy row: argmax record
   int v0;          // vocabulary index of the chunk's first entry
-  int pad;
+  int row;         // the chunk's row: seq (2 gamma + 1) + r
 };
 
 struct RowsCtl {
@@ -314,6 +314,28 @@ __device__ float2 sample_record_fast<float>(const float *sm, int e0, int e1, flo
   return make_float2(m, warp_sum(S));
 }
 
+// Maxima of the warp's 512-entry blocks [e0, e1) of the chunk (one lane reads
+// 16 entries of a block; entries past nb come from global memory), stored as
+// the element type: bmax[row][block].  Only calls with a row filter ask for
+// them; the filter kernel bounds each row's threshold with them.
+template <typename TE>
+__device__ void block_maxima(const Params &P, const SlotInfo &si, const TE *sm, int e0, int e1) {
+  const int lane = threadIdx.x & 31;
+  const TE *gl = static_cast<const TE *>(si.gl);
+  TE *out = static_cast<TE *>(P.bmax) + static_cast<long long>(si.row) * P.nblk;
+  for (int b0 = e0; b0 < e1; b0 += 512) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = b0 + lane * 16 + i;
+      if (e < e1) mx = fmaxf(mx, to_f32(e < si.nb ? sm[e] : gl[e]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    if (lane == 0) out[(si.v0 + b0) / 512] = from_f32<TE>(mx);
+  }
+}
+
 template <typename TE>
 __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring,
                               long long total) {
@@ -341,8 +363,9 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
       const unsigned long long bits =
           static_cast<unsigned long long>(__float_as_uint(rec.x)) |
           (static_cast<unsigned long long>(__float_as_uint(rec.y)) << 32);
-      P.srec[si.rec + warp] = bits;  // read by the decide kernel, after this kernel
+      P.srec[si.rec + warp] = bits;  // read by the draw kernel, after this kernel
     }
+    if (P.bmax && !si.arg) block_maxima<TE>(P, si, sm, e0, e1);
     __syncwarp();
     if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);
   }
@@ -380,6 +403,7 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
     si.k = arg ? 0.f : kLog2e / T;
     si.arg = arg ? 1 : 0;
     si.v0 = ci.c * CE;
+    si.row = ci.seq * (2 * P.gamma + 1) + ci.r;
     mbar_arrive_expect_tx(&ctl.full[slot], bytes);
     if (bytes) bulk_g2s_plain(ring + static_cast<size_t>(slot) * P.slot_bytes, gl, bytes,
                               &ctl.full[slot]);

@@ -22,6 +22,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
+// A float that holds a value of the element type back in that type (exact).
+template <typename TE>
+__device__ __forceinline__ TE from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ uint16_t from_f32<uint16_t>(float x) {
+  return static_cast<uint16_t>(__float_as_uint(x) >> 16);
+}
 __device__ __forceinline__ float to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }

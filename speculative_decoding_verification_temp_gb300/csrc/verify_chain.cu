@@ -127,6 +127,7 @@ __device__ __forceinline__ float pexp(float z, float m, float k) {
 // Probability of entry v with logit z under a row descriptor.
 __device__ __forceinline__ float pprob(const RowDesc &d, float z, int v) {
   if (d.onehot) return v == d.a ? 1.f : 0.f;
+  if (!(z >= d.thr)) return 0.f;  // below a filter's threshold
   return pexp(z, d.m, d.k) * d.invS;
 }
 
@@ -353,6 +354,20 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
   const int i = lane;
   RowDesc dp = row_desc(i <= gamma ? rr[i] : 0ull, p_arg, tp_bad, kp, V);
   RowDesc dq = row_desc(i < gamma ? rr[gamma + 1 + i] : 0ull, q_arg, tq_bad, kq, V);
+  if (P.frec) {
+    // filtered rows: the filter kernel's threshold and kept normaliser
+    const long long rb = static_cast<long long>(seq) * (2 * gamma + 1);
+    const float2 fp = i <= gamma ? __ldcg(P.frec + rb + i) : make_float2(-INFINITY, 0.f);
+    const float2 fq = i < gamma ? __ldcg(P.frec + rb + gamma + 1 + i) : make_float2(-INFINITY, 0.f);
+    if (!dp.onehot && fp.y > 0.f) {
+      dp.thr = fp.x;
+      dp.invS = 1.f / fp.y;
+    }
+    if (!dq.onehot && fq.y > 0.f) {
+      dq.thr = fq.x;
+      dq.invS = 1.f / fq.y;
+    }
+  }
   // rows whose sampling statistics were not finite: the finite argmax (rare)
   unsigned need = __ballot_sync(0xFFFFFFFFu, i <= gamma && !p_arg && dp.onehot);
   while (need) {
@@ -442,6 +457,391 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
 }
 
 // ---------------------------------------------------------------------------
+// 2b. filter kernel: top-k / top-p / min-p thresholds of filtered rows
+// ---------------------------------------------------------------------------
+
+constexpr int kFThreads = 256;
+constexpr int kFWarps = kFThreads / 32;
+constexpr int kFMaxBlocks = 4096;  // 512-entry blocks per row (V <= 2,097,152)
+
+struct FilterShared {
+  unsigned long long rec;  // the row's merged record
+  int hist[256];
+  unsigned long long mhist[256];
+  uint32_t prefix;
+  int kk;
+  int found;
+  unsigned long long need;
+  unsigned long long wtot[kFWarps];
+  float wsum[kFWarps];
+  int wcnt[kFWarps];
+  int ncand;
+  uint32_t bkey[kFMaxBlocks];  // block-max order keys
+  int cand[kFMaxBlocks];       // candidate blocks, ascending
+};
+
+// Scan of a 256-bin histogram from the top digit (warp 0): the digit at which
+// the running sum reaches `need`, and what is left of `need` inside it.  The
+// histogram total goes to `total`.
+template <typename T>
+__device__ __forceinline__ void scan_top(const T *hist, T need, int &digit, T &left, T &total) {
+  const int lane = threadIdx.x & 31;
+  // lane l owns digits 255 - 8 l - j, j = 0..7 (descending values)
+  T cnt[8];
+  T s = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    cnt[j] = hist[255 - 8 * lane - j];
+    s += cnt[j];
+  }
+  T incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  const unsigned bal = __ballot_sync(0xFFFFFFFFu, incl >= need);
+  const int first = bal ? __ffs(bal) - 1 : 31;
+  int d = 0;
+  T l = 0;
+  if (lane == first) {
+    T acc = incl - s;
+    d = 255 - 8 * lane - 7;
+    l = need - (acc < need ? acc : need);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (acc + cnt[j] >= need) {
+        d = 255 - 8 * lane - j;
+        l = need - acc;
+        break;
+      }
+      acc += cnt[j];
+    }
+  }
+  digit = __shfl_sync(0xFFFFFFFFu, d, first);
+  left = __shfl_sync(0xFFFFFFFFu, l, first);
+}
+
+// Order key of the kk-th largest of the n keys item(i, key) yields (false:
+// no key), 8 bits a round from the top of KB-bit keys; false when fewer
+// than kk keys exist.  The whole CTA calls it.
+template <int KB, typename F>
+__device__ bool kth_key(FilterShared &sh, int n, int kk, F item, uint32_t &out) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sh.prefix = 0u;
+    sh.kk = kk;
+    sh.found = 1;
+  }
+  for (int round = 0; round < KB / 8; ++round) {
+    const int shift = KB - 8 * (round + 1);
+    for (int i = tid; i < 256; i += kFThreads) sh.hist[i] = 0;
+    __syncthreads();
+    const uint32_t hmask = round == 0 ? 0u : (0xFFFFFFFFu << (KB - 8 * round));
+    const uint32_t want = round == 0 ? 0u : (sh.prefix << (KB - 8 * round));
+    for (int i = tid; i < n; i += kFThreads) {
+      uint32_t key;
+      if (item(i, key) && (key & hmask) == want) atomicAdd(&sh.hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      int d, left, total;
+      scan_top<int>(sh.hist, sh.kk, d, left, total);
+      if (tid == 0) {
+        if (round == 0 && total < sh.kk) sh.found = 0;
+        sh.prefix = (sh.prefix << 8) | static_cast<uint32_t>(d);
+        sh.kk = left;
+      }
+    }
+    __syncthreads();
+    if (!sh.found) return false;
+  }
+  out = sh.prefix;
+  return true;
+}
+
+template <typename TE>
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return sizeof(TE) == 2 ? key_value_bf16(k) : key_value_f32(k);
+}
+
+// Order key of a logit held as a float (for bf16 rows, the key of its bf16
+// bits).
+template <typename TE>
+__device__ __forceinline__ uint32_t zkey(float z) {
+  return sizeof(TE) == 2 ? order_key(static_cast<uint16_t>(__float_as_uint(z) >> 16))
+                         : order_key(z);
+}
+
+// One pass over the candidate blocks' entries, 8 at a time (64 groups a
+// block), four groups of a thread in flight: f(z[8], v0, ok) for every group,
+// v0 the vocabulary index of z[0] (entries at or past V read -inf), ok false
+// for a thread past the last group.  Every lane of a warp calls f the same
+// number of times, so f may use warp-collective operations.
+template <typename TE, typename F>
+__device__ void for_groups(const FilterShared &sh, const TE *g, int V, int ngroups, F f) {
+  const int lane = threadIdx.x & 31;
+  for (int jw = threadIdx.x - lane; jw < ngroups; jw += 4 * kFThreads) {
+    float z[4][8];
+    int v0[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = jw + lane + q * kFThreads;
+      const bool ok = j < ngroups;
+      v0[q] = ok ? sh.cand[j >> 6] * 512 + (j & 63) * 8 : V;
+      hp_load8<TE>(g, v0[q], ok ? V : 0, true, z[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (jw + q * kFThreads >= ngroups) break;  // warp-uniform
+      f(z[q], v0[q], jw + lane + q * kFThreads < ngroups);
+    }
+  }
+}
+
+// kth_key over the candidate entries (count histograms).
+template <typename TE>
+__device__ bool kth_entry(FilterShared &sh, const TE *g, int V, int ngroups, int kk,
+                          uint32_t &out) {
+  constexpr int KB = sizeof(TE) == 2 ? 16 : 32;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sh.prefix = 0u;
+    sh.kk = kk;
+    sh.found = 1;
+  }
+  for (int round = 0; round < KB / 8; ++round) {
+    const int shift = KB - 8 * (round + 1);
+    for (int i = tid; i < 256; i += kFThreads) sh.hist[i] = 0;
+    __syncthreads();
+    const uint32_t hmask = round == 0 ? 0u : (0xFFFFFFFFu << (KB - 8 * round));
+    const uint32_t want = round == 0 ? 0u : (sh.prefix << (KB - 8 * round));
+    for_groups<TE>(sh, g, V, ngroups, [&](const float *z, int v0, bool ok) {
+      if (!ok) return;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t key = zkey<TE>(z[e]);
+        if (v0 + e < V && (key & hmask) == want) atomicAdd(&sh.hist[(key >> shift) & 255u], 1);
+      }
+    });
+    __syncthreads();
+    if (tid < 32) {
+      int d, left, total;
+      scan_top<int>(sh.hist, sh.kk, d, left, total);
+      if (tid == 0) {
+        if (round == 0 && total < sh.kk) sh.found = 0;
+        sh.prefix = (sh.prefix << 8) | static_cast<uint32_t>(d);
+        sh.kk = left;
+      }
+    }
+    __syncthreads();
+    if (!sh.found) return false;
+  }
+  out = sh.prefix;
+  return true;
+}
+
+// mass_key over the candidate entries at or above lo.
+template <typename TE>
+__device__ bool mass_entry(FilterShared &sh, const TE *g, int V, int ngroups, float lo, float m,
+                           float k, unsigned long long need, uint32_t &out) {
+  constexpr int KB = sizeof(TE) == 2 ? 16 : 32;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sh.prefix = 0u;
+    sh.need = need;
+    sh.found = 1;
+  }
+  for (int round = 0; round < KB / 8; ++round) {
+    const int shift = KB - 8 * (round + 1);
+    for (int i = tid; i < 256; i += kFThreads) sh.mhist[i] = 0ull;
+    __syncthreads();
+    const uint32_t hmask = round == 0 ? 0u : (0xFFFFFFFFu << (KB - 8 * round));
+    const uint32_t want = round == 0 ? 0u : (sh.prefix << (KB - 8 * round));
+    for_groups<TE>(sh, g, V, ngroups, [&](const float *z, int v0, bool ok) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t key = zkey<TE>(z[e]);
+        const bool in = ok && v0 + e < V && z[e] >= lo && (key & hmask) == want;
+        warp_hist_mass(sh.mhist, in ? static_cast<int>((key >> shift) & 255u) : -1,
+                       in ? mass_fixed(z[e], m, k) : 0ull);
+      }
+    });
+    __syncthreads();
+    if (tid < 32) {
+      int d;
+      unsigned long long left, total;
+      scan_top<unsigned long long>(sh.mhist, sh.need, d, left, total);
+      if (tid == 0) {
+        if (round == 0 && total < sh.need) sh.found = 0;
+        sh.prefix = (sh.prefix << 8) | static_cast<uint32_t>(d);
+        sh.need = left;
+      }
+    }
+    __syncthreads();
+    if (!sh.found) return false;
+  }
+  out = sh.prefix;
+  return true;
+}
+
+// One CTA per row (grid: nseq (2 gamma + 1)), after the rows kernel.  For a
+// sampled row with a filter it writes frec[row] = (threshold, S over the kept
+// entries), else (-inf, 0).  The filters, in order: top-k on the logits (every
+// entry tied with the k-th largest kept), top-p on the distribution after
+// temperature and top-k (the smallest prefix of the descending values whose
+// mass reaches top_p of the kept mass, ties kept), min-p (p >= min_p max p,
+// i.e. z >= max + T ln min_p).  The kept set is {z >= max(thresholds)}.
+//
+// Only 512-entry blocks that can hold a kept entry are read: a lower bound L
+// of the final threshold selects them (block max >= L).  L is the k-th
+// largest block maximum (at most the k-th largest entry), or the min-p
+// boundary, or both; with top-p and no top-k, the top-p total needs either
+// every entry (no min-p: L = -inf) or the row statistics (with min-p: the
+// total is the single-precision S of the row).
+template <typename TE>
+__global__ void __launch_bounds__(kFThreads) chain_filter_kernel(const Params P) {
+  __shared__ FilterShared sh;
+  constexpr int KB = sizeof(TE) == 2 ? 16 : 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rps = 2 * P.gamma + 1;
+  const int rowid = static_cast<int>(blockIdx.x);
+  const int seq = rowid / rps, r = rowid - seq * rps;
+  const bool draft = r > P.gamma;
+  launch_dependents();
+  const float T = __ldg((draft ? P.Tq : P.Tp) + seq);
+  const int *kpa = draft ? P.kq : P.kp;
+  const float *ppa = draft ? P.pq : P.pp;
+  const float *mpa = draft ? P.mq : P.mp;
+  const int V = P.V, nblk = P.nblk;
+  int kk = kpa ? __ldg(kpa + seq) : 0;
+  if (kk <= 0 || kk >= V) kk = 0;
+  const float tpr = ppa ? __ldg(ppa + seq) : 1.f;
+  const float mpr = mpa ? __ldg(mpa + seq) : 0.f;
+  const bool topp = tpr < 1.f;  // NaN: off
+  const bool minp = mpr > 0.f;  // NaN: off
+  grid_dependency_wait();  // the rows kernel's records and block maxima
+  if (row_is_arg(T) || (!kk && !topp && !minp)) {
+    if (tid == 0) P.frec[rowid] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+  const TE *g = chain_row<TE>(P, seq, r);
+  if (warp == 0) {
+    const int R = P.cpr * kChainRecordsPerChunk;
+    const unsigned long long rec =
+        merge_row(P, seq, r, P.srec + static_cast<long long>(rowid) * R, false);
+    if (lane == 0) sh.rec = rec;
+  }
+  __syncthreads();
+  const float m = __uint_as_float(static_cast<uint32_t>(sh.rec));
+  const float Srow = __uint_as_float(static_cast<uint32_t>(sh.rec >> 32));
+  if (!(m > -INFINITY) || m == INFINITY || !(Srow > 0.f) || Srow == INFINITY) {
+    // statistics that are not finite: the draw kernel takes the one-hot
+    if (tid == 0) P.frec[rowid] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+  const float k = kLog2e / T;
+  const float Lm = minp ? m + T * logf(fminf(mpr, 1.f)) : -INFINITY;
+  // 1. the lower bound L and the candidate blocks
+  const TE *bm = static_cast<const TE *>(P.bmax) + static_cast<long long>(rowid) * nblk;
+  float L = -INFINITY;
+  if (kk) {
+    for (int b = tid; b < nblk; b += kFThreads) sh.bkey[b] = order_key(bm[b]);
+    __syncthreads();
+    uint32_t key;
+    const bool ok = kth_key<KB>(sh, nblk, kk, [&](int i, uint32_t &kx) {
+      kx = sh.bkey[i];
+      return true;
+    }, key);
+    L = ok ? key_value<TE>(key) : -INFINITY;
+    if (!topp) L = fmaxf(L, Lm);
+  } else if (minp) {
+    L = Lm;
+  }
+  {
+    int base = 0;
+    for (int b0 = 0; b0 < nblk; b0 += kFThreads) {
+      const int b = b0 + tid;
+      const bool c = b < nblk && to_f32(bm[b]) >= L;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, c);
+      if (lane == 0) sh.wcnt[warp] = __popc(bal);
+      __syncthreads();
+      int off = base;
+      for (int x = 0; x < warp; ++x) off += sh.wcnt[x];
+      if (c) sh.cand[off + __popc(bal & ((1u << lane) - 1u))] = b;
+      int tot = 0;
+      for (int x = 0; x < kFWarps; ++x) tot += sh.wcnt[x];
+      base += tot;
+      __syncthreads();
+    }
+    if (tid == 0) sh.ncand = base;
+    __syncthreads();
+  }
+  const int ngroups = sh.ncand * 64;
+  // 2. top-k: the k-th largest entry (every kept entry is a candidate)
+  float tk = -INFINITY;
+  if (kk) {
+    uint32_t key;
+    // not found: fewer than k candidates at or above the min-p boundary, so
+    // the top-k boundary lies below it
+    tk = kth_entry<TE>(sh, g, V, ngroups, kk, key) ? key_value<TE>(key) : -INFINITY;
+  }
+  // 3. top-p over the entries at or above the top-k boundary
+  float tpv = -INFINITY;
+  if (topp) {
+    unsigned long long total;
+    if (kk || !minp) {
+      // every entry of the top-k set is a candidate: the exact total
+      unsigned long long t = 0ull;
+      for_groups<TE>(sh, g, V, ngroups, [&](const float *z, int v0, bool ok) {
+        if (!ok) return;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (v0 + e < V && z[e] >= tk) t += mass_fixed(z[e], m, k);
+      });
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+      if (lane == 0) sh.wtot[warp] = t;
+      __syncthreads();
+      total = 0ull;
+      for (int x = 0; x < kFWarps; ++x) total += sh.wtot[x];
+      __syncthreads();
+    } else {
+      // top-p and min-p without top-k: the candidates are the min-p set; the
+      // total is the row's single-precision S (in the same fixed point)
+      total = __float2ull_rn(Srow * kMassScale);
+    }
+    const float tp = fmaxf(tpr, 0.f);
+    const double t = static_cast<double>(tp) * static_cast<double>(total);
+    unsigned long long need = static_cast<unsigned long long>(t);
+    if (static_cast<double>(need) < t) ++need;  // ceil: the mass must reach top_p
+    if (need == 0ull) need = 1ull;               // top_p <= 0 keeps the largest value
+    uint32_t key;
+    // not found: the top-p boundary lies below the min-p boundary
+    tpv = mass_entry<TE>(sh, g, V, ngroups, fmaxf(tk, Lm), m, k, need, key) ? key_value<TE>(key)
+                                                                            : -INFINITY;
+  }
+  // 4. the kept set and its normaliser
+  const float thr = fmaxf(fmaxf(tk, tpv), Lm);
+  float s = 0.f;
+  for_groups<TE>(sh, g, V, ngroups, [&](const float *z, int v0, bool ok) {
+    if (!ok) return;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (v0 + e < V && z[e] >= thr) s += pexp(z[e], m, k);
+  });
+  s = warp_sum(s);
+  if (lane == 0) sh.wsum[warp] = s;
+  __syncthreads();
+  if (tid == 0) {
+    float S = 0.f;
+    for (int x = 0; x < kFWarps; ++x) S += sh.wsum[x];
+    P.frec[rowid] = make_float2(thr, S);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 3. draw kernel: the draw weights
 // ---------------------------------------------------------------------------
 
@@ -477,11 +877,13 @@ struct Raw8<float> {
 };
 
 // Draw weights of the 8 entries from `base` given their logits.  Sampling
-// rows use packed pairs, rounding exactly like pprob().
+// rows without a filter threshold use packed pairs, rounding exactly like
+// pprob(); filtered rows take pprob() entry by entry.
 __device__ __forceinline__ void weights8(const RowDesc &dp, const RowDesc &dq, int residual,
                                          int base, const float zp[8], const float zq[8],
                                          float w[8]) {
-  if (!dp.onehot && (!residual || !dq.onehot)) {
+  if (!dp.onehot && (!residual || !dq.onehot) && dp.thr == -INFINITY &&
+      (!residual || dq.thr == -INFINITY)) {
     const uint64_t np2 = pack2(-dp.m, -dp.m), kp2 = pack2(dp.k, dp.k),
                    ip2 = pack2(dp.invS, dp.invS);
     const uint64_t nq2 = pack2(-dq.m, -dq.m), kq2 = pack2(dq.k, dq.k),
@@ -1222,6 +1624,24 @@ __global__ void __launch_bounds__(kPThreads, 2) chain_precise_kernel(const Param
 // launchers
 // ---------------------------------------------------------------------------
 
+// Launch with programmatic stream serialisation (the kernel may begin while
+// the previous one drains; it waits in grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launch with clusters of C CTAs and programmatic stream serialisation (the
 // kernel may begin while the previous one drains; it waits in
 // grid_dependency_wait).
@@ -1330,6 +1750,11 @@ cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
   if (e != cudaSuccess) return e;
   if (prof_stop) {
     e = cudaEventRecord(prof_stop, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (P.bmax) {  // a row filter: thresholds and kept normalisers first
+    e = launch_pdl(chain_filter_kernel<TE>, dim3(static_cast<unsigned>(P.nseq) * (2 * P.gamma + 1)),
+                   dim3(kFThreads), 0, stream, P);
     if (e != cudaSuccess) return e;
   }
   e = launch_cluster_pdl(chain_draw_kernel<TE>, P.nseq * Cd, kDThreads, Cd, dsmem, stream, P);

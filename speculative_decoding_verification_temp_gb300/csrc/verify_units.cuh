@@ -175,6 +175,10 @@ struct Params {
   int chunk_elems;                // entries per chunk
   int cpr;                        // chunks per row
   int steps;                      // draw search steps per row (256 entries each)
+  void *bmax;                     // [rows][nblk] the rows' 512-entry block maxima (element
+                                  //   type; NULL: no row filter in the call)
+  float2 *frec;                   // [rows] filtered rows: (threshold, kept normaliser S)
+  int nblk;                       // 512-entry blocks per row
   unsigned long long *pseqw;      // [nseq] PassSeq of each queued precise redraw
   int *near_list;                 // [nseq] sequence + 1 of each queued precise redraw
   uint32_t *pctr;                 // [0] precise redraws queued (cleared by every call)

@@ -20,10 +20,11 @@ RESID_TOL = {"f32": 1e-5, "bf16": 2e-3}
 
 def top_k_arg(k, V, force_resident):
     """The top-k argument of a call: None when no row filters (every k <= 0 or
-    >= V), which lets the library take its streaming kernels; the array itself
-    otherwise.  force_resident passes it as a CUDA tensor even when every row
-    is off: the binding forwards a device array as given, and any top-k array
-    selects the resident kernel."""
+    >= V), the array itself otherwise.  force_resident passes it as a CUDA
+    tensor even when every row is off: the binding forwards a device array as
+    given, and for trees any top-k array selects the resident kernel (chains
+    take the chain path with or without one; run_chain forces the resident
+    kernel with unaligned rows instead)."""
     if k is None:
         return None
     k = np.asarray(k)
@@ -41,8 +42,13 @@ def to_dev(arr, dtype):
 
 def run_chain(w, uniform_override=None, return_residual=False, seed=None, pad_to=None,
               workspace_tensor=None, force_resident=False):
+    """Chain verification of workload w through the binding.  force_resident:
+    rows one entry longer than V (not 16-byte aligned), which only the
+    resident kernel takes."""
     dt = w["dtype"]
     target = w["target"]
+    if force_resident and pad_to is None:
+        pad_to = target.shape[-1] + 1
     draft = w["draft"]
     if pad_to is not None:
         V = target.shape[-1]
