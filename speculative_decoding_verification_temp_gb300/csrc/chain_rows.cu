@@ -206,10 +206,13 @@ __device__ float2 chunk_record(const TE *sm, const TE *gl, int e0, int e1, int n
 // scale), then one sum of 2^((z - max) k) over independent packed chains.  A
 // NaN propagates into the sum and marks the record bad.
 template <typename TE>
-__device__ float2 sample_record_fast(const TE *sm, int e0, int e1, float k);
+__device__ float2 sample_record_fast(const TE *sm, int e0, int e1, float k, TE *bout);
 
+// bout (NULL: none): the maxima of the part's 512-entry blocks go to bout[0..]
+// (blocks that start at or past e1 are not written).
 template <>
-__device__ float2 sample_record_fast<uint16_t>(const uint16_t *sm, int e0, int e1, float k) {
+__device__ float2 sample_record_fast<uint16_t>(const uint16_t *sm, int e0, int e1, float k,
+                                               uint16_t *bout) {
   const int lane = threadIdx.x & 31;
   constexpr int G = 8;  // 2048 entries per warp
   uint4 w[G];
@@ -227,6 +230,16 @@ __device__ float2 sample_record_fast<uint16_t>(const uint16_t *sm, int e0, int e
   uint32_t h[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) h[g] = bf16x2_max(bf16x2_max(w[g].x, w[g].y), bf16x2_max(w[g].z, w[g].w));
+  if (bout) {
+#pragma unroll
+    for (int b = 0; b < G / 2; ++b) {
+      uint32_t hb = bf16x2_max(h[2 * b], h[2 * b + 1]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) hb = bf16x2_max(hb, __shfl_xor_sync(0xFFFFFFFFu, hb, off));
+      const uint32_t mb = bf16x2_max(hb, hb >> 16);  // low half: the larger of the two
+      if (lane == 0 && e0 + b * 512 < e1) bout[b] = static_cast<uint16_t>(mb & 0xFFFFu);
+    }
+  }
   uint32_t hh = bf16x2_max(bf16x2_max(bf16x2_max(h[0], h[1]), bf16x2_max(h[2], h[3])),
                            bf16x2_max(bf16x2_max(h[4], h[5]), bf16x2_max(h[6], h[7])));
 #pragma unroll
@@ -264,7 +277,8 @@ __device__ float2 sample_record_fast<uint16_t>(const uint16_t *sm, int e0, int e
 }
 
 template <>
-__device__ float2 sample_record_fast<float>(const float *sm, int e0, int e1, float k) {
+__device__ float2 sample_record_fast<float>(const float *sm, int e0, int e1, float k,
+                                            float *bout) {
   const int lane = threadIdx.x & 31;
   constexpr int G = 4;  // 1024 entries per warp
   float4 a[G], b[G];
@@ -288,6 +302,15 @@ __device__ float2 sample_record_fast<float>(const float *sm, int e0, int e1, flo
   for (int g = 0; g < G; ++g)
     mg[g] = fmaxf(fmaxf(fmaxf(a[g].x, a[g].y), fmaxf(a[g].z, a[g].w)),
                   fmaxf(fmaxf(b[g].x, b[g].y), fmaxf(b[g].z, b[g].w)));
+  if (bout) {
+#pragma unroll
+    for (int b = 0; b < G / 2; ++b) {
+      float mb = fmaxf(mg[2 * b], mg[2 * b + 1]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, off));
+      if (lane == 0 && e0 + b * 512 < e1) bout[b] = mb;
+    }
+  }
   float m = fmaxf(fmaxf(mg[0], mg[1]), fmaxf(mg[2], mg[3]));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
@@ -314,10 +337,12 @@ __device__ float2 sample_record_fast<float>(const float *sm, int e0, int e1, flo
   return make_float2(m, warp_sum(S));
 }
 
-// Maxima of the warp's 512-entry blocks [e0, e1) of the chunk (one lane reads
-// 16 entries of a block; entries past nb come from global memory), stored as
-// the element type: bmax[row][block].  Only calls with a row filter ask for
-// them; the filter kernel bounds each row's threshold with them.
+// Maxima of the warp's 512-entry blocks [e0, e1) of the chunk, stored as the
+// element type: bmax[row][block].  Only calls with a row filter ask for them;
+// the filter kernel bounds each row's threshold with them.  A lane reads 8
+// consecutive entries of each 256-entry half of a block (16-byte loads,
+// conflict-free); entries past nb (a chunk whose end is not 16-byte aligned)
+// come from global memory.
 template <typename TE>
 __device__ void block_maxima(const Params &P, const SlotInfo &si, const TE *sm, int e0, int e1) {
   const int lane = threadIdx.x & 31;
@@ -326,9 +351,20 @@ __device__ void block_maxima(const Params &P, const SlotInfo &si, const TE *sm, 
   for (int b0 = e0; b0 < e1; b0 += 512) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = b0 + lane * 16 + i;
-      if (e < e1) mx = fmaxf(mx, to_f32(e < si.nb ? sm[e] : gl[e]));
+    for (int h = 0; h < 2; ++h) {
+      const int base = b0 + h * 256 + lane * 8;
+      float z[8];
+      if (base + 8 <= e1 && base + 8 <= si.nb) {
+        load_vec<TE>(sm + base, z);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = base + i;
+          z[i] = e < e1 ? to_f32(e < si.nb ? sm[e] : gl[e]) : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, z[i]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
@@ -355,17 +391,21 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
     const SlotInfo si = ctl.info[slot];
     const TE *sm = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * P.slot_bytes);
     const int e0 = min(si.n, warp * EW), e1 = min(si.n, e0 + EW);
-    const float2 rec = (!si.arg && si.nb == si.n && (si.n & 7) == 0)
-                           ? sample_record_fast<TE>(sm, e0, e1, si.k)
-                           : chunk_record<TE>(sm, static_cast<const TE *>(si.gl), e0, e1, si.nb,
-                                              si.v0, si.arg != 0, si.k);
+    const bool fast = !si.arg && si.nb == si.n && (si.n & 7) == 0;
+    // the block maxima of a sampled row (calls with a row filter)
+    TE *bout = P.bmax && !si.arg ? static_cast<TE *>(P.bmax) +
+                                       static_cast<long long>(si.row) * P.nblk + (si.v0 + e0) / 512
+                                 : nullptr;
+    const float2 rec = fast ? sample_record_fast<TE>(sm, e0, e1, si.k, bout)
+                            : chunk_record<TE>(sm, static_cast<const TE *>(si.gl), e0, e1, si.nb,
+                                               si.v0, si.arg != 0, si.k);
     if (lane == 0) {
       const unsigned long long bits =
           static_cast<unsigned long long>(__float_as_uint(rec.x)) |
           (static_cast<unsigned long long>(__float_as_uint(rec.y)) << 32);
       P.srec[si.rec + warp] = bits;  // read by the draw kernel, after this kernel
     }
-    if (P.bmax && !si.arg) block_maxima<TE>(P, si, sm, e0, e1);
+    if (bout && !fast) block_maxima<TE>(P, si, sm, e0, e1);
     __syncwarp();
     if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);
   }

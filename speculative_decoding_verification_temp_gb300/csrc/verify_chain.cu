@@ -125,9 +125,11 @@ __device__ __forceinline__ float pexp(float z, float m, float k) {
 }
 
 // Probability of entry v with logit z under a row descriptor.
+// kF: the row may carry a filter threshold (calls with a row filter).
+template <bool kF = true>
 __device__ __forceinline__ float pprob(const RowDesc &d, float z, int v) {
   if (d.onehot) return v == d.a ? 1.f : 0.f;
-  if (!(z >= d.thr)) return 0.f;  // below a filter's threshold
+  if (kF && !(z >= d.thr)) return 0.f;  // below a filter's threshold
   return pexp(z, d.m, d.k) * d.invS;
 }
 
@@ -341,7 +343,7 @@ __device__ DecideIn decide_inputs(const Params &P, int seq) {
 // Decide sequence seq from its rows' records (one warp): the acceptance
 // tests, the first rejection j, and the draw's description in `out` (lane 0).
 // A one-hot draw needs no weights: the writer CTA writes its outputs.
-template <typename TE>
+template <typename TE, bool kF>
 __device__ void decide_seq(const Params &P, int seq, const unsigned long long *rr,
                            const DecideIn &in, bool writer, PassSeq &out) {
   const int lane = threadIdx.x & 31;
@@ -354,7 +356,7 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
   const int i = lane;
   RowDesc dp = row_desc(i <= gamma ? rr[i] : 0ull, p_arg, tp_bad, kp, V);
   RowDesc dq = row_desc(i < gamma ? rr[gamma + 1 + i] : 0ull, q_arg, tq_bad, kq, V);
-  if (P.frec) {
+  if (kF) {
     // filtered rows: the filter kernel's threshold and kept normaliser
     const long long rb = static_cast<long long>(seq) * (2 * gamma + 1);
     const float2 fp = i <= gamma ? __ldcg(P.frec + rb + i) : make_float2(-INFINITY, 0.f);
@@ -396,8 +398,8 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
     } else {
       f |= dq.flags;
       if (valid) {
-        const float px = pprob(dp, in.zp, x);
-        const float qx = pprob(dq, dq.onehot ? 0.f : in.zq, x);
+        const float px = pprob<kF>(dp, in.zp, x);
+        const float qx = pprob<kF>(dq, dq.onehot ? 0.f : in.zq, x);
         if (!(qx > 0.f)) {
           f |= SPEC_FLAG_ZERO_Q;
         } else {
@@ -561,17 +563,77 @@ __device__ bool kth_key(FilterShared &sh, int n, int kk, F item, uint32_t &out) 
   return true;
 }
 
-template <typename TE>
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return sizeof(TE) == 2 ? key_value_bf16(k) : key_value_f32(k);
-}
-
 // Order key of a logit held as a float (for bf16 rows, the key of its bf16
 // bits).
 template <typename TE>
 __device__ __forceinline__ uint32_t zkey(float z) {
   return sizeof(TE) == 2 ? order_key(static_cast<uint16_t>(__float_as_uint(z) >> 16))
                          : order_key(z);
+}
+
+// Per-warp regions of the compact candidate list (the block-key array's
+// storage, free once the candidate blocks are known).
+constexpr int kFCap = kFMaxBlocks / kFWarps;
+
+__device__ __forceinline__ const float *flist(const FilterShared &sh) {
+  return reinterpret_cast<const float *>(sh.bkey);
+}
+
+// Entry i of the compact list (warp region i / kFCap): false past the
+// region's count.
+__device__ __forceinline__ bool list_entry(const FilterShared &sh, int i, float &z) {
+  const int w = i / kFCap;
+  if (i - w * kFCap >= sh.wcnt[w]) return false;
+  z = flist(sh)[i];
+  return true;
+}
+
+// mass_key over the compact list's entries at or above lo.
+template <typename TE>
+__device__ bool mass_list(FilterShared &sh, float lo, float m, float k, unsigned long long need,
+                          uint32_t &out) {
+  constexpr int KB = sizeof(TE) == 2 ? 16 : 32;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) {
+    sh.prefix = 0u;
+    sh.need = need;
+    sh.found = 1;
+  }
+  for (int round = 0; round < KB / 8; ++round) {
+    const int shift = KB - 8 * (round + 1);
+    for (int i = tid; i < 256; i += kFThreads) sh.mhist[i] = 0ull;
+    __syncthreads();
+    const uint32_t hmask = round == 0 ? 0u : (0xFFFFFFFFu << (KB - 8 * round));
+    const uint32_t want = round == 0 ? 0u : (sh.prefix << (KB - 8 * round));
+    for (int i0 = tid - lane; i0 < kFWarps * kFCap; i0 += kFThreads) {  // warp-uniform
+      float z = 0.f;
+      const bool have = list_entry(sh, i0 + lane, z);
+      const uint32_t key = zkey<TE>(z);
+      const bool in = have && z >= lo && (key & hmask) == want;
+      warp_hist_mass(sh.mhist, in ? static_cast<int>((key >> shift) & 255u) : -1,
+                     in ? mass_fixed(z, m, k) : 0ull);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      int d;
+      unsigned long long left, total;
+      scan_top<unsigned long long>(sh.mhist, sh.need, d, left, total);
+      if (tid == 0) {
+        if (round == 0 && total < sh.need) sh.found = 0;
+        sh.prefix = (sh.prefix << 8) | static_cast<uint32_t>(d);
+        sh.need = left;
+      }
+    }
+    __syncthreads();
+    if (!sh.found) return false;
+  }
+  out = sh.prefix;
+  return true;
+}
+
+template <typename TE>
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return sizeof(TE) == 2 ? key_value_bf16(k) : key_value_f32(k);
 }
 
 // One pass over the candidate blocks' entries, 8 at a time (64 groups a
@@ -779,7 +841,83 @@ __global__ void __launch_bounds__(kFThreads) chain_filter_kernel(const Params P)
     __syncthreads();
   }
   const int ngroups = sh.ncand * 64;
-  // 2. top-k: the k-th largest entry (every kept entry is a candidate)
+  // 2. the candidate entries (z >= L) into per-warp regions of a compact
+  // list in shared memory, in a fixed order; the global passes below run only
+  // when a region overflows
+  {
+    float *list = reinterpret_cast<float *>(sh.bkey);
+    int wbase = 0;
+    for_groups<TE>(sh, g, V, ngroups, [&](const float *z, int v0, bool ok) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool in = ok && v0 + e < V && z[e] >= L;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+        const int pos = wbase + __popc(bal & ((1u << lane) - 1u));
+        if (in && pos < kFCap) list[warp * kFCap + pos] = z[e];
+        wbase += __popc(bal);
+      }
+    });
+    if (lane == 0) sh.wcnt[warp] = wbase;
+    __syncthreads();
+  }
+  bool over = false;
+  for (int x = 0; x < kFWarps; ++x) over |= sh.wcnt[x] > kFCap;
+  if (!over) {
+    float tk = -INFINITY;
+    if (kk) {
+      uint32_t key;
+      const bool ok = kth_key<KB>(sh, kFWarps * kFCap, kk, [&](int i, uint32_t &kx) {
+        float z;
+        if (!list_entry(sh, i, z)) return false;
+        kx = zkey<TE>(z);
+        return true;
+      }, key);
+      tk = ok ? key_value<TE>(key) : -INFINITY;
+    }
+    float tpv = -INFINITY;
+    if (topp) {
+      unsigned long long total;
+      if (kk) {
+        unsigned long long t = 0ull;
+        for (int i = tid; i < kFWarps * kFCap; i += kFThreads) {
+          float z;
+          if (list_entry(sh, i, z) && z >= tk) t += mass_fixed(z, m, k);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+        if (lane == 0) sh.wtot[warp] = t;
+        __syncthreads();
+        total = 0ull;
+        for (int x = 0; x < kFWarps; ++x) total += sh.wtot[x];
+        __syncthreads();
+      } else {
+        total = __float2ull_rn(Srow * kMassScale);
+      }
+      const float tp = fmaxf(tpr, 0.f);
+      const double t = static_cast<double>(tp) * static_cast<double>(total);
+      unsigned long long need = static_cast<unsigned long long>(t);
+      if (static_cast<double>(need) < t) ++need;
+      if (need == 0ull) need = 1ull;
+      uint32_t key;
+      tpv = mass_list<TE>(sh, fmaxf(tk, Lm), m, k, need, key) ? key_value<TE>(key) : -INFINITY;
+    }
+    const float thr = fmaxf(fmaxf(tk, tpv), Lm);
+    float s = 0.f;
+    for (int i = tid; i < kFWarps * kFCap; i += kFThreads) {
+      float z;
+      if (list_entry(sh, i, z) && z >= thr) s += pexp(z, m, k);
+    }
+    s = warp_sum(s);
+    if (lane == 0) sh.wsum[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+      float S = 0.f;
+      for (int x = 0; x < kFWarps; ++x) S += sh.wsum[x];
+      P.frec[rowid] = make_float2(thr, S);
+    }
+    return;
+  }
+  // 3. top-k: the k-th largest entry (every kept entry is a candidate)
   float tk = -INFINITY;
   if (kk) {
     uint32_t key;
@@ -787,7 +925,7 @@ __global__ void __launch_bounds__(kFThreads) chain_filter_kernel(const Params P)
     // the top-k boundary lies below it
     tk = kth_entry<TE>(sh, g, V, ngroups, kk, key) ? key_value<TE>(key) : -INFINITY;
   }
-  // 3. top-p over the entries at or above the top-k boundary
+  // 4. top-p over the entries at or above the top-k boundary
   float tpv = -INFINITY;
   if (topp) {
     unsigned long long total;
@@ -822,7 +960,7 @@ __global__ void __launch_bounds__(kFThreads) chain_filter_kernel(const Params P)
     tpv = mass_entry<TE>(sh, g, V, ngroups, fmaxf(tk, Lm), m, k, need, key) ? key_value<TE>(key)
                                                                             : -INFINITY;
   }
-  // 4. the kept set and its normaliser
+  // 5. the kept set and its normaliser
   const float thr = fmaxf(fmaxf(tk, tpv), Lm);
   float s = 0.f;
   for_groups<TE>(sh, g, V, ngroups, [&](const float *z, int v0, bool ok) {
@@ -879,11 +1017,12 @@ struct Raw8<float> {
 // Draw weights of the 8 entries from `base` given their logits.  Sampling
 // rows without a filter threshold use packed pairs, rounding exactly like
 // pprob(); filtered rows take pprob() entry by entry.
+template <bool kF>
 __device__ __forceinline__ void weights8(const RowDesc &dp, const RowDesc &dq, int residual,
                                          int base, const float zp[8], const float zq[8],
                                          float w[8]) {
-  if (!dp.onehot && (!residual || !dq.onehot) && dp.thr == -INFINITY &&
-      (!residual || dq.thr == -INFINITY)) {
+  if (!dp.onehot && (!residual || !dq.onehot) &&
+      (!kF || (dp.thr == -INFINITY && (!residual || dq.thr == -INFINITY)))) {
     const uint64_t np2 = pack2(-dp.m, -dp.m), kp2 = pack2(dp.k, dp.k),
                    ip2 = pack2(dp.invS, dp.invS);
     const uint64_t nq2 = pack2(-dq.m, -dq.m), kq2 = pack2(dq.k, dq.k),
@@ -906,14 +1045,14 @@ __device__ __forceinline__ void weights8(const RowDesc &dp, const RowDesc &dq, i
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    float x = pprob(dp, zp[e], base + e);
-    if (residual) x = fmaxf(x - pprob(dq, zq[e], base + e), 0.f);
+    float x = pprob<kF>(dp, zp[e], base + e);
+    if (residual) x = fmaxf(x - pprob<kF>(dq, zq[e], base + e), 0.f);
     w[e] = x;
   }
 }
 
 // Draw weights of 8 entries from `base` (entries at or past V are 0).
-template <typename TE>
+template <typename TE, bool kF>
 __device__ __forceinline__ void step_weights(const TE *gp, const TE *gq, const RowDesc &dp,
                                              const RowDesc &dq, int residual, int base, int V,
                                              float w[8]) {
@@ -937,7 +1076,7 @@ __device__ __forceinline__ void step_weights(const TE *gp, const TE *gq, const R
 #pragma unroll
     for (int e = 0; e < 8; ++e) zq[e] = 0.f;
   }
-  weights8(dp, dq, residual, base, zp, zq, w);  // the same arithmetic as the records
+  weights8<kF>(dp, dq, residual, base, zp, zq, w);  // the same arithmetic as the records
 #pragma unroll
   for (int e = 0; e < 8; ++e)
     if (base + e >= V) w[e] = 0.f;
@@ -946,41 +1085,87 @@ __device__ __forceinline__ void step_weights(const TE *gp, const TE *gq, const R
 // Totals of the draw weights of steps [b0, b1) (256 entries each) into
 // fst[step] (the NW warps of the CTA, one warp per step; full steps four (bf16)
 // or two (fp32) per warp at a time with their loads issued before any is used).
-template <typename TE, int NW>
+template <typename TE, int NW, bool kF>
 __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const RowDesc &dq,
-                            int residual, int V, int b0, int b1, float *fst) {
+                            int residual, int V, int b0, int b1, float *fst,
+                            const TE *bmp = nullptr) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   constexpr int kU = sizeof(TE) == 2 ? 4 : 2;  // 16 or 32 raw bytes a lane per step and row
   const int nfull = min(b1, V / kStep);
   int st0 = b0 + w;
-  if (!dp.onehot && (!residual || !dq.onehot)) {
-    for (; st0 + (kU - 1) * NW < nfull; st0 += NW * kU) {
-      Raw8<TE> rp[kU], rq[kU];
+  if constexpr (!kF) {
+    if (!dp.onehot && (!residual || !dq.onehot)) {
+      for (; st0 + (kU - 1) * NW < nfull; st0 += NW * kU) {
+        Raw8<TE> rp[kU], rq[kU];
 #pragma unroll
-      for (int q = 0; q < kU; ++q) {
-        const int base = (st0 + q * NW) * kStep + lane * 8;
-        rp[q].load(gp + base);
-        if (residual) rq[q].load(gq + base);
-      }
+        for (int q = 0; q < kU; ++q) {
+          const int base = (st0 + q * NW) * kStep + lane * 8;
+          rp[q].load(gp + base);
+          if (residual) rq[q].load(gq + base);
+        }
 #pragma unroll
-      for (int q = 0; q < kU; ++q) {
-        const int base = (st0 + q * NW) * kStep + lane * 8;
-        float zp[8], zq[8], x[8];
-        rp[q].get(zp);
-        rq[q].get(zq);
-        weights8(dp, dq, residual, base, zp, zq, x);
-        float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-        sm = warp_sum(sm);
-        if (lane == 0) fst[st0 + q * NW] = sm;
+        for (int q = 0; q < kU; ++q) {
+          const int base = (st0 + q * NW) * kStep + lane * 8;
+          float zp[8], zq[8], x[8];
+          rp[q].get(zp);
+          rq[q].get(zq);
+          weights8<kF>(dp, dq, residual, base, zp, zq, x);
+          float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+          sm = warp_sum(sm);
+          if (lane == 0) fst[st0 + q * NW] = sm;
+        }
       }
     }
-  }
-  for (int st = st0; st < b1; st += NW) {
-    float x[8];
-    step_weights<TE>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x);
-    float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-    sm = warp_sum(sm);
-    if (lane == 0) fst[st] = sm;
+    for (int st = st0; st < b1; st += NW) {
+      float x[8];
+      step_weights<TE, kF>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x);
+      float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+      sm = warp_sum(sm);
+      if (lane == 0) fst[st] = sm;
+    }
+  } else {
+    // a step of a filtered p row whose 512-entry block lies below the
+    // threshold has no positive weight: its total is 0 without a load
+    auto dead = [&](int st) { return bmp && to_f32(bmp[st >> 1]) < dp.thr; };
+    if (!dp.onehot && (!residual || !dq.onehot)) {
+      for (; st0 + (kU - 1) * NW < nfull; st0 += NW * kU) {
+        Raw8<TE> rp[kU], rq[kU];
+        bool dd[kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+          const int base = (st0 + q * NW) * kStep + lane * 8;
+          dd[q] = dead(st0 + q * NW);
+          if (!dd[q]) {
+            rp[q].load(gp + base);
+            if (residual) rq[q].load(gq + base);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+          const int base = (st0 + q * NW) * kStep + lane * 8;
+          float sm = 0.f;
+          if (!dd[q]) {
+            float zp[8], zq[8], x[8];
+            rp[q].get(zp);
+            rq[q].get(zq);
+            weights8<kF>(dp, dq, residual, base, zp, zq, x);
+            sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+            sm = warp_sum(sm);
+          }
+          if (lane == 0) fst[st0 + q * NW] = sm;
+        }
+      }
+    }
+    for (int st = st0; st < b1; st += NW) {
+      float sm = 0.f;
+      if (!dead(st)) {
+        float x[8];
+        step_weights<TE, kF>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x);
+        sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+        sm = warp_sum(sm);
+      }
+      if (lane == 0) fst[st] = sm;
+    }
   }
 }
 
@@ -1044,7 +1229,7 @@ struct DrawShared {
 // u * W, one warp scan of its weights the token.  The token goes to sh.token
 // (-1: no positive weight), the total to sh.W and the distance of the draw
 // from the nearer boundary of its token to sh.margin.
-template <typename TE>
+template <typename TE, bool kF>
 __device__ void step_search(DrawShared &sh, const float *tot, int nsteps, const TE *gp,
                             const TE *gq, const RowDesc &dp, const RowDesc &dq, int residual,
                             int V, float u) {
@@ -1121,7 +1306,7 @@ __device__ void step_search(DrawShared &sh, const float *tot, int nsteps, const 
       const float tr = sh.trel;
       const int base8 = step * kStep + lane * 8;
       float x[8];
-      step_weights<TE>(gp, gq, dp, dq, residual, base8, V, x);
+      step_weights<TE, kF>(gp, gq, dp, dq, residual, base8, V, x);
       float sm = 0.f;
       int lp = -1;
 #pragma unroll
@@ -1174,7 +1359,7 @@ __device__ void step_search(DrawShared &sh, const float *tot, int nsteps, const 
 // cluster resident at once for the batches the path is built for.  Dynamic
 // shared memory: the step totals tot[steps] (CTA 0 gathers all of them) and
 // room for kDrawRecords row records.
-template <typename TE>
+template <typename TE, bool kFilt>
 __global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char draw_smem[];
   __shared__ DrawShared sh;
@@ -1235,7 +1420,7 @@ __global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P
     for (int k = threadIdx.x; k < nmine; k += kDThreads) rr0[rank + k * C] = sh.rr[rank + k * C];
   cluster_sync_all();  // CTA 0 holds every merged record
   if (rank == 0) {
-    if (warp == 0) decide_seq<TE>(P, seq, sh.rr, sh.in[lane], true, sh.ps);
+    if (warp == 0) decide_seq<TE, kFilt>(P, seq, sh.rr, sh.in[lane], true, sh.ps);
     __syncthreads();
     // the description to every other CTA (as 32-bit words)
     constexpr int kWords = static_cast<int>(sizeof(PassSeq) / 4);
@@ -1254,7 +1439,10 @@ __global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P
   const int b0 = min(nsteps, rank * per), b1 = min(nsteps, b0 + per);
   const TE *gp, *gq;
   draw_rows<TE>(P, seq, ps.j, gp, gq);
-  step_totals<TE, kDWarps>(gp, gq, ps.dp, ps.dq, ps.residual, P.V, b0, b1, tot);
+  const TE *bmp = kFilt ? static_cast<const TE *>(P.bmax) +
+                              static_cast<long long>(seq * rps + ps.j) * P.nblk
+                        : nullptr;  // block maxima of the p row (filtered calls)
+  step_totals<TE, kDWarps, kFilt>(gp, gq, ps.dp, ps.dq, ps.residual, P.V, b0, b1, tot, bmp);
   __syncthreads();
   if (rank != 0) {
     float *dst = cluster.map_shared_rank(tot, 0);
@@ -1265,7 +1453,7 @@ __global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P
   cluster_arrive();
   cluster_wait();
   // 3. the search (CTA 0)
-  step_search<TE>(sh, tot, nsteps, gp, gq, ps.dp, ps.dq, ps.residual, P.V, ps.u);
+  step_search<TE, kFilt>(sh, tot, nsteps, gp, gq, ps.dp, ps.dq, ps.residual, P.V, ps.u);
   int token = sh.token;
   double W = sh.W;
   float margin = sh.margin;
@@ -1276,9 +1464,9 @@ __global__ void __launch_bounds__(kDThreads, 7) chain_draw_kernel(const Params P
     ps.dq = ps.dp;
     ps.dq.onehot = 1;
     ps.dq.a = 0;
-    step_totals<TE, kDWarps>(gp, gq, ps.dp, ps.dq, 0, P.V, 0, nsteps, tot);
+    step_totals<TE, kDWarps, kFilt>(gp, gq, ps.dp, ps.dq, 0, P.V, 0, nsteps, tot, bmp);
     __syncthreads();
-    step_search<TE>(sh, tot, nsteps, gp, gq, ps.dp, ps.dq, 0, P.V, ps.u);
+    step_search<TE, kFilt>(sh, tot, nsteps, gp, gq, ps.dp, ps.dq, 0, P.V, ps.u);
     token = sh.token;
     W = sh.W;
     margin = sh.margin;
@@ -1730,13 +1918,16 @@ cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
     prof_start = g_prof_start;
     prof_stop = g_prof_stop;
   }
-  static ClusterCache draw_cache, precise_cache;
+  static ClusterCache draw_cache, fdraw_cache, precise_cache;
   const size_t dsmem = (static_cast<size_t>(P.steps) * sizeof(float) + 15) / 16 * 16 +
                        kDrawRecords * sizeof(unsigned long long);
   const size_t psmem = static_cast<size_t>(P.steps) * 2 * sizeof(float2);
   int Cd = 1, Cp = 1;
-  cudaError_t e =
-      cluster_size(draw_cache, chain_draw_kernel<TE>, kDThreads, kDrawCluster, dsmem, Cd);
+  const bool filt = P.bmax != nullptr;
+  cudaError_t e = filt ? cluster_size(fdraw_cache, chain_draw_kernel<TE, true>, kDThreads,
+                                      kDrawCluster, dsmem, Cd)
+                       : cluster_size(draw_cache, chain_draw_kernel<TE, false>, kDThreads,
+                                      kDrawCluster, dsmem, Cd);
   if (e != cudaSuccess) return e;
   e = cluster_size(precise_cache, chain_precise_kernel<TE>, kPThreads, kPreciseCluster, psmem, Cp);
   if (e != cudaSuccess) return e;
@@ -1752,12 +1943,15 @@ cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
     e = cudaEventRecord(prof_stop, stream);
     if (e != cudaSuccess) return e;
   }
-  if (P.bmax) {  // a row filter: thresholds and kept normalisers first
+  if (filt) {  // a row filter: thresholds and kept normalisers first
     e = launch_pdl(chain_filter_kernel<TE>, dim3(static_cast<unsigned>(P.nseq) * (2 * P.gamma + 1)),
                    dim3(kFThreads), 0, stream, P);
     if (e != cudaSuccess) return e;
   }
-  e = launch_cluster_pdl(chain_draw_kernel<TE>, P.nseq * Cd, kDThreads, Cd, dsmem, stream, P);
+  e = filt ? launch_cluster_pdl(chain_draw_kernel<TE, true>, P.nseq * Cd, kDThreads, Cd, dsmem,
+                                stream, P)
+           : launch_cluster_pdl(chain_draw_kernel<TE, false>, P.nseq * Cd, kDThreads, Cd, dsmem,
+                                stream, P);
   if (e != cudaSuccess) return e;
   const int gy = std::min(P.nseq, kPreciseGrid);
   return launch_cluster_pdl(chain_precise_kernel<TE>, gy * Cp, kPThreads, Cp, psmem, stream, P,
