@@ -38,7 +38,7 @@ struct SlotInfo {
   int n;           // entries
   int nb;          // entries copied to shared memory
   float k;         // log2(e) / T, 0 for a greedy row
-  int arg;         // greedy row: argmax record
+  int arg;         // 1: greedy row (argmax record); 2: a row nobody reads (not copied)
   int v0;          // vocabulary index of the chunk's first entry
   int row;         // the chunk's row: seq (2 gamma + 1) + r
 };
@@ -389,6 +389,11 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
       mbar_wait_bounded(&ctl.full[slot], phase);
     }
     const SlotInfo si = ctl.info[slot];
+    if (si.arg == 2) {  // a row nobody reads: no copy, no record
+      __syncwarp();
+      if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);
+      continue;
+    }
     const TE *sm = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * P.slot_bytes);
     const int e0 = min(si.n, warp * EW), e1 = min(si.n, e0 + EW);
     const bool fast = !si.arg && si.nb == si.n && (si.n & 7) == 0;
@@ -430,10 +435,13 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
     const ChunkInfo ci = chunk_info(P, k);
     const float T = __ldg((ci.draft ? P.Tq : P.Tp) + ci.seq);
     const bool arg = row_is_arg(T);
+    // the draft rows of a sequence whose target is greedy are never read: a
+    // one-hot p accepts a draft iff it is p's argmax and needs no draw
+    const bool skip = ci.draft && row_is_arg(__ldg(P.Tp + ci.seq));
     const TE *gl = static_cast<const TE *>(row_ptr(ci.draft ? P.draft : P.target, ci.row,
                                                    ci.draft ? P.ld_d : P.ld_t, sizeof(TE))) +
                    static_cast<long long>(ci.c) * CE;
-    const uint32_t bytes = static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
+    const uint32_t bytes = skip ? 0u : static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
     SlotInfo &si = ctl.info[slot];
     si.gl = gl;
     si.rec = ((static_cast<long long>(ci.seq) * (2 * P.gamma + 1) + ci.r) * P.cpr + ci.c) *
@@ -441,7 +449,7 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
     si.n = ci.n;
     si.nb = static_cast<int>(bytes / sizeof(TE));
     si.k = arg ? 0.f : kLog2e / T;
-    si.arg = arg ? 1 : 0;
+    si.arg = skip ? 2 : (arg ? 1 : 0);
     si.v0 = ci.c * CE;
     si.row = ci.seq * (2 * P.gamma + 1) + ci.r;
     mbar_arrive_expect_tx(&ctl.full[slot], bytes);

@@ -355,7 +355,10 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
   // lane i holds target row i (i <= gamma) and draft row gamma + 1 + i (i < gamma)
   const int i = lane;
   RowDesc dp = row_desc(i <= gamma ? rr[i] : 0ull, p_arg, tp_bad, kp, V);
-  RowDesc dq = row_desc(i < gamma ? rr[gamma + 1 + i] : 0ull, q_arg, tq_bad, kq, V);
+  // a greedy target never reads q (its draft rows have no records): a one-hot
+  // stand-in
+  RowDesc dq = row_desc(i < gamma && !p_arg ? rr[gamma + 1 + i] : 0ull, q_arg || p_arg, tq_bad, kq, V);
+  if (p_arg) dq.flags = 0u;
   if (kF) {
     // filtered rows: the filter kernel's threshold and kept normaliser
     const long long rb = static_cast<long long>(seq) * (2 * gamma + 1);
@@ -378,7 +381,7 @@ __device__ void decide_seq(const Params &P, int seq, const unsigned long long *r
     const int a = warp_finite_argmax<TE>(chain_row<TE>(P, seq, src), V);
     if (lane == src) dp.a = a;
   }
-  need = __ballot_sync(0xFFFFFFFFu, i < gamma && !q_arg && dq.onehot);
+  need = __ballot_sync(0xFFFFFFFFu, i < gamma && !p_arg && !q_arg && dq.onehot);
   while (need) {
     const int src = __ffs(need) - 1;
     need &= need - 1;
@@ -784,7 +787,9 @@ __global__ void __launch_bounds__(kFThreads) chain_filter_kernel(const Params P)
   const bool topp = tpr < 1.f;  // NaN: off
   const bool minp = mpr > 0.f;  // NaN: off
   grid_dependency_wait();  // the rows kernel's records and block maxima
-  if (row_is_arg(T) || (!kk && !topp && !minp)) {
+  // greedy rows, and the draft rows of a greedy target (never read), take no
+  // filter
+  if (row_is_arg(T) || (draft && row_is_arg(__ldg(P.Tp + seq))) || (!kk && !topp && !minp)) {
     if (tid == 0) P.frec[rowid] = make_float2(-INFINITY, 0.f);
     return;
   }
