@@ -326,9 +326,11 @@ spec_status spec_set_profile_events(void *start_event, void *stop_event);
  */
 spec_status spec_set_wait_limit(int64_t cycles);
 
-/* Bytes of workspace spec_typical_accept needs: 8 per target row,
- * B * (gamma + 1) rows (0 for a negative size). */
-size_t spec_typical_workspace_size(int B, int gamma);
+/* Bytes of workspace spec_typical_accept needs for B sequences of gamma
+ * drafts over a vocabulary of V entries of type dtype: 256 bytes, 8 per target
+ * row (B (gamma + 1) rows), and 128 per 32 KB of each target row (the streaming
+ * form's records).  0 for a negative size, V < 1 or an unknown dtype. */
+size_t spec_typical_workspace_size(int B, int gamma, int V, spec_dtype dtype);
 
 /* Typical acceptance of a draft chain (an approximate rule: the output is not
  * distributed as the target's).  whoami-wesleyyou.top "Speculative Decoding"
@@ -351,11 +353,16 @@ size_t spec_typical_workspace_size(int B, int gamma);
  *                            +inf logit, no finite logit, or a bad temperature:
  *                            the row is the one-hot at its finite argmax) and
  *                            SPEC_FLAG_BAD_TOKEN (x_n outside [0, V): it fails).
- * workspace: device, >= spec_typical_workspace_size(B, gamma) bytes, 8-byte
- *            aligned; no contents carried between calls.
+ * workspace: device, >= spec_typical_workspace_size(B, gamma, V, dtype)
+ *            bytes, 8-byte aligned; no contents carried between calls (each
+ *            call first clears its first 256 bytes).
  * Errors: SPEC_ERR_INVALID_ARG (bad sizes, NULL pointers, ld_target < V, a
  * short or misaligned workspace, epsilon or delta negative or not finite),
- * before any launch; SPEC_ERR_CUDA for a failed launch.  Two launches.
+ * before any launch; SPEC_ERR_CUDA for a failed launch.  16-byte-aligned rows
+ * take the streaming form: one cudaMemsetAsync and three launches (the rows
+ * stream, a merge, the walk); other rows two launches.  A bounded wait of the
+ * stream that gives up sets SPEC_FLAG_TIMEOUT, 0 accepted drafts and every
+ * token -1.
  */
 spec_status spec_typical_accept(
     const void *target_logits, int64_t ld_target, spec_dtype dtype,

@@ -94,7 +94,7 @@ def load():
     lib.spec_overlap.argtypes = [_p, _i64, _p, _i64, _i, _i, _i, _i, spec_policy, spec_policy,
                                  _p, _p, _p]
     lib.spec_overlap.restype = _i
-    lib.spec_typical_workspace_size.argtypes = [_i, _i]
+    lib.spec_typical_workspace_size.argtypes = [_i, _i, _i, _i]
     lib.spec_typical_workspace_size.restype = _sz
     lib.spec_typical_accept.argtypes = [_p, _i64, _i, _i, _i, _i, spec_policy, _p,
                                         ctypes.c_float, ctypes.c_float, _p, _p, _p, _p, _sz, _p]

@@ -389,7 +389,7 @@ def typical_accept(target_logits, draft_tokens, target_temperature, epsilon, del
     out = torch.empty((B, G1), dtype=torch.int32, device=dev)
     flags = torch.empty(B, dtype=torch.int32, device=dev)
     lib = _abi.load()
-    nbytes = lib.spec_typical_workspace_size(B, gamma)
+    nbytes = lib.spec_typical_workspace_size(B, gamma, V, _DTYPES[target_logits.dtype])
     ws = workspace(dev, nbytes) if workspace_tensor is None else workspace_tensor
     code = lib.spec_typical_accept(_ptr(tl), ld_t, _DTYPES[target_logits.dtype], B, gamma, V,
                                    _abi.spec_policy(tp.data_ptr(), None),

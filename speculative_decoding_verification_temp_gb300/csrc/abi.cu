@@ -27,7 +27,7 @@ cudaError_t launch_overlap(const void *target, long long ld_t, const void *draft
 cudaError_t launch_tree_rerank(const int32_t *parent, const float *confidence, int T, int N, int m,
                                int32_t *out_nodes, int32_t *out_parent, float *out_value,
                                int32_t *out_count, uint32_t *out_flags, cudaStream_t stream);
-size_t typical_workspace_bytes(int B, int gamma);
+size_t typical_workspace_bytes(int B, int gamma, int V, int esize);
 cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B, int gamma, int V,
                            const float *Tp, const int32_t *tokens, float epsilon, float delta,
                            int32_t *out_num, int32_t *out_tokens, uint32_t *out_flags,
@@ -576,9 +576,10 @@ spec_status spec_overlap(const void *target_logits, int64_t ld_target, const voi
                                      draft_policy.temperature, out_beta, out_flags, st));
 }
 
-size_t spec_typical_workspace_size(int B, int gamma) {
-  if (B < 0 || gamma < 0 || gamma > kMaxGamma) return 0;
-  return sv::typical_workspace_bytes(B, gamma);
+size_t spec_typical_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
+  const int esize = esize_of(dtype);
+  if (B < 0 || gamma < 0 || gamma > kMaxGamma || V < 1 || esize == 0) return 0;
+  return sv::typical_workspace_bytes(B, gamma, V, esize);
 }
 
 spec_status spec_typical_accept(const void *target_logits, int64_t ld_target, spec_dtype dtype,
@@ -597,7 +598,7 @@ spec_status spec_typical_accept(const void *target_logits, int64_t ld_target, sp
     return SPEC_ERR_INVALID_ARG;
   if (target_policy.top_k || target_policy.top_p || target_policy.min_p) return SPEC_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * (gamma + 1) > 0x7FFFFFFFll / 8) return SPEC_ERR_INVALID_ARG;
-  if (workspace_bytes < sv::typical_workspace_bytes(B, gamma) ||
+  if (workspace_bytes < sv::typical_workspace_bytes(B, gamma, V, esize) ||
       (reinterpret_cast<uintptr_t>(workspace) & 7u) != 0)
     return SPEC_ERR_INVALID_ARG;
   return map_cuda(sv::launch_typical(target_logits, ld_target, esize, B, gamma, V,

@@ -12,6 +12,11 @@
 // logit costs one exponential; nothing else happens on this path (no atomics,
 // no cross-CTA waits).  Every mbarrier wait is bounded (about two seconds) and
 // sets the error word, which turns into SPEC_FLAG_TIMEOUT.
+//
+// The same stream serves typical acceptance (kTyp): only the gamma + 1 target
+// rows of each sequence, and each warp's record of a sampling row is
+// (max, S1 = sum 2^t, S2 = sum 2^t t, lowest index of the max), t = (z - max) k,
+// from which the row's entropy and p(x) follow.
 #include <mutex>
 
 #include "ops.cuh"
@@ -56,9 +61,10 @@ struct ChunkInfo {
   bool draft;
 };
 
+template <bool kTyp>
 __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
   ChunkInfo ci;
-  const int rps = 2 * P.gamma + 1;
+  const int rps = kTyp ? P.gamma + 1 : 2 * P.gamma + 1;
   const int per_seq = rps * P.cpr;
   const int k32 = static_cast<int>(k);  // the host keeps the chunk count below 2^31
   ci.seq = k32 / per_seq;
@@ -66,7 +72,7 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
   ci.r = rem / P.cpr;
   ci.c = rem - ci.r * P.cpr;
   ci.n = min(P.chunk_elems, P.V - ci.c * P.chunk_elems);
-  ci.draft = ci.r > P.gamma;
+  ci.draft = !kTyp && ci.r > P.gamma;
   ci.row = ci.draft ? static_cast<long long>(ci.seq) * P.gamma + (ci.r - P.gamma - 1)
                     : static_cast<long long>(ci.seq) * (P.gamma + 1) + ci.r;
   return ci;
@@ -372,7 +378,157 @@ __device__ void block_maxima(const Params &P, const SlotInfo &si, const TE *sm, 
   }
 }
 
+// Typical-acceptance record of this warp's part [e0, e1) of a sampling row's
+// chunk: (m, S1, S2, lowest index of m) with m the part's max, t = (z - m) k,
+// S1 = sum 2^t, S2 = sum 2^t max(t, -150) (a -inf entry adds 0 to both).  A
+// NaN or +inf entry makes S1 NaN (the record is bad).  Entries below nb come
+// from shared memory, the rest (fewer than 8) from global memory.
 template <typename TE>
+__device__ __noinline__ float4 typical_record(const TE *sm, const TE *gl, int e0, int e1, int nb,
+                                              int v0, float k) {
+  const int lane = threadIdx.x & 31;
+  auto group = [&](int base, float z[8]) {
+    if (base + 8 <= nb) {
+      load_vec<TE>(sm + base, z);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) z[e] = base + e < e1 ? to_f32(gl[base + e]) : -INFINITY;
+    }
+  };
+  float m = -INFINITY;
+  for (int base = e0 + lane * 8; base < e1; base += 256) {
+    float z[8];
+    group(base, z);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, z[e]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  const uint64_t nm2 = pack2(-m, -m), k2 = pack2(k, k);
+  uint64_t s1 = 0ull, s2 = 0ull;
+  uint32_t idx = kNoIndex;
+  bool nan = false;
+  for (int base = e0 + lane * 8; base < e1; base += 256) {
+    float z[8];
+    group(base, z);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      nan |= z[e] != z[e];
+      if (z[e] == m && m > -INFINITY && idx == kNoIndex) idx = static_cast<uint32_t>(v0 + base + e);
+    }
+    if (m == -INFINITY) continue;
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const uint64_t t2 = fmul2(fadd2(pack2(z[e], z[e + 1]), nm2), k2);
+      const uint64_t w2 = ex2_pair(t2);
+      float t0, t1;
+      unpack2(t2, t0, t1);
+      s1 = fadd2(s1, w2);
+      s2 = ffma2(w2, pack2(fmaxf(t0, -150.f), fmaxf(t1, -150.f)), s2);
+    }
+  }
+  float S1 = hsum2(s1), S2 = hsum2(s2);
+  S1 = warp_sum(S1);
+  S2 = warp_sum(S2);
+  nan = __any_sync(0xFFFFFFFFu, nan);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
+  if (nan || m == INFINITY) S1 = __int_as_float(0x7FC00000);
+  return make_float4(m, S1, S2, __uint_as_float(idx));
+}
+
+// typical_record when the warp's part is entirely in shared memory (entries a
+// multiple of 8): one load into registers, packed sums over independent
+// chains.  A NaN reaches S1 through the exponential; a -inf entry (whose
+// 2^t t would be NaN) sends the part to the clamped path.  The index field is
+// left empty: the merge kernel searches the one part that holds the row's max.
+template <typename TE>
+__device__ float4 typical_record_fast(const TE *sm, int e0, int e1, int v0, float k);
+
+template <>
+__device__ float4 typical_record_fast<uint16_t>(const uint16_t *sm, int e0, int e1, int v0,
+                                                float k) {
+  const int lane = threadIdx.x & 31;
+  constexpr int G = 8;  // 2048 entries per warp
+  uint4 w[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int base = e0 + g * 256 + lane * 8;
+    w[g] = base < e1 ? *reinterpret_cast<const uint4 *>(sm + base)
+                     : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+  }
+  uint32_t hh = 0xFF80FF80u;
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    hh = bf16x2_max(hh, bf16x2_max(bf16x2_max(w[g].x, w[g].y), bf16x2_max(w[g].z, w[g].w)));
+  const float lm = fmaxf(__uint_as_float(hh << 16), __uint_as_float(hh & 0xFFFF0000u));
+  float m = lm;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if (!(m > -INFINITY) || m == INFINITY) return make_float4(m, __int_as_float(0x7FC00000), 0.f, 0.f);
+  const uint64_t nm2 = pack2(-m, -m), k2 = pack2(k, k);
+  uint64_t a1[2] = {0ull, 0ull}, a2[2] = {0ull, 0ull};
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const uint32_t ws[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t t2 = fmul2(fadd2(bf16x2_to_pair(ws[q]), nm2), k2);
+      const uint64_t e2 = ex2_pair(t2);
+      a1[q & 1] = fadd2(a1[q & 1], e2);
+      a2[q & 1] = ffma2(e2, t2, a2[q & 1]);
+    }
+  }
+  float S1 = hsum2(fadd2(a1[0], a1[1]));
+  float S2 = hsum2(fadd2(a2[0], a2[1]));
+  S1 = warp_sum(S1);
+  S2 = warp_sum(S2);
+  return make_float4(m, S1, S2, __uint_as_float(kNoIndex));  // the merge finds the index
+}
+
+template <>
+__device__ float4 typical_record_fast<float>(const float *sm, int e0, int e1, int v0, float k) {
+  const int lane = threadIdx.x & 31;
+  constexpr int G = 4;  // 1024 entries per warp
+  float4 a[G], b[G];
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int base = e0 + g * 256 + lane * 8;
+    a[g] = base < e1 ? *reinterpret_cast<const float4 *>(sm + base) : ninf;
+    b[g] = base < e1 ? *reinterpret_cast<const float4 *>(sm + base + 4) : ninf;
+  }
+  float lm = -INFINITY;
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    lm = fmaxf(lm, fmaxf(fmaxf(fmaxf(a[g].x, a[g].y), fmaxf(a[g].z, a[g].w)),
+                         fmaxf(fmaxf(b[g].x, b[g].y), fmaxf(b[g].z, b[g].w))));
+  float m = lm;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if (!(m > -INFINITY) || m == INFINITY) return make_float4(m, __int_as_float(0x7FC00000), 0.f, 0.f);
+  const uint64_t nm2 = pack2(-m, -m), k2 = pack2(k, k);
+  uint64_t a1[4] = {0ull, 0ull, 0ull, 0ull}, a2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const uint64_t p[4] = {pack2(a[g].x, a[g].y), pack2(a[g].z, a[g].w), pack2(b[g].x, b[g].y),
+                           pack2(b[g].z, b[g].w)};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t t2 = fmul2(fadd2(p[q], nm2), k2);
+      const uint64_t e2 = ex2_pair(t2);
+      a1[q] = fadd2(a1[q], e2);
+      a2[q] = ffma2(e2, t2, a2[q]);
+    }
+  }
+  float S1 = hsum2(fadd2(fadd2(a1[0], a1[1]), fadd2(a1[2], a1[3])));
+  float S2 = hsum2(fadd2(fadd2(a2[0], a2[1]), fadd2(a2[2], a2[3])));
+  S1 = warp_sum(S1);
+  S2 = warp_sum(S2);
+  return make_float4(m, S1, S2, __uint_as_float(kNoIndex));  // the merge finds the index
+}
+
+template <typename TE, bool kTyp>
 __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring,
                               long long total) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,6 +552,26 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
     }
     const TE *sm = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * P.slot_bytes);
     const int e0 = min(si.n, warp * EW), e1 = min(si.n, e0 + EW);
+    if (kTyp) {
+      float4 rec;
+      if (si.arg) {
+        const float2 a = chunk_record<TE>(sm, static_cast<const TE *>(si.gl), e0, e1, si.nb,
+                                          si.v0, true, 0.f);
+        rec = make_float4(a.x, 0.f, 0.f, a.y);
+      } else {
+        rec = make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool fast = si.nb == si.n && (si.n & 7) == 0;
+        if (fast) rec = typical_record_fast<TE>(sm, e0, e1, si.v0, si.k);
+        // S2 is NaN with S1 finite only when a -inf entry met 2^t t: the
+        // clamped path then
+        if (!fast || (rec.z != rec.z && rec.y == rec.y) || !(rec.x > -INFINITY))
+          rec = typical_record<TE>(sm, static_cast<const TE *>(si.gl), e0, e1, si.nb, si.v0, si.k);
+      }
+      if (lane == 0) P.trec[si.rec + warp] = rec;  // read by the merge kernel, after this one
+      __syncwarp();
+      if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);
+      continue;
+    }
     const bool fast = !si.arg && si.nb == si.n && (si.n & 7) == 0;
     // the block maxima of a sampled row (calls with a row filter)
     TE *bout = P.bmax && !si.arg ? static_cast<TE *>(P.bmax) +
@@ -416,7 +592,7 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
   }
 }
 
-template <typename TE>
+template <typename TE, bool kTyp>
 __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring,
                               long long total) {
   const int NS = P.ring;
@@ -432,26 +608,27 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
   for (long long k = blockIdx.x; k < total; k += G, ++i) {
     const int slot = i % NS;
     if (i >= NS) wait_done(i - NS);
-    const ChunkInfo ci = chunk_info(P, k);
+    const ChunkInfo ci = chunk_info<kTyp>(P, k);
     const float T = __ldg((ci.draft ? P.Tq : P.Tp) + ci.seq);
     const bool arg = row_is_arg(T);
     // the draft rows of a sequence whose target is greedy are never read: a
     // one-hot p accepts a draft iff it is p's argmax and needs no draw
-    const bool skip = ci.draft && row_is_arg(__ldg(P.Tp + ci.seq));
+    const bool skip = !kTyp && ci.draft && row_is_arg(__ldg(P.Tp + ci.seq));
     const TE *gl = static_cast<const TE *>(row_ptr(ci.draft ? P.draft : P.target, ci.row,
                                                    ci.draft ? P.ld_d : P.ld_t, sizeof(TE))) +
                    static_cast<long long>(ci.c) * CE;
     const uint32_t bytes = skip ? 0u : static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
     SlotInfo &si = ctl.info[slot];
     si.gl = gl;
-    si.rec = ((static_cast<long long>(ci.seq) * (2 * P.gamma + 1) + ci.r) * P.cpr + ci.c) *
+    const int rps = kTyp ? P.gamma + 1 : 2 * P.gamma + 1;
+    si.rec = ((static_cast<long long>(ci.seq) * rps + ci.r) * P.cpr + ci.c) *
              kRConsumerWarps;
     si.n = ci.n;
     si.nb = static_cast<int>(bytes / sizeof(TE));
     si.k = arg ? 0.f : kLog2e / T;
     si.arg = skip ? 2 : (arg ? 1 : 0);
     si.v0 = ci.c * CE;
-    si.row = ci.seq * (2 * P.gamma + 1) + ci.r;
+    si.row = ci.seq * rps + ci.r;
     mbar_arrive_expect_tx(&ctl.full[slot], bytes);
     if (bytes) bulk_g2s_plain(ring + static_cast<size_t>(slot) * P.slot_bytes, gl, bytes,
                               &ctl.full[slot]);
@@ -460,14 +637,14 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
   for (int d = max(0, issued - NS); d < issued; ++d) wait_done(d);
 }
 
-template <typename TE>
+template <typename TE, bool kTyp>
 __global__ void __launch_bounds__(kRThreads, 3) chain_rows_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   RowsCtl &ctl = *reinterpret_cast<RowsCtl *>(smem_raw);
   unsigned char *ring = smem_raw + P.data_off;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long total =
-      static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * static_cast<long long>(P.cpr);
+  const long long total = static_cast<long long>(P.nseq) * (kTyp ? P.gamma + 1 : 2 * P.gamma + 1) *
+                          static_cast<long long>(P.cpr);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.ring; ++s) {
       mbar_init(&ctl.full[s], 1);
@@ -478,9 +655,9 @@ __global__ void __launch_bounds__(kRThreads, 3) chain_rows_kernel(const Params P
   }
   __syncthreads();
   if (warp < kRConsumerWarps) {
-    rows_consumer<TE>(P, ctl, ring, total);
+    rows_consumer<TE, kTyp>(P, ctl, ring, total);
   } else if (warp == kRProducerWarp && lane == 0) {
-    rows_producer<TE>(P, ctl, ring, total);
+    rows_producer<TE, kTyp>(P, ctl, ring, total);
   }
   // this CTA's work is done: the next kernel in the stream may start launching
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -488,12 +665,12 @@ __global__ void __launch_bounds__(kRThreads, 3) chain_rows_kernel(const Params P
 
 
 std::mutex g_occ_mu;
-int g_occ_dev = -1, g_occ_smem = -1, g_occ_blocks[2] = {0, 0};
+int g_occ_dev = -1, g_occ_smem = -1, g_occ_blocks[4] = {0, 0, 0, 0};
 
-template <typename TE>
+template <typename TE, bool kTyp>
 cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
-  auto kern = chain_rows_kernel<TE>;
-  const int which = sizeof(TE) == 2 ? 0 : 1;
+  auto kern = chain_rows_kernel<TE, kTyp>;
+  const int which = (sizeof(TE) == 2 ? 0 : 1) + (kTyp ? 2 : 0);
   int blocks = 0;
   {
     // resident CTAs per SM for the last (device, shared memory) pair, shared
@@ -503,7 +680,7 @@ cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_occ_mu);
     if (dev != g_occ_dev || static_cast<int>(smem) != g_occ_smem) {
-      g_occ_blocks[0] = g_occ_blocks[1] = 0;
+      g_occ_blocks[0] = g_occ_blocks[1] = g_occ_blocks[2] = g_occ_blocks[3] = 0;
       g_occ_dev = dev;
       g_occ_smem = static_cast<int>(smem);
     }
@@ -521,7 +698,8 @@ cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
     }
     blocks = g_occ_blocks[which];
   }
-  const long long total = static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * P.cpr;
+  const long long total =
+      static_cast<long long>(P.nseq) * (kTyp ? P.gamma + 1 : 2 * P.gamma + 1) * P.cpr;
   kern<<<static_cast<int>(total < blocks ? total : blocks), kRThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }
@@ -532,8 +710,13 @@ size_t chain_rows_ctl_bytes() { return sizeof(RowsCtl); }
 int chain_records_per_chunk() { return kRConsumerWarps; }
 
 cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStream_t stream) {
-  return esize == 2 ? launch_rows_t<uint16_t>(P, smem, stream)
-                    : launch_rows_t<float>(P, smem, stream);
+  return esize == 2 ? launch_rows_t<uint16_t, false>(P, smem, stream)
+                    : launch_rows_t<float, false>(P, smem, stream);
+}
+
+cudaError_t launch_typical_rows(const Params &P, int esize, size_t smem, cudaStream_t stream) {
+  return esize == 2 ? launch_rows_t<uint16_t, true>(P, smem, stream)
+                    : launch_rows_t<float, true>(P, smem, stream);
 }
 
 }  // namespace sv

@@ -36,6 +36,9 @@
 
 namespace sv {
 
+size_t chain_rows_ctl_bytes();
+cudaError_t launch_typical_rows(const Params &P, int esize, size_t smem, cudaStream_t stream);
+
 namespace {
 
 constexpr int kTyCluster = 4;
@@ -289,6 +292,164 @@ __global__ void typical_decide_kernel(const int2 *rows, const int32_t *tokens, i
   if (out_flags) out_flags[b] = flags;
 }
 
+// ---------------------------------------------------------------------------
+// the streaming form (16-byte aligned rows): the chain rows kernel's stream
+// leaves per-warp records (max, S1, S2, lowest index of the max) of every
+// target row; one warp per row merges them and runs the test
+// ---------------------------------------------------------------------------
+
+constexpr int kMWarps = 8;  // rows per CTA of the merge kernel
+constexpr uint32_t kNoIdx = 0x3FFFFFFFu;
+constexpr uint32_t kBadIdx = 0x80000000u;
+
+// Lowest index of the largest finite entry of a row (one warp; 0 when none).
+template <typename TE>
+__device__ int warp_finite_argmax_row(const TE *g, int V) {
+  const int lane = threadIdx.x & 31;
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  for (int v = lane; v < V; v += 32) {
+    const float x = to_f32(g[v]);
+    if (x == x && x != INFINITY && x > bv) {
+      bv = x;
+      bi = v;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+    if (v2 > bv || (v2 == bv && i2 < bi)) {
+      bv = v2;
+      bi = i2;
+    }
+  }
+  return bi == INT_MAX ? 0 : bi;
+}
+
+// One warp per target row: the row's statistics from its R = cpr 8 records,
+// merged in double (S1' = f S1, S2' = f (S2 + d S1) for a max that is d / k
+// below the row's, f = 2^d), then the test of the row's draft token and its
+// greedy token (the argmax, lowest index).
+template <typename TE>
+__global__ void __launch_bounds__(kMWarps * 32) typical_merge_kernel(const Params P,
+                                                                     float epsilon, float delta,
+                                                                     int2 *rows_out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gamma = P.gamma, V = P.V;
+  const long long nrows = static_cast<long long>(P.nseq) * (gamma + 1);
+  const long long row = static_cast<long long>(blockIdx.x) * kMWarps + warp;
+  if (row >= nrows) return;
+  const int seq = static_cast<int>(row / (gamma + 1)), i = static_cast<int>(row % (gamma + 1));
+  if (__ldcg(P.err)) {
+    // a bounded wait of the rows kernel gave up: no pass, no token
+    if (lane == 0) rows_out[row] = make_int2(static_cast<int>(SPEC_FLAG_TIMEOUT << 8), -1);
+    return;
+  }
+  const float T = __ldg(P.Tp + seq);
+  const bool sampled = T > 0.f && T != INFINITY;
+  const float k = sampled ? kLog2e / T : 0.f;
+  const int R = P.cpr * 8;
+  const float4 *rec = P.trec + row * R;
+  float M = -INFINITY;
+  for (int x = lane; x < R; x += 32) M = fmaxf(M, __ldcg(&rec[x].x));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  double s1 = 0.0, s2 = 0.0;
+  uint32_t idx = kNoIdx;
+  int bad = 0;
+  for (int x = lane; x < R; x += 32) {
+    const float4 r = __ldcg(&rec[x]);
+    const uint32_t bits = __float_as_uint(r.w);
+    if (sampled) {
+      if (r.y != r.y) {
+        bad = 1;
+      } else if (r.x > -INFINITY && M < INFINITY) {
+        // the record's max is d / k below the row's (r.x - M exact for the
+        // element types); single-precision scale, double sums
+        const float d = __fmul_rn(__fsub_rn(r.x, M), k);
+        const double f = static_cast<double>(fast_exp2(d));
+        s1 += f * static_cast<double>(r.y);
+        s2 += f * (static_cast<double>(r.z) + static_cast<double>(d) * static_cast<double>(r.y));
+      }
+    } else {
+      bad |= static_cast<int>(bits >> 31);
+      if (r.x == M && M > -INFINITY) idx = min(idx, (bits & ~kBadIdx) - 1u);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, off);
+    s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, off);
+    idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, off));
+    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
+  }
+  const TE *g = static_cast<const TE *>(P.target) + row * P.ld_t;
+  if (sampled && M > -INFINITY && M < INFINITY) {
+    // the lowest index of the max: in the first part (records run in
+    // vocabulary order) whose max is the row's; its record holds it when the
+    // stream computed it, else the warp searches the part
+    int first = -1;
+    for (int x0 = 0; x0 < R && first < 0; x0 += 32) {
+      const int x = x0 + lane;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, x < R && __ldcg(&rec[x].x) == M);
+      if (bal) first = x0 + __ffs(bal) - 1;
+    }
+    if (first >= 0) {
+      const uint32_t bits = __float_as_uint(__ldcg(&rec[first].w));
+      if (bits < kNoIdx) {
+        idx = bits;
+      } else {
+        const int EW = P.chunk_elems / 8;
+        const int lo = (first / 8) * P.chunk_elems + (first % 8) * EW;
+        const int hi = min(V, lo + EW);
+        for (int v0 = lo; v0 < hi && idx >= kNoIdx; v0 += 32 * 8) {
+          uint32_t mine = kNoIdx;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int v = v0 + lane * 8 + e;
+            if (v < hi && mine == kNoIdx && to_f32(g[v]) == M) mine = static_cast<uint32_t>(v);
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mine = min(mine, __shfl_xor_sync(0xFFFFFFFFu, mine, off));
+          idx = mine;
+        }
+      }
+    }
+  }
+  const bool onehot = !sampled || bad || !(s1 > 0.0);
+  int a;
+  if (onehot && sampled && M == INFINITY) {
+    a = warp_finite_argmax_row<TE>(g, V);  // +inf seen: the finite argmax
+  } else {
+    a = idx >= kNoIdx ? 0 : static_cast<int>(idx);
+  }
+  if (lane != 0) return;
+  const bool tbad = !(T >= 0.f) || T == INFINITY;
+  uint32_t flags = 0;
+  if (onehot && (tbad || bad || (sampled && !(s1 > 0.0)) || idx >= kNoIdx))
+    flags |= SPEC_FLAG_NONFINITE;
+  int pass = 0;
+  if (i < gamma) {
+    const int x = __ldg(P.tokens + static_cast<long long>(seq) * gamma + i);
+    if (x < 0 || x >= V) {
+      flags |= SPEC_FLAG_BAD_TOKEN;
+    } else if (onehot) {
+      const double thr = fmin(static_cast<double>(epsilon), static_cast<double>(delta));
+      pass = (x == a ? 1.0 : 0.0) > thr;
+    } else {
+      const double L = log2(s1);
+      const double H = 0.6931471805599453 * (L - s2 / s1);
+      const double px = exp2((static_cast<double>(to_f32(g[x])) - static_cast<double>(M)) *
+                                 static_cast<double>(k) - L);
+      const double thr =
+          fmin(static_cast<double>(epsilon), static_cast<double>(delta) * exp(-H));
+      pass = px > thr;
+    }
+  }
+  rows_out[row] = make_int2(static_cast<int>(flags << 8) | (pass ? kPass : 0), a);
+}
+
 template <typename TE>
 cudaError_t launch_rows(const void *target, long long ld_t, int B, int gamma, int V,
                         const float *Tp, const int32_t *tokens, float epsilon, float delta,
@@ -320,8 +481,18 @@ cudaError_t launch_rows(const void *target, long long ld_t, int B, int gamma, in
 
 }  // namespace
 
-size_t typical_workspace_bytes(int B, int gamma) {
-  return static_cast<size_t>(B) * (gamma + 1) * sizeof(int2);
+// Workspace: the error word (256 bytes), the per-row results, then the
+// streaming form's records.
+namespace {
+constexpr size_t kTyHead = 256;
+constexpr int kTyChunk = 32 * 1024;  // bytes of a chunk of the rows kernel
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+size_t typical_workspace_bytes(int B, int gamma, int V, int esize) {
+  const size_t rows = static_cast<size_t>(B) * (gamma + 1);
+  const size_t cpr = (static_cast<size_t>(V) * esize + kTyChunk - 1) / kTyChunk;
+  return kTyHead + align256(rows * sizeof(int2)) + rows * cpr * 8 * sizeof(float4);
 }
 
 cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B, int gamma, int V,
@@ -329,14 +500,50 @@ cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B,
                            int32_t *out_num, int32_t *out_tokens, uint32_t *out_flags,
                            void *workspace, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  if (static_cast<long long>(B) * (gamma + 1) * kTyCluster > 0x7FFFFFFFll)
-    return cudaErrorInvalidValue;
-  int2 *rows = static_cast<int2 *>(workspace);
-  const cudaError_t e =
-      esize == 2 ? launch_rows<uint16_t>(target, ld_t, B, gamma, V, Tp, tokens, epsilon, delta,
-                                         rows, stream)
-                 : launch_rows<float>(target, ld_t, B, gamma, V, Tp, tokens, epsilon, delta, rows,
-                                      stream);
+  const long long nrows = static_cast<long long>(B) * (gamma + 1);
+  char *ws = static_cast<char *>(workspace);
+  int2 *rows = reinterpret_cast<int2 *>(ws + kTyHead);
+  const bool aligned = (reinterpret_cast<uintptr_t>(target) & 15u) == 0 && (ld_t * esize) % 16 == 0;
+  const int chunk = kTyChunk / esize;
+  const long long cpr = (static_cast<long long>(V) + chunk - 1) / chunk;
+  cudaError_t e;
+  if (aligned && nrows * cpr * 8 < 0x7FFFFFFFll) {
+    // the stream: every target row read once, records, then one warp per row
+    e = cudaMemsetAsync(ws, 0, kTyHead, stream);
+    if (e != cudaSuccess) return e;
+    Params P{};
+    P.nseq = B;
+    P.gamma = gamma;
+    P.V = V;
+    P.target = target;
+    P.ld_t = ld_t;
+    P.Tp = Tp;
+    P.tokens = tokens;
+    P.err = reinterpret_cast<uint32_t *>(ws);
+    P.trec = reinterpret_cast<float4 *>(ws + kTyHead + align256(nrows * sizeof(int2)));
+    P.chunk_elems = chunk;
+    P.cpr = static_cast<int>(cpr);
+    P.ring = 2;
+    P.slot_bytes = kTyChunk;
+    P.first_wait = kWaitLimitCycles;
+    const size_t off = (chain_rows_ctl_bytes() + 127) / 128 * 128;
+    P.data_off = static_cast<int>(off);
+    e = launch_typical_rows(P, esize, off + 2 * static_cast<size_t>(kTyChunk), stream);
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = static_cast<unsigned>((nrows + kMWarps - 1) / kMWarps);
+    if (esize == 2)
+      typical_merge_kernel<uint16_t><<<blocks, kMWarps * 32, 0, stream>>>(P, epsilon, delta, rows);
+    else
+      typical_merge_kernel<float><<<blocks, kMWarps * 32, 0, stream>>>(P, epsilon, delta, rows);
+    e = cudaGetLastError();
+  } else {
+    // unaligned rows: one cluster of CTAs per row reads its slices
+    if (nrows * kTyCluster > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+    e = esize == 2 ? launch_rows<uint16_t>(target, ld_t, B, gamma, V, Tp, tokens, epsilon, delta,
+                                           rows, stream)
+                   : launch_rows<float>(target, ld_t, B, gamma, V, Tp, tokens, epsilon, delta, rows,
+                                        stream);
+  }
   if (e != cudaSuccess) return e;
   typical_decide_kernel<<<(B + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
       rows, tokens, B, gamma, out_num, out_tokens, out_flags);

@@ -171,6 +171,7 @@ struct Params {
   uint32_t *rbar;                 // grid-barrier arrivals of the redraw kernel
   // streaming chain path (rows kernel, draw kernel, precise kernel)
   unsigned long long *srec;       // [rows][chunks][8] per-warp records of the rows kernel
+  float4 *trec;                   // typical acceptance: [rows][chunks][8] (max, S1, S2, index)
   uint32_t *err;                  // bit 0: a bounded wait gave up
   int chunk_elems;                // entries per chunk
   int cpr;                        // chunks per row

@@ -47,7 +47,7 @@ def test_algorithmic_bytes_of_the_headline_workload():
 def test_committed_profiles_name_their_kernels():
     for path, unit in ((bench.TRAFFIC_FILE, bench.TRAFFIC_UNIT),
                        (bench.OVERLAP_TRAFFIC_FILE, "overlap.cu"),
-                       (bench.TYPICAL_TRAFFIC_FILE, "typical.cu")):
+                       (bench.TYPICAL_TRAFFIC_FILE, "chain_rows.cu")):
         assert os.path.exists(path)
         assert os.path.exists(os.path.join(bench.CSRC, unit))
         with open(path, encoding="utf-8") as f:

@@ -223,15 +223,20 @@ def typical_call(lib, B=2, gamma=3, V=100, dtype=1, target=FAKE, tokens=FAKE, ou
                  ld=None, eps=0.1, delta=0.5, ws=FAKE, ws_bytes=None):
     pol = pol or policy()
     if ws_bytes is None:
-        ws_bytes = lib.spec_typical_workspace_size(B, gamma)
+        ws_bytes = lib.spec_typical_workspace_size(B, gamma, V, dtype)
     return lib.spec_typical_accept(target, ld if ld is not None else V, dtype, B, gamma, V, pol,
                                    tokens, eps, delta, out, out, None, ws, ws_bytes, None)
 
 
 def test_typical_workspace_size(lib):
-    assert lib.spec_typical_workspace_size(3, 4) == 3 * 5 * 8
-    assert lib.spec_typical_workspace_size(-1, 4) == 0
-    assert lib.spec_typical_workspace_size(3, -1) == 0
+    # 256 bytes, 8 per row (rounded up to 256), 128 per 32 KB chunk of a row
+    assert lib.spec_typical_workspace_size(3, 4, 100, 1) == 256 + 256 + 15 * 1 * 128
+    assert lib.spec_typical_workspace_size(256, 7, 128256, 1) == 256 + 16384 + 2048 * 8 * 128
+    assert lib.spec_typical_workspace_size(2, 1, 16385, 0) == 256 + 256 + 4 * 3 * 128
+    assert lib.spec_typical_workspace_size(-1, 4, 100, 1) == 0
+    assert lib.spec_typical_workspace_size(3, -1, 100, 1) == 0
+    assert lib.spec_typical_workspace_size(3, 4, 0, 1) == 0
+    assert lib.spec_typical_workspace_size(3, 4, 100, 9) == 0
 
 
 def test_typical_rejects_bad_arguments(lib):
