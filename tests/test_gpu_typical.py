@@ -149,3 +149,26 @@ def test_typical_large_vocab(dtype):
     rng = np.random.default_rng(55)
     w = make(rng, 2, 3, 262147, dtype, [1.0, 0.4])
     check(w, range(2))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_typical_masked_vocabulary_and_nonfinite_large_rows(dtype):
+    # 16-byte-aligned rows take the streaming form: rows whose masked half is
+    # -inf (the records' clamped path), whole 32 KB chunks of -inf, NaN and
+    # +inf entries far from the row's max, a max shared by two entries
+    rng = np.random.default_rng(57)
+    V = 40000
+    w = make(rng, 8, 3, V, dtype, [1.0, 0.7, 1.3, 1.0, 0.0, 1.0, 2.0, 1.0])
+    t, toks = w["target"], w["tokens"]
+    t[0, :, V // 2:] = -np.inf                 # masked half
+    t[1, :, :20000] = -np.inf                  # whole chunks of -inf, then finite
+    t[2, 1, 39999] = np.nan                    # NaN at the end: one-hot at the finite argmax
+    t[3, 0, 12345] = np.inf                    # +inf: one-hot at the finite argmax
+    top = t[5, 0].max()
+    t[5, 0, 300] = top + 1.0                   # a max held twice: the lower index wins
+    t[5, 0, 30000] = top + 1.0
+    if dtype == "bf16":
+        workloads.round_bf16_inplace(t)
+    toks[0, 0] = t[0, 0].argmax()
+    toks[5, 0] = 300
+    check(w, range(8))
