@@ -194,6 +194,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def clocks_of(clk, gpu_index, call):
+    """The clocks sampled during a timed region, or, when it was too short for
+    three samples of the 100 ms sampler, those of a 1.5 s window of
+    back-to-back calls right after it."""
+    import torch
+    clocks = clk.summary()
+    if clocks["samples"] >= 3:
+        return clocks
+    with ClockSampler(gpu_index) as clk2:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 1.5:
+            for _ in range(50):
+                call()
+            torch.cuda.synchronize()
+    clocks = clk2.summary()
+    clocks["window"] = "1.5 s of back-to-back calls right after the timed region"
+    return clocks
+
+
 def oracle_sample_rate(w, n_seqs, min_s=0.0, max_passes=1):
     """The CPU oracle on the first n_seqs sequences, repeated until min_s seconds
     (at most max_passes passes): (verified rows per second, seconds, passes).
@@ -425,18 +444,7 @@ def run_ours(args):
     kernel_ms = [s_.elapsed_time(e_) for s_, e_ in zip(k_starts, k_ends)]
     ms_per_step = elapsed_ms / args.steps
     value = job_rate(world, rows, args.steps, elapsed_ms / 1e3)
-    clocks = clk.summary()
-    if clocks["samples"] < 3:
-        # the timed region was too short for the 100 ms sampler: sample a
-        # window of back-to-back calls right after it instead
-        with ClockSampler(local) as clk2:
-            t0 = time.perf_counter()
-            while time.perf_counter() - t0 < 1.5:
-                for _ in range(50):
-                    step()
-                torch.cuda.synchronize()
-        clocks = clk2.summary()
-        clocks["window"] = "1.5 s of back-to-back calls right after the timed region"
+    clocks = clocks_of(clk, local, step)
 
     # what the pages ask a verifier to report beside its speed: the accepted
     # length per target invocation and the per-position acceptance rate beta
@@ -699,6 +707,7 @@ def run_rowop(args):
             dist.barrier()
     elapsed_ms = max_over_ranks(t_begin.elapsed_time(t_end), world, dev)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clocks = clocks_of(clk, local, lambda: call(target, draft, tokens))
 
     # end to end: the inputs the op reads copied from pinned host memory, the
     # result read back
@@ -728,7 +737,7 @@ def run_rowop(args):
         "unit": op["unit"], "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": op["config"](w),
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": {"value": job_rate(world, units, 1, e2e_s), "unit": op["unit"],
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 4},
         "gpu_launches": op["launches"] * args.steps,
@@ -836,6 +845,7 @@ def run_rerank(args):
             dist.barrier()
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     elapsed_ms = max_over_ranks(sum(launch_ms), world, dev)
+    clocks = clocks_of(clk, local, lambda: sv.tree_rerank(par, conf, RERANK_M))
     e2e_steps = max(1, args.e2e_steps)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -858,7 +868,7 @@ def run_rerank(args):
         "unit": "trees/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": rerank_config(),
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": {"value": job_rate(world, RERANK_T, 1, e2e_s), "unit": "trees/s",
                 "h2d_bytes_per_step": (par_h.numel() + conf_h.numel()) * 4,
                 "d2h_bytes_per_step": out.numel() * 4},
