@@ -34,6 +34,7 @@ cudaError_t launch_typical(const void *target, long long ld_t, int esize, int B,
                            void *workspace, cudaStream_t stream);
 cudaError_t launch_chain(const Params &P, int esize, const Exp2Table &tab, size_t smem,
                          cudaStream_t stream);
+cudaError_t launch_tree_walk(const Params &P, int esize, size_t smem, cudaStream_t stream);
 size_t chain_rows_ctl_bytes();
 int chain_records_per_chunk();
 bool set_profile_events(void *start, void *stop);
@@ -152,6 +153,15 @@ long long pass_records(long long B, int gamma, long long V, int esize) {
   return B * (2 * gamma + 1) * static_cast<long long>(pp.cpr) * sv::chain_records_per_chunk();
 }
 
+// 64-bit records the rows kernel writes for T trees of N nodes on the tree
+// walk path (N target and N draft rows a tree; 0 when the walk cannot run the
+// shape).
+long long walk_records(long long T, long long N, long long V, int esize) {
+  PassPlan pp{};
+  if (N > sv::kWalkMaxNodes || !make_pass_plan(V, esize, 0, pp)) return 0;
+  return T * 2 * N * static_cast<long long>(pp.cpr) * sv::chain_records_per_chunk();
+}
+
 // 512-entry blocks of a row (the filter kernel's candidates).
 long long pass_blocks(long long V) { return (V + 511) / 512; }
 
@@ -267,7 +277,9 @@ int esize_of(spec_dtype d) { return d == SPEC_BF16 ? 2 : (d == SPEC_F32 ? 4 : 0)
 // Shared launch path of the chain and tree verifiers.  16-byte aligned rows
 // take the streaming chain path (chains of gamma <= 31 and V <= 2,097,152:
 // the rows, filter (with a top-k, top-p or min-p array), draw and precise
-// kernels); aligned rows without filters of trees and longer chains the
+// kernels) or the tree walk path (trees of at most 256 nodes without a row
+// filter, V <= 2,097,152: the first-child, rows, walk and refine kernels);
+// aligned rows without filters of larger trees and longer chains the
 // streaming kernel; everything else the resident kernel.
 spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
                       float *out_residual, void *workspace, size_t workspace_bytes,
@@ -284,18 +296,26 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
   const bool pass = vec && P.mode == sv::kModeChain &&
                     make_pass_plan(P.V, esize, P.gamma, pp) &&
                     static_cast<long long>(P.nseq) * (2 * P.gamma + 1) * pp.cpr < 0x7FFFFFFFll;
-  const bool streaming = !pass && vec && !topk && make_stream_plan(P.V, esize, sp);
-  if (!pass && !streaming && !make_plan(P.V, esize, extra, topk, topp, pl))
+  // trees of at most kWalkMaxNodes nodes without a row filter: the rows
+  // stream and the tree walk
+  const bool walk = vec && P.mode == sv::kModeTree && !topk && P.ups <= sv::kWalkMaxNodes &&
+                    make_pass_plan(P.V, esize, 0, pp) &&
+                    static_cast<long long>(P.nseq) * 2 * P.ups * pp.cpr < 0x7FFFFFFFll;
+  const bool streaming = !pass && !walk && vec && !topk && make_stream_plan(P.V, esize, sp);
+  if (!pass && !walk && !streaming && !make_plan(P.V, esize, extra, topk, topp, pl))
     return SPEC_ERR_UNSUPPORTED;
   // the caller's workspace must hold what the size query promised for the shape
   const bool chain = P.mode == sv::kModeChain;
   const size_t promised =
       layout(P.nseq, n_units, stream_slices(P.V, esize),
-             chain ? pass_records(P.nseq, P.gamma, P.V, esize) : 0,
+             chain ? pass_records(P.nseq, P.gamma, P.V, esize)
+                   : walk_records(P.nseq, P.ups, P.V, esize),
              chain ? pass_filter_bytes(P.nseq, P.gamma, P.V, esize) : 0)
           .total;
   if (workspace_bytes < promised) return SPEC_ERR_INVALID_ARG;
-  const long long rows = pass ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1) : 0;
+  const long long rows = pass   ? static_cast<long long>(P.nseq) * (2 * P.gamma + 1)
+                         : walk ? static_cast<long long>(P.nseq) * 2 * P.ups
+                                : 0;
   const long long recs = rows * pp.cpr * sv::chain_records_per_chunk();
   const size_t fbytes = pass && topk ? pass_filter_bytes(P.nseq, P.gamma, P.V, esize) : 0;
   const Layout L = layout(P.nseq, n_units, streaming ? sp.slices : 0, recs, fbytes);
@@ -339,6 +359,25 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     P.data_off = static_cast<int>(rows_off);
     e = sv::launch_chain(P, esize, exp2_table(), rows_off + static_cast<size_t>(pp.ring) * pp.slot_bytes,
                          stream);
+  } else if (walk) {
+    P.ring = pp.ring;
+    P.slot_bytes = pp.slot_bytes;
+    P.chunk_elems = pp.chunk_elems;
+    P.cpr = pp.cpr;
+    P.steps = pp.steps;
+    P.srec = reinterpret_cast<unsigned long long *>(ws + L.srec);
+    P.bmax = nullptr;
+    P.frec = nullptr;
+    P.first_wait = g_first_wait.load(std::memory_order_relaxed);
+    // the rows kernel skips the draft rows of leaves: first children first
+    int32_t *fc = reinterpret_cast<int32_t *>(ws + L.first_child);
+    e = sv::launch_first_child(P.parent, P.nseq, P.ups, fc, stream);
+    if (e != cudaSuccess) return map_cuda(e);
+    P.first_child = fc;
+    const size_t rows_off = align_up(sv::chain_rows_ctl_bytes(), 128);
+    P.data_off = static_cast<int>(rows_off);
+    e = sv::launch_tree_walk(P, esize, rows_off + static_cast<size_t>(pp.ring) * pp.slot_bytes,
+                             stream);
   } else if (streaming) {
     P.slice = sp.slice;
     P.cluster = sp.slices;
@@ -380,7 +419,7 @@ spec_status run_units(sv::Params &P, int esize, long long n_units, size_t extra,
     e = sv::launch_units(P, esize, vec, static_cast<int>(n_units), pl.smem, stream);
   }
   if (e != cudaSuccess) return map_cuda(e);
-  if (!pass) {  // the streaming chain path has its own precise redraw
+  if (!pass) {  // the streaming chain path has its own precise redraw; trees take this one
     e = sv::launch_refine(P, esize, exp2_table(), stream);
     if (e != cudaSuccess) return map_cuda(e);
   }
@@ -448,7 +487,9 @@ size_t spec_verify_chain_workspace_size(int B, int gamma, int V, spec_dtype dtyp
 size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype) {
   const int esize = esize_of(dtype);
   if (T < 0 || N < 0 || V < 1 || esize == 0) return 0;
-  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize), 0, 0).total;
+  return layout(T, static_cast<long long>(T) * N, stream_slices(V, esize),
+                walk_records(T, N, V, esize), 0)
+      .total;
 }
 
 spec_status spec_verify_chain(const void *target_logits, int64_t ld_target,

@@ -13,6 +13,11 @@
 // no cross-CTA waits).  Every mbarrier wait is bounded (about two seconds) and
 // sets the error word, which turns into SPEC_FLAG_TIMEOUT.
 //
+// Trees take the same stream (the tree walk of verify_chain.cu reads the
+// records): the N target rows of each tree, then its N draft rows, of which
+// those of leaves (no child is ever tested against them) and all of them when
+// the target is greedy are skipped.
+//
 // The same stream serves typical acceptance (kTyp): only the gamma + 1 target
 // rows of each sequence, and each warp's record of a sampling row is
 // (max, S1 = sum 2^t, S2 = sum 2^t t, lowest index of the max), t = (z - max) k,
@@ -45,7 +50,7 @@ struct SlotInfo {
   float k;         // log2(e) / T, 0 for a greedy row
   int arg;         // 1: greedy row (argmax record); 2: a row nobody reads (not copied)
   int v0;          // vocabulary index of the chunk's first entry
-  int row;         // the chunk's row: seq (2 gamma + 1) + r
+  int row;         // the chunk's row: seq * (rows per sequence) + r
 };
 
 struct RowsCtl {
@@ -61,10 +66,18 @@ struct ChunkInfo {
   bool draft;
 };
 
+// Rows a sequence (or tree) puts on the stream: a chain's gamma + 1 target and
+// gamma draft rows, a tree's N target and N draft rows, typical acceptance's
+// gamma + 1 target rows.
+template <bool kTyp>
+__device__ __forceinline__ int stream_rows(const Params &P) {
+  return kTyp ? P.gamma + 1 : (P.mode == kModeTree ? 2 * P.ups : 2 * P.gamma + 1);
+}
+
 template <bool kTyp>
 __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
   ChunkInfo ci;
-  const int rps = kTyp ? P.gamma + 1 : 2 * P.gamma + 1;
+  const int rps = stream_rows<kTyp>(P);
   const int per_seq = rps * P.cpr;
   const int k32 = static_cast<int>(k);  // the host keeps the chunk count below 2^31
   ci.seq = k32 / per_seq;
@@ -72,6 +85,11 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
   ci.r = rem / P.cpr;
   ci.c = rem - ci.r * P.cpr;
   ci.n = min(P.chunk_elems, P.V - ci.c * P.chunk_elems);
+  if (!kTyp && P.mode == kModeTree) {
+    ci.draft = ci.r >= P.ups;
+    ci.row = static_cast<long long>(ci.seq) * P.ups + (ci.draft ? ci.r - P.ups : ci.r);
+    return ci;
+  }
   ci.draft = !kTyp && ci.r > P.gamma;
   ci.row = ci.draft ? static_cast<long long>(ci.seq) * P.gamma + (ci.r - P.gamma - 1)
                     : static_cast<long long>(ci.seq) * (P.gamma + 1) + ci.r;
@@ -612,15 +630,17 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
     const float T = __ldg((ci.draft ? P.Tq : P.Tp) + ci.seq);
     const bool arg = row_is_arg(T);
     // the draft rows of a sequence whose target is greedy are never read: a
-    // one-hot p accepts a draft iff it is p's argmax and needs no draw
-    const bool skip = !kTyp && ci.draft && row_is_arg(__ldg(P.Tp + ci.seq));
+    // one-hot p accepts a draft iff it is p's argmax and needs no draw; nor
+    // are the draft rows of a tree's leaves
+    bool skip = !kTyp && ci.draft && row_is_arg(__ldg(P.Tp + ci.seq));
+    if (!kTyp && ci.draft && !skip && P.mode == kModeTree) skip = __ldg(P.first_child + ci.row) < 0;
     const TE *gl = static_cast<const TE *>(row_ptr(ci.draft ? P.draft : P.target, ci.row,
                                                    ci.draft ? P.ld_d : P.ld_t, sizeof(TE))) +
                    static_cast<long long>(ci.c) * CE;
     const uint32_t bytes = skip ? 0u : static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
     SlotInfo &si = ctl.info[slot];
     si.gl = gl;
-    const int rps = kTyp ? P.gamma + 1 : 2 * P.gamma + 1;
+    const int rps = stream_rows<kTyp>(P);
     si.rec = ((static_cast<long long>(ci.seq) * rps + ci.r) * P.cpr + ci.c) *
              kRConsumerWarps;
     si.n = ci.n;
@@ -643,8 +663,8 @@ __global__ void __launch_bounds__(kRThreads, 3) chain_rows_kernel(const Params P
   RowsCtl &ctl = *reinterpret_cast<RowsCtl *>(smem_raw);
   unsigned char *ring = smem_raw + P.data_off;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long total = static_cast<long long>(P.nseq) * (kTyp ? P.gamma + 1 : 2 * P.gamma + 1) *
-                          static_cast<long long>(P.cpr);
+  const long long total =
+      static_cast<long long>(P.nseq) * stream_rows<kTyp>(P) * static_cast<long long>(P.cpr);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.ring; ++s) {
       mbar_init(&ctl.full[s], 1);
@@ -698,8 +718,9 @@ cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
     }
     blocks = g_occ_blocks[which];
   }
-  const long long total =
-      static_cast<long long>(P.nseq) * (kTyp ? P.gamma + 1 : 2 * P.gamma + 1) * P.cpr;
+  const long long rps =
+      kTyp ? P.gamma + 1 : (P.mode == kModeTree ? 2ll * P.ups : 2ll * P.gamma + 1);
+  const long long total = static_cast<long long>(P.nseq) * rps * P.cpr;
   kern<<<static_cast<int>(total < blocks ? total : blocks), kRThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }

@@ -252,13 +252,15 @@ __device__ void write_outputs(const Params &P, int s, const PassSeq &ps, int tok
   P.final_unit[s] = static_cast<int>(unit);
 }
 
-// The merged record of row r of sequence seq (one warp; the value in every
-// lane) from the row's R records at `rec` (global memory, or a shared-memory
-// copy): the rows kernel stored all of them before this kernel.
+// The merged record of row r of sequence (or tree) seq (one warp; the value in
+// every lane) from the row's R records at `rec` (global memory, or a
+// shared-memory copy): the rows kernel stored all of them before this kernel.
+// A chain's rows are its gamma + 1 target rows, then its draft rows; a tree's
+// its N target rows, then its N draft rows.
 __device__ unsigned long long merge_row(const Params &P, int seq, int r,
                                         const unsigned long long *rec, bool shared) {
   const int lane = threadIdx.x & 31;
-  const bool draft = r > P.gamma;
+  const bool draft = P.mode == kModeTree ? r >= P.ups : r > P.gamma;
   const float T = __ldg((draft ? P.Tq : P.Tp) + seq);
   const bool arg = row_is_arg(T);
   const float k = arg ? 0.f : kLog2e / T;
@@ -1814,6 +1816,433 @@ __global__ void __launch_bounds__(kPThreads, 2) chain_precise_kernel(const Param
 }
 
 // ---------------------------------------------------------------------------
+// 5. tree walk kernel: one cluster per tree
+// ---------------------------------------------------------------------------
+
+constexpr int kWalkCluster = 16;  // CTAs per tree (fewer when such a cluster cannot run)
+static_assert(kWalkMaxNodes <= 2 * kDThreads, "the shape pass takes two nodes a thread");
+
+struct WalkShared {
+  unsigned long long rr[2 * kWalkMaxNodes];  // merged records: target rows, then draft rows
+  int par[kWalkMaxNodes];                    // parent of each node
+  int kids[kWalkMaxNodes];                   // children of the current node, ascending
+  int path[kWalkMaxNodes];                   // the walked path, root first
+  int rows[2 * kWalkMaxNodes];               // the rows that have records
+  int cx[32];                                // acceptance-test inputs of the first 32
+  float czp[32], czq[32], cua[32];           //   children: token, its logits, uniform
+  double part[2][kMaxCluster];               // every CTA's share of a pass total (by parity)
+  RowDesc dp, dq;                            // the current node's rows
+  int nk, nrows, accept;
+  uint32_t tf;
+};
+
+// One pass of the cluster over the current node's rows (every thread of every
+// CTA): the 256-entry step totals of the draw weights [p - c q]_+ (p itself
+// for c = 0) of this CTA's share of the steps, into CTA 0's array, and the
+// total over the row, the same double in every CTA (the CTAs' shares added
+// in rank order).  `parity` alternates between consecutive passes: a CTA
+// reads the shares of a pass before it arrives at the next pass's barrier, so
+// the pass after next may overwrite them.
+template <typename TE>
+__device__ double walk_pass(WalkShared &ws, cg::cluster_group &cluster, int C, int rank,
+                            float *tot, const TE *gp, const TE *gq, const RowDesc &dp,
+                            const RowDesc &dq, float c, int V, int nsteps, int parity) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (nsteps + C - 1) / C;
+  const int b0 = min(nsteps, rank * per), b1 = min(nsteps, b0 + per);
+  const int residual = c > 0.f ? 1 : 0;
+  RowDesc dqc = dq;
+  if (residual && !dq.onehot) dqc.invS = dq.invS * c;  // c q_v = 2^((z - m) k) (c / S_q)
+  step_totals<TE, kDWarps, false>(gp, gq, dp, dqc, residual, V, b0, b1, tot);
+  __syncthreads();
+  if (warp == 0) {
+    double s = 0.0;
+    for (int st = b0 + lane; st < b1; st += 32) s += static_cast<double>(tot[st]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    if (lane < C) cluster.map_shared_rank(&ws.part[parity][0], lane)[rank] = s;
+  }
+  if (rank != 0) {
+    float *dst = cluster.map_shared_rank(tot, 0);
+    for (int st = b0 + threadIdx.x; st < b1; st += kDThreads) dst[st] = tot[st];
+  }
+  cluster_sync_all();
+  double W = 0.0;
+  for (int r = 0; r < C; ++r) W += ws.part[parity][r];
+  return W;
+}
+
+// Outputs of a walked tree (every thread of CTA 0): the path, the accepted
+// tokens and the final token at position `depth`, and the final unit's record
+// that the refine and residual-output kernels read.
+__device__ void walk_outputs(const Params &P, const WalkShared &ws, int tree, int depth,
+                             int token, uint32_t flags, const RowDesc &dp, const RowDesc &dq,
+                             float c, float total, int kind, int nres, int near) {
+  const int N = P.ups;
+  const long long nbase = static_cast<long long>(tree) * N;
+  const int width = P.max_depth + 1;
+  const long long obase = static_cast<long long>(tree) * width;
+  for (int i = threadIdx.x; i < width; i += kDThreads) {
+    P.out_path[obase + i] = i <= depth ? ws.path[i] : -1;
+    int v = -1;
+    if (i < depth) v = __ldg(P.tokens + nbase + ws.path[i + 1]);
+    else if (i == depth) v = token;
+    P.out_tokens[obase + i] = v;
+  }
+  if (threadIdx.x == 0) {
+    const int cur = ws.path[depth];
+    const long long unit = nbase + cur;
+    P.out_num[tree] = depth;
+    if (P.out_flags) P.out_flags[tree] = flags;
+    UnitOut o;
+    o.next = -1;
+    o.token = token;
+    o.flags = flags;
+    o.near = near;
+    P.outs[unit] = o;
+    UnitStats st;
+    st.p = dp;
+    st.q = dq;
+    st.c = c;
+    st.total = total;
+    st.kind = kind;
+    st.node = cur;
+    st.n_res = nres;
+    st.pad = 0;
+    P.stats[unit] = st;
+    P.final_unit[tree] = static_cast<int>(unit);
+    queue_refine(P, tree, unit, depth, near);
+  }
+}
+
+// A tree without a walk (every thread of CTA 0): an invalid tree (num = -1)
+// or a bounded wait of the rows kernel that gave up (num = 0); every path
+// entry and token -1.
+__device__ void walk_no_result(const Params &P, int tree, int num, uint32_t flags) {
+  const int width = P.max_depth + 1;
+  const long long obase = static_cast<long long>(tree) * width;
+  for (int i = threadIdx.x; i < width; i += kDThreads) {
+    P.out_path[obase + i] = -1;
+    P.out_tokens[obase + i] = -1;
+  }
+  if (threadIdx.x == 0) {
+    P.out_num[tree] = num;
+    if (P.out_flags) P.out_flags[tree] = flags;
+    P.final_unit[tree] = -1;
+  }
+}
+
+// One cluster of C CTAs per tree (grid: T * C CTAs), after the rows kernel
+// has left the records of the tree's N target rows and of the draft rows of
+// its internal nodes.  Every CTA merges its share of the rows and hands the
+// merged records to every CTA; then all CTAs walk the tree together, taking
+// the same decisions from the same data: at node n with sampled p, child
+// tokens are tested in ascending id against the held distribution
+// [p - c q]_+ / M (p itself before the first rejection: c = 0, M = 1), each
+// rejection followed by one pass of the cluster over n's rows for the next
+// multiplier c' = c + M and its total M' (a zero M' keeps the held
+// distribution and flags the residual degenerate); a greedy p accepts the
+// first child equal to its argmax.  Only the nodes on the walked path are
+// ever touched.  The final draw (every child rejected, or a leaf's bonus
+// draw from p) is CTA 0's double-float search over the step totals of the
+// last pass; a draw within the refine guard of a boundary is queued for the
+// refine kernel, which recomputes the multipliers in double precision.
+// Dynamic shared memory: the step totals tot[steps] and room for
+// kDrawRecords records.
+template <typename TE>
+__global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char walk_smem[];
+  __shared__ WalkShared ws;
+  __shared__ DrawShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int tree = static_cast<int>(blockIdx.x) / C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = P.ups, V = P.V, nsteps = P.steps;
+  const long long nbase = static_cast<long long>(tree) * N;
+  float *tot = reinterpret_cast<float *>(walk_smem);
+  unsigned long long *srec = reinterpret_cast<unsigned long long *>(
+      walk_smem + (static_cast<size_t>(nsteps) * sizeof(float) + 15) / 16 * 16);
+  // every CTA of the cluster has started before the first remote access: the
+  // arrive here pairs with the first wait below
+  cluster_arrive();
+  launch_dependents();
+  // 1. the tree's shape, from the inputs alone: every parent id below its
+  // child's, every depth within max_depth (depths by pointer jumping, with
+  // kids and path as scratch)
+  int *anc = ws.kids, *dep = ws.path;
+  int bad = 0;
+  for (int n = tid; n < N; n += kDThreads) {
+    const int a = __ldg(P.parent + nbase + n);
+    ws.par[n] = a;
+    if (n == 0 ? a != -1 : !(a >= 0 && a < n)) bad = 1;
+    anc[n] = n == 0 ? 0 : a;
+    dep[n] = n == 0 ? 0 : 1;
+  }
+  uint32_t tflags = __syncthreads_or(bad) ? SPEC_FLAG_BAD_TREE : 0u;
+  if (!tflags) {
+    for (int span = 1; span < N; span <<= 1) {
+      int la[2] = {0, 0}, ld[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int n = tid + i * kDThreads;
+        if (n < N) {
+          const int a = anc[n];
+          la[i] = anc[a];
+          ld[i] = dep[n] + dep[a];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int n = tid + i * kDThreads;
+        if (n < N) {
+          anc[n] = la[i];
+          dep[n] = ld[i];
+        }
+      }
+      __syncthreads();
+    }
+    int deep = 0;
+    for (int n = tid; n < N; n += kDThreads)
+      if (dep[n] > P.max_depth) deep = 1;
+    if (__syncthreads_or(deep)) tflags = SPEC_FLAG_DEPTH;
+  }
+  const float Tp = __ldg(P.Tp + tree), Tq = __ldg(P.Tq + tree);
+  const bool p_arg = row_is_arg(Tp), q_arg = row_is_arg(Tq);
+  const bool tp_bad = !(Tp >= 0.f) || Tp == INFINITY, tq_bad = !(Tq >= 0.f) || Tq == INFINITY;
+  const float kp = p_arg ? 0.f : kLog2e / Tp, kq = q_arg ? 0.f : kLog2e / Tq;
+  if (!tflags) {
+    // the rows that have records: the N target rows, then the draft rows of
+    // the nodes with children (none for a greedy target)
+    for (int n = tid; n < N; n += kDThreads) dep[n] = 0;
+    __syncthreads();
+    for (int n = tid + 1; n < N; n += kDThreads) dep[ws.par[n]] = 1;
+    __syncthreads();
+    if (warp == 0) {
+      int cnt = N;
+      for (int base = 0; base < N; base += 32) {
+        const int n = base + lane;
+        if (n < N) ws.rows[n] = n;
+        const bool has = n < N && !p_arg && dep[n] != 0;
+        const unsigned b = __ballot_sync(0xFFFFFFFFu, has);
+        if (has) ws.rows[cnt + __popc(b & ((1u << lane) - 1u))] = N + n;
+        cnt += __popc(b);
+      }
+      if (lane == 0) ws.nrows = cnt;
+    }
+  }
+  grid_dependency_wait();  // the rows kernel's records are visible
+  if (tflags) {
+    if (rank == 0) walk_no_result(P, tree, -1, tflags);
+    return;  // every CTA of the cluster returns here
+  }
+  __syncthreads();
+  // 2. CTA r merges listed rows r, r + C, ... (records staged in shared memory
+  // with all loads in flight at once when they fit) and hands the merged
+  // records to every CTA
+  const int nrows = ws.nrows;
+  const int rps = 2 * N;
+  const int R = P.cpr * kChainRecordsPerChunk;
+  const int nmine = rank < nrows ? (nrows - 1 - rank) / C + 1 : 0;
+  const int nrec = nmine * R;
+  const bool staged = nrec <= kDrawRecords;
+  if (staged) {
+    for (int x0 = tid; x0 < nrec; x0 += 4 * kDThreads) {
+      unsigned long long b[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int x = x0 + q * kDThreads;
+        b[q] = 0ull;
+        if (x < nrec) {
+          const int r = ws.rows[rank + (x / R) * C];
+          b[q] = __ldcg(P.srec + (static_cast<long long>(tree) * rps + r) * R + x % R);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (x0 + q * kDThreads < nrec) srec[x0 + q * kDThreads] = b[q];
+    }
+    __syncthreads();
+  }
+  for (int k = warp; k < nmine; k += kDWarps) {
+    const int r = ws.rows[rank + k * C];
+    const unsigned long long *src = staged ? srec + static_cast<long long>(k) * R
+                                           : P.srec + (static_cast<long long>(tree) * rps + r) * R;
+    const unsigned long long rec = merge_row(P, tree, r, src, staged);
+    if (lane == 0) ws.rr[r] = rec;
+  }
+  __syncthreads();
+  cluster_wait();  // every CTA has started
+  for (int x = tid; x < nmine * C; x += kDThreads) {
+    const int k = x / C, dst = x - k * C;
+    if (dst == rank) continue;
+    const int r = ws.rows[rank + k * C];
+    cluster.map_shared_rank(ws.rr, dst)[r] = ws.rr[r];
+  }
+  cluster_sync_all();  // every CTA holds every merged record
+  if (__ldcg(P.err)) {
+    // a bounded wait of the rows kernel gave up: the documented fallback
+    if (rank == 0) walk_no_result(P, tree, 0, SPEC_FLAG_TIMEOUT);
+    return;
+  }
+  // 3. the walk
+  if (tid == 0) ws.path[0] = 0;
+  int cur = 0, depth = 0, parity = 0;
+  uint32_t flags = 0u;
+  for (;;) {
+    const TE *gp = static_cast<const TE *>(row_ptr(P.target, nbase + cur, P.ld_t, sizeof(TE)));
+    const TE *gq = static_cast<const TE *>(row_ptr(P.draft, nbase + cur, P.ld_d, sizeof(TE)));
+    // the node's row descriptors, its children, and the test inputs of the
+    // first 32 children (warp 0)
+    if (warp == 0) {
+      RowDesc dp = row_desc(ws.rr[cur], p_arg, tp_bad, kp, V);
+      if (!p_arg && dp.onehot) dp.a = warp_finite_argmax<TE>(gp, V);  // statistics not finite
+      int nk = 0;
+      for (int base = cur + 1; base < N; base += 32) {
+        const int c = base + lane;
+        const bool hit = c < N && ws.par[c] == cur;
+        const unsigned b = __ballot_sync(0xFFFFFFFFu, hit);
+        if (hit) ws.kids[nk + __popc(b & ((1u << lane) - 1u))] = c;
+        nk += __popc(b);
+      }
+      RowDesc dq = dp;  // a one-hot stand-in where q is never read
+      dq.onehot = 1;
+      dq.a = 0;
+      dq.flags = 0u;
+      if (nk > 0 && !dp.onehot) {
+        dq = row_desc(ws.rr[N + cur], q_arg, tq_bad, kq, V);
+        if (!q_arg && dq.onehot) dq.a = warp_finite_argmax<TE>(gq, V);
+      }
+      __syncwarp();
+      if (lane < nk) {
+        const int c = ws.kids[lane];
+        const int x = __ldg(P.tokens + nbase + c);
+        const bool valid = x >= 0 && x < V;
+        ws.cx[lane] = x;
+        ws.czp[lane] = valid && !dp.onehot ? to_f32(gp[x]) : 0.f;
+        ws.czq[lane] = valid && !dp.onehot && !dq.onehot ? to_f32(gq[x]) : 0.f;
+        ws.cua[lane] = dp.onehot ? 0.f : unit_uniform(P, tree, c, 0);
+      }
+      if (lane == 0) {
+        ws.dp = dp;
+        ws.dq = dq;
+        ws.nk = nk;
+      }
+    }
+    __syncthreads();
+    const RowDesc dp = ws.dp, dq = ws.dq;
+    const int nk = ws.nk;
+    flags |= dp.flags;
+    int next = -1;
+    if (dp.onehot) {
+      // greedy rule: the first child whose token is p's argmax; q is not used
+      for (int i = 0; i < nk; ++i) {
+        const int x = i < 32 ? ws.cx[i] : __ldg(P.tokens + nbase + ws.kids[i]);
+        if (!(x >= 0 && x < V)) flags |= SPEC_FLAG_BAD_TOKEN;
+        if (x == dp.a) {
+          next = ws.kids[i];
+          break;
+        }
+      }
+      if (next < 0) {
+        if (rank == 0) walk_outputs(P, ws, tree, depth, dp.a, flags, dp, dq, 0.f, 0.f,
+                                    nk > 0 ? 1 : 0, 0, 0);
+        return;
+      }
+    } else {
+      float c = 0.f, M = 1.f;  // the held distribution [p - c q]_+ / M
+      int nres = 0;
+      bool held = false;  // CTA 0 holds the step totals of the held distribution
+      if (nk > 0) flags |= dq.flags;
+      for (int i = 0; i < nk; ++i) {
+        if (tid == 0) {
+          int x;
+          float zp, zq, ua;
+          if (i < 32) {
+            x = ws.cx[i];
+            zp = ws.czp[i];
+            zq = ws.czq[i];
+            ua = ws.cua[i];
+          } else {
+            const int ch = ws.kids[i];
+            x = __ldg(P.tokens + nbase + ch);
+            const bool valid = x >= 0 && x < V;
+            zp = valid ? to_f32(gp[x]) : 0.f;
+            zq = valid && !dq.onehot ? to_f32(gq[x]) : 0.f;
+            ua = unit_uniform(P, tree, ch, 0);
+          }
+          uint32_t f = 0u;
+          int acc = 0;
+          if (!(x >= 0 && x < V)) {
+            f = SPEC_FLAG_BAD_TOKEN;
+          } else {
+            const float px = pprob<false>(dp, zp, x);
+            const float qx = pprob<false>(dq, zq, x);
+            if (!(qx > 0.f)) {
+              f = SPEC_FLAG_ZERO_Q;
+            } else {
+              const float w = c > 0.f ? fmaxf(fmaf(-c, qx, px), 0.f) / M : px;
+              acc = ua < fminf(1.f, w / qx) ? 1 : 0;
+            }
+          }
+          ws.accept = acc;
+          ws.tf = f;
+        }
+        __syncthreads();
+        flags |= ws.tf;
+        if (ws.accept) {
+          next = ws.kids[i];
+          break;
+        }
+        // rejected: the residual for the next multiplier and its total (the
+        // pass's barriers also order this read of ws.accept before the next
+        // write)
+        const float cn = c + M;
+        const double W =
+            walk_pass<TE>(ws, cluster, C, rank, tot, gp, gq, dp, dq, cn, V, nsteps, parity);
+        parity ^= 1;
+        if (W > 0.0) {
+          c = cn;
+          M = static_cast<float>(W);
+          ++nres;
+          held = true;
+        } else {
+          flags |= SPEC_FLAG_DEGENERATE_RESIDUAL;
+          held = false;
+        }
+      }
+      if (next < 0) {
+        // every child rejected, or a leaf: draw from the held distribution
+        if (!held) {
+          walk_pass<TE>(ws, cluster, C, rank, tot, gp, gq, dp, dq, c, V, nsteps, parity);
+          parity ^= 1;
+        }
+        if (rank != 0) return;  // no remote access follows
+        const int residual = c > 0.f ? 1 : 0;
+        RowDesc dqc = dq;
+        if (residual && !dq.onehot) dqc.invS = dq.invS * c;
+        step_search<TE, false>(sh, tot, nsteps, gp, gq, dp, dqc, residual, V,
+                               unit_uniform(P, tree, cur, 1));
+        int token = sh.token;
+        if (token < 0) token = dp.a;  // no positive weight (not reachable with finite rows)
+        const int near = sh.margin < kRefineGuard * (1.f + c) ? 1 : 0;
+        walk_outputs(P, ws, tree, depth, token, flags, dp, dq, residual ? c : 0.f,
+                     static_cast<float>(sh.W), nk > 0 ? 2 : 0, residual ? nres : 0, near);
+        return;
+      }
+    }
+    // the accepted child is the next node (every thread has read this node's
+    // shared state before warp 0 rewrites it)
+    ++depth;
+    cur = next;
+    if (tid == 0) ws.path[depth] = cur;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 
@@ -1963,6 +2392,21 @@ cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
                             tab);
 }
 
+template <typename TE>
+cudaError_t launch_tree_walk_t(const Params &P, size_t smem, cudaStream_t stream) {
+  static ClusterCache walk_cache;
+  const size_t wsmem = (static_cast<size_t>(P.steps) * sizeof(float) + 15) / 16 * 16 +
+                       kDrawRecords * sizeof(unsigned long long);
+  int Cw = 1;
+  cudaError_t e =
+      cluster_size(walk_cache, tree_walk_kernel<TE>, kDThreads, kWalkCluster, wsmem, Cw);
+  if (e != cudaSuccess) return e;
+  Cw = std::max(1, std::min(Cw, P.steps));
+  e = launch_chain_rows(P, sizeof(TE), smem, stream);
+  if (e != cudaSuccess) return e;
+  return launch_cluster_pdl(tree_walk_kernel<TE>, P.nseq * Cw, kDThreads, Cw, wsmem, stream, P);
+}
+
 }  // namespace
 
 bool set_profile_events(void *start, void *stop) {
@@ -1977,6 +2421,11 @@ cudaError_t launch_chain(const Params &P, int esize, const Exp2Table &tab, size_
                          cudaStream_t stream) {
   return esize == 2 ? launch_chain_t<uint16_t>(P, tab, smem, stream)
                     : launch_chain_t<float>(P, tab, smem, stream);
+}
+
+cudaError_t launch_tree_walk(const Params &P, int esize, size_t smem, cudaStream_t stream) {
+  return esize == 2 ? launch_tree_walk_t<uint16_t>(P, smem, stream)
+                    : launch_tree_walk_t<float>(P, smem, stream);
 }
 
 }  // namespace sv

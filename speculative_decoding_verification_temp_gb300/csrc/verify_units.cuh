@@ -84,6 +84,10 @@ constexpr int kRefineMaxGrid = 1024;
 // consumer warp).
 constexpr int kChainRecordsPerChunk = 8;
 
+// Largest tree (nodes) the tree walk over the rows stream takes; larger trees
+// go to the streaming or resident kernel.
+constexpr int kWalkMaxNodes = 256;
+
 // One work unit of the precise redraw (a slice of one queued draw's
 // vocabulary): its partial sums, published for the other units of the draw.
 // A chain's final draw: the decision the chain draw kernel's CTAs share, and
