@@ -86,8 +86,20 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
   ci.c = rem - ci.r * P.cpr;
   ci.n = min(P.chunk_elems, P.V - ci.c * P.chunk_elems);
   if (!kTyp && P.mode == kModeTree) {
-    ci.draft = ci.r >= P.ups;
-    ci.row = static_cast<long long>(ci.seq) * P.ups + (ci.draft ? ci.r - P.ups : ci.r);
+    // node-major, from the last node to the root (its draft rows, then its
+    // target rows, over every tree): the rows of the shallow nodes, where the
+    // walk's passes mostly run, are the last streamed and still in L2 when
+    // the walk begins
+    const int N = P.ups, T = P.nseq;
+    const int g = k32 / P.cpr;  // global row in stream order
+    ci.c = k32 - g * P.cpr;
+    ci.n = min(P.chunk_elems, P.V - ci.c * P.chunk_elems);
+    const int j = g / (2 * T), h = (g / T) & 1;
+    ci.seq = g - (g / T) * T;
+    const int node = N - 1 - j;
+    ci.draft = h == 0;
+    ci.r = ci.draft ? N + node : node;
+    ci.row = static_cast<long long>(ci.seq) * N + node;
     return ci;
   }
   ci.draft = !kTyp && ci.r > P.gamma;
@@ -616,6 +628,9 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
   const int NS = P.ring;
   const int CE = P.chunk_elems;
   const long long G = gridDim.x;
+  // launched behind the first-child kernel (trees): its marks are visible
+  // after this wait (a no-op for a launch without programmatic serialisation)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the consumers of the id-th chunk handed its slot back
   auto wait_done = [&](int id) {
     const int slot = id % NS;
@@ -688,7 +703,7 @@ std::mutex g_occ_mu;
 int g_occ_dev = -1, g_occ_smem = -1, g_occ_blocks[4] = {0, 0, 0, 0};
 
 template <typename TE, bool kTyp>
-cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
+cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream, bool pdl) {
   auto kern = chain_rows_kernel<TE, kTyp>;
   const int which = (sizeof(TE) == 2 ? 0 : 1) + (kTyp ? 2 : 0);
   int blocks = 0;
@@ -721,8 +736,24 @@ cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
   const long long rps =
       kTyp ? P.gamma + 1 : (P.mode == kModeTree ? 2ll * P.ups : 2ll * P.gamma + 1);
   const long long total = static_cast<long long>(P.nseq) * rps * P.cpr;
-  kern<<<static_cast<int>(total < blocks ? total : blocks), kRThreads, smem, stream>>>(P);
-  return cudaGetLastError();
+  const int grid = static_cast<int>(total < blocks ? total : blocks);
+  if (!pdl) {
+    kern<<<grid, kRThreads, smem, stream>>>(P);
+    return cudaGetLastError();
+  }
+  // programmatic serialisation: the CTAs may start while the previous kernel
+  // drains; only the producer reads what it wrote, after its wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kRThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace
@@ -730,14 +761,15 @@ cudaError_t launch_rows_t(const Params &P, size_t smem, cudaStream_t stream) {
 size_t chain_rows_ctl_bytes() { return sizeof(RowsCtl); }
 int chain_records_per_chunk() { return kRConsumerWarps; }
 
-cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStream_t stream) {
-  return esize == 2 ? launch_rows_t<uint16_t, false>(P, smem, stream)
-                    : launch_rows_t<float, false>(P, smem, stream);
+cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStream_t stream,
+                              bool pdl) {
+  return esize == 2 ? launch_rows_t<uint16_t, false>(P, smem, stream, pdl)
+                    : launch_rows_t<float, false>(P, smem, stream, pdl);
 }
 
 cudaError_t launch_typical_rows(const Params &P, int esize, size_t smem, cudaStream_t stream) {
-  return esize == 2 ? launch_rows_t<uint16_t, true>(P, smem, stream)
-                    : launch_rows_t<float, true>(P, smem, stream);
+  return esize == 2 ? launch_rows_t<uint16_t, true>(P, smem, stream, false)
+                    : launch_rows_t<float, true>(P, smem, stream, false);
 }
 
 }  // namespace sv

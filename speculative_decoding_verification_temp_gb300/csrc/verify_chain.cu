@@ -36,7 +36,8 @@
 
 namespace sv {
 
-cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStream_t stream);
+cudaError_t launch_chain_rows(const Params &P, int esize, size_t smem, cudaStream_t stream,
+                              bool pdl);
 
 namespace {
 
@@ -1058,26 +1059,29 @@ __device__ __forceinline__ void weights8(const RowDesc &dp, const RowDesc &dq, i
   }
 }
 
-// Draw weights of 8 entries from `base` (entries at or past V are 0).
+// Draw weights of 8 entries from `base` (entries at or past V are 0).  The
+// rows' entry v is at gp[v - off], gq[v - off] (off: the first entry of a
+// shared-memory copy of part of the rows, else 0).
 template <typename TE, bool kF>
 __device__ __forceinline__ void step_weights(const TE *gp, const TE *gq, const RowDesc &dp,
                                              const RowDesc &dq, int residual, int base, int V,
-                                             float w[8]) {
+                                             float w[8], int off = 0) {
   float zp[8], zq[8];
   const bool full = base + 8 <= V;
   if (full && !dp.onehot) {
-    load_vec<TE>(gp + base, zp);
+    load_vec<TE>(gp + (base - off), zp);
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) zp[e] = (!dp.onehot && base + e < V) ? to_f32(gp[base + e]) : 0.f;
+    for (int e = 0; e < 8; ++e)
+      zp[e] = (!dp.onehot && base + e < V) ? to_f32(gp[base + e - off]) : 0.f;
   }
   if (residual) {
     if (full && !dq.onehot) {
-      load_vec<TE>(gq + base, zq);
+      load_vec<TE>(gq + (base - off), zq);
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        zq[e] = (!dq.onehot && base + e < V) ? to_f32(gq[base + e]) : 0.f;
+        zq[e] = (!dq.onehot && base + e < V) ? to_f32(gq[base + e - off]) : 0.f;
     }
   } else {
 #pragma unroll
@@ -1090,14 +1094,16 @@ __device__ __forceinline__ void step_weights(const TE *gp, const TE *gq, const R
 }
 
 // Totals of the draw weights of steps [b0, b1) (256 entries each) into
-// fst[step] (the NW warps of the CTA, one warp per step; full steps four (bf16)
-// or two (fp32) per warp at a time with their loads issued before any is used).
-template <typename TE, int NW, bool kF>
+// fst[step] (the NW warps of the CTA, one warp per step; full steps 4 kM
+// (bf16) or 2 kM (fp32) per warp at a time with their loads issued before any
+// is used).  Entry v of the rows is at gp[v - off], gq[v - off].
+template <typename TE, int NW, bool kF, int kM = 1>
 __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const RowDesc &dq,
                             int residual, int V, int b0, int b1, float *fst,
-                            const TE *bmp = nullptr) {
+                            const TE *bmp = nullptr, int off = 0) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  constexpr int kU = sizeof(TE) == 2 ? 4 : 2;  // 16 or 32 raw bytes a lane per step and row
+  // 16 or 32 raw bytes a lane per step and row
+  constexpr int kU = (sizeof(TE) == 2 ? 4 : 2) * kM;
   const int nfull = min(b1, V / kStep);
   int st0 = b0 + w;
   if constexpr (!kF) {
@@ -1107,8 +1113,8 @@ __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const
 #pragma unroll
         for (int q = 0; q < kU; ++q) {
           const int base = (st0 + q * NW) * kStep + lane * 8;
-          rp[q].load(gp + base);
-          if (residual) rq[q].load(gq + base);
+          rp[q].load(gp + (base - off));
+          if (residual) rq[q].load(gq + (base - off));
         }
 #pragma unroll
         for (int q = 0; q < kU; ++q) {
@@ -1125,7 +1131,7 @@ __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const
     }
     for (int st = st0; st < b1; st += NW) {
       float x[8];
-      step_weights<TE, kF>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x);
+      step_weights<TE, kF>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x, off);
       float sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
       sm = warp_sum(sm);
       if (lane == 0) fst[st] = sm;
@@ -1143,8 +1149,8 @@ __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const
           const int base = (st0 + q * NW) * kStep + lane * 8;
           dd[q] = dead(st0 + q * NW);
           if (!dd[q]) {
-            rp[q].load(gp + base);
-            if (residual) rq[q].load(gq + base);
+            rp[q].load(gp + (base - off));
+            if (residual) rq[q].load(gq + (base - off));
           }
         }
 #pragma unroll
@@ -1167,7 +1173,7 @@ __device__ void step_totals(const TE *gp, const TE *gq, const RowDesc &dp, const
       float sm = 0.f;
       if (!dead(st)) {
         float x[8];
-        step_weights<TE, kF>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x);
+        step_weights<TE, kF>(gp, gq, dp, dq, residual, st * kStep + lane * 8, V, x, off);
         sm = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
         sm = warp_sum(sm);
       }
@@ -1819,8 +1825,11 @@ __global__ void __launch_bounds__(kPThreads, 2) chain_precise_kernel(const Param
 // 5. tree walk kernel: one cluster per tree
 // ---------------------------------------------------------------------------
 
-constexpr int kWalkCluster = 16;  // CTAs per tree (fewer when such a cluster cannot run)
-static_assert(kWalkMaxNodes <= 2 * kDThreads, "the shape pass takes two nodes a thread");
+constexpr int kWWarps = 8;
+constexpr int kWThreads = kWWarps * 32;
+constexpr int kWalkCluster = 8;  // CTAs per tree (fewer when such a cluster cannot run)
+static_assert(kWalkMaxNodes <= 2 * kWThreads, "the shape pass takes two nodes a thread");
+static_assert(kWThreads >= kDThreads, "the draw search runs on the first kDThreads threads");
 
 struct WalkShared {
   unsigned long long rr[2 * kWalkMaxNodes];  // merged records: target rows, then draft rows
@@ -1828,47 +1837,105 @@ struct WalkShared {
   int kids[kWalkMaxNodes];                   // children of the current node, ascending
   int path[kWalkMaxNodes];                   // the walked path, root first
   int rows[2 * kWalkMaxNodes];               // the rows that have records
-  int cx[32];                                // acceptance-test inputs of the first 32
-  float czp[32], czq[32], cua[32];           //   children: token, its logits, uniform
-  double part[2][kMaxCluster];               // every CTA's share of a pass total (by parity)
+  int cx[kWalkMaxNodes];                     // per node c: its token x, the logits of x in
+  float czp[kWalkMaxNodes], czq[kWalkMaxNodes];  //   its parent's target and draft rows,
+  float cua[kWalkMaxNodes], cud[kWalkMaxNodes];  //   its acceptance and draw uniforms
+  Df part[2][kMaxCluster];                   // every CTA's share of a pass total (by parity)
   RowDesc dp, dq;                            // the current node's rows
   int nk, nrows, accept;
   uint32_t tf;
 };
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// This CTA's share of the steps of a row of V entries split over C CTAs:
+// steps [b0, b1), and whether both rows' shares fit in the staging buffer.
+struct WalkShare {
+  int b0, b1, cap;  // cap: entries of a row the buffer holds
+  bool staged;
+};
+template <typename TE>
+__device__ __forceinline__ WalkShare walk_share(int C, int rank, int nsteps, int bufcap) {
+  WalkShare w;
+  const int per = (nsteps + C - 1) / C;
+  w.b0 = min(nsteps, rank * per);
+  w.b1 = min(nsteps, w.b0 + per);
+  w.cap = per * kStep;
+  w.staged = w.cap * static_cast<int>(sizeof(TE)) * 2 <= bufcap;
+  return w;
+}
+
+// Start copying this CTA's share of a node's target row (and of its draft row
+// when `withq`) into the staging buffer: 16-byte asynchronous copies, all in
+// flight at once (every thread); walk_pass waits for them.  The ragged tail
+// of the row (less than 16 bytes) is copied with plain loads.
+template <typename TE>
+__device__ void walk_prefetch(const WalkShare &sh, TE *buf, const TE *gp, const TE *gq, bool withq,
+                              int V) {
+  constexpr int kPer16 = 16 / static_cast<int>(sizeof(TE));
+  TE *sp = buf, *sq = buf + sh.cap;
+  const int e0 = sh.b0 * kStep;
+  const int n = max(0, min(V, sh.b1 * kStep) - e0);
+  const int nvec = n / kPer16;
+  for (int i = threadIdx.x; i < nvec; i += kWThreads) {
+    cp_async16(sp + i * kPer16, gp + e0 + i * kPer16);
+    if (withq) cp_async16(sq + i * kPer16, gq + e0 + i * kPer16);
+  }
+  for (int v = nvec * kPer16 + threadIdx.x; v < n; v += kWThreads) {
+    sp[v] = gp[e0 + v];
+    if (withq) sq[v] = gq[e0 + v];
+  }
+}
+
 // One pass of the cluster over the current node's rows (every thread of every
 // CTA): the 256-entry step totals of the draw weights [p - c q]_+ (p itself
 // for c = 0) of this CTA's share of the steps, into CTA 0's array, and the
-// total over the row, the same double in every CTA (the CTAs' shares added
-// in rank order).  `parity` alternates between consecutive passes: a CTA
-// reads the shares of a pass before it arrives at the next pass's barrier, so
-// the pass after next may overwrite them.
+// total over the row, the same double-float in every CTA (each CTA's share,
+// lane 0's value, added in rank order).  A staged share is read from the
+// staging buffer, which walk_prefetch filled before the first pass at the
+// node (every later pass at the node reads the same copy); else from global
+// memory.
+// `parity` alternates between consecutive passes: a CTA reads the shares of a
+// pass before it arrives at the next pass's barrier, so the pass after next
+// may overwrite them.
 template <typename TE>
-__device__ double walk_pass(WalkShared &ws, cg::cluster_group &cluster, int C, int rank,
-                            float *tot, const TE *gp, const TE *gq, const RowDesc &dp,
-                            const RowDesc &dq, float c, int V, int nsteps, int parity) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = (nsteps + C - 1) / C;
-  const int b0 = min(nsteps, rank * per), b1 = min(nsteps, b0 + per);
+__device__ Df walk_pass(WalkShared &ws, cg::cluster_group &cluster, const WalkShare &sr, int C,
+                        int rank, float *tot, const TE *buf, const TE *gp, const TE *gq,
+                        const RowDesc &dp, const RowDesc &dq, float c, int V, int parity) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b0 = sr.b0, b1 = sr.b1;
   const int residual = c > 0.f ? 1 : 0;
   RowDesc dqc = dq;
   if (residual && !dq.onehot) dqc.invS = dq.invS * c;  // c q_v = 2^((z - m) k) (c / S_q)
-  step_totals<TE, kDWarps, false>(gp, gq, dp, dqc, residual, V, b0, b1, tot);
+  if (sr.staged) {
+    cp_async_wait_all();
+    __syncthreads();
+    step_totals<TE, kWWarps, false>(buf, buf + sr.cap, dp, dqc, residual, V, b0, b1, tot,
+                                    nullptr, b0 * kStep);
+  } else {
+    step_totals<TE, kWWarps, false>(gp, gq, dp, dqc, residual, V, b0, b1, tot);
+  }
   __syncthreads();
   if (warp == 0) {
-    double s = 0.0;
-    for (int st = b0 + lane; st < b1; st += 32) s += static_cast<double>(tot[st]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    Df s{0.f, 0.f};
+    for (int st = b0 + lane; st < b1; st += 32) s = df_add(s, Df{tot[st], 0.f});
+    s = df_shfl(df_warp_sum(s), 0);  // lane 0's value, sent to every CTA
     if (lane < C) cluster.map_shared_rank(&ws.part[parity][0], lane)[rank] = s;
   }
   if (rank != 0) {
     float *dst = cluster.map_shared_rank(tot, 0);
-    for (int st = b0 + threadIdx.x; st < b1; st += kDThreads) dst[st] = tot[st];
+    for (int st = b0 + tid; st < b1; st += kWThreads) dst[st] = tot[st];
   }
   cluster_sync_all();
-  double W = 0.0;
-  for (int r = 0; r < C; ++r) W += ws.part[parity][r];
+  Df W{0.f, 0.f};
+  for (int r = 0; r < C; ++r) W = df_add(W, ws.part[parity][r]);
   return W;
 }
 
@@ -1882,10 +1949,10 @@ __device__ void walk_outputs(const Params &P, const WalkShared &ws, int tree, in
   const long long nbase = static_cast<long long>(tree) * N;
   const int width = P.max_depth + 1;
   const long long obase = static_cast<long long>(tree) * width;
-  for (int i = threadIdx.x; i < width; i += kDThreads) {
+  for (int i = threadIdx.x; i < width; i += kWThreads) {
     P.out_path[obase + i] = i <= depth ? ws.path[i] : -1;
     int v = -1;
-    if (i < depth) v = __ldg(P.tokens + nbase + ws.path[i + 1]);
+    if (i < depth) v = ws.cx[ws.path[i + 1]];
     else if (i == depth) v = token;
     P.out_tokens[obase + i] = v;
   }
@@ -1921,7 +1988,7 @@ __device__ void walk_outputs(const Params &P, const WalkShared &ws, int tree, in
 __device__ void walk_no_result(const Params &P, int tree, int num, uint32_t flags) {
   const int width = P.max_depth + 1;
   const long long obase = static_cast<long long>(tree) * width;
-  for (int i = threadIdx.x; i < width; i += kDThreads) {
+  for (int i = threadIdx.x; i < width; i += kWThreads) {
     P.out_path[obase + i] = -1;
     P.out_tokens[obase + i] = -1;
   }
@@ -1947,10 +2014,11 @@ __device__ void walk_no_result(const Params &P, int tree, int num, uint32_t flag
 // draw from p) is CTA 0's double-float search over the step totals of the
 // last pass; a draw within the refine guard of a boundary is queued for the
 // refine kernel, which recomputes the multipliers in double precision.
-// Dynamic shared memory: the step totals tot[steps] and room for
-// kDrawRecords records.
+// Dynamic shared memory: the step totals tot[steps], then a staging buffer of
+// P.walk_buf bytes (the records while they are merged, then each pass's share
+// of the rows).
 template <typename TE>
-__global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P) {
+__global__ void __launch_bounds__(kWThreads, 2) tree_walk_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char walk_smem[];
   __shared__ WalkShared ws;
   __shared__ DrawShared sh;
@@ -1962,23 +2030,37 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
   const int N = P.ups, V = P.V, nsteps = P.steps;
   const long long nbase = static_cast<long long>(tree) * N;
   float *tot = reinterpret_cast<float *>(walk_smem);
-  unsigned long long *srec = reinterpret_cast<unsigned long long *>(
-      walk_smem + (static_cast<size_t>(nsteps) * sizeof(float) + 15) / 16 * 16);
+  unsigned char *bufb = walk_smem + (static_cast<size_t>(nsteps) * sizeof(float) + 15) / 16 * 16;
+  unsigned long long *srec = reinterpret_cast<unsigned long long *>(bufb);
+  TE *buf = reinterpret_cast<TE *>(bufb);
   // every CTA of the cluster has started before the first remote access: the
   // arrive here pairs with the first wait below
   cluster_arrive();
   launch_dependents();
-  // 1. the tree's shape, from the inputs alone: every parent id below its
+  // 1. from the inputs alone: every node's acceptance-test inputs (all loads
+  // in flight at once), and the tree's shape: every parent id below its
   // child's, every depth within max_depth (depths by pointer jumping, with
   // kids and path as scratch)
   int *anc = ws.kids, *dep = ws.path;
   int bad = 0;
-  for (int n = tid; n < N; n += kDThreads) {
+  for (int n = tid; n < N; n += kWThreads) {
     const int a = __ldg(P.parent + nbase + n);
+    const int x = __ldg(P.tokens + nbase + n);
     ws.par[n] = a;
-    if (n == 0 ? a != -1 : !(a >= 0 && a < n)) bad = 1;
+    const bool link = n == 0 ? a == -1 : (a >= 0 && a < n);
+    if (!link) bad = 1;
     anc[n] = n == 0 ? 0 : a;
     dep[n] = n == 0 ? 0 : 1;
+    float zp = 0.f, zq = 0.f;
+    if (n > 0 && link && x >= 0 && x < V) {
+      zp = to_f32(static_cast<const TE *>(row_ptr(P.target, nbase + a, P.ld_t, sizeof(TE)))[x]);
+      zq = to_f32(static_cast<const TE *>(row_ptr(P.draft, nbase + a, P.ld_d, sizeof(TE)))[x]);
+    }
+    ws.cx[n] = x;
+    ws.czp[n] = zp;
+    ws.czq[n] = zq;
+    ws.cua[n] = unit_uniform(P, tree, n, 0);
+    ws.cud[n] = unit_uniform(P, tree, n, 1);
   }
   uint32_t tflags = __syncthreads_or(bad) ? SPEC_FLAG_BAD_TREE : 0u;
   if (!tflags) {
@@ -1986,7 +2068,7 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
       int la[2] = {0, 0}, ld[2] = {0, 0};
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int n = tid + i * kDThreads;
+        const int n = tid + i * kWThreads;
         if (n < N) {
           const int a = anc[n];
           la[i] = anc[a];
@@ -1996,7 +2078,7 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int n = tid + i * kDThreads;
+        const int n = tid + i * kWThreads;
         if (n < N) {
           anc[n] = la[i];
           dep[n] = ld[i];
@@ -2005,7 +2087,7 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
       __syncthreads();
     }
     int deep = 0;
-    for (int n = tid; n < N; n += kDThreads)
+    for (int n = tid; n < N; n += kWThreads)
       if (dep[n] > P.max_depth) deep = 1;
     if (__syncthreads_or(deep)) tflags = SPEC_FLAG_DEPTH;
   }
@@ -2016,9 +2098,9 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
   if (!tflags) {
     // the rows that have records: the N target rows, then the draft rows of
     // the nodes with children (none for a greedy target)
-    for (int n = tid; n < N; n += kDThreads) dep[n] = 0;
+    for (int n = tid; n < N; n += kWThreads) dep[n] = 0;
     __syncthreads();
-    for (int n = tid + 1; n < N; n += kDThreads) dep[ws.par[n]] = 1;
+    for (int n = tid + 1; n < N; n += kWThreads) dep[ws.par[n]] = 1;
     __syncthreads();
     if (warp == 0) {
       int cnt = N;
@@ -2047,13 +2129,13 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
   const int R = P.cpr * kChainRecordsPerChunk;
   const int nmine = rank < nrows ? (nrows - 1 - rank) / C + 1 : 0;
   const int nrec = nmine * R;
-  const bool staged = nrec <= kDrawRecords;
+  const bool staged = static_cast<long long>(nrec) * 8 <= P.walk_buf;
   if (staged) {
-    for (int x0 = tid; x0 < nrec; x0 += 4 * kDThreads) {
+    for (int x0 = tid; x0 < nrec; x0 += 4 * kWThreads) {
       unsigned long long b[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int x = x0 + q * kDThreads;
+        const int x = x0 + q * kWThreads;
         b[q] = 0ull;
         if (x < nrec) {
           const int r = ws.rows[rank + (x / R) * C];
@@ -2062,11 +2144,11 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (x0 + q * kDThreads < nrec) srec[x0 + q * kDThreads] = b[q];
+        if (x0 + q * kWThreads < nrec) srec[x0 + q * kWThreads] = b[q];
     }
     __syncthreads();
   }
-  for (int k = warp; k < nmine; k += kDWarps) {
+  for (int k = warp; k < nmine; k += kWWarps) {
     const int r = ws.rows[rank + k * C];
     const unsigned long long *src = staged ? srec + static_cast<long long>(k) * R
                                            : P.srec + (static_cast<long long>(tree) * rps + r) * R;
@@ -2075,7 +2157,7 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
   }
   __syncthreads();
   cluster_wait();  // every CTA has started
-  for (int x = tid; x < nmine * C; x += kDThreads) {
+  for (int x = tid; x < nmine * C; x += kWThreads) {
     const int k = x / C, dst = x - k * C;
     if (dst == rank) continue;
     const int r = ws.rows[rank + k * C];
@@ -2089,13 +2171,14 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
   }
   // 3. the walk
   if (tid == 0) ws.path[0] = 0;
+  const WalkShare sr = walk_share<TE>(C, rank, nsteps, P.walk_buf);
   int cur = 0, depth = 0, parity = 0;
+  int loaded = -1;  // the node whose rows the staging buffer holds
   uint32_t flags = 0u;
   for (;;) {
     const TE *gp = static_cast<const TE *>(row_ptr(P.target, nbase + cur, P.ld_t, sizeof(TE)));
     const TE *gq = static_cast<const TE *>(row_ptr(P.draft, nbase + cur, P.ld_d, sizeof(TE)));
-    // the node's row descriptors, its children, and the test inputs of the
-    // first 32 children (warp 0)
+    // the node's row descriptors and its children (warp 0)
     if (warp == 0) {
       RowDesc dp = row_desc(ws.rr[cur], p_arg, tp_bad, kp, V);
       if (!p_arg && dp.onehot) dp.a = warp_finite_argmax<TE>(gp, V);  // statistics not finite
@@ -2115,16 +2198,6 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
         dq = row_desc(ws.rr[N + cur], q_arg, tq_bad, kq, V);
         if (!q_arg && dq.onehot) dq.a = warp_finite_argmax<TE>(gq, V);
       }
-      __syncwarp();
-      if (lane < nk) {
-        const int c = ws.kids[lane];
-        const int x = __ldg(P.tokens + nbase + c);
-        const bool valid = x >= 0 && x < V;
-        ws.cx[lane] = x;
-        ws.czp[lane] = valid && !dp.onehot ? to_f32(gp[x]) : 0.f;
-        ws.czq[lane] = valid && !dp.onehot && !dq.onehot ? to_f32(gq[x]) : 0.f;
-        ws.cua[lane] = dp.onehot ? 0.f : unit_uniform(P, tree, c, 0);
-      }
       if (lane == 0) {
         ws.dp = dp;
         ws.dq = dq;
@@ -2139,7 +2212,7 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
     if (dp.onehot) {
       // greedy rule: the first child whose token is p's argmax; q is not used
       for (int i = 0; i < nk; ++i) {
-        const int x = i < 32 ? ws.cx[i] : __ldg(P.tokens + nbase + ws.kids[i]);
+        const int x = ws.cx[ws.kids[i]];
         if (!(x >= 0 && x < V)) flags |= SPEC_FLAG_BAD_TOKEN;
         if (x == dp.a) {
           next = ws.kids[i];
@@ -2158,21 +2231,9 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
       if (nk > 0) flags |= dq.flags;
       for (int i = 0; i < nk; ++i) {
         if (tid == 0) {
-          int x;
-          float zp, zq, ua;
-          if (i < 32) {
-            x = ws.cx[i];
-            zp = ws.czp[i];
-            zq = ws.czq[i];
-            ua = ws.cua[i];
-          } else {
-            const int ch = ws.kids[i];
-            x = __ldg(P.tokens + nbase + ch);
-            const bool valid = x >= 0 && x < V;
-            zp = valid ? to_f32(gp[x]) : 0.f;
-            zq = valid && !dq.onehot ? to_f32(gq[x]) : 0.f;
-            ua = unit_uniform(P, tree, ch, 0);
-          }
+          const int ch = ws.kids[i];
+          const int x = ws.cx[ch];
+          const float zp = ws.czp[ch], zq = dq.onehot ? 0.f : ws.czq[ch], ua = ws.cua[ch];
           uint32_t f = 0u;
           int acc = 0;
           if (!(x >= 0 && x < V)) {
@@ -2200,12 +2261,16 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
         // pass's barriers also order this read of ws.accept before the next
         // write)
         const float cn = c + M;
-        const double W =
-            walk_pass<TE>(ws, cluster, C, rank, tot, gp, gq, dp, dq, cn, V, nsteps, parity);
+        if (sr.staged && loaded != cur) {  // the node's first pass: its rows to the buffer
+          walk_prefetch<TE>(sr, buf, gp, gq, !dq.onehot, V);
+          loaded = cur;
+        }
+        const Df W = walk_pass<TE>(ws, cluster, sr, C, rank, tot, buf, gp, gq, dp, dq, cn, V,
+                                   parity);
         parity ^= 1;
-        if (W > 0.0) {
+        if (W.hi > 0.f) {
           c = cn;
-          M = static_cast<float>(W);
+          M = W.hi + W.lo;
           ++nres;
           held = true;
         } else {
@@ -2216,15 +2281,20 @@ __global__ void __launch_bounds__(kDThreads, 6) tree_walk_kernel(const Params P)
       if (next < 0) {
         // every child rejected, or a leaf: draw from the held distribution
         if (!held) {
-          walk_pass<TE>(ws, cluster, C, rank, tot, gp, gq, dp, dq, c, V, nsteps, parity);
+          if (sr.staged && loaded != cur) {
+            walk_prefetch<TE>(sr, buf, gp, gq, c > 0.f && !dq.onehot, V);
+            loaded = cur;
+          }
+          walk_pass<TE>(ws, cluster, sr, C, rank, tot, buf, gp, gq, dp, dq, c, V, parity);
           parity ^= 1;
         }
         if (rank != 0) return;  // no remote access follows
         const int residual = c > 0.f ? 1 : 0;
         RowDesc dqc = dq;
         if (residual && !dq.onehot) dqc.invS = dq.invS * c;
-        step_search<TE, false>(sh, tot, nsteps, gp, gq, dp, dqc, residual, V,
-                               unit_uniform(P, tree, cur, 1));
+        if (tid < kDThreads)
+          step_search<TE, false>(sh, tot, nsteps, gp, gq, dp, dqc, residual, V, ws.cud[cur]);
+        __syncthreads();
         int token = sh.token;
         if (token < 0) token = dp.a;  // no positive weight (not reachable with finite rows)
         const int near = sh.margin < kRefineGuard * (1.f + c) ? 1 : 0;
@@ -2371,7 +2441,7 @@ cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
     e = cudaEventRecord(prof_start, stream);
     if (e != cudaSuccess) return e;
   }
-  e = launch_chain_rows(P, sizeof(TE), smem, stream);
+  e = launch_chain_rows(P, sizeof(TE), smem, stream, false);
   if (e != cudaSuccess) return e;
   if (prof_stop) {
     e = cudaEventRecord(prof_stop, stream);
@@ -2392,19 +2462,31 @@ cudaError_t launch_chain_t(const Params &P, const Exp2Table &tab, size_t smem,
                             tab);
 }
 
+// Staging buffer of a walk CTA: its share of both rows for clusters of C CTAs
+// when that fits in kWalkMaxBuf bytes, and at least the records' staging area.
+constexpr int kWalkMaxBuf = 96 * 1024;
+int walk_buf_bytes(const Params &P, int esize, int C) {
+  const long long share = static_cast<long long>((P.steps + C - 1) / C) * kStep * esize * 2;
+  const long long recs = static_cast<long long>(kDrawRecords) * sizeof(unsigned long long);
+  return static_cast<int>(share <= kWalkMaxBuf ? std::max(share, recs) : recs);
+}
+
 template <typename TE>
 cudaError_t launch_tree_walk_t(const Params &P, size_t smem, cudaStream_t stream) {
   static ClusterCache walk_cache;
+  Params Pw = P;
+  Pw.walk_buf = walk_buf_bytes(P, sizeof(TE), kWalkCluster);
   const size_t wsmem = (static_cast<size_t>(P.steps) * sizeof(float) + 15) / 16 * 16 +
-                       kDrawRecords * sizeof(unsigned long long);
+                       static_cast<size_t>(Pw.walk_buf);
   int Cw = 1;
   cudaError_t e =
-      cluster_size(walk_cache, tree_walk_kernel<TE>, kDThreads, kWalkCluster, wsmem, Cw);
+      cluster_size(walk_cache, tree_walk_kernel<TE>, kWThreads, kWalkCluster, wsmem, Cw);
   if (e != cudaSuccess) return e;
+  // a smaller cluster whose shares do not fit reads the rows from global memory
   Cw = std::max(1, std::min(Cw, P.steps));
-  e = launch_chain_rows(P, sizeof(TE), smem, stream);
+  e = launch_chain_rows(P, sizeof(TE), smem, stream, true);  // behind the first-child kernel
   if (e != cudaSuccess) return e;
-  return launch_cluster_pdl(tree_walk_kernel<TE>, P.nseq * Cw, kDThreads, Cw, wsmem, stream, P);
+  return launch_cluster_pdl(tree_walk_kernel<TE>, P.nseq * Cw, kWThreads, Cw, wsmem, stream, Pw);
 }
 
 }  // namespace

@@ -1014,6 +1014,9 @@ __global__ void __launch_bounds__(kThreads) tree_combine_kernel(const Params P) 
 __global__ void __launch_bounds__(kThreads) tree_first_child_kernel(const int32_t *parent, int N,
                                                                     int32_t *first_child) {
   extern __shared__ int fc[];
+  // a kernel launched behind this one with programmatic serialisation may
+  // start now; it waits for these results before it reads them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long base = static_cast<long long>(blockIdx.x) * N;
   for (int n = threadIdx.x; n < N; n += kThreads) fc[n] = INT_MAX;
   __syncthreads();

@@ -184,6 +184,7 @@ struct Params {
                                   //   type; NULL: no row filter in the call)
   float2 *frec;                   // [rows] filtered rows: (threshold, kept normaliser S)
   int nblk;                       // 512-entry blocks per row
+  int walk_buf;                   // tree walk: bytes of a CTA's staging buffer
   unsigned long long *pseqw;      // [nseq] PassSeq of each queued precise redraw
   int *near_list;                 // [nseq] sequence + 1 of each queued precise redraw
   uint32_t *pctr;                 // [0] precise redraws queued (cleared by every call)
