@@ -48,7 +48,7 @@ struct SlotInfo {
   int n;           // entries
   int nb;          // entries copied to shared memory
   float k;         // log2(e) / T, 0 for a greedy row
-  int arg;         // 1: greedy row (argmax record); 2: a row nobody reads (not copied)
+  int arg;         // 1: greedy row (argmax record)
   int v0;          // vocabulary index of the chunk's first entry
   int row;         // the chunk's row: seq * (rows per sequence) + r
 };
@@ -110,6 +110,17 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
 
 // Policy of a row: greedy (argmax) or sampling with k = log2(e) / T.
 __device__ __forceinline__ bool row_is_arg(float T) { return !(T > 0.f) || T == INFINITY; }
+
+// Rows nobody reads are not streamed: the draft rows of a sequence whose
+// target is greedy (a one-hot p accepts a draft iff it is p's argmax and needs
+// no draw), and the draft rows of a tree's leaves.  The producer decides it;
+// such a chunk takes no slot.
+template <bool kTyp>
+__device__ __forceinline__ bool chunk_skipped(const Params &P, const ChunkInfo &ci) {
+  if (kTyp || !ci.draft) return false;
+  if (row_is_arg(__ldg(P.Tp + ci.seq))) return true;
+  return P.mode == kModeTree && __ldg(P.first_child + ci.row) < 0;
+}
 
 template <typename TE>
 __device__ __forceinline__ void load_vec(const TE *s, float z[8]);
@@ -564,9 +575,11 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = P.ring;
   const int EW = P.chunk_elems / kRConsumerWarps;  // entries per warp (a multiple of 256)
-  int i = 0;
-  for (long long k = blockIdx.x; k < total; k += gridDim.x, ++i) {
-    const int slot = i % NS;
+  // the slots the producer fills: this CTA's chunks that are streamed, then
+  // an end marker (n < 0); at most one per chunk of this CTA, plus the marker
+  const long long cap = (total - blockIdx.x + gridDim.x - 1) / gridDim.x + 1;
+  for (long long i = 0; i < cap; ++i) {
+    const int slot = static_cast<int>(i % NS);
     const uint32_t phase = static_cast<uint32_t>(i / NS) & 1u;
     if (!mbar_wait_limit(&ctl.full[slot], phase, P.first_wait)) {
       // gave up: flag it, then wait again with the full bound, so that no copy
@@ -575,10 +588,10 @@ __device__ void rows_consumer(const Params &P, RowsCtl &ctl, unsigned char *ring
       mbar_wait_bounded(&ctl.full[slot], phase);
     }
     const SlotInfo si = ctl.info[slot];
-    if (si.arg == 2) {  // a row nobody reads: no copy, no record
+    if (si.n < 0) {  // the end marker
       __syncwarp();
       if (lane == 0) mbar_arrive1_c(&ctl.empty[slot]);
-      continue;
+      break;
     }
     const TE *sm = reinterpret_cast<const TE *>(ring + static_cast<size_t>(slot) * P.slot_bytes);
     const int e0 = min(si.n, warp * EW), e1 = min(si.n, e0 + EW);
@@ -638,21 +651,18 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
     if (!mbar_wait_bounded(&ctl.empty[slot], phase)) atomicOr(P.err, 1u);
   };
   int i = 0;
-  for (long long k = blockIdx.x; k < total; k += G, ++i) {
-    const int slot = i % NS;
-    if (i >= NS) wait_done(i - NS);
+  for (long long k = blockIdx.x; k < total; k += G) {
     const ChunkInfo ci = chunk_info<kTyp>(P, k);
+    if (chunk_skipped<kTyp>(P, ci)) continue;
     const float T = __ldg((ci.draft ? P.Tq : P.Tp) + ci.seq);
     const bool arg = row_is_arg(T);
-    // the draft rows of a sequence whose target is greedy are never read: a
-    // one-hot p accepts a draft iff it is p's argmax and needs no draw; nor
-    // are the draft rows of a tree's leaves
-    bool skip = !kTyp && ci.draft && row_is_arg(__ldg(P.Tp + ci.seq));
-    if (!kTyp && ci.draft && !skip && P.mode == kModeTree) skip = __ldg(P.first_child + ci.row) < 0;
+    const int slot = i % NS;
+    if (i >= NS) wait_done(i - NS);
+    ++i;
     const TE *gl = static_cast<const TE *>(row_ptr(ci.draft ? P.draft : P.target, ci.row,
                                                    ci.draft ? P.ld_d : P.ld_t, sizeof(TE))) +
                    static_cast<long long>(ci.c) * CE;
-    const uint32_t bytes = skip ? 0u : static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
+    const uint32_t bytes = static_cast<uint32_t>(ci.n * sizeof(TE)) / 16u * 16u;
     SlotInfo &si = ctl.info[slot];
     si.gl = gl;
     const int rps = stream_rows<kTyp>(P);
@@ -661,12 +671,19 @@ __device__ void rows_producer(const Params &P, RowsCtl &ctl, unsigned char *ring
     si.n = ci.n;
     si.nb = static_cast<int>(bytes / sizeof(TE));
     si.k = arg ? 0.f : kLog2e / T;
-    si.arg = skip ? 2 : (arg ? 1 : 0);
+    si.arg = arg ? 1 : 0;
     si.v0 = ci.c * CE;
     si.row = ci.seq * rps + ci.r;
     mbar_arrive_expect_tx(&ctl.full[slot], bytes);
     if (bytes) bulk_g2s_plain(ring + static_cast<size_t>(slot) * P.slot_bytes, gl, bytes,
                               &ctl.full[slot]);
+  }
+  {  // the end marker: a slot without bytes
+    const int slot = i % NS;
+    if (i >= NS) wait_done(i - NS);
+    ++i;
+    ctl.info[slot].n = -1;
+    mbar_arrive_expect_tx(&ctl.full[slot], 0u);
   }
   const int issued = i;
   for (int d = max(0, issued - NS); d < issued; ++d) wait_done(d);
