@@ -66,10 +66,13 @@
  *
  * Limits: 0 <= gamma <= 4095; 1 <= N <= 4096; V >= 1, and for the verifiers
  * a V that the call's kernel path takes (SPEC_ERR_UNSUPPORTED otherwise):
- *   - chains of gamma <= 31 with 16-byte-aligned rows and no row filter
- *     (top-k, top-p, min-p) stream their rows: V <= 2,097,152;
- *   - trees and longer chains with aligned rows and no row filter stream
- *     slices of at most 32 KB, 64 per row: V <= 1,048,576 bf16 / 524,288 fp32;
+ *   - chains of gamma <= 31 with 16-byte-aligned rows (with or without a
+ *     row filter: top-k, top-p, min-p) stream their rows: V <= 2,097,152;
+ *   - trees of at most 256 nodes with aligned rows and no row filter stream
+ *     their rows and walk the accepted path: V <= 2,097,152;
+ *   - larger trees and longer chains with aligned rows and no row filter
+ *     stream slices of at most 32 KB, 64 per row: V <= 1,048,576 bf16 /
+ *     524,288 fp32;
  *   - rows with a filter, or unaligned rows, hold a target+draft row pair in
  *     16 thread blocks' shared memory: about 800k bf16 or 400k fp32 entries.
  * spec_overlap and spec_typical_accept read rows from global memory and take
@@ -137,7 +140,9 @@ typedef struct {
 #define SPEC_FLAG_TIMEOUT 32u            /* a bounded on-device wait gave up; on the
                                             streaming chain path the sequence then
                                             gets the fallback outputs: 0 accepted
-                                            drafts, every token -1 */
+                                            drafts, every token -1; on the tree walk
+                                            path the tree: 0 accepted nodes, every
+                                            path entry and token -1 */
 #define SPEC_FLAG_BAD_TREE 64u           /* parent[0] != -1 or parent[n] not in [0, n) */
 
 /* Bytes of workspace spec_verify_chain needs for B sequences of gamma drafts
@@ -244,6 +249,10 @@ size_t spec_verify_tree_workspace_size(int T, int N, int V, spec_dtype dtype);
  *   out_flags [T] (nullable), out_residual [T, V] (nullable): the distribution the
  *                          final token was drawn from when every child of the last
  *                          node was rejected; zeros for a bonus draw at a leaf.
+ * Launches (trees of at most 256 nodes, aligned rows, no row filter): one
+ * cudaMemsetAsync, then the first-child, rows, walk and refine kernels; the
+ * rows kernel reads every target row and the draft rows of internal nodes once,
+ * the walk re-reads the row pair of each node where a sibling is rejected.
  */
 spec_status spec_verify_tree(
     const void *target_logits, int64_t ld_target,
