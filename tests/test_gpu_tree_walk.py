@@ -1,16 +1,18 @@
 """The tree walk over the rows stream (aligned rows, at most 256 nodes, no row
 filter) against the oracle, on the cases its design singles out.
 
-- more than 32 children at a node (test inputs past the first 32 are loaded
-  on demand), the largest tree it takes (256 nodes) and the first one it
-  does not (257 nodes: the streaming kernel);
+- more children at a node than a warp has lanes, the largest tree it takes
+  (256 nodes) and the first one it does not (257 nodes: the streaming
+  kernel);
 - a degenerate residual: p = q with children whose tokens are rejected for a
   bad token, so that every residual pass has total 0 and the draw falls back
   to the held p;
 - a greedy draft (one-hot q: q(x) = 0 off its argmax) and a greedy target;
 - non-finite target and draft rows on the path;
 - a bounded wait of the rows kernel that runs out (the documented fallback),
-  and the next call bit-exact with one made before.
+  and the next call bit-exact with one made before;
+- rows whose per-CTA share does not fit the staging buffer (the passes then
+  read global memory).
 """
 
 import numpy as np
@@ -76,7 +78,8 @@ def test_degenerate_residual(exception_log):
     w["tokens"][:, 4] = 10**6
     res = run_tree(w, return_residual=True)
     want = oracle_tree(w)
-    assert all(r["flags"] & 1 for r in want)  # the oracle flags the degenerate residual
+    # the oracle flags the bad tokens and the degenerate residual
+    assert all(r["flags"] & 1 and r["flags"] & 8 for r in want)
     compare_tree(res, want, exception_log, "walk-degenerate", "f32", check_residual=True)
 
 
@@ -125,3 +128,13 @@ def test_wait_runs_out_then_recovers(dtype):
     after = call()
     for a, b in zip(before, after):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("dtype,V", [("f32", 100_000), ("bf16", 200_000)])
+def test_rows_from_global_memory(dtype, V, exception_log):
+    # a CTA's share of a row pair larger than its staging buffer: the passes
+    # read the rows from global memory
+    w = workloads.make_tree(3, 10, V, dtype=dtype, seed=306, sigma=1.2, branching=(3, 2, 1))
+    res = run_tree(w, return_residual=True)
+    compare_tree(res, oracle_tree(w), exception_log, f"walk-global-{dtype}", dtype,
+                 check_residual=True)
