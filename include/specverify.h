@@ -200,7 +200,7 @@ spec_status spec_verify_chain(
  * Size limit: shapes with spec_verify_chain_workspace_size(B, gamma, V, dtype)
  *   > SPEC_STATIC_SCRATCH_BYTES return SPEC_ERR_UNSUPPORTED before any CUDA
  *   call; use spec_verify_chain there.  For V = 128256 bf16 and gamma = 7,
- *   B = 512 fits (8.7 MiB) and B = 1024 does not (17.3 MiB).
+ *   B = 512 fits (9.6 MiB) and B = 1024 does not (19.1 MiB).
  * Address: every call looks the array's address up with cudaGetSymbolAddress
  *   in the device context current on the calling thread, so a call made after
  *   a device reset works in the new context.  The first call on each device
