@@ -21,6 +21,8 @@ from speculative_decoding_verification_temp_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 
+# "stream": the streaming paths (the chain path, the tree walk); "resident": an
+# all-off top-k array selects the resident cluster kernel on the same inputs
 PATHS = ["stream", "resident"]
 TIE = 1e-12
 

@@ -34,8 +34,11 @@ def built():
 # the five workloads at full size (the bench's launch configuration)
 # ---------------------------------------------------------------------------
 
-# "stream": no top-k array, the streaming kernel runs; "resident": an all-off
-# top-k array selects the resident cluster kernel on the same inputs.
+# "stream": no top-k array: chains of gamma <= 31 take the streaming chain path
+# (rows, draw and precise kernels), trees of at most 256 nodes the tree walk
+# (rows and walk kernels), longer chains and larger trees the streaming
+# kernel; "resident": an all-off top-k array selects the resident cluster
+# kernel on the same inputs.
 PATHS = ["stream", "resident"]
 
 
