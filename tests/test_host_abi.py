@@ -56,6 +56,24 @@ def test_workspace_sizes(lib):
     assert lib.spec_verify_tree_workspace_size(1, -1, 10, 0) == 0
 
 
+def test_tree_walk_workspace_holds_the_row_records(lib):
+    # trees of at most 256 nodes take the rows stream and the walk: the
+    # workspace holds one 64-bit record per consumer warp (8) per 32 KB chunk
+    # of each of the 2N rows of a tree.  At V = 1,500,000 bf16 a 257-node tree
+    # takes the resident kernel (beyond the streaming kernel's vocabulary),
+    # whose workspace has no such records.
+    T, V = 4, 1_500_000
+    chunks = -(-V * 2 // 32768)  # bf16 rows of V entries in 32 KB chunks
+    records = T * 2 * 256 * chunks * 8 * 8
+    with_walk = lib.spec_verify_tree_workspace_size(T, 256, V, _abi.SPEC_BF16)
+    without = lib.spec_verify_tree_workspace_size(T, 257, V, _abi.SPEC_BF16)
+    assert with_walk >= records
+    assert with_walk - without >= records * 0.9
+    # at the tree workload's size the records fit the workspace as well
+    assert lib.spec_verify_tree_workspace_size(32, 60, 128256, _abi.SPEC_BF16) >= \
+        32 * 120 * 8 * 8 * 8
+
+
 FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails its host checks
 
 
