@@ -2,8 +2,9 @@
 // the batch from HBM exactly once (see verify_chain.cu for the whole path).
 //
 // Every logit row of the batch - the gamma + 1 target rows and the gamma draft
-// rows of each sequence - is cut into 32 KB chunks, numbered sequence-major and
-// handed out round-robin over a persistent grid (three CTAs per SM).  In each
+// rows of each sequence - is cut into 32 KB chunks, numbered position-major
+// (the bonus rows last) and handed out round-robin over a persistent grid
+// (three CTAs per SM).  In each
 // CTA one producer warp streams its chunks into a ring of two shared-memory
 // slots with bulk asynchronous copies (cp.async.bulk, one "full" and one
 // "empty" mbarrier per slot); eight consumer warps reduce each chunk to one
@@ -102,9 +103,35 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Params &P, long long k) {
     ci.row = static_cast<long long>(ci.seq) * N + node;
     return ci;
   }
-  ci.draft = !kTyp && ci.r > P.gamma;
-  ci.row = ci.draft ? static_cast<long long>(ci.seq) * P.gamma + (ci.r - P.gamma - 1)
-                    : static_cast<long long>(ci.seq) * (P.gamma + 1) + ci.r;
+  if (!kTyp) {
+    // chains, position-major: the target and draft rows of positions
+    // gamma - 1, ..., 1, 0 over every sequence, then the bonus rows.  The rows
+    // a draw reads again are most often the bonus row (every draft accepted)
+    // and then the pairs of the first positions: streamed last, they are the
+    // ones still in L2 when the draw kernel starts.
+    const int B = P.nseq, gamma = P.gamma;
+    const int g = k32 / P.cpr;  // global row in stream order
+    ci.c = k32 - g * P.cpr;
+    ci.n = min(P.chunk_elems, P.V - ci.c * P.chunk_elems);
+    const int npair = gamma * 2 * B;
+    if (g < npair) {
+      const int pos = gamma - 1 - g / (2 * B);
+      const int h = (g / B) & 1;
+      ci.seq = g - (g / B) * B;
+      ci.draft = h == 1;
+      ci.r = ci.draft ? gamma + 1 + pos : pos;
+      ci.row = ci.draft ? static_cast<long long>(ci.seq) * gamma + pos
+                        : static_cast<long long>(ci.seq) * (gamma + 1) + pos;
+    } else {
+      ci.seq = g - npair;
+      ci.draft = false;
+      ci.r = gamma;
+      ci.row = static_cast<long long>(ci.seq) * (gamma + 1) + gamma;
+    }
+    return ci;
+  }
+  ci.draft = false;
+  ci.row = static_cast<long long>(ci.seq) * (P.gamma + 1) + ci.r;
   return ci;
 }
 
