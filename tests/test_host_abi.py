@@ -175,6 +175,11 @@ def test_tree_rejects_bad_arguments(lib):
     assert tree(lib, out=None) == INV
     assert tree(lib) == INV  # workspace too small
     assert tree(lib, T=0, parent=None, tokens=None, out=None) == _abi.SPEC_OK
+    # aligned bf16 rows of 128 entries take the tree walk: a workspace one byte
+    # short of the size query is refused before anything is launched
+    need = lib.spec_verify_tree_workspace_size(2, 5, 128, _abi.SPEC_BF16)
+    assert need > 0
+    assert tree(lib, V=128, ws_bytes=need - 1) == INV
 
 
 def test_mask_rejects_bad_arguments(lib):
